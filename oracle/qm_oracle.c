@@ -1,0 +1,124 @@
+/*
+ * Oracle for the GGML Q4_0 x f32 quantized matmul — TEST INFRASTRUCTURE ONLY.
+ * See qm_oracle.h for what it follows and who may use it.  Plain loops, fp64,
+ * single-threaded, no blocking or reordering: a reader can check each line
+ * against the definitions in the kernel-contract page
+ * ("fuel-vulkan-kernels — quantized (GGML) kernel contracts").
+ */
+#include "qm_oracle.h"
+
+#include <math.h>
+#include <stddef.h>
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ *   exponent 0      -> subnormal, value = fraction * 2^-24
+ *   exponent 1..30  -> normal,    value = (1 + fraction/1024) * 2^(exponent-15)
+ *   exponent 31     -> infinity (fraction 0) or NaN (fraction != 0)        */
+double oracle_f16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int exponent = (h >> 10) & 0x1F;
+    int fraction = h & 0x3FF;
+    double magnitude;
+
+    if (exponent == 0) {
+        magnitude = ldexp((double)fraction, -24);
+    } else if (exponent == 31) {
+        magnitude = (fraction == 0) ? INFINITY : NAN;
+    } else {
+        magnitude = ldexp(1.0 + (double)fraction / 1024.0, exponent - 15);
+    }
+    return sign ? -magnitude : magnitude;
+}
+
+void oracle_f16_to_double_array(const uint16_t* h, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_double(h[i]);
+}
+
+/* The block's scale d: bytes 0 and 1, little-endian binary16. */
+static double block_scale(const uint8_t* block)
+{
+    uint16_t bits = (uint16_t)(block[0] | ((uint16_t)block[1] << 8));
+    return oracle_f16_to_double(bits);
+}
+
+/* The unsigned 4-bit quant of element j (0..31): the quant bytes start at
+ * block offset 2; element j < 16 is the low nibble of quant byte j, element
+ * j >= 16 the high nibble of quant byte j - 16. */
+static int block_nibble(const uint8_t* block, int j)
+{
+    const uint8_t* qs = block + 2;
+    if (j < 16) return qs[j] & 0x0F;
+    return (qs[j - 16] >> 4) & 0x0F;
+}
+
+/* Dequantized weight W[n][k] of a row-major [N][K/32] block stream, exact in
+ * double: (nibble - 8) has at most 4 significant bits, d at most 11. */
+static double weight_at(const uint8_t* wq, int64_t K, int64_t n, int64_t k)
+{
+    int64_t blocks_per_row = K / ORACLE_Q4_0_BLOCK_ELEMS;
+    int64_t b = k / ORACLE_Q4_0_BLOCK_ELEMS;
+    int j = (int)(k % ORACLE_Q4_0_BLOCK_ELEMS);
+    const uint8_t* block = wq + (n * blocks_per_row + b) * ORACLE_Q4_0_BLOCK_BYTES;
+    return (double)(block_nibble(block, j) - 8) * block_scale(block);
+}
+
+void oracle_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t* block = wq + b * ORACLE_Q4_0_BLOCK_BYTES;
+        double d = block_scale(block);
+        for (int j = 0; j < ORACLE_Q4_0_BLOCK_ELEMS; ++j) {
+            double x = (double)(block_nibble(block, j) - 8) * d;
+            out[b * ORACLE_Q4_0_BLOCK_ELEMS + j] = (float)x;
+        }
+    }
+}
+
+static int sizes_ok(int64_t M, int64_t N, int64_t K)
+{
+    return M >= 0 && N >= 0 && K >= 0 && (K % ORACLE_Q4_0_BLOCK_ELEMS) == 0;
+}
+
+/* One output entry: the fp64 sum over ascending k and its absolute sum. */
+static void entry(const float* A, const uint8_t* wq, int64_t K, int64_t m,
+                  int64_t n, double* c_out, double* s_out)
+{
+    double c = 0.0;
+    double s = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+        double product = (double)A[m * K + k] * weight_at(wq, K, n, k);
+        c += product;
+        s += fabs(product);
+    }
+    *c_out = c;
+    if (s_out) *s_out = s;
+}
+
+int oracle_matmul_q4_0(const float* A, const uint8_t* wq, int64_t M, int64_t N,
+                       int64_t K, double* C, double* S)
+{
+    if (!sizes_ok(M, N, K)) return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            entry(A, wq, K, m, n, &C[m * N + n], S ? &S[m * N + n] : NULL);
+        }
+    }
+    return 0;
+}
+
+int oracle_matmul_q4_0_entries(const float* A, const uint8_t* wq, int64_t M,
+                               int64_t N, int64_t K, const int64_t* m_idx,
+                               const int64_t* n_idx, int64_t count, double* C,
+                               double* S)
+{
+    if (!sizes_ok(M, N, K) || count < 0) return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        if (m_idx[i] < 0 || m_idx[i] >= M || n_idx[i] < 0 || n_idx[i] >= N) return -1;
+    }
+    for (int64_t i = 0; i < count; ++i) {
+        entry(A, wq, K, m_idx[i], n_idx[i], &C[i], S ? &S[i] : NULL);
+    }
+    return 0;
+}

@@ -1,0 +1,219 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each ``pin_*`` takes a loaded oracle and raises ``AssertionError`` if the
+oracle disagrees with a fact that the kernel-contract page ("fuel-vulkan-kernels
+— quantized (GGML) kernel contracts", sections ``dequant_q4_0``,
+``qmatvec_q4_0``, ``matmul_q4_0_tiled``) or plain mathematics fixes:
+
+* an independent binary16 decoder (numpy's), exhaustively;
+* hand-built blocks and a hand-computed product (``tests/golden/``);
+* closed forms (all-8 nibbles, zero scale, one-hot and all-ones activations);
+* agreement with an independent dense fp64 product (numpy) on dequantized
+  weights, row-independence (M=1 against a row of M=8) and invariance under a
+  joint permutation of K-blocks.
+
+The same functions run against copies of the oracle with a planted mistake
+(``test_oracle_mutants.py``); every such copy must fail at least one pin.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _same_bits_or_nan(got, want) -> bool:
+    """Bit equality of float32 arrays, except that NaN matches any NaN."""
+    got = np.asarray(got, dtype=np.float32)
+    want = np.asarray(want, dtype=np.float32)
+    if got.shape != want.shape:
+        return False
+    nan_w = np.isnan(want)
+    if not np.array_equal(np.isnan(got), nan_w):
+        return False
+    return np.array_equal(got.view(np.uint32)[~nan_w], want.view(np.uint32)[~nan_w])
+
+
+def load_golden_blocks():
+    blocks, values = [], []
+    with open(os.path.join(GOLDEN, "q4_0_hand_blocks.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "block":
+                blocks.append(bytes(int(x, 16) for x in parts[1:]))
+                assert len(blocks[-1]) == 18
+            elif parts[0] == "values":
+                values.append(np.array([float(x) for x in parts[1:]], dtype=np.float32))
+                assert values[-1].size == 32
+    assert len(blocks) == len(values) and blocks
+    return blocks, values
+
+
+def load_golden_matmul():
+    rec = {"wrow": [], "arow": []}
+    with open(os.path.join(GOLDEN, "q4_0_hand_matmul.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            key, rest = parts[0], parts[1:]
+            if key in ("M", "N", "K"):
+                rec[key] = int(rest[0])
+            elif key == "wrow":
+                rec["wrow"].append(bytes(int(x, 16) for x in rest))
+            elif key == "arow":
+                rec["arow"].append([float(x) for x in rest])
+            elif key in ("C", "S"):
+                rec[key] = np.array([float(x) for x in rest]).reshape(rec["M"], rec["N"])
+    blob = np.frombuffer(b"".join(rec["wrow"]), dtype=np.uint8)
+    A = np.array(rec["arow"], dtype=np.float32)
+    return rec["M"], rec["N"], rec["K"], A, blob, rec["C"], rec["S"]
+
+
+# ---------------------------------------------------------------- binary16
+
+def pin_f16_exhaustive(o):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = o.f16_to_double(bits)
+    want = bits.view(np.float16).astype(np.float64)
+    nan_w = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan_w), "NaN class differs"
+    assert np.array_equal(got[~nan_w], want[~nan_w]), "binary16 values differ"
+    assert np.array_equal(np.signbit(got[~nan_w]), np.signbit(want[~nan_w])), "zero sign differs"
+
+
+# ---------------------------------------------------------------- dequant
+
+def pin_golden_blocks(o):
+    blocks, values = load_golden_blocks()
+    got = o.dequant_q4_0(np.frombuffer(b"".join(blocks), dtype=np.uint8))
+    want = np.concatenate(values)
+    for i in range(len(blocks)):
+        sl = slice(32 * i, 32 * i + 32)
+        assert _same_bits_or_nan(got[sl], want[sl]), f"hand-built block {i} differs"
+
+
+def pin_all8_and_zero_scale(o):
+    g = synth.rng(11, (0,))
+    nb = 64
+    d = (g.standard_normal(nb) * 0.05).astype(np.float16)
+    blob = synth.assemble_blocks(d, np.full((nb, 16), 0x88, dtype=np.uint8))
+    out = o.dequant_q4_0(blob).reshape(nb, 32)
+    assert np.all(out == 0), "all-8 nibbles must give zeros"
+    want_sign = np.signbit(d.astype(np.float32))[:, None].repeat(32, axis=1)
+    assert np.array_equal(np.signbit(out), want_sign), "zero sign must follow d"
+    qb = synth.rng(11, (1,)).integers(0, 256, size=(nb, 16), dtype=np.uint8)
+    zero = o.dequant_q4_0(synth.assemble_blocks(np.zeros(nb, np.float16), qb))
+    assert np.all(zero == 0), "d = 0 must give zeros"
+    A = synth.activations(3, 64, 12)
+    C, S = o.matmul_q4_0(A, blob[: 2 * 2 * 18], 2, 64)
+    assert np.all(C == 0) and np.all(S == 0), "all-8 weights must give C = 0"
+
+
+def pin_extreme_nibbles(o):
+    # q = 0 gives -8d and q = 15 gives 7d, for a d with all 11 significand bits.
+    d = np.array([np.float16(0.0999755859375)], dtype=np.float16)  # 0x2E66
+    for byte, lo, hi in ((0x00, -8.0, -8.0), (0xFF, 7.0, 7.0), (0xF0, -8.0, 7.0)):
+        out = o.dequant_q4_0(synth.assemble_blocks(d, np.full((1, 16), byte, np.uint8)))
+        dd = float(d[0])
+        assert np.array_equal(out[:16], np.full(16, lo * dd, np.float32))
+        assert np.array_equal(out[16:], np.full(16, hi * dd, np.float32))
+
+
+# ---------------------------------------------------------------- matmul
+
+def pin_golden_matmul(o):
+    M, N, K, A, blob, C_want, S_want = load_golden_matmul()
+    C, S = o.matmul_q4_0(A, blob, N, K)
+    assert np.array_equal(C, C_want), f"hand product differs: {C} vs {C_want}"
+    assert np.array_equal(S, S_want), f"hand |product| sum differs: {S} vs {S_want}"
+
+
+def pin_one_hot(o):
+    # A = rows of the identity picks single weights: C[m][n] = W[n][k_m].
+    N, K = 5, 96
+    blob = synth.q4_0_weights(N, K, 21)
+    W = o.dequant_q4_0(blob).reshape(N, K).astype(np.float64)
+    ks = np.array([0, 15, 16, 31, 32, 63, 64, 95])
+    A = np.zeros((ks.size, K), np.float32)
+    A[np.arange(ks.size), ks] = 1.0
+    C, S = o.matmul_q4_0(A, blob, N, K)
+    assert np.array_equal(C, W[:, ks].T), "one-hot rows must select W[n][k]"
+    assert np.array_equal(S, np.abs(W[:, ks].T))
+
+
+def pin_ones_closed_form(o):
+    # A = 1: C[n] = sum_b d_b * (sum of the block's 32 nibbles - 256), and the
+    # nibble sum of a byte is (byte & 15) + (byte >> 4) whatever the order.
+    N, K = 7, 160
+    blob = synth.q4_0_weights(N, K, 22)
+    blocks = blob.reshape(N, K // 32, 18)
+    d = blocks[:, :, 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    qb = blocks[:, :, 2:].astype(np.int64)
+    nib_sum = (qb & 15).sum(-1) + (qb >> 4).sum(-1) - 256
+    want = (d * nib_sum).sum(-1)
+    C, _ = o.matmul_q4_0(np.ones((1, K), np.float32), blob, N, K)
+    assert np.allclose(C[0], want, rtol=1e-13, atol=0), "all-ones closed form differs"
+
+
+def pin_dense_equivalence(o):
+    # Fused product == dense fp64 product of A and the dequantized W (numpy).
+    for (M, N, K, seed) in ((3, 4, 64, 23), (9, 7, 96, 24), (1, 33, 32, 25)):
+        blob = synth.q4_0_weights(N, K, seed)
+        A = synth.activations(M, K, seed, dist="outliers")
+        W = o.dequant_q4_0(blob).reshape(N, K).astype(np.float64)
+        dense = A.astype(np.float64) @ W.T
+        dense_abs = np.abs(A.astype(np.float64)) @ np.abs(W).T
+        C, S = o.matmul_q4_0(A, blob, N, K)
+        assert np.allclose(C, dense, rtol=0, atol=1e-12 * dense_abs.max() + 1e-300)
+        assert np.allclose(S, dense_abs, rtol=1e-13, atol=0)
+
+
+def pin_rows_independent(o):
+    # Row r of an M=8 product equals the M=1 product of A's row r alone.
+    N, K = 6, 128
+    blob = synth.q4_0_weights(N, K, 26)
+    A = synth.activations(8, K, 26)
+    C8, S8 = o.matmul_q4_0(A, blob, N, K)
+    for r in (0, 3, 7):
+        C1, S1 = o.matmul_q4_0(A[r:r + 1], blob, N, K)
+        assert np.array_equal(C1[0], C8[r]) and np.array_equal(S1[0], S8[r])
+
+
+def pin_block_permutation(o):
+    # Permuting whole K-blocks of A and W together leaves C unchanged.
+    N, K = 4, 256
+    nbk = K // 32
+    blob = synth.q4_0_weights(N, K, 27)
+    A = synth.activations(2, K, 27)
+    perm = synth.rng(27, (9,)).permutation(nbk)
+    blob_p = blob.reshape(N, nbk, 18)[:, perm, :].ravel()
+    A_p = A.reshape(2, nbk, 32)[:, perm, :].reshape(2, K)
+    C, S = o.matmul_q4_0(A, blob, N, K)
+    Cp, Sp = o.matmul_q4_0(A_p, blob_p, N, K)
+    assert np.allclose(C, Cp, rtol=0, atol=1e-12 * S.max())
+    assert np.allclose(S, Sp, rtol=1e-13, atol=0)
+
+
+def pin_entries_match_full(o):
+    # The sampled-entry routine agrees exactly with the full product.
+    N, K, M = 9, 64, 5
+    blob = synth.q4_0_weights(N, K, 28)
+    A = synth.activations(M, K, 28)
+    C, S = o.matmul_q4_0(A, blob, N, K)
+    mi = np.array([0, 4, 2, 4, 1])
+    ni = np.array([8, 0, 3, 8, 5])
+    Ce, Se = o.matmul_q4_0_entries(A, blob, N, K, mi, ni)
+    assert np.array_equal(Ce, C[mi, ni]) and np.array_equal(Se, S[mi, ni])
+
+
+ALL_PINS = (pin_f16_exhaustive, pin_golden_blocks, pin_all8_and_zero_scale,
+            pin_extreme_nibbles, pin_golden_matmul, pin_one_hot,
+            pin_ones_closed_form, pin_dense_equivalence, pin_rows_independent,
+            pin_block_permutation, pin_entries_match_full)
