@@ -1,0 +1,203 @@
+"""GGML Q4_0 x f32 quantized matmul and Q4_0 dequant on GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libqm.so`` (``include/qm.h``): it
+only marshals arguments.  Every step of the computation runs in the library's
+CUDA kernels; there is no host fallback, and calls fail loudly when the
+library has not been built.  PyTorch supplies device memory and streams.
+
+Entry points (same names as the C ABI):
+
+* ``qm_dequant_q4_0(wq, out=None, stream=None)`` -> f32 tensor ``[n_blocks*32]``
+* ``qm_matmul_q4_0(A, wq, N, out=None, stream=None)`` -> f32 tensor ``[M, N]``
+* ``qm_matmul_q4_0_algo(A, wq, N, algo, out=None, stream=None)``
+* ``qm_device_status(stream=None, clear=True)``, ``qm_status_string(code)``,
+  ``qm_version()``
+
+The ``*_ptr`` variants take raw device addresses (ints) instead of tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "QMError", "load_library", "library_path", "qm_version", "qm_status_string",
+    "qm_dequant_q4_0", "qm_matmul_q4_0", "qm_matmul_q4_0_algo", "qm_device_status",
+    "qm_launch_count",
+    "qm_dequant_q4_0_ptr", "qm_matmul_q4_0_ptr", "qm_matmul_q4_0_algo_ptr",
+    "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
+    "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER",
+    "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "EXPORTED_SYMBOLS",
+]
+
+QM_OK = 0
+QM_ERR_NULL = -1
+QM_ERR_SHAPE = -2
+QM_ERR_ALIGN = -3
+QM_ERR_ALIAS = -4
+QM_ERR_CUDA = -5
+QM_ERR_TIMEOUT = -6
+QM_ERR_UNSUPPORTED = -7
+QM_ERR_POINTER = -8
+
+QM_ALGO_AUTO = 0
+QM_ALGO_GEMV = 1
+QM_ALGO_GEMM_SIMT = 2
+
+BLOCK_BYTES = 18
+BLOCK_ELEMS = 32
+
+# Every symbol include/qm.h declares.
+EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
+                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class QMError(RuntimeError):
+    """A negative status returned by libqm."""
+
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {qm_status_string(code)} (status {code})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libqm.so (built by ``bit_block_quantized_qm_gb300.build.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"libqm.so is not built ({_LIB_PATH}); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            lib = ctypes.CDLL(_LIB_PATH)
+            i64, p, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            lib.qm_version.argtypes = []
+            lib.qm_version.restype = i32
+            lib.qm_status_string.argtypes = [i32]
+            lib.qm_status_string.restype = ctypes.c_char_p
+            lib.qm_dequant_q4_0.argtypes = [p, i64, p, p]
+            lib.qm_dequant_q4_0.restype = i32
+            lib.qm_matmul_q4_0.argtypes = [p, p, p, i64, i64, i64, p]
+            lib.qm_matmul_q4_0.restype = i32
+            lib.qm_matmul_q4_0_algo.argtypes = [p, p, p, i64, i64, i64, i32, p]
+            lib.qm_matmul_q4_0_algo.restype = i32
+            lib.qm_device_status.argtypes = [p, i32]
+            lib.qm_device_status.restype = i32
+            lib.qm_launch_count.argtypes = []
+            lib.qm_launch_count.restype = ctypes.c_uint64
+            _lib = lib
+    return _lib
+
+
+def qm_version() -> int:
+    return load_library().qm_version()
+
+
+def qm_status_string(code: int) -> str:
+    return load_library().qm_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str) -> int:
+    if code != QM_OK:
+        raise QMError(code, where)
+    return code
+
+
+# ------------------------------------------------------------ raw pointers
+
+def qm_dequant_q4_0_ptr(wq: int, n_blocks: int, out: int, stream: int = 0) -> int:
+    return load_library().qm_dequant_q4_0(wq, n_blocks, out, stream)
+
+
+def qm_matmul_q4_0_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, stream: int = 0) -> int:
+    return load_library().qm_matmul_q4_0(A, wq, C, M, N, K, stream)
+
+
+def qm_matmul_q4_0_algo_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, algo: int,
+                            stream: int = 0) -> int:
+    return load_library().qm_matmul_q4_0_algo(A, wq, C, M, N, K, algo, stream)
+
+
+# ------------------------------------------------------------ torch tensors
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _require(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def qm_dequant_q4_0(wq, out=None, stream=None):
+    """Dequantize a Q4_0 block stream (uint8 CUDA tensor, n_blocks*18 bytes)
+    into f32 ``[n_blocks*32]``."""
+    import torch
+    _require(wq, torch.uint8, "wq")
+    if wq.numel() % BLOCK_BYTES:
+        raise ValueError("wq length is not a multiple of 18 bytes")
+    n_blocks = wq.numel() // BLOCK_BYTES
+    if out is None:
+        out = torch.empty(n_blocks * BLOCK_ELEMS, dtype=torch.float32, device=wq.device)
+    _require(out, torch.float32, "out")
+    if out.numel() != n_blocks * BLOCK_ELEMS:
+        raise ValueError("out has the wrong number of elements")
+    _check(qm_dequant_q4_0_ptr(wq.data_ptr(), n_blocks, out.data_ptr(), _stream_handle(stream)),
+           "qm_dequant_q4_0")
+    return out
+
+
+def qm_matmul_q4_0_algo(A, wq, N: int, algo: int, out=None, stream=None):
+    """C[M, N] = A[M, K] x dequant(W)^T with the algorithm forced."""
+    import torch
+    _require(A, torch.float32, "A")
+    _require(wq, torch.uint8, "wq")
+    if A.dim() != 2:
+        raise ValueError("A must be 2-D [M, K]")
+    M, K = A.shape
+    if K % BLOCK_ELEMS or wq.numel() != N * (K // BLOCK_ELEMS) * BLOCK_BYTES:
+        raise ValueError("wq size does not match N x K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _require(out, torch.float32, "out")
+    if out.numel() != M * N:
+        raise ValueError("out has the wrong number of elements")
+    _check(qm_matmul_q4_0_algo_ptr(A.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K, algo,
+                                   _stream_handle(stream)), "qm_matmul_q4_0")
+    return out
+
+
+def qm_matmul_q4_0(A, wq, N: int, out=None, stream=None):
+    """C[M, N] = A[M, K] x dequant(W)^T; GEMV kernels for M <= 8, GEMM above."""
+    return qm_matmul_q4_0_algo(A, wq, N, QM_ALGO_AUTO, out=out, stream=stream)
+
+
+def qm_launch_count() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(load_library().qm_launch_count())
+
+
+def qm_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronize the stream and return the device error status (QM_OK or
+    QM_ERR_TIMEOUT); see include/qm.h."""
+    return load_library().qm_device_status(_stream_handle(stream), 1 if clear else 0)

@@ -1,0 +1,220 @@
+// The C ABI of libqm (declared in include/qm.h): argument checks, algorithm
+// choice and launches on the caller's stream.  No allocation, no
+// synchronization (except qm_device_status), no host fallback.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/qm.h"
+#include "qm_internal.h"
+
+namespace qm {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+int g_dev_ready[kMaxDevices] = {0};
+std::mutex g_dev_mutex;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+uint64_t g_launches = 0;
+std::once_flag g_encode_once;
+
+}  // namespace
+
+void note_launch() { __atomic_fetch_add(&g_launches, 1, __ATOMIC_RELAXED); }
+
+uint64_t launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+cudaError_t current_device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (__atomic_load_n(&g_dev_ready[dev], __ATOMIC_ACQUIRE)) {
+        *out = g_dev[dev];
+        return cudaSuccess;
+    }
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo info;
+        info.device = dev;
+        err = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceGetAttribute(&info.max_smem_optin,
+                                     cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (err != cudaSuccess) return err;
+        g_dev[dev] = info;
+        __atomic_store_n(&g_dev_ready[dev], 1, __ATOMIC_RELEASE);
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+// 2-D tensor map over a weight stream viewed as a byte matrix [rows][row_bytes]
+// (row stride row_bytes, a multiple of 16), with a box of box_rows x box_bytes
+// and zero fill outside the matrix.
+cudaError_t encode_weight_map_2d(CUtensorMap* map, const void* base, int64_t row_bytes,
+                                 int64_t rows, int box_bytes, int box_rows) {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess) {
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    });
+    if (!g_encode_tiled) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                                strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace qm
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > INT64_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    if (a_bytes <= 0 || b_bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+// The pointer must be device-accessible memory of `device`: device or managed
+// memory, or host memory registered/mapped with a device address.
+int check_pointer(const void* p, int device) {
+    cudaPointerAttributes attr;
+    cudaError_t err = cudaPointerGetAttributes(&attr, p);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return QM_ERR_POINTER;
+    }
+    switch (attr.type) {
+        case cudaMemoryTypeDevice:
+            return attr.device == device ? QM_OK : QM_ERR_POINTER;
+        case cudaMemoryTypeManaged:
+            return QM_OK;
+        case cudaMemoryTypeHost:
+            return attr.devicePointer == p ? QM_OK : QM_ERR_POINTER;
+        default:
+            return QM_ERR_POINTER;
+    }
+}
+
+int from_cuda(cudaError_t err) { return err == cudaSuccess ? QM_OK : QM_ERR_CUDA; }
+
+int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
+                int algo, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QM_ERR_SHAPE;
+    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMM_SIMT) return QM_ERR_SHAPE;
+    int64_t a_elems, c_elems, w_elems, a_bytes, c_bytes, w_bytes;
+    if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, &a_bytes) || !mul_ok(M, N, &c_elems) ||
+        !mul_ok(c_elems, 4, &c_bytes) || !mul_ok(N, K / 32, &w_elems) ||
+        !mul_ok(w_elems, 18, &w_bytes))
+        return QM_ERR_SHAPE;
+    if (algo == QM_ALGO_GEMV && M > 8) return QM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return QM_OK;
+    if (!C) return QM_ERR_NULL;
+    if (K > 0 && (!A || !wq)) return QM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(C) & 3u) != 0) return QM_ERR_ALIGN;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3u) != 0 ||
+                  (reinterpret_cast<uintptr_t>(wq) & 1u) != 0))
+        return QM_ERR_ALIGN;
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, wq, w_bytes)) return QM_ERR_ALIAS;
+    if (M > 0x7FFFFFFF || N > 0x7FFFFFFF) return QM_ERR_SHAPE;
+
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    int rc = check_pointer(C, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(A, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(wq, dev.device);
+    if (rc != QM_OK) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(c_bytes), s));
+    const uint8_t* w = static_cast<const uint8_t*>(wq);
+    if (algo == QM_ALGO_AUTO) algo = (M <= 8) ? QM_ALGO_GEMV : QM_ALGO_GEMM_SIMT;
+    if (algo == QM_ALGO_GEMV)
+        return from_cuda(qm::launch_gemv_q4_0(A, w, C, static_cast<int>(M), N, K, s, dev));
+    return from_cuda(qm::launch_gemm_q4_0_simt(A, w, C, M, N, K, s, dev));
+}
+
+}  // namespace
+
+extern "C" {
+
+int qm_version(void) { return kVersion; }
+
+const char* qm_status_string(int status) {
+    switch (status) {
+        case QM_OK: return "ok";
+        case QM_ERR_NULL: return "a required pointer is NULL";
+        case QM_ERR_SHAPE: return "invalid size (negative, K not a multiple of 32, or overflow)";
+        case QM_ERR_ALIGN: return "misaligned pointer (wq needs 2 bytes, A/C/out 4 bytes)";
+        case QM_ERR_ALIAS: return "an output overlaps an input";
+        case QM_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case QM_ERR_TIMEOUT: return "a kernel gave up waiting for an asynchronous copy";
+        case QM_ERR_UNSUPPORTED: return "the forced algorithm cannot run this shape";
+        case QM_ERR_POINTER: return "a pointer is not device memory of the current device";
+        default: return "unknown status";
+    }
+}
+
+int qm_dequant_q4_0(const void* wq, int64_t n_blocks, float* out, void* stream) {
+    if (n_blocks < 0) return QM_ERR_SHAPE;
+    int64_t in_bytes, out_bytes;
+    if (!mul_ok(n_blocks, 18, &in_bytes) || !mul_ok(n_blocks, 128, &out_bytes)) return QM_ERR_SHAPE;
+    if (n_blocks == 0) return QM_OK;
+    if (!wq || !out) return QM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(wq) & 1u) != 0 || (reinterpret_cast<uintptr_t>(out) & 3u) != 0)
+        return QM_ERR_ALIGN;
+    if (overlaps(out, out_bytes, wq, in_bytes)) return QM_ERR_ALIAS;
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    int rc = check_pointer(wq, dev.device);
+    if (rc == QM_OK) rc = check_pointer(out, dev.device);
+    if (rc != QM_OK) return rc;
+    return from_cuda(qm::launch_dequant_q4_0(static_cast<const uint8_t*>(wq), n_blocks, out,
+                                             static_cast<cudaStream_t>(stream), dev));
+}
+
+int qm_matmul_q4_0(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
+                   void* stream) {
+    return matmul_impl(A, wq, C, M, N, K, QM_ALGO_AUTO, stream);
+}
+
+int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
+                        int algo, void* stream) {
+    return matmul_impl(A, wq, C, M, N, K, algo, stream);
+}
+
+uint64_t qm_launch_count(void) { return qm::launch_count(); }
+
+int qm_device_status(void* stream, int clear) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QM_ERR_CUDA;
+    unsigned int bits = 0;
+    if (qm::gemv_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
+    return bits ? QM_ERR_TIMEOUT : QM_OK;
+}
+
+}  // extern "C"

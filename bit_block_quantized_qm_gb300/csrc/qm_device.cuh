@@ -1,0 +1,116 @@
+// Device-side helpers shared by the libqm kernels (sm_103a): Q4_0 block
+// decoding primitives, mbarrier and TMA wrappers with bounded waits.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace qm {
+
+constexpr int kBlockBytes = 18;  // Q4_0 block: f16 d + 16 quant bytes
+constexpr int kBlockElems = 32;
+
+// Bits of the float 2^23: OR-ing a value v < 2^23 into its mantissa gives the
+// float 2^23 + v exactly; subtracting 2^23 + 8 then leaves (v - 8) exactly.
+constexpr uint32_t kMagicBits = 0x4B000000u;
+constexpr float kMagicPlus8 = 8388616.0f;  // 2^23 + 8
+
+// Device error bits (one word per translation unit that waits on copies).
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+// Polls of an mbarrier before a wait gives up.  try_wait blocks for a
+// hardware-defined slice per poll, so this bounds a wait to well under a
+// second while never firing on a healthy copy.
+constexpr uint32_t kMaxWaitPolls = 1u << 22;
+
+// The f16 scale d -> f32 (exact).
+__device__ __forceinline__ float f16_bits_to_float(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16)));
+}
+
+// (nibble - 8) as f32, exactly, for a value v in 0..15 already placed in the
+// low bits of a word whose other bits match kMagicBits.
+__device__ __forceinline__ float magic_minus8(uint32_t word_with_magic) {
+    return __uint_as_float(word_with_magic) - kMagicPlus8;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false (and sets bit
+// kErrWaitTimeout in *err) if the phase did not complete within the limit.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned int* err) {
+    for (uint32_t i = 0; i < kMaxWaitPolls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+    }
+    atomicOr(err, kErrWaitTimeout);
+    return false;
+}
+
+// 2-D TMA tile load (global -> this CTA's shared memory), completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 16-byte streaming store (output written once, not re-read by this kernel).
+__device__ __forceinline__ void st_global_cs_v4(float* p, float a, float b, float c, float d) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// 16-byte read-only load through the non-coherent path.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+}  // namespace qm

@@ -1,0 +1,134 @@
+/*
+ * qm.h — C ABI of libqm: the GGML Q4_0 x f32 quantized matmul and the Q4_0
+ * dequant, as hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Operations (defined in "fuel-vulkan-kernels — quantized (GGML) kernel
+ * contracts", fuel-dispatch 0.20.71, kernel-contracts/vulkan/quantized.fkc.md):
+ *
+ *   Q4_0 block: 18 bytes for 32 elements.  Bytes 0-1: the scale d, IEEE
+ *   binary16, little-endian.  Bytes 2-17: 16 quant bytes; element j (0..15) is
+ *   the low nibble of quant byte j and element j+16 its high nibble.  Element
+ *   value = (nibble - 8) * d, nibble unsigned 0..15   (section "dequant_q4_0").
+ *
+ *   Matmul: C[m][n] = sum over k of A[m][k] * W[n][k], A f32 row-major [M][K],
+ *   W a row-major [N][K/32] stream of Q4_0 blocks (row n holds blocks
+ *   n*K/32 .. n*K/32 + K/32 - 1), C f32 row-major [M][N], K a multiple of 32
+ *   (sections "qmatvec_q4_0" and "matmul_q4_0_tiled").  M = 1..8 runs the
+ *   decode-regime GEMV kernels, M >= 9 the prefill GEMM.  The sum is taken in
+ *   f32 in an order of the kernel's choosing; results agree with the exact
+ *   sum to |error| <= 1e-5 * sum_k |A[m][k] * W[n][k]| + 1e-7 per element.
+ *   The same call on the same inputs gives bitwise the same C (no atomics).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device memory owned by the caller (cudaMalloc'd, managed,
+ *     or mapped host memory with a device address).  The library allocates
+ *     and frees nothing and never synchronizes: work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*; NULL means the legacy default stream)
+ *     on the current device, and results are visible once that stream has
+ *     been synchronized.  Calls are thread-safe.
+ *   - Operands are contiguous; no strides, offsets or broadcasts.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     failed check returns a negative status and leaves memory untouched.
+ *   - An output never aliases an input: overlapping byte ranges are rejected.
+ */
+#ifndef QM_H
+#define QM_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QM_API __attribute__((visibility("default")))
+#else
+#define QM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define QM_OK 0
+#define QM_ERR_NULL (-1)        /* a required pointer is NULL                    */
+#define QM_ERR_SHAPE (-2)       /* negative size, K % 32 != 0, or a size whose
+                                   byte count does not fit in int64              */
+#define QM_ERR_ALIGN (-3)       /* wq not 2-byte aligned, or A/C/out not 4-byte  */
+#define QM_ERR_ALIAS (-4)       /* an output overlaps an input                   */
+#define QM_ERR_CUDA (-5)        /* a CUDA call or kernel launch failed           */
+#define QM_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait (see
+                                   qm_device_status)                             */
+#define QM_ERR_UNSUPPORTED (-7) /* the forced algorithm cannot run this shape    */
+#define QM_ERR_POINTER (-8)     /* a pointer is not device memory of the current
+                                   device                                        */
+
+/* Algorithms for qm_matmul_q4_0_algo. */
+#define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks                          */
+#define QM_ALGO_GEMV 1      /* decode-regime GEMV; M must be 1..8                 */
+#define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+QM_API int qm_version(void);
+
+/* A static, human-readable string for a status code. */
+QM_API const char* qm_status_string(int status);
+
+/*
+ * qm_dequant_q4_0 — section "dequant_q4_0": out[32*b + j] = (q_j(b) - 8) * d(b)
+ * for every block b < n_blocks and j < 32.
+ *   wq       : n_blocks * 18 bytes of Q4_0 blocks, 2-byte aligned (16-byte
+ *              aligned takes the fast path).
+ *   n_blocks : number of blocks, >= 0.  0 enqueues nothing.
+ *   out      : n_blocks * 32 floats, 4-byte aligned (16-byte aligned takes the
+ *              fast path); must not overlap wq.
+ * Exact: the product of an integer in [-8, 7] and a binary16 scale is
+ * representable in f32, so the result is bit-identical to the definition,
+ * including the sign of zero (q = 8 with d < 0 gives -0.0), infinities
+ * (q != 8 with d = +-inf) and NaN (q = 8 with d infinite, or d NaN).
+ * Returns QM_OK or a negative status.
+ */
+QM_API int qm_dequant_q4_0(const void* wq, int64_t n_blocks, float* out, void* stream);
+
+/*
+ * qm_matmul_q4_0 — C = A x dequant(W)^T (see the header comment).
+ *   A  : M*K floats, row-major [M][K], 4-byte aligned.
+ *   wq : N*(K/32) Q4_0 blocks = N*K*9/16 bytes, row-major [N][K/32], 2-byte
+ *        aligned.  Rows are 16-byte aligned, and the fastest GEMV path is
+ *        taken, when wq is 16-byte aligned and K % 256 == 0.
+ *   C  : M*N floats, row-major [M][N], 4-byte aligned; must overlap neither A
+ *        nor wq.  Every element of C is written.
+ *   M, N, K : M, N >= 0; K >= 0 with K % 32 == 0.
+ * M == 0 or N == 0 enqueues nothing.  K == 0 sets C to +0.0 (the empty sum).
+ * Returns QM_OK or a negative status.
+ */
+QM_API int qm_matmul_q4_0(const float* A, const void* wq, float* C, int64_t M,
+                   int64_t N, int64_t K, void* stream);
+
+/*
+ * qm_matmul_q4_0_algo — qm_matmul_q4_0 with the algorithm forced (QM_ALGO_*),
+ * for tests and benchmarks.  Returns QM_ERR_UNSUPPORTED when the algorithm
+ * cannot run the shape (QM_ALGO_GEMV with M > 8), QM_ERR_SHAPE for an unknown
+ * algorithm number.
+ */
+QM_API int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t M,
+                        int64_t N, int64_t K, int algo, void* stream);
+
+/*
+ * qm_device_status — synchronizes `stream` and reads the library's device
+ * error word for the current device.  Kernels that wait on asynchronous
+ * copies give up after a bounded number of polls, set this word and return
+ * early (their output is then incomplete).  Returns QM_OK if the word is
+ * clear, QM_ERR_TIMEOUT if a wait gave up, QM_ERR_CUDA if the synchronize or
+ * the read failed.  With clear != 0 the word is reset after reading.
+ */
+QM_API int qm_device_status(void* stream, int clear);
+
+/*
+ * qm_launch_count — the number of kernels this library has enqueued in this
+ * process (all devices, all threads), for accounting in benchmarks.
+ */
+QM_API uint64_t qm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QM_H */

@@ -1,0 +1,108 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol
+include/qm.h declares, and argument errors are caught on the host before any
+CUDA call (so they are testable here)."""
+import os
+import re
+
+import pytest
+
+import bit_block_quantized_qm_gb300 as qm
+from bit_block_quantized_qm_gb300 import build as qm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qm_build.build()
+    return qm.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "qm.h")).read()
+    return set(re.findall(r"QM_API\s+[\w\s\*]+?\b(qm_\w+)\s*\(", text))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert names == set(qm.EXPORTED_SYMBOLS)
+    for name in names:
+        assert getattr(lib, name) is not None
+
+
+def test_only_declared_symbols_are_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", qm.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T qm_" in line}
+    assert exported == declared_symbols()
+
+
+def test_version_and_status_strings(lib):
+    assert qm.qm_version() >= 100
+    for code in range(-8, 1):
+        assert qm.qm_status_string(code) != "unknown status"
+    assert qm.qm_status_string(-99) == "unknown status"
+
+
+# Fake, well-aligned addresses: every check below fails before the library
+# asks CUDA anything, so no address is ever dereferenced.
+A_ADDR, W_ADDR, C_ADDR = 0x10000000, 0x20000000, 0x30000000
+
+
+def test_shape_errors(lib):
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR, -1, 4, 32) == qm.QM_ERR_SHAPE
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR, 1, -4, 32) == qm.QM_ERR_SHAPE
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR, 1, 4, -32) == qm.QM_ERR_SHAPE
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR, 1, 4, 33) == qm.QM_ERR_SHAPE
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR, 1 << 40, 1 << 40, 32) == qm.QM_ERR_SHAPE
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR, -1, C_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR, 1 << 62, C_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_matmul_q4_0_algo_ptr(A_ADDR, W_ADDR, C_ADDR, 1, 4, 32, 99) == qm.QM_ERR_SHAPE
+
+
+def test_empty_shapes_enqueue_nothing(lib):
+    assert qm.qm_matmul_q4_0_ptr(0, 0, 0, 0, 4, 32) == qm.QM_OK
+    assert qm.qm_matmul_q4_0_ptr(0, 0, 0, 4, 0, 32) == qm.QM_OK
+    assert qm.qm_dequant_q4_0_ptr(0, 0, 0) == qm.QM_OK
+
+
+def test_null_pointers(lib):
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, 0, 1, 4, 32) == qm.QM_ERR_NULL
+    assert qm.qm_matmul_q4_0_ptr(0, W_ADDR, C_ADDR, 1, 4, 32) == qm.QM_ERR_NULL
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, 0, C_ADDR, 1, 4, 32) == qm.QM_ERR_NULL
+    assert qm.qm_dequant_q4_0_ptr(0, 3, C_ADDR) == qm.QM_ERR_NULL
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR, 3, 0) == qm.QM_ERR_NULL
+
+
+def test_alignment(lib):
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR + 1, C_ADDR, 1, 4, 32) == qm.QM_ERR_ALIGN
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR + 2, W_ADDR, C_ADDR, 1, 4, 32) == qm.QM_ERR_ALIGN
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, C_ADDR + 2, 1, 4, 32) == qm.QM_ERR_ALIGN
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR + 1, 3, C_ADDR) == qm.QM_ERR_ALIGN
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR, 3, C_ADDR + 1) == qm.QM_ERR_ALIGN
+
+
+def test_aliasing(lib):
+    # C (4 x 4 floats = 64 B) starting inside A (4 x 32 floats)
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, A_ADDR + 64, 4, 4, 32) == qm.QM_ERR_ALIAS
+    # C overlapping the tail of the weight stream (4 rows x 1 block = 72 B)
+    assert qm.qm_matmul_q4_0_ptr(A_ADDR, W_ADDR, W_ADDR + 68, 4, 4, 32) == qm.QM_ERR_ALIAS
+    assert qm.qm_dequant_q4_0_ptr(W_ADDR, 4, W_ADDR + 64) == qm.QM_ERR_ALIAS
+    # adjacent, not overlapping: passes the alias check (and fails later only
+    # for want of a device, or because the fake address is not device memory)
+    rc = qm.qm_dequant_q4_0_ptr(W_ADDR, 4, W_ADDR + 72)
+    assert rc in (qm.QM_ERR_CUDA, qm.QM_ERR_POINTER)
+
+
+def test_forced_algorithm_limits(lib):
+    assert qm.qm_matmul_q4_0_algo_ptr(A_ADDR, W_ADDR, C_ADDR, 9, 4, 32,
+                                      qm.QM_ALGO_GEMV) == qm.QM_ERR_UNSUPPORTED
+
+
+def test_python_wrappers_validate_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):
+        qm.qm_dequant_q4_0(torch.zeros(18, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        qm.qm_dequant_q4_0(torch.zeros(18, dtype=torch.uint8))  # not a CUDA tensor
