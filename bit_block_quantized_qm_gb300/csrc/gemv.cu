@@ -4,31 +4,34 @@
 // contracts"; element j < 16 of a block is the low nibble of quant byte j,
 // element j + 16 its high nibble, value (nibble - 8) * d).
 //
-// Fast kernel (K % 256 == 0, 16-byte aligned wq and A):
+// Persistent kernel (K % 256 == 0, 16-byte aligned wq and A):
 //   * A "unit" is 8 consecutive blocks of one weight row: 144 bytes = 9
-//     aligned 16-byte words covering 256 k.  A CTA owns 32 rows and a range of
-//     units; each unit's 32 x 144-byte tile is brought into shared memory by
-//     one 2-D TMA load, so HBM sees whole-line reads and the SM spends no load
-//     instructions on the weight stream.
-//   * Lane l of every warp owns row l.  It reads its row's unit with nine
-//     16-byte shared loads (a 144-byte row stride maps the 8 lanes of each
-//     quarter-warp to 8 distinct 4-bank groups: conflict-free) and decodes
-//     the 8 blocks with fixed byte permutes.  All lanes of a warp use the same
-//     activations, so A is read with broadcast 16-byte loads.
-//   * Decode: nibbles are masked in place, moved under the exponent of 2^23
-//     with one byte-permute each and turned into (q - 8) by one subtraction,
-//     all exact; 32 products are summed per block and scaled once by d.
-//   * K is split over the CTAs of a thread-block cluster when there are too
-//     few row groups to fill the GPU; partial sums are combined in a fixed
-//     order through distributed shared memory, so results are deterministic.
+//     aligned 16-byte words covering 256 k.  A "row group" is 32 rows.  The
+//     work is the grid of (row group, unit) tiles; the launch splits it into
+//     G row-group ranges x S unit ranges, one CTA (one per SM) for each,
+//     sized so every CTA gets nearly the same number of tiles.
+//   * In each CTA a producer warp streams the CTA's 32-row x 144-byte tiles
+//     into a ring of shared-memory stages with 2-D TMA loads (and the CTA's
+//     activation slice with 1-D bulk copies), so HBM latency overlaps the
+//     decode of earlier tiles.  Eight consumer warps take tiles in turn.
+//   * Lane l of a consumer warp owns row l of the tile.  It reads its row's
+//     unit with nine 16-byte shared loads (the 144-byte row stride sends the
+//     8 lanes of each quarter-warp to 8 distinct 4-bank groups) and decodes
+//     the 8 blocks with fixed byte permutes; the activations are broadcast
+//     16-byte shared loads.  Nibbles are masked in place, moved under the
+//     exponent of 2^23 with one byte permute and turned into (q - 8) by one
+//     subtraction, all exact; 32 products are summed per block and scaled
+//     once by d (element by element when d is not finite).
+//   * Partial sums of a row group meet in shared memory (fixed warp order).
+//     When K is split (S > 1) each CTA writes its row groups' partials to a
+//     workspace and the last of the S CTAs to arrive at a row group adds them
+//     in split order and writes C, so results do not depend on timing.
 // Generic kernel (any K % 32 == 0, 2-byte aligned wq, 4-byte aligned A): one
 // warp per row, lanes striding over blocks, shuffle reduction.
-#include <cooperative_groups.h>
+#include <algorithm>
 
 #include "qm_device.cuh"
 #include "qm_internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace qm {
 
@@ -38,53 +41,113 @@ namespace {
 
 constexpr int kUnitBytes = 144;  // 8 blocks
 constexpr int kUnitElems = 256;
-constexpr int kRowsPerCta = 32;  // one row per lane
-constexpr int kTileBytes = kUnitBytes * kRowsPerCta;
-constexpr int kMaxUnitsPerCta = 40;  // 184 KB of tiles
-constexpr int kMaxCluster = 8;
+constexpr int kRowsPerTile = 32;  // one row per lane
+constexpr int kTileBytes = kUnitBytes * kRowsPerTile;
+// Consumer warps per CTA: as many as the registers of one CTA per SM allow.
+template <int M>
+__host__ __device__ constexpr int consumer_warps() { return M <= 4 ? 16 : 8; }
+template <int M>
+__host__ __device__ constexpr int cta_threads() { return (consumer_warps<M>() + 1) * 32; }  // + producer warp
+constexpr int kMaxSplits = 16;  // at most 16 K ranges
+constexpr int kMaxRowGroupsPerCta = 16;
 
-template <bool kVecA>
+// Where block_dot reads activations from.
+enum class ASrc { kGlobalVec, kGlobalScalar, kShared };
+
+template <ASrc kSrc>
 __device__ __forceinline__ float4 load_a4(const float* p) {
-    if constexpr (kVecA) {
+    if constexpr (kSrc == ASrc::kGlobalVec) {
         return __ldg(reinterpret_cast<const float4*>(p));
+    } else if constexpr (kSrc == ASrc::kShared) {
+        return *reinterpret_cast<const float4*>(p);
     } else {
         return make_float4(__ldg(p), __ldg(p + 1), __ldg(p + 2), __ldg(p + 3));
     }
 }
 
-// t[m] = sum over the 32 elements of one block of A[m][k0 + j] * (q_j - 8).
-// q[w] holds quant bytes 4w..4w+3 (byte 4w in the low 8 bits).
-template <int M, bool kVecA>
-__device__ __forceinline__ void block_dot(const float* __restrict__ A, int64_t K, int64_t k0,
+// t[m] = sum over the 32 elements of one block of A[m][k0 + j] * (q_j - 8),
+// with row m of the activations at A + m * lda.  q[w] holds quant bytes
+// 4w..4w+3 (byte 4w in the low 8 bits).
+template <int M, ASrc kSrc>
+__device__ __forceinline__ void block_dot(const float* __restrict__ A, int64_t lda, int64_t k0,
                                           const uint32_t q[4], float t[M]) {
+    // Independent FMA chains per activation row (more when M is small) so a
+    // warp keeps several multiply-adds in flight.
+    constexpr int kChains = (M == 1) ? 4 : (M <= 3 ? 2 : 1);
+    float c[M][kChains];
 #pragma unroll
-    for (int m = 0; m < M; ++m) t[m] = 0.f;
+    for (int m = 0; m < M; ++m)
+#pragma unroll
+        for (int h = 0; h < kChains; ++h) c[m][h] = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         const uint32_t lo = q[w] & 0x0F0F0F0Fu;         // elements 4w .. 4w+3
         const uint32_t hi = (q[w] >> 4) & 0x0F0F0F0Fu;  // elements 16+4w .. 16+4w+3
-        float vl[4], vh[4];
+        float v[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            vl[c] = magic_minus8(__byte_perm(lo, kMagicBits, 0x7540u + c));
-            vh[c] = magic_minus8(__byte_perm(hi, kMagicBits, 0x7540u + c));
+        for (int e = 0; e < 4; ++e) {
+            v[e] = magic_minus8(__byte_perm(lo, kMagicBits, 0x7540u + e));
+            v[4 + e] = magic_minus8(__byte_perm(hi, kMagicBits, 0x7540u + e));
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            const float* am = A + m * K + k0 + 4 * w;
-            const float4 al = load_a4<kVecA>(am);
-            const float4 ah = load_a4<kVecA>(am + 16);
-            float s = t[m];
-            s = fmaf(al.x, vl[0], s);
-            s = fmaf(al.y, vl[1], s);
-            s = fmaf(al.z, vl[2], s);
-            s = fmaf(al.w, vl[3], s);
-            s = fmaf(ah.x, vh[0], s);
-            s = fmaf(ah.y, vh[1], s);
-            s = fmaf(ah.z, vh[2], s);
-            s = fmaf(ah.w, vh[3], s);
-            t[m] = s;
+            const float* am = A + m * lda + k0 + 4 * w;
+            const float4 al = load_a4<kSrc>(am);
+            const float4 ah = load_a4<kSrc>(am + 16);
+            const float a[8] = {al.x, al.y, al.z, al.w, ah.x, ah.y, ah.z, ah.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[m][e % kChains] = fmaf(a[e], v[e], c[m][e % kChains]);
         }
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        float x = c[m][0];
+#pragma unroll
+        for (int h = 1; h < kChains; ++h) x += c[m][h];
+        t[m] = x;
+    }
+}
+
+// The block's contribution taken element by element, sum_j A[m][k0+j] *
+// ((q_j - 8) * d).  Used only when d is infinite or NaN: there the factored
+// form d * sum_j A_j (q_j - 8) can lose the NaN that a zero weight (q = 8)
+// times an infinite d, or infinities of both signs, put into the sum.
+template <int M, ASrc kSrc>
+__device__ __noinline__ void block_exact(const float* __restrict__ A, int64_t lda, int64_t k0,
+                                         const uint32_t q[4], float d, float t[M]) {
+#pragma unroll
+    for (int m = 0; m < M; ++m) t[m] = 0.f;
+    for (int j = 0; j < 32; ++j) {
+        const int byte = j & 15;
+        const uint32_t b = (q[byte >> 2] >> (8 * (byte & 3))) & 0xFFu;
+        const uint32_t nib = (j < 16) ? (b & 0xFu) : (b >> 4);
+        const float w = magic_minus8(nib | kMagicBits) * d;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float a;
+            if constexpr (kSrc == ASrc::kShared) {
+                a = A[m * lda + k0 + j];
+            } else {
+                a = __ldg(A + m * lda + k0 + j);
+            }
+            t[m] = fmaf(a, w, t[m]);
+        }
+    }
+}
+
+// acc[m] += d * t[m], or the exact per-element sum when d is not finite.
+template <int M, ASrc kSrc>
+__device__ __forceinline__ void scale_block(const float* __restrict__ A, int64_t lda, int64_t k0,
+                                            const uint32_t q[4], float d, const float t[M],
+                                            float acc[M]) {
+    if (isfinite(d)) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] = fmaf(d, t[m], acc[m]);
+    } else {
+        float e[M];
+        block_exact<M, kSrc>(A, lda, k0, q, d, e);
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] += e[m];
     }
 }
 
@@ -95,7 +158,7 @@ __device__ __forceinline__ void block_dot(const float* __restrict__ A, int64_t K
 // words 5..8.
 template <int M>
 __device__ __forceinline__ void unit_dot(const uint8_t* tile_row, const float* __restrict__ A,
-                                         int64_t K, int64_t kbase, float acc[M]) {
+                                         int64_t lda, int64_t kbase, float acc[M]) {
     uint32_t w[36];
     const uint4* src = reinterpret_cast<const uint4*>(tile_row);
 #pragma unroll
@@ -112,85 +175,181 @@ __device__ __forceinline__ void unit_dot(const uint8_t* tile_row, const float* _
         float t[M];
         const uint32_t qa[4] = {__byte_perm(W[0], W[1], 0x5432u), __byte_perm(W[1], W[2], 0x5432u),
                                 __byte_perm(W[2], W[3], 0x5432u), __byte_perm(W[3], W[4], 0x5432u)};
-        block_dot<M, true>(A, K, kbase + 64 * p, qa, t);
+        block_dot<M, ASrc::kShared>(A, lda, kbase + 64 * p, qa, t);
         const float da = f16_bits_to_float(W[0] & 0xFFFFu);
-#pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = fmaf(da, t[m], acc[m]);
+        scale_block<M, ASrc::kShared>(A, lda, kbase + 64 * p, qa, da, t, acc);
         const uint32_t qb[4] = {W[5], W[6], W[7], W[8]};
-        block_dot<M, true>(A, K, kbase + 64 * p + 32, qb, t);
+        block_dot<M, ASrc::kShared>(A, lda, kbase + 64 * p + 32, qb, t);
         const float db = f16_bits_to_float(W[4] >> 16);
-#pragma unroll
-        for (int m = 0; m < M; ++m) acc[m] = fmaf(db, t[m], acc[m]);
+        scale_block<M, ASrc::kShared>(A, lda, kbase + 64 * p + 32, qb, db, t, acc);
     }
 }
 
+// Work decomposition of one persistent launch.
+struct GemvGrid {
+    int N;
+    int64_t K;
+    int U;          // units per row, K / 256
+    int RG;         // row groups, ceil(N / 32)
+    int S;          // unit ranges (K splits); U is a multiple of S
+    int nu;         // units per range, U / S
+    int box0;       // units in the first TMA box of a stage (the second has nu - box0)
+    int rpg;        // row groups per range of rows
+    int stages;     // ring depth in row-group stages
+    float* part;    // [RG][S][M][32] split partial sums (S > 1)
+    unsigned* ctr;  // [RG] arrival counters (S > 1), zero between launches
+};
+
 template <int M>
-__global__ void __launch_bounds__(256)
-    gemv_q4_0_tma(const __grid_constant__ CUtensorMap wmap, const float* __restrict__ A,
-                  float* __restrict__ C, int N, int64_t K, int units_total, int units_per_cta,
-                  int cluster) {
+__global__ void __launch_bounds__(cta_threads<M>(), 1)
+    gemv_q4_0_persistent(const __grid_constant__ CUtensorMap map0,
+                         const __grid_constant__ CUtensorMap map1, const float* __restrict__ A,
+                         float* __restrict__ C, const GemvGrid g) {
+    constexpr int W = consumer_warps<M>();
     extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + units_per_cta * kTileBytes);
-    float* partial = reinterpret_cast<float*>(bars + units_per_cta);  // [nwarps][M][32]
+    // ring [stages][32 rows x nu units x 144 B] (first box0 units of every row,
+    // then the rest) | activations [M][nu * 256] f32 | partial sums
+    // [rpg][W][M][32] | full[stages] | empty[stages] | a_bar | seq[stages]
+    const int stage_bytes = kTileBytes * g.nu;
+    uint8_t* ring = smem;
+    float* a_s = reinterpret_cast<float*>(smem + g.stages * stage_bytes);
+    const int lda = g.nu * kUnitElems;
+    float* partial = a_s + M * lda;
+    uint64_t* full = reinterpret_cast<uint64_t*>(partial + g.rpg * W * M * 32);
+    uint64_t* empty = full + g.stages;
+    uint64_t* a_bar = empty + g.stages;
+    // seq[st]: the row group the producer last issued into stage st.  A warp
+    // waits for its row group's number before the parity wait on full[st],
+    // so it can never mistake an older phase of the stage for its own.
+    volatile int* seq = reinterpret_cast<volatile int*>(a_bar + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    const int rank = static_cast<int>(blockIdx.x) % cluster;
-    const int row0 = (static_cast<int>(blockIdx.x) / cluster) * kRowsPerCta;
-    const int u0 = rank * units_per_cta;
-    int nunits = units_total - u0;
-    nunits = nunits < 0 ? 0 : (nunits > units_per_cta ? units_per_cta : nunits);
+    const int split = static_cast<int>(blockIdx.x) % g.S;
+    const int rg0 = (static_cast<int>(blockIdx.x) / g.S) * g.rpg;
+    const int nrg = max(0, min(g.rpg, g.RG - rg0));
+    const int u0 = split * g.nu;
+    const int nu = g.nu;
+    const int box1 = nu - g.box0;
+    const int items = nrg * nu;
 
+    for (int i = threadIdx.x; i < g.rpg * W * M * 32; i += blockDim.x) partial[i] = 0.f;
     if (threadIdx.x == 0) {
-        prefetch_tensormap(&wmap);
-        for (int j = 0; j < nunits; ++j) mbar_init(&bars[j], 1);
+        for (int s = 0; s < g.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nu);  // one arrival per consumed tile
+            seq[s] = -1;
+        }
+        mbar_init(a_bar, 1);
         fence_barrier_init();
-        for (int j = 0; j < nunits; ++j) {
-            mbar_arrive_expect_tx(&bars[j], kTileBytes);
-            tma_load_2d(tiles + j * kTileBytes, &wmap, (u0 + j) * kUnitBytes, row0, &bars[j]);
-        }
     }
     __syncthreads();
 
-    float acc[M];
-#pragma unroll
-    for (int m = 0; m < M; ++m) acc[m] = 0.f;
-    for (int j = warp; j < nunits; j += nwarps) {
-        if (!mbar_wait_bounded(&bars[j], 0, &g_gemv_error)) continue;
-        unit_dot<M>(tiles + j * kTileBytes + lane * kUnitBytes, A, K,
-                    static_cast<int64_t>(u0 + j) * kUnitElems, acc);
-    }
-#pragma unroll
-    for (int m = 0; m < M; ++m) partial[(warp * M + m) * 32 + lane] = acc[m];
-    __syncthreads();
-
-    const int row = row0 + lane;
-    if (cluster == 1) {
-        if (warp == 0 && row < N) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float s = 0.f;
-                for (int w = 0; w < nwarps; ++w) s += partial[(w * M + m) * 32 + lane];
-                C[static_cast<int64_t>(m) * N + row] = s;
+    if (warp == W) {
+        // Producer: the activation slice, then one row group per stage.
+        if (lane == 0 && items > 0) {
+            prefetch_tensormap(&map0);
+            if (box1 > 0) prefetch_tensormap(&map1);
+            const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
+            mbar_arrive_expect_tx(a_bar, a_bytes * M);
+            for (int m = 0; m < M; ++m)
+                bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
+                             a_bytes, a_bar);
+            for (int r = 0; r < nrg; ++r) {
+                const int st = r % g.stages;
+                if (r >= g.stages &&
+                    !mbar_wait_bounded(&empty[st], ((r / g.stages) - 1) & 1, &g_gemv_error))
+                    break;
+                uint8_t* dst = ring + st * stage_bytes;
+                const int row = (rg0 + r) * kRowsPerTile;
+                seq[st] = r;
+                mbar_arrive_expect_tx(&full[st], stage_bytes);
+                tma_load_3d(dst, &map0, 0, u0, row, &full[st]);
+                if (box1 > 0)
+                    tma_load_3d(dst + kTileBytes * g.box0, &map1, 0, u0 + g.box0, row, &full[st]);
             }
         }
-    } else {
-        cg::cluster_group cl = cg::this_cluster();
-        cl.sync();
-        if (rank == 0 && warp == 0 && row < N) {
+    } else if (items > 0 && mbar_wait_bounded(a_bar, 0, &g_gemv_error)) {
+        // Consumers: tile i (row group i / nu, unit i % nu) goes to warp i % W.
+        float acc[M];
+        int cur = -1;
+        for (int i = warp; i < items; i += W) {
+            const int r = i / nu;
+            const int j = i - r * nu;
+            if (r != cur) {
+                if (cur >= 0) {
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float s = 0.f;
-                for (int q = 0; q < cluster; ++q) {
-                    const float* rp = cl.map_shared_rank(partial, q);
-                    for (int w = 0; w < nwarps; ++w) s += rp[(w * M + m) * 32 + lane];
+                    for (int m = 0; m < M; ++m) partial[((cur * W + warp) * M + m) * 32 + lane] += acc[m];
                 }
-                C[static_cast<int64_t>(m) * N + row] = s;
+#pragma unroll
+                for (int m = 0; m < M; ++m) acc[m] = 0.f;
+                cur = r;
+            }
+            const int st = r % g.stages;
+            bool issued = false;
+            for (uint32_t poll = 0; poll < kMaxWaitPolls; ++poll) {
+                if (seq[st] == r) {
+                    issued = true;
+                    break;
+                }
+            }
+            if (!issued) atomicOr(&g_gemv_error, kErrWaitTimeout);
+            if (issued && mbar_wait_bounded(&full[st], (r / g.stages) & 1, &g_gemv_error)) {
+                const uint8_t* base = ring + st * stage_bytes;
+                const uint8_t* row_unit =
+                    (j < g.box0) ? base + (lane * g.box0 + j) * kUnitBytes
+                                 : base + kTileBytes * g.box0 + (lane * box1 + (j - g.box0)) * kUnitBytes;
+                unit_dot<M>(row_unit, a_s, lda, j * kUnitElems, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        if (cur >= 0) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) partial[((cur * W + warp) * M + m) * 32 + lane] += acc[m];
+        }
+    }
+    __syncthreads();
+
+    // Row-group totals in fixed warp order; split partials meet in the workspace.
+    if (warp < W) {
+        for (int r = warp; r < nrg; r += W) {
+            const int row = (rg0 + r) * kRowsPerTile + lane;
+            float tot[M];
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float v = 0.f;
+                for (int w = 0; w < W; ++w) v += partial[((r * W + w) * M + m) * 32 + lane];
+                tot[m] = v;
+            }
+            if (g.S == 1) {
+                if (row < g.N) {
+#pragma unroll
+                    for (int m = 0; m < M; ++m) C[static_cast<int64_t>(m) * g.N + row] = tot[m];
+                }
+                continue;
+            }
+            const int64_t rg = rg0 + r;
+            float* slot = g.part + (rg * g.S + split) * (M * 32);
+#pragma unroll
+            for (int m = 0; m < M; ++m) slot[m * 32 + lane] = tot[m];
+            __threadfence();
+            __syncwarp();
+            unsigned old = 0;
+            if (lane == 0) old = atomicAdd(&g.ctr[rg], 1u);
+            old = __shfl_sync(0xFFFFFFFFu, old, 0);
+            if (old == static_cast<unsigned>(g.S - 1)) {
+                __threadfence();
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    float v = 0.f;
+                    for (int q = 0; q < g.S; ++q)
+                        v += __ldcg(g.part + (rg * g.S + q) * (M * 32) + m * 32 + lane);
+                    if (row < g.N) C[static_cast<int64_t>(m) * g.N + row] = v;
+                }
+                if (lane == 0) atomicExch(&g.ctr[rg], 0u);
             }
         }
-        cl.sync();  // peers keep their shared memory alive until rank 0 has read it
     }
 }
 
@@ -215,10 +374,9 @@ __global__ void __launch_bounds__(256)
                        (static_cast<uint32_t>(h[2 + 2 * w]) << 16);
             }
             float t[M];
-            block_dot<M, false>(A, K, b * kBlockElems, q, t);
+            block_dot<M, ASrc::kGlobalScalar>(A, K, b * kBlockElems, q, t);
             const float d = f16_bits_to_float(h[0]);
-#pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = fmaf(d, t[m], acc[m]);
+            scale_block<M, ASrc::kGlobalScalar>(A, K, b * kBlockElems, q, d, t, acc);
         }
 #pragma unroll
         for (int m = 0; m < M; ++m) {
@@ -238,13 +396,85 @@ template <int M>
 cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE) >= bytes) return cudaSuccess;
-    const int want = dev.max_smem_optin;
-    cudaError_t err =
-        cudaFuncSetAttribute(gemv_q4_0_tma<M>, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
+    if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_persistent<M>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           dev.max_smem_optin);
     if (err != cudaSuccess) return err;
-    __atomic_store_n(&configured[dev.device], want, __ATOMIC_RELEASE);
-    return bytes <= want ? cudaSuccess : cudaErrorInvalidValue;
+    __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
+    return cudaSuccess;
+}
+
+int64_t smem_bytes(int M, int W, int stages, int nu, int rpg) {
+    return static_cast<int64_t>(stages) * kTileBytes * nu + static_cast<int64_t>(M) * nu * kUnitElems * 4 +
+           static_cast<int64_t>(rpg) * W * M * 32 * 4 + (2 * stages + 1) * 8 + stages * 4;
+}
+
+// Split a stage's nu units into at most two TMA boxes whose widths keep the
+// 144-byte row stride from piling the lanes of a quarter-warp onto one bank
+// group: an odd width is conflict-free, 2 mod 4 is two-way.
+int first_box(int nu) {
+    if (nu % 4 != 0) return nu;
+    return nu / 2 - 1;  // nu / 2 is even, so both halves become odd
+}
+
+// Choose (G row-group ranges) x (S unit ranges) for one CTA per SM.  The
+// largest share (rpg * nu tiles, times the number of waves) decides; among
+// shapes whose stages are at least kMinStageBytes (small TMA copies stream
+// poorly), the cheapest wins, fewer splits breaking ties.
+constexpr int64_t kMinStageBytes = 16 * 1024;
+
+bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws,
+               GemvGrid* g, int* grid, int* smem) {
+    const int U = static_cast<int>(K / kUnitElems);
+    const int64_t RG = (N + kRowsPerTile - 1) / kRowsPerTile;
+    const int P = dev.sm_count;
+    int64_t best[2] = {INT64_MAX, INT64_MAX};  // [small stages, big stages]
+    GemvGrid cand[2];
+    int cgrid[2] = {0, 0}, csmem[2] = {0, 0};
+    for (int S = 1; S <= kMaxSplits && S <= U; ++S) {
+        if (U % S != 0) continue;
+        const int nu = U / S;
+        if (nu > 2 * 255) continue;
+        const int G = std::max(1, P / S);
+        const int64_t rpg = std::min<int64_t>((RG + G - 1) / G, kMaxRowGroupsPerCta);
+        const int64_t g_used = (RG + rpg - 1) / rpg;
+        int stages = 4;
+        while (stages > 1 && smem_bytes(M, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
+            --stages;
+        if (smem_bytes(M, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin) continue;
+        if (stages < 2 && rpg > 1) continue;
+        if (S > 1 && (RG * S * M * 32 > static_cast<int64_t>(ws.part_floats) ||
+                      RG > static_cast<int64_t>(ws.ctr_count)))
+            continue;
+        const int64_t waves = (g_used * S + P - 1) / P;
+        const int64_t cost = rpg * nu * waves;
+        const int big = (static_cast<int64_t>(kTileBytes) * nu >= kMinStageBytes) ? 1 : 0;
+        if (cost < best[big]) {
+            best[big] = cost;
+            GemvGrid& c = cand[big];
+            c.N = static_cast<int>(N);
+            c.K = K;
+            c.U = U;
+            c.RG = static_cast<int>(RG);
+            c.S = S;
+            c.nu = nu;
+            c.box0 = first_box(nu);
+            c.rpg = static_cast<int>(rpg);
+            c.stages = stages;
+            c.part = ws.part;
+            c.ctr = ws.ctr;
+            cgrid[big] = static_cast<int>(g_used * S);
+            csmem[big] = static_cast<int>(smem_bytes(M, W, stages, nu, static_cast<int>(rpg)));
+        }
+    }
+    const int pick = (best[1] != INT64_MAX) ? 1 : 0;
+    if (best[pick] == INT64_MAX) return false;
+    *g = cand[pick];
+    *grid = cgrid[pick];
+    *smem = csmem[pick];
+    return g->box0 <= 255 && g->nu - g->box0 <= 255;
 }
 
 template <int M>
@@ -255,54 +485,36 @@ cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int
     const bool fast = (K % kUnitElems) == 0 && units > 0 &&
                       (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 &&
                       (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && N <= (int64_t(1) << 30) &&
-                      row_bytes < (int64_t(1) << 32);
+                      units <= (int64_t(1) << 20);
     if (fast) {
-        const int64_t row_groups = (N + kRowsPerCta - 1) / kRowsPerCta;
-        const int64_t target = static_cast<int64_t>(dev.sm_count) * 6;
-        int cluster = 1;
-        while (cluster < kMaxCluster && row_groups * cluster < target && cluster * 2 <= units)
-            cluster *= 2;
-        int64_t upc = (units + cluster - 1) / cluster;
-        while (upc > kMaxUnitsPerCta && cluster < kMaxCluster) {
-            cluster *= 2;
-            upc = (units + cluster - 1) / cluster;
-        }
-        if (upc <= kMaxUnitsPerCta) {
-            int nwarps = upc < 8 ? static_cast<int>(upc) : 8;
-            for (int d = 8; d >= 4; --d) {
-                if (upc % d == 0) {
-                    nwarps = d;
-                    break;
-                }
+        Workspace ws;
+        cudaError_t err = stream_workspace(dev, stream, &ws);
+        if (err != cudaSuccess) return err;
+        GemvGrid g;
+        int grid = 0, smem = 0;
+        if (plan_grid(M, consumer_warps<M>(), N, K, dev, ws, &g, &grid, &smem)) {
+            err = ensure_smem_attr<M>(dev, smem);
+            if (err != cudaSuccess) return err;
+            // The weight stream as bytes [N rows][U units][144 B]; boxes of
+            // 32 rows x box units x 144 B.
+            const int64_t dims[3] = {kUnitBytes, units, N};
+            const int64_t strides[2] = {kUnitBytes, row_bytes};
+            CUtensorMap map0, map1;
+            const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
+            err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
+            if (err != cudaSuccess) return err;
+            map1 = map0;
+            if (g.nu > g.box0) {
+                const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
+                err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
+                if (err != cudaSuccess) return err;
             }
-            const int smem = static_cast<int>(upc * kTileBytes + upc * 8 + nwarps * M * 32 * 4);
-            cudaError_t err = ensure_smem_attr<M>(dev, smem);
-            if (err != cudaSuccess) return err;
-            CUtensorMap map;
-            err = encode_weight_map_2d(&map, wq, row_bytes, N, kUnitBytes, kRowsPerCta);
-            if (err != cudaSuccess) return err;
-
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(static_cast<unsigned>(row_groups * cluster));
-            cfg.blockDim = dim3(nwarps * 32);
-            cfg.dynamicSmemBytes = smem;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = cluster;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            err = cudaLaunchKernelEx(&cfg, gemv_q4_0_tma<M>, map, A, C, static_cast<int>(N), K,
-                                     static_cast<int>(units), static_cast<int>(upc), cluster);
-            if (err != cudaSuccess) return err;
+            gemv_q4_0_persistent<M><<<grid, cta_threads<M>(), smem, stream>>>(map0, map1, A, C, g);
             note_launch();
             return cudaGetLastError();
         }
     }
-    const int64_t warps_needed = N;
-    const int64_t ctas = (warps_needed + 7) / 8;
+    const int64_t ctas = (N + 7) / 8;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
     const unsigned grid = static_cast<unsigned>(ctas < cap ? ctas : cap);
     gemv_q4_0_generic<M><<<grid, 256, 0, stream>>>(A, wq, C, N, K);

@@ -7,8 +7,9 @@
 
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
-#include "../../include/qm.h"
+#include "qm.h"
 #include "qm_internal.h"
 
 namespace qm {
@@ -20,11 +21,61 @@ DeviceInfo g_dev[kMaxDevices];
 int g_dev_ready[kMaxDevices] = {0};
 std::mutex g_dev_mutex;
 
+// Split-K workspaces, one per (device, stream).
+constexpr size_t kWorkspacePartFloats = size_t(2) << 20;  // 8 MB of partial sums
+constexpr int kWorkspaceCounters = 1 << 16;
+struct WorkspaceEntry {
+    int device;
+    cudaStream_t stream;
+    Workspace ws;
+};
+std::vector<WorkspaceEntry> g_workspaces;
+std::mutex g_ws_mutex;
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 uint64_t g_launches = 0;
 std::once_flag g_encode_once;
 
 }  // namespace
+
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* out) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    for (const WorkspaceEntry& e : g_workspaces) {
+        if (e.device == dev.device && e.stream == stream) {
+            *out = e.ws;
+            return cudaSuccess;
+        }
+    }
+    Workspace ws;
+    const size_t bytes = kWorkspacePartFloats * sizeof(float) + kWorkspaceCounters * sizeof(unsigned);
+    void* p = nullptr;
+    cudaError_t err = cudaMalloc(&p, bytes);
+    if (err != cudaSuccess) return err;
+    ws.part = static_cast<float*>(p);
+    ws.ctr = reinterpret_cast<unsigned*>(ws.part + kWorkspacePartFloats);
+    ws.part_floats = kWorkspacePartFloats;
+    ws.ctr_count = kWorkspaceCounters;
+    err = cudaMemsetAsync(ws.ctr, 0, kWorkspaceCounters * sizeof(unsigned), stream);
+    if (err != cudaSuccess) {
+        cudaFree(p);
+        return err;
+    }
+    g_workspaces.push_back({dev.device, stream, ws});
+    *out = ws;
+    return cudaSuccess;
+}
+
+// Zero the arrival counters of every workspace of `device` (after a kernel
+// gave up a wait and may have left one behind).
+cudaError_t reset_workspaces(int device) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    for (const WorkspaceEntry& e : g_workspaces) {
+        if (e.device != device) continue;
+        cudaError_t err = cudaMemset(e.ws.ctr, 0, e.ws.ctr_count * sizeof(unsigned));
+        if (err != cudaSuccess) return err;
+    }
+    return cudaDeviceSynchronize();
+}
 
 void note_launch() { __atomic_fetch_add(&g_launches, 1, __ATOMIC_RELAXED); }
 
@@ -55,11 +106,11 @@ cudaError_t current_device_info(DeviceInfo* out) {
     return cudaSuccess;
 }
 
-// 2-D tensor map over a weight stream viewed as a byte matrix [rows][row_bytes]
-// (row stride row_bytes, a multiple of 16), with a box of box_rows x box_bytes
-// and zero fill outside the matrix.
-cudaError_t encode_weight_map_2d(CUtensorMap* map, const void* base, int64_t row_bytes,
-                                 int64_t rows, int box_bytes, int box_rows) {
+// Tiled TMA descriptor over bytes: `rank` dimensions (innermost first), the
+// byte strides of dimensions 1..rank-1 (multiples of 16), a box of box[d]
+// elements, zero fill outside the tensor.
+cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims,
+                            const int64_t* strides, const int* box) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -70,14 +121,18 @@ cudaError_t encode_weight_map_2d(CUtensorMap* map, const void* base, int64_t row
         }
     });
     if (!g_encode_tiled) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t elem_strides[2] = {1, 1};
-    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                                strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = static_cast<cuuint64_t>(dims[i]);
+        b[i] = static_cast<cuuint32_t>(box[i]);
+        es[i] = 1;
+        if (i > 0) st[i - 1] = static_cast<cuuint64_t>(strides[i - 1]);
+    }
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d,
+                                st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -214,6 +269,11 @@ int qm_device_status(void* stream, int clear) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QM_ERR_CUDA;
     unsigned int bits = 0;
     if (qm::gemv_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
+    if (bits && clear) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || qm::reset_workspaces(dev) != cudaSuccess)
+            return QM_ERR_CUDA;
+    }
     return bits ? QM_ERR_TIMEOUT : QM_OK;
 }
 

@@ -13,14 +13,27 @@ struct DeviceInfo {
     int max_smem_optin = 0;  // bytes of dynamic shared memory a CTA may opt into
 };
 
+// Scratch memory of the split-K GEMV: partial sums and per-row-group arrival
+// counters.  One workspace per (device, stream), allocated on first use and
+// kept until exit; kernels leave the counters at zero.
+struct Workspace {
+    float* part = nullptr;
+    unsigned* ctr = nullptr;
+    size_t part_floats = 0;
+    int ctr_count = 0;
+};
+
+// The workspace of `stream` on device dev.device (the current device).
+cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* out);
+
 // Cached properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo* out);
 
-// 2-D TMA descriptor over a weight stream seen as a byte matrix
-// [rows][row_bytes] (row_bytes a multiple of 16), box box_rows x box_bytes,
-// zero fill outside the matrix.
-cudaError_t encode_weight_map_2d(CUtensorMap* map, const void* base, int64_t row_bytes,
-                                 int64_t rows, int box_bytes, int box_rows);
+// Tiled TMA descriptor over bytes: `rank` dimensions (innermost first), the
+// byte strides of dimensions 1..rank-1 (multiples of 16), a box of box[d]
+// elements, zero fill outside the tensor.
+cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims,
+                            const int64_t* strides, const int* box);
 
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);

@@ -35,7 +35,7 @@ def env():
 
 
 def dev(x):
-    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+    return torch.from_numpy(np.array(x, copy=True)).cuda()
 
 
 def dequant_gpu(qm, blob, in_off=0, out_off=0):
@@ -46,7 +46,7 @@ def dequant_gpu(qm, blob, in_off=0, out_off=0):
     raw[in_off:in_off + blob.size] = dev(blob)
     guard = 64
     out_buf = torch.full((nb * 32 + 2 * guard + 4,), 0, dtype=torch.int32, device="cuda")
-    out_buf.fill_(GUARD_BITS - (1 << 32))
+    out_buf.fill_(GUARD_BITS)
     out_base = out_buf.data_ptr() + 4 * guard + out_off
     rc = qm.qm_dequant_q4_0_ptr(raw.data_ptr() + in_off, nb, out_base, 0)
     assert rc == qm.QM_OK, qm.qm_status_string(rc)
@@ -78,7 +78,7 @@ def matmul_gpu(qm, A, blob, N, algo=0, a_off=0, w_off=0):
     w_raw[w_off:w_off + blob.size] = dev(blob)
     guard = 32
     c_buf = torch.empty(M * N + 2 * guard, dtype=torch.int32, device="cuda")
-    c_buf.fill_(GUARD_BITS - (1 << 32))
+    c_buf.fill_(GUARD_BITS)
     rc = qm.qm_matmul_q4_0_algo_ptr(a_raw.data_ptr() + a_off, w_raw.data_ptr() + w_off,
                                     c_buf.data_ptr() + 4 * guard, M, N, K, algo, 0)
     assert rc == qm.QM_OK, qm.qm_status_string(rc)
@@ -161,11 +161,13 @@ def test_matmul_tail_shapes(env, shape):
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
 
 
-# GEMV TMA path: K % 256 == 0, aligned; N ragged against 32-row groups, K
-# split over clusters of different sizes.
+# GEMV TMA path: K % 256 == 0, aligned; N ragged against 32-row groups; K
+# split into 1..16 ranges (combined through the workspace); more row groups
+# than fit one wave of CTAs.
 GEMV_FAST = [(M, N, K) for M in (1, 2, 4, 7, 8)
              for (N, K) in ((1, 256), (31, 512), (33, 768), (100, 2048), (1000, 256),
-                            (64, 14336), (4096, 512))]
+                            (64, 14336), (4096, 512), (1024, 4096), (300, 3840))] + \
+            [(1, 80000, 256), (3, 4096, 4096), (8, 4096, 4096)]
 
 
 @pytest.mark.parametrize("shape", GEMV_FAST, ids=lambda s: "x".join(map(str, s)))
