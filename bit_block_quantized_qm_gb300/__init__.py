@@ -27,7 +27,8 @@ __all__ = [
     "qm_launch_count",
     "qm_dequant_q4_0_ptr", "qm_matmul_q4_0_ptr", "qm_matmul_q4_0_algo_ptr",
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
-    "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER",
+    "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
+    "qm_matmul_q4_0_noalloc_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "EXPORTED_SYMBOLS",
 ]
 
@@ -40,6 +41,7 @@ QM_ERR_CUDA = -5
 QM_ERR_TIMEOUT = -6
 QM_ERR_UNSUPPORTED = -7
 QM_ERR_POINTER = -8
+QM_ERR_TOO_LARGE = -9
 
 QM_ALGO_AUTO = 0
 QM_ALGO_GEMV = 1
@@ -50,7 +52,8 @@ BLOCK_ELEMS = 32
 
 # Every symbol include/qm.h declares.
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
-                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count")
+                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count",
+                    "qm_matmul_q4_0_noalloc")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
@@ -93,6 +96,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_matmul_q4_0_algo.restype = i32
             lib.qm_device_status.argtypes = [p, i32]
             lib.qm_device_status.restype = i32
+            lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
+            lib.qm_matmul_q4_0_noalloc.restype = i32
             lib.qm_launch_count.argtypes = []
             lib.qm_launch_count.restype = ctypes.c_uint64
             _lib = lib
@@ -126,6 +131,12 @@ def qm_matmul_q4_0_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, stream: 
 def qm_matmul_q4_0_algo_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, algo: int,
                             stream: int = 0) -> int:
     return load_library().qm_matmul_q4_0_algo(A, wq, C, M, N, K, algo, stream)
+
+
+def qm_matmul_q4_0_noalloc_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
+                               stream: int = 0) -> int:
+    """The allocation-free GEMV (M <= 8); see include/qm.h."""
+    return load_library().qm_matmul_q4_0_noalloc(A, wq, C, M, N, K, stream)
 
 
 # ------------------------------------------------------------ torch tensors

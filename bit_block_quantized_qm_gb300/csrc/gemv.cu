@@ -29,6 +29,7 @@
 // Generic kernel (any K % 32 == 0, 2-byte aligned wq, 4-byte aligned A): one
 // warp per row, lanes striding over blocks, shuffle reduction.
 #include <algorithm>
+#include <mutex>
 
 #include "qm_device.cuh"
 #include "qm_internal.h"
@@ -549,6 +550,108 @@ cudaError_t gemv_read_device_error(unsigned int* bits, bool clear) {
         err = cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof(zero));
     }
     return err;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant (qm_matmul_q4_0_noalloc).  Some callers cannot call
+// cudaMalloc: code that runs where the CUDA allocator is off limits (inside a
+// custom allocator or memory-pool callback, under a process-wide memory cap,
+// or in a runtime that owns all device memory and forbids stray allocations).
+// For them the split-K GEMV takes its scratch from this fixed array instead of
+// a per-stream workspace.  Every GPU that loads the library holds the array
+// until the process exits; all calls share it.
+constexpr size_t kStaticPartFloats = size_t(256) * 1024;  // 1 MB of split partial sums
+constexpr int kStaticCounters = 4096;                      // row groups with a split K
+static __device__ __align__(256) float g_noalloc_scratch[kStaticPartFloats + kStaticCounters];
+
+namespace {
+
+// Device address of g_noalloc_scratch, found once per device with that device
+// current.  (In host code the array's name is only a host-side stand-in.)
+void* g_noalloc_addr[64] = {nullptr};
+std::mutex g_noalloc_mutex;
+
+cudaError_t noalloc_workspace(const DeviceInfo& dev, Workspace* out) {
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev.device]) {
+        void* p = nullptr;
+        cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_addr[dev.device] = p;
+    }
+    float* base = static_cast<float*>(g_noalloc_addr[dev.device]);
+    out->part = base;
+    out->part_floats = kStaticPartFloats;
+    out->ctr = reinterpret_cast<unsigned*>(base + kStaticPartFloats);
+    out->ctr_count = kStaticCounters;
+    return cudaSuccess;
+}
+
+template <int M>
+cudaError_t launch_m_noalloc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
+                             cudaStream_t stream, const DeviceInfo& dev) {
+    const int64_t units = K / kUnitElems;
+    const int64_t row_bytes = units * kUnitBytes;
+    const bool fast = (K % kUnitElems) == 0 && units > 0 &&
+                      (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 &&
+                      (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && N <= (int64_t(1) << 30) &&
+                      units <= (int64_t(1) << 20);
+    if (fast) {
+        Workspace ws;
+        cudaError_t err = noalloc_workspace(dev, &ws);
+        if (err != cudaSuccess) return err;
+        GemvGrid g;
+        int grid = 0, smem = 0;
+        if (plan_grid(M, consumer_warps<M>(), N, K, dev, ws, &g, &grid, &smem)) {
+            err = ensure_smem_attr<M>(dev, smem);
+            if (err != cudaSuccess) return err;
+            if (g.S > 1) {
+                // The arrival counters must start at zero; the array keeps
+                // whatever the previous call (or an abandoned one) left.
+                err = cudaMemsetAsync(g.ctr, 0, static_cast<size_t>(g.RG) * sizeof(unsigned), stream);
+                if (err != cudaSuccess) return err;
+            }
+            const int64_t dims[3] = {kUnitBytes, units, N};
+            const int64_t strides[2] = {kUnitBytes, row_bytes};
+            CUtensorMap map0, map1;
+            const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
+            err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
+            if (err != cudaSuccess) return err;
+            map1 = map0;
+            if (g.nu > g.box0) {
+                const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
+                err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
+                if (err != cudaSuccess) return err;
+            }
+            gemv_q4_0_persistent<M><<<grid, cta_threads<M>(), smem, stream>>>(map0, map1, A, C, g);
+            note_launch();
+            return cudaGetLastError();
+        }
+    }
+    const int64_t ctas = (N + 7) / 8;
+    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
+    const unsigned grid = static_cast<unsigned>(ctas < cap ? ctas : cap);
+    gemv_q4_0_generic<M><<<grid, 256, 0, stream>>>(A, wq, C, N, K);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_q4_0_noalloc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                     int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+    switch (M) {
+        case 1: return launch_m_noalloc<1>(A, wq, C, N, K, stream, dev);
+        case 2: return launch_m_noalloc<2>(A, wq, C, N, K, stream, dev);
+        case 3: return launch_m_noalloc<3>(A, wq, C, N, K, stream, dev);
+        case 4: return launch_m_noalloc<4>(A, wq, C, N, K, stream, dev);
+        case 5: return launch_m_noalloc<5>(A, wq, C, N, K, stream, dev);
+        case 6: return launch_m_noalloc<6>(A, wq, C, N, K, stream, dev);
+        case 7: return launch_m_noalloc<7>(A, wq, C, N, K, stream, dev);
+        case 8: return launch_m_noalloc<8>(A, wq, C, N, K, stream, dev);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace qm

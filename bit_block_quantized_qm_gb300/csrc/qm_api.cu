@@ -231,6 +231,7 @@ const char* qm_status_string(int status) {
         case QM_ERR_TIMEOUT: return "a kernel gave up waiting for an asynchronous copy";
         case QM_ERR_UNSUPPORTED: return "the forced algorithm cannot run this shape";
         case QM_ERR_POINTER: return "a pointer is not device memory of the current device";
+        case QM_ERR_TOO_LARGE: return "beyond the fixed scratch of qm_matmul_q4_0_noalloc (M > 8)";
         default: return "unknown status";
     }
 }
@@ -261,6 +262,38 @@ int qm_matmul_q4_0(const float* A, const void* wq, float* C, int64_t M, int64_t 
 int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
                         int algo, void* stream) {
     return matmul_impl(A, wq, C, M, N, K, algo, stream);
+}
+
+// Allocation-free GEMV: the same checks as qm_matmul_q4_0, scratch from a
+// fixed device array (see include/qm.h).
+int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M, int64_t N,
+                           int64_t K, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QM_ERR_SHAPE;
+    int64_t a_elems, c_elems, w_elems, a_bytes, c_bytes, w_bytes;
+    if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, &a_bytes) || !mul_ok(M, N, &c_elems) ||
+        !mul_ok(c_elems, 4, &c_bytes) || !mul_ok(N, K / 32, &w_elems) ||
+        !mul_ok(w_elems, 18, &w_bytes))
+        return QM_ERR_SHAPE;
+    if (M > 8) return QM_ERR_TOO_LARGE;
+    if (M == 0 || N == 0) return QM_OK;
+    if (!C) return QM_ERR_NULL;
+    if (K > 0 && (!A || !wq)) return QM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(C) & 3u) != 0) return QM_ERR_ALIGN;
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3u) != 0 ||
+                  (reinterpret_cast<uintptr_t>(wq) & 1u) != 0))
+        return QM_ERR_ALIGN;
+    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, wq, w_bytes)) return QM_ERR_ALIAS;
+    if (N > 0x7FFFFFFF) return QM_ERR_SHAPE;
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    int rc = check_pointer(C, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(A, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(wq, dev.device);
+    if (rc != QM_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(c_bytes), s));
+    return from_cuda(qm::launch_gemv_q4_0_noalloc(A, static_cast<const uint8_t*>(wq), C,
+                                                  static_cast<int>(M), N, K, s, dev));
 }
 
 uint64_t qm_launch_count(void) { return qm::launch_count(); }

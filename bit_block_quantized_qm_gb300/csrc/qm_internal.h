@@ -43,6 +43,12 @@ cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                              int64_t K, cudaStream_t stream, const DeviceInfo& dev);
 
+// The same GEMV with its split-K scratch in a fixed device array instead of
+// a workspace (no allocation).  The first call on a device looks up the
+// array's address.
+cudaError_t launch_gemv_q4_0_noalloc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                     int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+
 // Prefill GEMM on FP32 FMA, any M >= 1.
 cudaError_t launch_gemm_q4_0_simt(const float* A, const uint8_t* wq, float* C, int64_t M,
                                   int64_t N, int64_t K, cudaStream_t stream,

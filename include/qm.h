@@ -59,6 +59,8 @@ extern "C" {
 #define QM_ERR_UNSUPPORTED (-7) /* the forced algorithm cannot run this shape    */
 #define QM_ERR_POINTER (-8)     /* a pointer is not device memory of the current
                                    device                                        */
+#define QM_ERR_TOO_LARGE (-9)   /* beyond the fixed scratch of
+                                   qm_matmul_q4_0_noalloc (M > 8)               */
 
 /* Algorithms for qm_matmul_q4_0_algo. */
 #define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks                          */
@@ -120,6 +122,35 @@ QM_API int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t
  * the read failed.  With clear != 0 the word is reset after reading.
  */
 QM_API int qm_device_status(void* stream, int clear);
+
+/*
+ * qm_matmul_q4_0_noalloc — the decode-regime product C = A x dequant(W)^T for
+ * M = 1..8, for callers that cannot call cudaMalloc.  No counterpart on the
+ * kernel-contract pages: it exists for code that must not allocate device
+ * memory at call time, such as a custom allocator or memory-pool callback,
+ * a process running under a hard device-memory cap, or a runtime that owns
+ * all device memory.  qm_matmul_q4_0 gives each stream a small workspace
+ * (cudaMalloc on first use) for the partial sums of a split K; this entry
+ * point takes that scratch from a fixed array compiled into the library
+ * instead, and allocates nothing, ever.
+ *   Arguments, layouts, alignment and aliasing rules: as qm_matmul_q4_0.
+ *   Limit: M <= 8 (the GEMV regime); M > 8 returns QM_ERR_TOO_LARGE.  The
+ *   array holds 1 MB of partial sums and 4096 row-group counters; when a
+ *   shape's split would not fit, the kernel splits K less (down to not at
+ *   all), so every N and K within the other limits is accepted.
+ *   Memory: every GPU that loads the library holds the array (about 1 MB)
+ *   until the process exits.
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Sharing: all calls use the same array, which keeps the last call's
+ *   contents; a call clears the counters it needs before its kernel runs.
+ *   Calls that overlap on the GPU (different streams, or concurrent graph
+ *   launches) race on the array and may produce wrong results: order them.
+ * Returns QM_OK or a negative status.
+ */
+QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M,
+                                  int64_t N, int64_t K, void* stream);
 
 /*
  * qm_launch_count — the number of kernels this library has enqueued in this

@@ -40,7 +40,7 @@ def test_only_declared_symbols_are_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert qm.qm_version() >= 100
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         assert qm.qm_status_string(code) != "unknown status"
     assert qm.qm_status_string(-99) == "unknown status"
 
