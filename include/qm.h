@@ -21,11 +21,18 @@
  *
  * Conventions for every entry point:
  *   - Pointers are device memory owned by the caller (cudaMalloc'd, managed,
- *     or mapped host memory with a device address).  The library allocates
- *     and frees nothing and never synchronizes: work is enqueued on `stream`
- *     (a cudaStream_t passed as void*; NULL means the legacy default stream)
- *     on the current device, and results are visible once that stream has
- *     been synchronized.  Calls are thread-safe.
+ *     or mapped host memory with a device address).  Work is enqueued on
+ *     `stream` (a cudaStream_t passed as void*; NULL means the legacy default
+ *     stream) on the current device, and results are visible once that
+ *     stream has been synchronized; no entry point but qm_device_status
+ *     synchronizes.  Calls are thread-safe.
+ *   - Memory: the GEMV (M <= 8) splits K over several CTAs when the matrix
+ *     has few rows; their partial sums go through a workspace of about 8 MB
+ *     that the library allocates with cudaMalloc on the first such call on
+ *     each (device, stream) and keeps until exit.  Make that first call
+ *     before capturing the stream into a CUDA graph.  Calls on one stream
+ *     share its workspace in stream order; calls on different streams use
+ *     different workspaces.  qm_matmul_q4_0_noalloc allocates nothing.
  *   - Operands are contiguous; no strides, offsets or broadcasts.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     failed check returns a negative status and leaves memory untouched.
