@@ -29,7 +29,7 @@ __all__ = [
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
-    "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "EXPORTED_SYMBOLS",
+    "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "EXPORTED_SYMBOLS",
 ]
 
 QM_OK = 0
@@ -46,6 +46,7 @@ QM_ERR_TOO_LARGE = -9
 QM_ALGO_AUTO = 0
 QM_ALGO_GEMV = 1
 QM_ALGO_GEMM_SIMT = 2
+QM_ALGO_GEMV_SIMT = 3
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32

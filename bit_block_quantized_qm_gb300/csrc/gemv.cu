@@ -45,10 +45,12 @@ constexpr int kUnitElems = 256;
 constexpr int kRowsPerTile = 32;  // one row per lane
 constexpr int kTileBytes = kUnitBytes * kRowsPerTile;
 // Consumer warps per CTA: as many as the registers of one CTA per SM allow.
-template <int M>
-__host__ __device__ constexpr int consumer_warps() { return M <= 4 ? 16 : 8; }
-template <int M>
-__host__ __device__ constexpr int cta_threads() { return (consumer_warps<M>() + 1) * 32; }  // + producer warp
+template <int M, bool kTC>
+__host__ __device__ constexpr int consumer_warps() { return M <= 4 ? 16 : (kTC ? 12 : 8); }
+template <int M, bool kTC>
+__host__ __device__ constexpr int cta_threads() {
+    return (consumer_warps<M, kTC>() + 1) * 32;  // + producer warp
+}
 constexpr int kMaxSplits = 16;  // at most 16 K ranges
 constexpr int kMaxRowGroupsPerCta = 16;
 
@@ -186,6 +188,234 @@ __device__ __forceinline__ void unit_dot(const uint8_t* tile_row, const float* _
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core decode (mma.sync m16n8k16, bf16 operands, f32 accumulators).
+//
+// A (16 x 16, row-major) = weights: 16 rows of the tile x 16 k.  (q - 8) is
+// exact in bf16.  B (16 x 8) = activations: column c is a bf16 piece of one
+// activation row, hi = bf16(a) or lo = bf16(a - hi), so a - hi - lo is at
+// most 2^-18 |a| and every product is exact in f32.  Each lane scales its own
+// weight rows' accumulators by d once per block.
+//
+// Fragment layout (lane = 4 g + t): A regs {row g, k 2t..2t+1}, {row g+8, k
+// 2t..2t+1}, {row g, k 2t+8..2t+9}, {row g+8, k 2t+8..2t+9}; B regs {k
+// 2t..2t+1, col g}, {k 2t+8..2t+9, col g}; D {row g, col 2t}, {row g, col
+// 2t+1}, {row g+8, col 2t}, {row g+8, col 2t+1}.  The k order inside a block
+// is free as long as A and B agree: lane t takes quant bytes 4t..4t+3 of the
+// block, so for the block's two k-steps the fragment k pairs map to elements
+//   step 0: (4t, 4t+2) and (16+4t, 18+4t);  step 1: (4t+1, 4t+3) and (17+4t, 19+4t).
+//
+// Columns: for M <= 4 one MMA per k-step carries both pieces (column m = hi
+// of row m, column 4 + m = lo of row m); for M > 4 two MMAs per k-step, the
+// first with the hi pieces in columns 0..M-1 and the second with the lo pieces,
+// both into the same accumulators.
+
+template <int M>
+__host__ __device__ constexpr int tc_sets() { return M <= 4 ? 1 : 2; }
+
+__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (q - 8) as bf16 pairs from quant bytes 4t..4t+3 (Q, byte 4t lowest):
+// R0 = elements (4t, 4t+2), R1 = (16+4t, 18+4t), R2 = (4t+1, 4t+3), R3 = (17+4t, 19+4t).
+// A nibble under the bf16 exponent of 128 reads as 128 + q; subtracting 136
+// leaves q - 8, both steps exact.
+__device__ __forceinline__ void decode_bf16(uint32_t Q, uint32_t R[4]) {
+    constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
+    constexpr uint32_t kOne = 0x3F803F80u;    // bf16 1.0
+    constexpr uint32_t kBias = 0xC308C308u;   // bf16 -136.0
+    const uint32_t r[4] = {(Q & 0x000F000Fu) | kMagic, ((Q >> 4) & 0x000F000Fu) | kMagic,
+                           ((Q >> 8) & 0x000F000Fu) | kMagic, ((Q >> 12) & 0x000F000Fu) | kMagic};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(R[i]) : "r"(r[i]), "r"(kOne), "r"(kBias));
+}
+
+// Element indices (within a block) of the four fragment k values a lane with
+// quarter t holds at k-step h: pairs (e[0], e[1]) and (e[2], e[3]).
+__device__ __forceinline__ void step_elems(int t, int h, int e[4]) {
+    e[0] = 4 * t + h;
+    e[1] = 4 * t + 2 + h;
+    e[2] = 16 + 4 * t + h;
+    e[3] = 18 + 4 * t + h;
+}
+
+// Quant bytes 4t..4t+3 of a block at byte offset `off` of a 16-byte-aligned
+// row unit (off = 18 b): aligned for odd b, two halves for even b.
+__device__ __forceinline__ uint32_t quant_word(const uint8_t* unit, int b, int t) {
+    const uint8_t* p = unit + 18 * b + 2 + 4 * t;
+    if (b & 1) return *reinterpret_cast<const uint32_t*>(p);
+    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) |
+           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p + 2)) << 16);
+}
+
+// B-fragment slot of column c for set p (NS = 2M slots per (k-step, t)); -1
+// when the column carries no activation row.
+template <int M>
+__device__ __forceinline__ int tc_slot(int c, int p) {
+    if constexpr (tc_sets<M>() == 1) {
+        if (c < 4) return c < M ? c : -1;
+        return (c - 4) < M ? M + (c - 4) : -1;
+    } else {
+        return c < M ? p * M + c : -1;
+    }
+}
+
+// (piece, activation row) of D column c in set p: piece 0 = hi, 1 = lo.
+template <int M>
+__device__ __forceinline__ void tc_col(int c, int& piece, int& m) {
+    if constexpr (tc_sets<M>() == 1) {
+        piece = c >= 4 ? 1 : 0;
+        m = c & 3;
+    } else {
+        piece = 0;  // both pieces accumulate into the same column
+        m = c;
+    }
+}
+
+// Convert the CTA's activations (rows of length `lda` from `a`, global memory,
+// starting at the CTA's first k) into B fragments:
+// bfrag[(s * 2M + slot) * 4 + t] = {b0, b1} for k-step s (16 k).  Lanes of a
+// half-warp then read 16 distinct 8-byte entries: no bank conflicts.
+template <int M>
+__device__ void build_bfrag(const float* __restrict__ a, int64_t lda, int steps, uint2* bfrag,
+                            int tid, int nthreads) {
+    const int total = steps * 4 * 2 * M;
+    for (int i = tid; i < total; i += nthreads) {
+        const int t = i % 4;
+        const int slot = (i / 4) % (2 * M);
+        const int s = i / (8 * M);
+        const int piece = slot < M ? 0 : 1;
+        const int m = slot < M ? slot : slot - M;
+        int e[4];
+        step_elems(t, s & 1, e);
+        const float* am = a + m * lda + (s >> 1) * 32;
+        uint32_t h[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float x = __ldg(am + e[q]);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+            __nv_bfloat16 v = hi;
+            if (piece == 1) {
+                const float rest = x - __bfloat162float(hi);
+                v = __float2bfloat16_rn(isfinite(rest) ? rest : 0.f);
+            }
+            h[q] = static_cast<uint32_t>(__bfloat16_as_ushort(v));
+        }
+        bfrag[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+    }
+}
+
+// Exact contribution of one block of one weight row to activation row m:
+// sum_j A[m][k0 + j] * ((q_j - 8) * d), element by element (non-finite d).
+__device__ __noinline__ float row_block_exact(const uint8_t* unit, int b, const float* a_m,
+                                              float d) {
+    const uint8_t* qs = unit + 18 * b + 2;
+    float s = 0.f;
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t byte = qs[j & 15];
+        const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+        s = fmaf(__ldg(a_m + j), magic_minus8(nib | kMagicBits) * d, s);
+    }
+    return s;
+}
+
+// One tile (32 rows x 1 unit) on tensor cores.  rows[i] points at the unit
+// of tile rows g, g+8, 16+g, 24+g; bfr at the unit's B fragments; a_unit at
+// the unit's first activation in global memory, rows lda apart (read only
+// for blocks whose scale is not finite).
+template <int M>
+__device__ __forceinline__ void unit_mma(const uint8_t* const rows[4], const uint2* bfr,
+                                         const float* a_unit, int64_t lda, int lane,
+                                         float acc[2][4]) {
+    constexpr int P = tc_sets<M>();
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    int slot[P];
+#pragma unroll
+    for (int p = 0; p < P; ++p) slot[p] = tc_slot<M>(g, p);
+#pragma unroll 2
+    for (int b = 0; b < 8; ++b) {
+        uint32_t bb[2][P][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint2* f = bfr + (2 * b + h) * (2 * M) * 4 + t;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                const uint2 v = slot[p] >= 0 ? f[slot[p] * 4] : make_uint2(0u, 0u);
+                bb[h][p][0] = v.x;
+                bb[h][p][1] = v.y;
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint8_t* u0 = rows[2 * hh];
+            const uint8_t* u1 = rows[2 * hh + 1];
+            uint32_t r0[4], r1[4];
+            decode_bf16(quant_word(u0, b, t), r0);
+            decode_bf16(quant_word(u1, b, t), r1);
+            float D[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                mma_bf16_16816(D, r0[0], r1[0], r0[1], r1[1], bb[0][p][0], bb[0][p][1]);
+#pragma unroll
+            for (int p = 0; p < P; ++p)
+                mma_bf16_16816(D, r0[2], r1[2], r0[3], r1[3], bb[1][p][0], bb[1][p][1]);
+            // Scales of this lane's D rows: tile rows g (u0) and g + 8 (u1).
+            const float d0 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u0 + 18 * b));
+            const float d1 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u1 + 18 * b));
+            if (isfinite(d0) && isfinite(d1)) {
+                acc[hh][0] = fmaf(d0, D[0], acc[hh][0]);
+                acc[hh][1] = fmaf(d0, D[1], acc[hh][1]);
+                acc[hh][2] = fmaf(d1, D[2], acc[hh][2]);
+                acc[hh][3] = fmaf(d1, D[3], acc[hh][3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float d = (i < 2) ? d0 : d1;
+                    if (isfinite(d)) {
+                        acc[hh][i] = fmaf(d, D[i], acc[hh][i]);
+                        continue;
+                    }
+                    int piece, m;
+                    tc_col<M>(2 * t + (i & 1), piece, m);
+                    if (piece != 0 || m >= M) continue;
+                    acc[hh][i] += row_block_exact(i < 2 ? u0 : u1, b, a_unit + m * lda + 32 * b, d);
+                }
+            }
+        }
+    }
+}
+
+// Add a tile's accumulators into partial[m][row] (row within the 32-row tile).
+template <int M>
+__device__ __forceinline__ void flush_mma(const float acc[2][4], float* partial_w, int lane) {
+    const int g = lane >> 2;
+    const int t = lane & 3;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float v = acc[hh][i];
+            const int row = 16 * hh + g + ((i >= 2) ? 8 : 0);
+            if constexpr (tc_sets<M>() == 1) {
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);  // hi (t) + lo (t ^ 2) pieces
+                const int m = 2 * t + (i & 1);
+                if (t < 2 && m < M) partial_w[m * 32 + row] += v;
+            } else {
+                const int m = 2 * t + (i & 1);
+                if (m < M) partial_w[m * 32 + row] += v;
+            }
+        }
+    }
+}
+
 // Work decomposition of one persistent launch.
 struct GemvGrid {
     int N;
@@ -201,22 +431,27 @@ struct GemvGrid {
     unsigned* ctr;  // [RG] arrival counters (S > 1), zero between launches
 };
 
-template <int M>
-__global__ void __launch_bounds__(cta_threads<M>(), 1)
+template <int M, bool kTC>
+__global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
     gemv_q4_0_persistent(const __grid_constant__ CUtensorMap map0,
                          const __grid_constant__ CUtensorMap map1, const float* __restrict__ A,
                          float* __restrict__ C, const GemvGrid g) {
-    constexpr int W = consumer_warps<M>();
+    constexpr int W = consumer_warps<M, kTC>();
     extern __shared__ __align__(128) uint8_t smem[];
     // ring [stages][32 rows x nu units x 144 B] (first box0 units of every row,
-    // then the rest) | activations [M][nu * 256] f32 | partial sums
-    // [rpg][W][M][32] | full[stages] | empty[stages] | a_bar | seq[stages]
+    // then the rest) | activations: f32 [M][nu * 256] (FP32 FMA decode) or B
+    // fragments [nu * 16 k-steps][2M][4] (tensor cores) | partial sums
+    // [rpg][slots][M][32] | full[stages] | empty[stages] | a_bar | seq[stages]
     const int stage_bytes = kTileBytes * g.nu;
     uint8_t* ring = smem;
     float* a_s = reinterpret_cast<float*>(smem + g.stages * stage_bytes);
+    uint2* bfrag = reinterpret_cast<uint2*>(a_s);
     const int lda = g.nu * kUnitElems;
+    // Row group r's tiles go to warps (r * nu + j) % W, j < nu: min(nu, W)
+    // distinct warps, each with its own partial-sum slot.
+    const int slots = min(g.nu, W);
     float* partial = a_s + M * lda;
-    uint64_t* full = reinterpret_cast<uint64_t*>(partial + g.rpg * W * M * 32);
+    uint64_t* full = reinterpret_cast<uint64_t*>(partial + g.rpg * slots * M * 32);
     uint64_t* empty = full + g.stages;
     uint64_t* a_bar = empty + g.stages;
     // seq[st]: the row group the producer last issued into stage st.  A warp
@@ -234,7 +469,7 @@ __global__ void __launch_bounds__(cta_threads<M>(), 1)
     const int box1 = nu - g.box0;
     const int items = nrg * nu;
 
-    for (int i = threadIdx.x; i < g.rpg * W * M * 32; i += blockDim.x) partial[i] = 0.f;
+    for (int i = threadIdx.x; i < g.rpg * slots * M * 32; i += blockDim.x) partial[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.stages; ++s) {
             mbar_init(&full[s], 1);
@@ -251,11 +486,13 @@ __global__ void __launch_bounds__(cta_threads<M>(), 1)
         if (lane == 0 && items > 0) {
             prefetch_tensormap(&map0);
             if (box1 > 0) prefetch_tensormap(&map1);
-            const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
-            mbar_arrive_expect_tx(a_bar, a_bytes * M);
-            for (int m = 0; m < M; ++m)
-                bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
-                             a_bytes, a_bar);
+            if constexpr (!kTC) {
+                const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
+                mbar_arrive_expect_tx(a_bar, a_bytes * M);
+                for (int m = 0; m < M; ++m)
+                    bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
+                                 a_bytes, a_bar);
+            }
             for (int r = 0; r < nrg; ++r) {
                 const int st = r % g.stages;
                 if (r >= g.stages &&
@@ -270,20 +507,33 @@ __global__ void __launch_bounds__(cta_threads<M>(), 1)
                     tma_load_3d(dst + kTileBytes * g.box0, &map1, 0, u0 + g.box0, row, &full[st]);
             }
         }
-    } else if (items > 0 && mbar_wait_bounded(a_bar, 0, &g_gemv_error)) {
+    } else if (items > 0 && (kTC || mbar_wait_bounded(a_bar, 0, &g_gemv_error))) {
+        const float* a_cta = A + static_cast<int64_t>(u0) * kUnitElems;  // CTA's first k
+        if constexpr (kTC) {
+            // B fragments of the CTA's k-range, built once by the consumer warps.
+            build_bfrag<M>(a_cta, g.K, nu * 16, bfrag, threadIdx.x, W * 32);
+            asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
+        }
         // Consumers: tile i (row group i / nu, unit i % nu) goes to warp i % W.
-        float acc[M];
+        float acc[kTC ? 8 : M];
         int cur = -1;
+        auto flush = [&](int r) {
+            const int slot = (g.nu >= W) ? warp : ((warp - (r * g.nu) % W) + W) % W;
+            float* pw = partial + (r * slots + slot) * M * 32;
+            if constexpr (kTC) {
+                flush_mma<M>(reinterpret_cast<const float(*)[4]>(acc), pw, lane);
+            } else {
+#pragma unroll
+                for (int m = 0; m < M; ++m) pw[m * 32 + lane] += acc[m];
+            }
+        };
         for (int i = warp; i < items; i += W) {
             const int r = i / nu;
             const int j = i - r * nu;
             if (r != cur) {
-                if (cur >= 0) {
+                if (cur >= 0) flush(cur);
 #pragma unroll
-                    for (int m = 0; m < M; ++m) partial[((cur * W + warp) * M + m) * 32 + lane] += acc[m];
-                }
-#pragma unroll
-                for (int m = 0; m < M; ++m) acc[m] = 0.f;
+                for (int q = 0; q < (kTC ? 8 : M); ++q) acc[q] = 0.f;
                 cur = r;
             }
             const int st = r % g.stages;
@@ -297,22 +547,30 @@ __global__ void __launch_bounds__(cta_threads<M>(), 1)
             if (!issued) atomicOr(&g_gemv_error, kErrWaitTimeout);
             if (issued && mbar_wait_bounded(&full[st], (r / g.stages) & 1, &g_gemv_error)) {
                 const uint8_t* base = ring + st * stage_bytes;
-                const uint8_t* row_unit =
-                    (j < g.box0) ? base + (lane * g.box0 + j) * kUnitBytes
-                                 : base + kTileBytes * g.box0 + (lane * box1 + (j - g.box0)) * kUnitBytes;
-                unit_dot<M>(row_unit, a_s, lda, j * kUnitElems, acc);
+                // Start of unit j of tile row `row` in this stage.
+                auto row_unit = [&](int row) -> const uint8_t* {
+                    return (j < g.box0)
+                               ? base + (row * g.box0 + j) * kUnitBytes
+                               : base + kTileBytes * g.box0 + (row * box1 + (j - g.box0)) * kUnitBytes;
+                };
+                if constexpr (kTC) {
+                    const int gq = lane >> 2;
+                    const uint8_t* const rows[4] = {row_unit(gq), row_unit(gq + 8), row_unit(gq + 16),
+                                                    row_unit(gq + 24)};
+                    unit_mma<M>(rows, bfrag + j * 16 * 4 * 2 * M, a_cta + j * kUnitElems, g.K, lane,
+                                reinterpret_cast<float(*)[4]>(acc));
+                } else {
+                    unit_dot<M>(row_unit(lane), a_s, lda, j * kUnitElems, acc);
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
-        if (cur >= 0) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) partial[((cur * W + warp) * M + m) * 32 + lane] += acc[m];
-        }
+        if (cur >= 0) flush(cur);
     }
     __syncthreads();
 
-    // Row-group totals in fixed warp order; split partials meet in the workspace.
+    // Row-group totals in fixed slot order; split partials meet in the workspace.
     if (warp < W) {
         for (int r = warp; r < nrg; r += W) {
             const int row = (rg0 + r) * kRowsPerTile + lane;
@@ -320,7 +578,7 @@ __global__ void __launch_bounds__(cta_threads<M>(), 1)
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 float v = 0.f;
-                for (int w = 0; w < W; ++w) v += partial[((r * W + w) * M + m) * 32 + lane];
+                for (int q = 0; q < slots; ++q) v += partial[((r * slots + q) * M + m) * 32 + lane];
                 tot[m] = v;
             }
             if (g.S == 1) {
@@ -393,13 +651,13 @@ __global__ void __launch_bounds__(256)
 }
 
 // Per-device one-time opt-in to large dynamic shared memory.
-template <int M>
+template <int M, bool kTC>
 cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
     if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_persistent<M>,
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_persistent<M, kTC>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            dev.max_smem_optin);
     if (err != cudaSuccess) return err;
@@ -407,9 +665,12 @@ cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     return cudaSuccess;
 }
 
-int64_t smem_bytes(int M, int W, int stages, int nu, int rpg) {
-    return static_cast<int64_t>(stages) * kTileBytes * nu + static_cast<int64_t>(M) * nu * kUnitElems * 4 +
-           static_cast<int64_t>(rpg) * W * M * 32 * 4 + (2 * stages + 1) * 8 + stages * 4;
+int64_t smem_bytes(int M, bool tc, int W, int stages, int nu, int rpg) {
+    (void)tc;  // f32 activations and B fragments take the same space
+    return static_cast<int64_t>(stages) * kTileBytes * nu +
+           static_cast<int64_t>(M) * nu * kUnitElems * 4 +
+           static_cast<int64_t>(rpg) * std::min(nu, W) * M * 32 * 4 + (2 * stages + 1) * 8 +
+           stages * 4;
 }
 
 // Split a stage's nu units into at most two TMA boxes whose widths keep the
@@ -426,8 +687,8 @@ int first_box(int nu) {
 // poorly), the cheapest wins, fewer splits breaking ties.
 constexpr int64_t kMinStageBytes = 16 * 1024;
 
-bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws,
-               GemvGrid* g, int* grid, int* smem) {
+bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& dev,
+               const Workspace& ws, GemvGrid* g, int* grid, int* smem) {
     const int U = static_cast<int>(K / kUnitElems);
     const int64_t RG = (N + kRowsPerTile - 1) / kRowsPerTile;
     const int P = dev.sm_count;
@@ -442,9 +703,10 @@ bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev, const 
         const int64_t rpg = std::min<int64_t>((RG + G - 1) / G, kMaxRowGroupsPerCta);
         const int64_t g_used = (RG + rpg - 1) / rpg;
         int stages = 4;
-        while (stages > 1 && smem_bytes(M, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
+        while (stages > 1 &&
+               smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
             --stages;
-        if (smem_bytes(M, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin) continue;
+        if (smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin) continue;
         if (stages < 2 && rpg > 1) continue;
         if (S > 1 && (RG * S * M * 32 > static_cast<int64_t>(ws.part_floats) ||
                       RG > static_cast<int64_t>(ws.ctr_count)))
@@ -467,7 +729,7 @@ bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev, const 
             c.part = ws.part;
             c.ctr = ws.ctr;
             cgrid[big] = static_cast<int>(g_used * S);
-            csmem[big] = static_cast<int>(smem_bytes(M, W, stages, nu, static_cast<int>(rpg)));
+            csmem[big] = static_cast<int>(smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)));
         }
     }
     const int pick = (best[1] != INT64_MAX) ? 1 : 0;
@@ -478,43 +740,56 @@ bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev, const 
     return g->box0 <= 255 && g->nu - g->box0 <= 255;
 }
 
-template <int M>
-cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
-                     cudaStream_t stream, const DeviceInfo& dev) {
+// Whether the persistent kernel can take this operand layout at all.
+bool persistent_ok(const float* A, const uint8_t* wq, int64_t N, int64_t K) {
     const int64_t units = K / kUnitElems;
-    const int64_t row_bytes = units * kUnitBytes;
-    const bool fast = (K % kUnitElems) == 0 && units > 0 &&
-                      (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 &&
-                      (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && N <= (int64_t(1) << 30) &&
-                      units <= (int64_t(1) << 20);
-    if (fast) {
-        Workspace ws;
-        cudaError_t err = stream_workspace(dev, stream, &ws);
+    return (K % kUnitElems) == 0 && units > 0 && (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 &&
+           (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && N <= (int64_t(1) << 30) &&
+           units <= (int64_t(1) << 20);
+}
+
+// Plan and launch the persistent kernel with split-K scratch `ws`.  Sets
+// *launched = false (and launches nothing) when no plan fits.  With
+// clear_counters the row-group counters are zeroed on the stream first.
+template <int M, bool kTC>
+cudaError_t launch_persistent(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
+                              cudaStream_t stream, const DeviceInfo& dev, const Workspace& ws,
+                              bool clear_counters, bool* launched) {
+    *launched = false;
+    GemvGrid g;
+    int grid = 0, smem = 0;
+    if (!plan_grid(M, kTC, consumer_warps<M, kTC>(), N, K, dev, ws, &g, &grid, &smem))
+        return cudaSuccess;
+    cudaError_t err = ensure_smem_attr<M, kTC>(dev, smem);
+    if (err != cudaSuccess) return err;
+    if (clear_counters && g.S > 1) {
+        err = cudaMemsetAsync(g.ctr, 0, static_cast<size_t>(g.RG) * sizeof(unsigned), stream);
         if (err != cudaSuccess) return err;
-        GemvGrid g;
-        int grid = 0, smem = 0;
-        if (plan_grid(M, consumer_warps<M>(), N, K, dev, ws, &g, &grid, &smem)) {
-            err = ensure_smem_attr<M>(dev, smem);
-            if (err != cudaSuccess) return err;
-            // The weight stream as bytes [N rows][U units][144 B]; boxes of
-            // 32 rows x box units x 144 B.
-            const int64_t dims[3] = {kUnitBytes, units, N};
-            const int64_t strides[2] = {kUnitBytes, row_bytes};
-            CUtensorMap map0, map1;
-            const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
-            err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
-            if (err != cudaSuccess) return err;
-            map1 = map0;
-            if (g.nu > g.box0) {
-                const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
-                err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
-                if (err != cudaSuccess) return err;
-            }
-            gemv_q4_0_persistent<M><<<grid, cta_threads<M>(), smem, stream>>>(map0, map1, A, C, g);
-            note_launch();
-            return cudaGetLastError();
-        }
     }
+    // The weight stream as bytes [N rows][U units][144 B]; boxes of
+    // 32 rows x box units x 144 B.
+    const int64_t units = K / kUnitElems;
+    const int64_t dims[3] = {kUnitBytes, units, N};
+    const int64_t strides[2] = {kUnitBytes, units * kUnitBytes};
+    CUtensorMap map0, map1;
+    const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
+    err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
+    if (err != cudaSuccess) return err;
+    map1 = map0;
+    if (g.nu > g.box0) {
+        const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
+        err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
+        if (err != cudaSuccess) return err;
+    }
+    gemv_q4_0_persistent<M, kTC><<<grid, cta_threads<M, kTC>(), smem, stream>>>(map0, map1, A, C, g);
+    note_launch();
+    *launched = true;
+    return cudaGetLastError();
+}
+
+template <int M>
+cudaError_t launch_generic(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
+                           cudaStream_t stream, const DeviceInfo& dev) {
     const int64_t ctas = (N + 7) / 8;
     const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
     const unsigned grid = static_cast<unsigned>(ctas < cap ? ctas : cap);
@@ -523,19 +798,34 @@ cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int
     return cudaGetLastError();
 }
 
+template <int M>
+cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
+                     cudaStream_t stream, const DeviceInfo& dev, bool tc) {
+    if (persistent_ok(A, wq, N, K)) {
+        Workspace ws;
+        cudaError_t err = stream_workspace(dev, stream, &ws);
+        if (err != cudaSuccess) return err;
+        bool launched = false;
+        err = tc ? launch_persistent<M, true>(A, wq, C, N, K, stream, dev, ws, false, &launched)
+                 : launch_persistent<M, false>(A, wq, C, N, K, stream, dev, ws, false, &launched);
+        if (err != cudaSuccess || launched) return err;
+    }
+    return launch_generic<M>(A, wq, C, N, K, stream, dev);
+}
+
 }  // namespace
 
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
-                             int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool tc) {
     switch (M) {
-        case 1: return launch_m<1>(A, wq, C, N, K, stream, dev);
-        case 2: return launch_m<2>(A, wq, C, N, K, stream, dev);
-        case 3: return launch_m<3>(A, wq, C, N, K, stream, dev);
-        case 4: return launch_m<4>(A, wq, C, N, K, stream, dev);
-        case 5: return launch_m<5>(A, wq, C, N, K, stream, dev);
-        case 6: return launch_m<6>(A, wq, C, N, K, stream, dev);
-        case 7: return launch_m<7>(A, wq, C, N, K, stream, dev);
-        case 8: return launch_m<8>(A, wq, C, N, K, stream, dev);
+        case 1: return launch_m<1>(A, wq, C, N, K, stream, dev, tc);
+        case 2: return launch_m<2>(A, wq, C, N, K, stream, dev, tc);
+        case 3: return launch_m<3>(A, wq, C, N, K, stream, dev, tc);
+        case 4: return launch_m<4>(A, wq, C, N, K, stream, dev, tc);
+        case 5: return launch_m<5>(A, wq, C, N, K, stream, dev, tc);
+        case 6: return launch_m<6>(A, wq, C, N, K, stream, dev, tc);
+        case 7: return launch_m<7>(A, wq, C, N, K, stream, dev, tc);
+        case 8: return launch_m<8>(A, wq, C, N, K, stream, dev, tc);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -591,50 +881,17 @@ cudaError_t noalloc_workspace(const DeviceInfo& dev, Workspace* out) {
 template <int M>
 cudaError_t launch_m_noalloc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
                              cudaStream_t stream, const DeviceInfo& dev) {
-    const int64_t units = K / kUnitElems;
-    const int64_t row_bytes = units * kUnitBytes;
-    const bool fast = (K % kUnitElems) == 0 && units > 0 &&
-                      (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 &&
-                      (reinterpret_cast<uintptr_t>(A) & 15u) == 0 && N <= (int64_t(1) << 30) &&
-                      units <= (int64_t(1) << 20);
-    if (fast) {
+    if (persistent_ok(A, wq, N, K)) {
         Workspace ws;
         cudaError_t err = noalloc_workspace(dev, &ws);
         if (err != cudaSuccess) return err;
-        GemvGrid g;
-        int grid = 0, smem = 0;
-        if (plan_grid(M, consumer_warps<M>(), N, K, dev, ws, &g, &grid, &smem)) {
-            err = ensure_smem_attr<M>(dev, smem);
-            if (err != cudaSuccess) return err;
-            if (g.S > 1) {
-                // The arrival counters must start at zero; the array keeps
-                // whatever the previous call (or an abandoned one) left.
-                err = cudaMemsetAsync(g.ctr, 0, static_cast<size_t>(g.RG) * sizeof(unsigned), stream);
-                if (err != cudaSuccess) return err;
-            }
-            const int64_t dims[3] = {kUnitBytes, units, N};
-            const int64_t strides[2] = {kUnitBytes, row_bytes};
-            CUtensorMap map0, map1;
-            const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
-            err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
-            if (err != cudaSuccess) return err;
-            map1 = map0;
-            if (g.nu > g.box0) {
-                const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
-                err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
-                if (err != cudaSuccess) return err;
-            }
-            gemv_q4_0_persistent<M><<<grid, cta_threads<M>(), smem, stream>>>(map0, map1, A, C, g);
-            note_launch();
-            return cudaGetLastError();
-        }
+        // The arrival counters must start at zero; the array keeps whatever
+        // the previous call (or an abandoned one) left, so clear them first.
+        bool launched = false;
+        err = launch_persistent<M, true>(A, wq, C, N, K, stream, dev, ws, true, &launched);
+        if (err != cudaSuccess || launched) return err;
     }
-    const int64_t ctas = (N + 7) / 8;
-    const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
-    const unsigned grid = static_cast<unsigned>(ctas < cap ? ctas : cap);
-    gemv_q4_0_generic<M><<<grid, 256, 0, stream>>>(A, wq, C, N, K);
-    note_launch();
-    return cudaGetLastError();
+    return launch_generic<M>(A, wq, C, N, K, stream, dev);
 }
 
 }  // namespace

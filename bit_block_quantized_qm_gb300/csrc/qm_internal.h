@@ -38,10 +38,11 @@ cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const 
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
 
-// Decode-regime GEMV, M = 1..8.  Picks the TMA-staged kernel when wq and A
-// are 16-byte aligned and K % 256 == 0, else the generic kernel.
+// Decode-regime GEMV, M = 1..8.  Picks the persistent TMA-fed kernel (its
+// decode on tensor cores when tc, else on FP32 FMA) when wq and A are 16-byte
+// aligned and K % 256 == 0, else the generic kernel.
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
-                             int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool tc);
 
 // The same GEMV with its split-K scratch in a fixed device array instead of
 // a workspace (no allocation).  The first call on a device looks up the

@@ -71,8 +71,9 @@ extern "C" {
 
 /* Algorithms for qm_matmul_q4_0_algo. */
 #define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks                          */
-#define QM_ALGO_GEMV 1      /* decode-regime GEMV; M must be 1..8                 */
+#define QM_ALGO_GEMV 1      /* decode-regime GEMV, decode on tensor cores; M 1..8 */
 #define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
+#define QM_ALGO_GEMV_SIMT 3 /* decode-regime GEMV on FP32 FMA; M 1..8             */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 QM_API int qm_version(void);
@@ -114,7 +115,7 @@ QM_API int qm_matmul_q4_0(const float* A, const void* wq, float* C, int64_t M,
 /*
  * qm_matmul_q4_0_algo — qm_matmul_q4_0 with the algorithm forced (QM_ALGO_*),
  * for tests and benchmarks.  Returns QM_ERR_UNSUPPORTED when the algorithm
- * cannot run the shape (QM_ALGO_GEMV with M > 8), QM_ERR_SHAPE for an unknown
+ * cannot run the shape (a GEMV with M > 8), QM_ERR_SHAPE for an unknown
  * algorithm number.
  */
 QM_API int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t M,

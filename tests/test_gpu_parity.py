@@ -156,7 +156,8 @@ def test_matmul_tail_shapes(env, shape):
     blob = synth.q4_0_weights(N, K, M * 7 + N)
     A = synth.activations(M, K, K + M, dist="outliers")
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
-    algos = [qm.QM_ALGO_AUTO, qm.QM_ALGO_GEMM_SIMT] + ([qm.QM_ALGO_GEMV] if M <= 8 else [])
+    algos = [qm.QM_ALGO_AUTO, qm.QM_ALGO_GEMM_SIMT] + \
+        ([qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT] if M <= 8 else [])
     for algo in algos:
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
 
@@ -177,7 +178,8 @@ def test_gemv_tma_path(env, shape):
     blob = synth.q4_0_weights(N, K, 11 * M + N)
     A = synth.activations(M, K, 13 * M + K)
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
-    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV), C_ref, S_ref)
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV), C_ref, S_ref, "tensor cores")
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV_SIMT), C_ref, S_ref, "fp32 fma")
 
 
 @pytest.mark.parametrize("offs", [(4, 0), (0, 2), (0, 18), (8, 8)])
@@ -223,7 +225,7 @@ def test_nonfinite_scales(env):
     blob = blob.ravel()
     A = synth.activations(M, K, 52)
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
-    for algo in (qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMM_SIMT):
+    for algo in (qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT, qm.QM_ALGO_GEMM_SIMT):
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
 
 
