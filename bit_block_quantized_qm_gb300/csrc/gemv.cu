@@ -180,11 +180,13 @@ __device__ __forceinline__ void unit_dot(const uint8_t* tile_row, const float* _
                                 __byte_perm(W[2], W[3], 0x5432u), __byte_perm(W[3], W[4], 0x5432u)};
         block_dot<M, ASrc::kShared>(A, lda, kbase + 64 * p, qa, t);
         const float da = f16_bits_to_float(W[0] & 0xFFFFu);
-        scale_block<M, ASrc::kShared>(A, lda, kbase + 64 * p, qa, da, t, acc);
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] = fmaf(da, t[m], acc[m]);
         const uint32_t qb[4] = {W[5], W[6], W[7], W[8]};
         block_dot<M, ASrc::kShared>(A, lda, kbase + 64 * p + 32, qb, t);
         const float db = f16_bits_to_float(W[4] >> 16);
-        scale_block<M, ASrc::kShared>(A, lda, kbase + 64 * p + 32, qb, db, t, acc);
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[m] = fmaf(db, t[m], acc[m]);
     }
 }
 
@@ -279,49 +281,67 @@ __device__ __forceinline__ void tc_col(int c, int& piece, int& m) {
     }
 }
 
-// Convert the CTA's activations (rows of length `lda` from `a`, global memory,
-// starting at the CTA's first k) into B fragments:
-// bfrag[(s * 2M + slot) * 4 + t] = {b0, b1} for k-step s (16 k).  Lanes of a
-// half-warp then read 16 distinct 8-byte entries: no bank conflicts.
+// Turn one unit of staged activations, f32 [M][256] (as a TMA box of the
+// activation matrix lands), into that unit's B fragments in place:
+// entry (s * 2M + slot) * 4 + t = {b0, b1} for k-step s (16 k), lane quarter t
+// and slot (hi pieces of rows 0..M-1, then lo pieces).  The f32 values and the
+// fragments take the same 1 KB * M, so a warp reads everything into registers,
+// syncs, and overwrites.  Lanes of a half-warp later read 16 distinct 8-byte
+// entries: no bank conflicts.
 template <int M>
-__device__ void build_bfrag(const float* __restrict__ a, int64_t lda, int steps, uint2* bfrag,
-                            int tid, int nthreads) {
-    const int total = steps * 4 * 2 * M;
-    for (int i = tid; i < total; i += nthreads) {
-        const int t = i % 4;
-        const int slot = (i / 4) % (2 * M);
-        const int s = i / (8 * M);
-        const int piece = slot < M ? 0 : 1;
-        const int m = slot < M ? slot : slot - M;
+__device__ __forceinline__ void convert_unit_inplace(uint8_t* unit, int lane) {
+    constexpr int kPerLane = 2 * M;  // (k-step, row, quarter) triples per lane
+    const float* f = reinterpret_cast<const float*>(unit);
+    float x[kPerLane][4];
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int tr = lane + 32 * i;
+        const int t = tr & 3;
+        const int m = (tr >> 2) % M;
+        const int s = tr / (4 * M);
         int e[4];
         step_elems(t, s & 1, e);
-        const float* am = a + m * lda + (s >> 1) * 32;
-        uint32_t h[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[i][q] = f[m * 256 + 32 * (s >> 1) + e[q]];
+    }
+    __syncwarp();
+    uint2* out = reinterpret_cast<uint2*>(unit);
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) {
+        const int tr = lane + 32 * i;
+        const int t = tr & 3;
+        const int m = (tr >> 2) % M;
+        const int s = tr / (4 * M);
+        uint32_t hi[4], lo[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float x = __ldg(am + e[q]);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-            __nv_bfloat16 v = hi;
-            if (piece == 1) {
-                const float rest = x - __bfloat162float(hi);
-                v = __float2bfloat16_rn(isfinite(rest) ? rest : 0.f);
-            }
-            h[q] = static_cast<uint32_t>(__bfloat16_as_ushort(v));
+            const __nv_bfloat16 h = __float2bfloat16_rn(x[i][q]);
+            const float rest = x[i][q] - __bfloat162float(h);
+            hi[q] = __bfloat16_as_ushort(h);
+            lo[q] = __bfloat16_as_ushort(__float2bfloat16_rn(isfinite(rest) ? rest : 0.f));
         }
-        bfrag[i] = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        out[(s * 2 * M + m) * 4 + t] = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+        out[(s * 2 * M + M + m) * 4 + t] = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
     }
 }
 
-// Exact contribution of one block of one weight row to activation row m:
-// sum_j A[m][k0 + j] * ((q_j - 8) * d), element by element (non-finite d).
-__device__ __noinline__ float row_block_exact(const uint8_t* unit, int b, const float* a_m,
-                                              float d) {
-    const uint8_t* qs = unit + 18 * b + 2;
+// Exact sum over units [u0, u0 + nu) of one weight row for activation row
+// `a_m` (global, at the range's first k): sum_k A[m][k] * ((q_k - 8) * d),
+// element by element.  Taken for a row whose block-scaled sum came out
+// infinite or NaN: there a non-finite d times a zero weight (q = 8), or
+// infinities of both signs, must give NaN exactly as the definition does.
+__device__ __noinline__ float row_range_exact(const uint8_t* row_blocks, int nblocks,
+                                              const float* a_m) {
     float s = 0.f;
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t byte = qs[j & 15];
-        const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
-        s = fmaf(__ldg(a_m + j), magic_minus8(nib | kMagicBits) * d, s);
+    for (int b = 0; b < nblocks; ++b) {
+        const uint8_t* blk = row_blocks + 18 * b;
+        const float d = f16_bits_to_float(static_cast<uint32_t>(blk[0]) |
+                                          (static_cast<uint32_t>(blk[1]) << 8));
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t byte = blk[2 + (j & 15)];
+            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+            s = fmaf(__ldg(a_m + 32 * b + j), magic_minus8(nib | kMagicBits) * d, s);
+        }
     }
     return s;
 }
@@ -370,25 +390,12 @@ __device__ __forceinline__ void unit_mma(const uint8_t* const rows[4], const uin
             // Scales of this lane's D rows: tile rows g (u0) and g + 8 (u1).
             const float d0 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u0 + 18 * b));
             const float d1 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u1 + 18 * b));
-            if (isfinite(d0) && isfinite(d1)) {
-                acc[hh][0] = fmaf(d0, D[0], acc[hh][0]);
-                acc[hh][1] = fmaf(d0, D[1], acc[hh][1]);
-                acc[hh][2] = fmaf(d1, D[2], acc[hh][2]);
-                acc[hh][3] = fmaf(d1, D[3], acc[hh][3]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float d = (i < 2) ? d0 : d1;
-                    if (isfinite(d)) {
-                        acc[hh][i] = fmaf(d, D[i], acc[hh][i]);
-                        continue;
-                    }
-                    int piece, m;
-                    tc_col<M>(2 * t + (i & 1), piece, m);
-                    if (piece != 0 || m >= M) continue;
-                    acc[hh][i] += row_block_exact(i < 2 ? u0 : u1, b, a_unit + m * lda + 32 * b, d);
-                }
-            }
+            // A non-finite d makes this row's sum non-finite; the row-group
+            // total then recomputes that row element by element.
+            acc[hh][0] = fmaf(d0, D[0], acc[hh][0]);
+            acc[hh][1] = fmaf(d0, D[1], acc[hh][1]);
+            acc[hh][2] = fmaf(d1, D[2], acc[hh][2]);
+            acc[hh][3] = fmaf(d1, D[3], acc[hh][3]);
         }
     }
 }
@@ -418,13 +425,15 @@ __device__ __forceinline__ void flush_mma(const float acc[2][4], float* partial_
 
 // Work decomposition of one persistent launch.
 struct GemvGrid {
+    const uint8_t* wq;  // the weight stream (read directly only by the exact fix-up)
     int N;
     int64_t K;
     int U;          // units per row, K / 256
     int RG;         // row groups, ceil(N / 32)
     int S;          // unit ranges (K splits); U is a multiple of S
     int nu;         // units per range, U / S
-    int box0;       // units in the first TMA box of a stage (the second has nu - box0)
+    int uc;         // units per stage (a divisor of nu): a stage is 32 rows x uc units
+    int box0;       // units in the first TMA box of a stage (the second has uc - box0)
     int rpg;        // row groups per range of rows
     int stages;     // ring depth in row-group stages
     float* part;    // [RG][S][M][32] split partial sums (S > 1)
@@ -434,7 +443,8 @@ struct GemvGrid {
 template <int M, bool kTC>
 __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
     gemv_q4_0_persistent(const __grid_constant__ CUtensorMap map0,
-                         const __grid_constant__ CUtensorMap map1, const float* __restrict__ A,
+                         const __grid_constant__ CUtensorMap map1,
+                         const __grid_constant__ CUtensorMap amap, const float* __restrict__ A,
                          float* __restrict__ C, const GemvGrid g) {
     constexpr int W = consumer_warps<M, kTC>();
     extern __shared__ __align__(128) uint8_t smem[];
@@ -442,7 +452,7 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
     // then the rest) | activations: f32 [M][nu * 256] (FP32 FMA decode) or B
     // fragments [nu * 16 k-steps][2M][4] (tensor cores) | partial sums
     // [rpg][slots][M][32] | full[stages] | empty[stages] | a_bar | seq[stages]
-    const int stage_bytes = kTileBytes * g.nu;
+    const int stage_bytes = kTileBytes * g.uc;
     uint8_t* ring = smem;
     float* a_s = reinterpret_cast<float*>(smem + g.stages * stage_bytes);
     uint2* bfrag = reinterpret_cast<uint2*>(a_s);
@@ -454,9 +464,9 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(partial + g.rpg * slots * M * 32);
     uint64_t* empty = full + g.stages;
     uint64_t* a_bar = empty + g.stages;
-    // seq[st]: the row group the producer last issued into stage st.  A warp
-    // waits for its row group's number before the parity wait on full[st],
-    // so it can never mistake an older phase of the stage for its own.
+    // seq[st]: the chunk the producer last issued into stage st.  A warp waits
+    // for its chunk's number before the parity wait on full[st], so it can
+    // never mistake an older phase of the stage for its own.
     volatile int* seq = reinterpret_cast<volatile int*>(a_bar + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -466,14 +476,16 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
     const int nrg = max(0, min(g.rpg, g.RG - rg0));
     const int u0 = split * g.nu;
     const int nu = g.nu;
-    const int box1 = nu - g.box0;
+    const int uc = g.uc;
+    const int chunks = nu / uc;  // stages per row group
+    const int box1 = uc - g.box0;
     const int items = nrg * nu;
 
     for (int i = threadIdx.x; i < g.rpg * slots * M * 32; i += blockDim.x) partial[i] = 0.f;
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.stages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], nu);  // one arrival per consumed tile
+            mbar_init(&empty[s], uc);  // one arrival per consumed tile
             seq[s] = -1;
         }
         mbar_init(a_bar, 1);
@@ -486,32 +498,43 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
         if (lane == 0 && items > 0) {
             prefetch_tensormap(&map0);
             if (box1 > 0) prefetch_tensormap(&map1);
-            if constexpr (!kTC) {
+            if constexpr (kTC) {
+                // One [M][256] f32 box per unit, landing where the unit's B
+                // fragments will be built.
+                prefetch_tensormap(&amap);
+                mbar_arrive_expect_tx(a_bar, static_cast<uint32_t>(nu) * M * 1024);
+                for (int j = 0; j < nu; ++j)
+                    tma_load_2d(reinterpret_cast<uint8_t*>(bfrag) + j * M * 1024, &amap,
+                                (u0 + j) * kUnitElems, 0, a_bar);
+            } else {
                 const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
                 mbar_arrive_expect_tx(a_bar, a_bytes * M);
                 for (int m = 0; m < M; ++m)
                     bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
                                  a_bytes, a_bar);
             }
-            for (int r = 0; r < nrg; ++r) {
-                const int st = r % g.stages;
-                if (r >= g.stages &&
-                    !mbar_wait_bounded(&empty[st], ((r / g.stages) - 1) & 1, &g_gemv_error))
+            // Chunk c = (row group c / chunks, units [(c % chunks) * uc, +uc)).
+            for (int c = 0; c < nrg * chunks; ++c) {
+                const int st = c % g.stages;
+                if (c >= g.stages &&
+                    !mbar_wait_bounded(&empty[st], ((c / g.stages) - 1) & 1, &g_gemv_error))
                     break;
                 uint8_t* dst = ring + st * stage_bytes;
-                const int row = (rg0 + r) * kRowsPerTile;
-                seq[st] = r;
+                const int row = (rg0 + c / chunks) * kRowsPerTile;
+                const int ub = u0 + (c % chunks) * uc;
+                seq[st] = c;
                 mbar_arrive_expect_tx(&full[st], stage_bytes);
-                tma_load_3d(dst, &map0, 0, u0, row, &full[st]);
+                tma_load_3d(dst, &map0, 0, ub, row, &full[st]);
                 if (box1 > 0)
-                    tma_load_3d(dst + kTileBytes * g.box0, &map1, 0, u0 + g.box0, row, &full[st]);
+                    tma_load_3d(dst + kTileBytes * g.box0, &map1, 0, ub + g.box0, row, &full[st]);
             }
         }
-    } else if (items > 0 && (kTC || mbar_wait_bounded(a_bar, 0, &g_gemv_error))) {
+    } else if (items > 0 && mbar_wait_bounded(a_bar, 0, &g_gemv_error)) {
         const float* a_cta = A + static_cast<int64_t>(u0) * kUnitElems;  // CTA's first k
         if constexpr (kTC) {
-            // B fragments of the CTA's k-range, built once by the consumer warps.
-            build_bfrag<M>(a_cta, g.K, nu * 16, bfrag, threadIdx.x, W * 32);
+            // B fragments of the CTA's k-range: one warp per unit, in place.
+            for (int j = warp; j < nu; j += W)
+                convert_unit_inplace<M>(reinterpret_cast<uint8_t*>(bfrag) + j * M * 1024, lane);
             asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
         }
         // Consumers: tile i (row group i / nu, unit i % nu) goes to warp i % W.
@@ -536,22 +559,25 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
                 for (int q = 0; q < (kTC ? 8 : M); ++q) acc[q] = 0.f;
                 cur = r;
             }
-            const int st = r % g.stages;
+            const int c = i / uc;  // chunk (items of a chunk are consecutive)
+            const int jc = i - c * uc;
+            const int st = c % g.stages;
             bool issued = false;
             for (uint32_t poll = 0; poll < kMaxWaitPolls; ++poll) {
-                if (seq[st] == r) {
+                if (seq[st] == c) {
                     issued = true;
                     break;
                 }
+                __nanosleep(32);
             }
             if (!issued) atomicOr(&g_gemv_error, kErrWaitTimeout);
-            if (issued && mbar_wait_bounded(&full[st], (r / g.stages) & 1, &g_gemv_error)) {
+            if (issued && mbar_wait_bounded(&full[st], (c / g.stages) & 1, &g_gemv_error)) {
                 const uint8_t* base = ring + st * stage_bytes;
-                // Start of unit j of tile row `row` in this stage.
+                // Start of the tile's unit (jc of this stage) in tile row `row`.
                 auto row_unit = [&](int row) -> const uint8_t* {
-                    return (j < g.box0)
-                               ? base + (row * g.box0 + j) * kUnitBytes
-                               : base + kTileBytes * g.box0 + (row * box1 + (j - g.box0)) * kUnitBytes;
+                    return (jc < g.box0)
+                               ? base + (row * g.box0 + jc) * kUnitBytes
+                               : base + kTileBytes * g.box0 + (row * box1 + (jc - g.box0)) * kUnitBytes;
                 };
                 if constexpr (kTC) {
                     const int gq = lane >> 2;
@@ -580,6 +606,16 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
                 float v = 0.f;
                 for (int q = 0; q < slots; ++q) v += partial[((r * slots + q) * M + m) * 32 + lane];
                 tot[m] = v;
+            }
+            if (row < g.N) {
+                const uint8_t* row_blocks =
+                    g.wq + (static_cast<int64_t>(row) * g.U + u0) * kUnitBytes;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    if (!isfinite(tot[m]))
+                        tot[m] = row_range_exact(row_blocks, nu * 8,
+                                                 A + m * g.K + static_cast<int64_t>(u0) * kUnitElems);
+                }
             }
             if (g.S == 1) {
                 if (row < g.N) {
@@ -665,9 +701,9 @@ cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     return cudaSuccess;
 }
 
-int64_t smem_bytes(int M, bool tc, int W, int stages, int nu, int rpg) {
+int64_t smem_bytes(int M, bool tc, int W, int stages, int uc, int nu, int rpg) {
     (void)tc;  // f32 activations and B fragments take the same space
-    return static_cast<int64_t>(stages) * kTileBytes * nu +
+    return static_cast<int64_t>(stages) * kTileBytes * uc +
            static_cast<int64_t>(M) * nu * kUnitElems * 4 +
            static_cast<int64_t>(rpg) * std::min(nu, W) * M * 32 * 4 + (2 * stages + 1) * 8 +
            stages * 4;
@@ -702,34 +738,48 @@ bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& de
         const int G = std::max(1, P / S);
         const int64_t rpg = std::min<int64_t>((RG + G - 1) / G, kMaxRowGroupsPerCta);
         const int64_t g_used = (RG + rpg - 1) / rpg;
-        int stages = 4;
-        while (stages > 1 &&
-               smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
-            --stages;
-        if (smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)) > dev.max_smem_optin) continue;
-        if (stages < 2 && rpg > 1) continue;
+        // Stage = 32 rows x uc units.  Halve uc while the stage stays at least
+        // kMinStageBytes and the ring would hold fewer than four stages, so
+        // more copies stay in flight and refills start sooner.
+        int uc = nu;
+        auto fit = [&](int u) {
+            int st = 8;
+            while (st > 1 && smem_bytes(M, tc, W, st, u, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
+                --st;
+            return smem_bytes(M, tc, W, st, u, nu, static_cast<int>(rpg)) <= dev.max_smem_optin ? st : 0;
+        };
+        int stages = fit(uc);
+        while (uc % 2 == 0 && static_cast<int64_t>(kTileBytes) * (uc / 2) >= kMinStageBytes &&
+               stages < 4 && fit(uc / 2) > stages) {
+            uc /= 2;
+            stages = fit(uc);
+        }
+        if (stages == 0) continue;
+        if (stages < 2 && rpg * (nu / uc) > 1) continue;
         if (S > 1 && (RG * S * M * 32 > static_cast<int64_t>(ws.part_floats) ||
                       RG > static_cast<int64_t>(ws.ctr_count)))
             continue;
         const int64_t waves = (g_used * S + P - 1) / P;
         const int64_t cost = rpg * nu * waves;
-        const int big = (static_cast<int64_t>(kTileBytes) * nu >= kMinStageBytes) ? 1 : 0;
+        const int big = (static_cast<int64_t>(kTileBytes) * uc >= kMinStageBytes) ? 1 : 0;
         if (cost < best[big]) {
             best[big] = cost;
             GemvGrid& c = cand[big];
+            c.wq = nullptr;
             c.N = static_cast<int>(N);
             c.K = K;
             c.U = U;
             c.RG = static_cast<int>(RG);
             c.S = S;
             c.nu = nu;
-            c.box0 = first_box(nu);
+            c.uc = uc;
+            c.box0 = first_box(uc);
             c.rpg = static_cast<int>(rpg);
             c.stages = stages;
             c.part = ws.part;
             c.ctr = ws.ctr;
             cgrid[big] = static_cast<int>(g_used * S);
-            csmem[big] = static_cast<int>(smem_bytes(M, tc, W, stages, nu, static_cast<int>(rpg)));
+            csmem[big] = static_cast<int>(smem_bytes(M, tc, W, stages, uc, nu, static_cast<int>(rpg)));
         }
     }
     const int pick = (best[1] != INT64_MAX) ? 1 : 0;
@@ -737,7 +787,7 @@ bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& de
     *g = cand[pick];
     *grid = cgrid[pick];
     *smem = csmem[pick];
-    return g->box0 <= 255 && g->nu - g->box0 <= 255;
+    return g->box0 <= 255 && g->uc - g->box0 <= 255;
 }
 
 // Whether the persistent kernel can take this operand layout at all.
@@ -760,6 +810,7 @@ cudaError_t launch_persistent(const float* A, const uint8_t* wq, float* C, int64
     int grid = 0, smem = 0;
     if (!plan_grid(M, kTC, consumer_warps<M, kTC>(), N, K, dev, ws, &g, &grid, &smem))
         return cudaSuccess;
+    g.wq = wq;
     cudaError_t err = ensure_smem_attr<M, kTC>(dev, smem);
     if (err != cudaSuccess) return err;
     if (clear_counters && g.S > 1) {
@@ -773,15 +824,25 @@ cudaError_t launch_persistent(const float* A, const uint8_t* wq, float* C, int64
     const int64_t strides[2] = {kUnitBytes, units * kUnitBytes};
     CUtensorMap map0, map1;
     const int box_a[3] = {kUnitBytes, g.box0, kRowsPerTile};
-    err = encode_tiled_u8(&map0, wq, 3, dims, strides, box_a);
+    err = encode_tiled(&map0, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, dims, strides, box_a);
     if (err != cudaSuccess) return err;
     map1 = map0;
-    if (g.nu > g.box0) {
-        const int box_b[3] = {kUnitBytes, g.nu - g.box0, kRowsPerTile};
-        err = encode_tiled_u8(&map1, wq, 3, dims, strides, box_b);
+    if (g.uc > g.box0) {
+        const int box_b[3] = {kUnitBytes, g.uc - g.box0, kRowsPerTile};
+        err = encode_tiled(&map1, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, dims, strides, box_b);
         if (err != cudaSuccess) return err;
     }
-    gemv_q4_0_persistent<M, kTC><<<grid, cta_threads<M, kTC>(), smem, stream>>>(map0, map1, A, C, g);
+    CUtensorMap amap = map0;
+    if constexpr (kTC) {
+        // The activations as f32 [M][K]; boxes of M rows x 256 k.
+        const int64_t adims[2] = {K, M};
+        const int64_t astrides[1] = {K * 4};
+        const int abox[2] = {kUnitElems, M};
+        err = encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
+        if (err != cudaSuccess) return err;
+    }
+    gemv_q4_0_persistent<M, kTC><<<grid, cta_threads<M, kTC>(), smem, stream>>>(map0, map1, amap, A,
+                                                                                 C, g);
     note_launch();
     *launched = true;
     return cudaGetLastError();

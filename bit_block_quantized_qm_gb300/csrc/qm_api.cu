@@ -106,11 +106,11 @@ cudaError_t current_device_info(DeviceInfo* out) {
     return cudaSuccess;
 }
 
-// Tiled TMA descriptor over bytes: `rank` dimensions (innermost first), the
-// byte strides of dimensions 1..rank-1 (multiples of 16), a box of box[d]
-// elements, zero fill outside the tensor.
-cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims,
-                            const int64_t* strides, const int* box) {
+// Tiled TMA descriptor: `rank` dimensions of `dtype` elements (innermost
+// first), the byte strides of dimensions 1..rank-1 (multiples of 16), a box
+// of box[d] elements, zero fill outside the tensor.
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                         const int64_t* dims, const int64_t* strides, const int* box) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -130,7 +130,7 @@ cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const 
         es[i] = 1;
         if (i > 0) st[i - 1] = static_cast<cuuint64_t>(strides[i - 1]);
     }
-    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d,
+    CUresult r = g_encode_tiled(map, dtype, rank, const_cast<void*>(base), d,
                                 st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;

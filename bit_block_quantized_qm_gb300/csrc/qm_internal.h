@@ -29,11 +29,11 @@ cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspa
 // Cached properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo* out);
 
-// Tiled TMA descriptor over bytes: `rank` dimensions (innermost first), the
-// byte strides of dimensions 1..rank-1 (multiples of 16), a box of box[d]
-// elements, zero fill outside the tensor.
-cudaError_t encode_tiled_u8(CUtensorMap* map, const void* base, int rank, const int64_t* dims,
-                            const int64_t* strides, const int* box);
+// Tiled TMA descriptor: `rank` dimensions of `dtype` elements (innermost
+// first), the byte strides of dimensions 1..rank-1 (multiples of 16), a box
+// of box[d] elements, zero fill outside the tensor.
+cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
+                         const int64_t* dims, const int64_t* strides, const int* box);
 
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
