@@ -55,6 +55,35 @@ def measured_peaks() -> dict:
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+KERNEL_SOURCES = {"dequant_q4_0": "dequant.cu", "gemv_q4_0": "gemv.cu"}
+
+
+def source_digest(kernel: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "bit_block_quantized_qm_gb300", "csrc", KERNEL_SOURCES[kernel])
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or
+    None when there is none for this kernel and workload, or when the
+    kernel's source changed after the counters were taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    digest = source_digest(kernel)
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            fields = dict(kv.split("=", 1) for kv in line.split())
+            if (fields.get("kernel") == kernel and fields.get("workload") == workload and
+                    fields.get("source_sha256_16") == digest):
+                return int(fields["dram_bytes_per_launch"])
+    return None
+
+
 def step_cases():
     cases = synth.workload(1)
     up = next(c for c in cases if c.name == "gemv_m8_k4096_n14336")
@@ -413,17 +442,23 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         achieved = paths["dequant"]["alg_gbs"]
         roofline = {"bound": "hbm", "kernel": "dequant_q4_0", "achieved": achieved,
                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": None, "peak_source": peaks["source"],
+                    "traffic": measured_traffic("dequant_q4_0", deq.name),
+                    "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": dequant_bytes(deq)}
     else:
         c = up if dominant == "gemv_up" else down
         achieved = paths[dominant]["alg_gbs"]
         roofline = {"bound": "hbm", "kernel": "gemv_q4_0 (" + dominant + ")",
                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": None, "peak_source": peaks["source"],
+                    "frac": achieved / hbm, "traffic": measured_traffic("gemv_q4_0", c.name),
+                    "peak_source": peaks["source"],
                     "algorithmic_bytes_per_launch": gemv_bytes(c),
                     "alu_tflops": paths[dominant]["tflops"], "fp32_peak_tflops_max_clock":
                     fp32_peak_max, "fp32_peak_tflops_live_clock": fp32_peak_live}
+
+    prefill = None
+    if not args.no_prefill:
+        prefill = prefill_leg(qm, dev, stream, fp32_peak_max, fp32_peak_live, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -440,6 +475,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
+        "prefill": prefill,
         "clocks": clocks,
         "hbm_peak_gbs": hbm, "peak_source": peaks["source"],
     }
@@ -451,6 +487,47 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         dist.destroy_process_group()
 
 
+def prefill_leg(qm, dev, stream, fp32_peak_max, fp32_peak_live, peaks) -> dict:
+    """Prefill throughput: one decoder layer's seven projections (hidden 4096,
+    grouped-query attention) at M = 512, through qm_matmul_q4_0, timed with
+    CUDA events over several passes after warm-up.  Reported as TFLOP/s
+    (2*M*N*K) and as a fraction of the FP32 FMA peak at the maximum and at
+    the sampled SM clock."""
+    import torch
+    cases = [c for c in synth.workload(4, layers=1, sweep_m=(512,))]
+    sh = int(stream.cuda_stream)
+    bufs = []
+    for c in cases:
+        bufs.append((torch.from_numpy(c.acts()).to(dev), torch.from_numpy(c.weights()).to(dev),
+                     torch.empty((c.M, c.N), dtype=torch.float32, device=dev), c))
+    flops = sum(2.0 * c.M * c.N * c.K for c in cases)
+
+    def one_pass():
+        for a, w, o, c in bufs:
+            rc = qm.qm_matmul_q4_0_ptr(a.data_ptr(), w.data_ptr(), o.data_ptr(), c.M, c.N, c.K, sh)
+            if rc != qm.QM_OK:
+                raise RuntimeError(f"prefill {c.name}: {qm.qm_status_string(rc)}")
+
+    for _ in range(3):
+        one_pass()
+    torch.cuda.synchronize()
+    passes = 5
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(passes):
+        one_pass()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / passes
+    tflops = flops / (ms * 1e-3) / 1e12
+    return {"workload": "decoder layer (q,k,v,o,gate,up,down) at M=512, hidden 4096",
+            "ms_per_layer": ms, "tflops": tflops, "roofline": {
+                "bound": "fp32_fma", "peak_tflops_max_clock": fp32_peak_max,
+                "frac_max_clock": tflops / fp32_peak_max,
+                "peak_tflops_live_clock": fp32_peak_live,
+                "frac_live_clock": (tflops / fp32_peak_live) if fp32_peak_live else None}}
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -459,6 +536,8 @@ def main(argv=None) -> None:
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip the CPU oracle timing (for profiler runs)")
+    p.add_argument("--no-prefill", action="store_true",
+                   help="skip the M=512 prefill report (for profiler runs)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
