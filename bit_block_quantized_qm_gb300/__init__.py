@@ -29,7 +29,8 @@ __all__ = [
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
-    "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "EXPORTED_SYMBOLS",
+    "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
+    "EXPORTED_SYMBOLS",
 ]
 
 QM_OK = 0
@@ -47,6 +48,7 @@ QM_ALGO_AUTO = 0
 QM_ALGO_GEMV = 1
 QM_ALGO_GEMM_SIMT = 2
 QM_ALGO_GEMV_SIMT = 3
+QM_ALGO_GEMM_TC = 4
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32

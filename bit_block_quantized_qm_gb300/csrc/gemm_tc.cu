@@ -1,0 +1,438 @@
+// Prefill GEMM on 5th-generation tensor cores (tcgen05, sm_103a):
+// C[M][N] = A[M][K] x dequant(W)^T, W a Q4_0 block stream (section
+// "matmul_q4_0_tiled" of "fuel-vulkan-kernels — quantized (GGML) kernel
+// contracts": tiles of the weight are decoded once and reused over many
+// activation rows).
+//
+// Exactness of the split-precision products:
+//   * a weight (q - 8) * d has at most 4 + 11 significant bits, so it is
+//     exactly W_hi + W_lo with W_hi = bf16(W), W_lo = bf16(W - W_hi);
+//   * an activation a is a_hi + a_lo + r with a_hi = bf16(a),
+//     a_lo = bf16(a - a_hi), |r| <= 2^-18 |a|;
+//   * D += a_hi W_hi + a_hi W_lo + a_lo W_hi; the dropped a_lo W_lo and r
+//     terms are at most 2^-17 |a W| together.  bf16 x bf16 products are exact
+//     in the f32 accumulator.
+//
+// Structure (one 128 x 128 output tile per CTA, K in 64-wide steps):
+//   * a pre-pass splits A once into bf16 hi / lo matrices (workspace);
+//   * warp 0 (one thread) streams, with TMA, the hi / lo activation tiles
+//     (128 rows x 64 k, 128-byte swizzle, 3 stages) and the weight's raw
+//     Q4_0 units (128 rows x 8 blocks, 2 stages);
+//   * warps 2..9 decode each 128 x 64 weight tile into W_hi / W_lo, written
+//     in the same swizzled K-major layout (2 stages), then run the epilogue;
+//   * warp 1 owns the TMEM accumulator (128 lanes x 128 f32 columns) and one
+//     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16) per k-step,
+//     committing completion to the stages' "empty" barriers;
+//   * the epilogue reads TMEM with tcgen05.ld (each warp its 32-lane quarter)
+//     and writes C.  An entry that comes out infinite or NaN is recomputed
+//     element by element from A and the Q4_0 stream, so non-finite scales
+//     keep the per-element semantics.
+// Every wait is bounded; a wait that gives up sets the device error word.
+#include <algorithm>
+
+#include "qm_device.cuh"
+#include "qm_internal.h"
+
+namespace qm {
+
+__device__ unsigned int g_gemm_error = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+constexpr int kAStages = 3;
+constexpr int kWStages = 2;
+constexpr int kRawStages = 2;
+constexpr int kDecodeWarps = 8;
+constexpr int kThreads = (2 + kDecodeWarps) * 32;
+constexpr int kTile = BM * BK * 2;    // one bf16 operand tile: 16 KB (BM == BN)
+constexpr int kRawBytes = BN * 144;   // one Q4_0 unit (8 blocks) of BN rows
+constexpr int kTmemCols = BN;         // f32 accumulator columns
+constexpr int kSmemBytes = (kAStages * 2 + kWStages * 2) * kTile + kRawStages * kRawBytes +
+                           16 * 8 + 1024;  // + barriers, TMEM slot, alignment slack
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
+// N = BN, M = BM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle (rows of 128 B,
+// 8-row atoms 1024 B apart), start address in 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset: one 8-row atom
+    d |= static_cast<uint64_t>(1) << 46;            // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// Decode one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared memory)
+// into 32 weights, split them into bf16 hi / lo pieces and store both as
+// row n, k = 32 * half .. 32 * half + 31 of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void decode_block_to_tiles(const uint8_t* blk, int n, int half,
+                                                      uint8_t* tile_hi, uint8_t* tile_lo) {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
+    const float d = f16_bits_to_float(h[0]);
+    uint32_t qb[4];  // quant bytes 0..15, four per word
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        qb[i] = static_cast<uint32_t>(h[1 + 2 * i]) | (static_cast<uint32_t>(h[2 + 2 * i]) << 16);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {  // 16-byte chunk c of this block's 64 bytes: k = 8c .. 8c+7
+        float w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int j = 8 * c + e;  // element of the block
+            const int byte = j & 15;
+            const uint32_t b = (qb[byte >> 2] >> (8 * (byte & 3))) & 0xFFu;
+            const uint32_t nib = (j < 16) ? (b & 0xFu) : (b >> 4);
+            w[e] = magic_minus8(nib | kMagicBits) * d;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float h0 = __bfloat162float(__float2bfloat16_rn(w[2 * e]));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(w[2 * e + 1]));
+            hi[e] = pack_bf16(h0, h1);
+            const float r0 = w[2 * e] - h0, r1 = w[2 * e + 1] - h1;
+            lo[e] = pack_bf16(isfinite(r0) ? r0 : 0.f, isfinite(r1) ? r1 : 0.f);
+        }
+        const int chunk = 4 * half + c;
+        const int off = n * 128 + ((chunk ^ (n & 7)) << 4);
+        *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// Exact C[m][n] for an entry whose tensor-core sum is not finite:
+// sum_k A[m][k] * ((q - 8) * d) element by element.
+__device__ __noinline__ float entry_exact(const float* __restrict__ A, const uint8_t* __restrict__ wq,
+                                          int64_t K, int64_t m, int64_t n) {
+    const int64_t nb = K / kBlockElems;
+    const uint8_t* row = wq + n * nb * kBlockBytes;
+    const float* a = A + m * K;
+    float s = 0.f;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t* blk = row + b * kBlockBytes;
+        const float d = f16_bits_to_float(static_cast<uint32_t>(blk[0]) |
+                                          (static_cast<uint32_t>(blk[1]) << 8));
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t byte = blk[2 + (j & 15)];
+            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+            s = fmaf(a[b * 32 + j], magic_minus8(nib | kMagicBits) * d, s);
+        }
+    }
+    return s;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_ahi,
+                 const __grid_constant__ CUtensorMap map_alo,
+                 const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
+                 const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* a_st = base;                                // [kAStages][hi, lo][16 KB]
+    uint8_t* w_st = a_st + kAStages * 2 * kTile;         // [kWStages][hi, lo][16 KB]
+    uint8_t* raw = w_st + kWStages * 2 * kTile;          // [kRawStages][128 rows][144 B]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRawBytes);
+    uint64_t* a_full = bars;
+    uint64_t* a_empty = bars + kAStages;
+    uint64_t* w_full = bars + 2 * kAStages;
+    uint64_t* w_empty = w_full + kWStages;
+    uint64_t* raw_full = w_empty + kWStages;
+    uint64_t* raw_empty = raw_full + kRawStages;
+    uint64_t* acc_full = raw_empty + kRawStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m0 = static_cast<int>(blockIdx.y) * BM;
+    const int n0 = static_cast<int>(blockIdx.x) * BN;
+    const int KT = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&a_full[s], 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int s = 0; s < kWStages; ++s) {
+            mbar_init(&w_full[s], kDecodeWarps);
+            mbar_init(&w_empty[s], 1);
+        }
+        for (int s = 0; s < kRawStages; ++s) {
+            mbar_init(&raw_full[s], 1);
+            mbar_init(&raw_empty[s], kDecodeWarps);
+        }
+        mbar_init(acc_full, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_addr(tmem_slot)),
+            "r"(kTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // Producer: raw weight units (one per 4 k-steps) and activation tiles.
+            prefetch_tensormap(&map_ahi);
+            prefetch_tensormap(&map_alo);
+            prefetch_tensormap(&map_w);
+            for (int kt = 0; kt < KT; ++kt) {
+                if ((kt & 3) == 0) {
+                    const int u = kt >> 2;
+                    const int rs = u % kRawStages;
+                    if (u >= kRawStages &&
+                        !mbar_wait_bounded(&raw_empty[rs], ((u / kRawStages) - 1) & 1, &g_gemm_error))
+                        break;
+                    mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
+                    tma_load_3d(raw + rs * kRawBytes, &map_w, 0, u, n0, &raw_full[rs]);
+                }
+                const int as = kt % kAStages;
+                if (kt >= kAStages &&
+                    !mbar_wait_bounded(&a_empty[as], ((kt / kAStages) - 1) & 1, &g_gemm_error))
+                    break;
+                mbar_arrive_expect_tx(&a_full[as], 2 * kTile);
+                tma_load_2d(a_st + (2 * as) * kTile, &map_ahi, kt * BK, m0, &a_full[as]);
+                tma_load_2d(a_st + (2 * as + 1) * kTile, &map_alo, kt * BK, m0, &a_full[as]);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer: 3 pieces x 4 k-steps of 16 per 64-wide k-step.
+            bool ok = true;
+            for (int kt = 0; kt < KT && ok; ++kt) {
+                const int as = kt % kAStages;
+                const int ws = kt % kWStages;
+                ok = mbar_wait_bounded(&a_full[as], (kt / kAStages) & 1, &g_gemm_error) &&
+                     mbar_wait_bounded(&w_full[ws], (kt / kWStages) & 1, &g_gemm_error);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ahi = smem_addr(a_st + (2 * as) * kTile);
+                const uint32_t alo = ahi + kTile;
+                const uint32_t whi = smem_addr(w_st + (2 * ws) * kTile);
+                const uint32_t wlo = whi + kTile;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint32_t off = kk * 32;  // 16 bf16 along K
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), (kt | kk) != 0);
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), 1u);
+                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), 1u);
+                }
+                mma_commit(&a_empty[as]);
+                mma_commit(&w_empty[ws]);
+            }
+            mma_commit(acc_full);
+        }
+    } else {
+        // Decode warps: thread t of 256 owns weight row t / 2 and block half t % 2
+        // of each 64-wide k-step.
+        const int dt = threadIdx.x - 64;
+        const int n = dt >> 1;
+        const int half = dt & 1;
+        bool ok = true;
+        for (int kt = 0; kt < KT && ok; ++kt) {
+            const int u = kt >> 2;
+            const int sub = kt & 3;
+            const int rs = u % kRawStages;
+            const int ws = kt % kWStages;
+            if (sub == 0) ok = mbar_wait_bounded(&raw_full[rs], (u / kRawStages) & 1, &g_gemm_error);
+            if (ok && kt >= kWStages)
+                ok = mbar_wait_bounded(&w_empty[ws], ((kt / kWStages) - 1) & 1, &g_gemm_error);
+            if (!ok) break;
+            const uint8_t* blk = raw + rs * kRawBytes + n * 144 + (2 * sub + half) * kBlockBytes;
+            decode_block_to_tiles(blk, n, half, w_st + (2 * ws) * kTile, w_st + (2 * ws + 1) * kTile);
+            fence_proxy_async_shared();  // make the tiles visible to the tensor cores
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_full[ws]);
+            if (sub == 3) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[rs]);
+            }
+        }
+        // Epilogue: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4.
+        if (mbar_wait_bounded(acc_full, 0, &g_gemm_error)) {
+            tc_fence_after();
+            const int q = warp & 3;
+            const int ch = (warp - 2) >> 2;
+            const int m = m0 + 32 * q + lane;
+#pragma unroll
+            for (int cb = 0; cb < 2; ++cb) {
+                const int col = 64 * ch + 32 * cb;
+                float v[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+                if (m < M) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int nn = n0 + col + i;
+                        if (nn < N) {
+                            float x = v[i];
+                            if (!isfinite(x)) x = entry_exact(A, wq, K, m, nn);
+                            C[static_cast<int64_t>(m) * N + nn] = x;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// A f32 -> bf16 hi = bf16(a), lo = bf16(a - hi) (lo = 0 where a - hi is not finite).
+__global__ void __launch_bounds__(256)
+    split_bf16(const float4* __restrict__ a, uint2* __restrict__ hi, uint2* __restrict__ lo,
+               int64_t n4) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 v = __ldg(a + i);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        float h[4], l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            h[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
+            const float r = x[j] - h[j];
+            l[j] = isfinite(r) ? r : 0.f;
+        }
+        hi[i] = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
+        lo[i] = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+    }
+}
+
+}  // namespace
+
+bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, int64_t K) {
+    return M >= 1 && N >= 1 && (K % 256) == 0 && K > 0 && K <= (int64_t(1) << 24) &&
+           M <= (int64_t(65535) * BM) && N <= (int64_t(1) << 30) &&
+           (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
+}
+
+cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
+                                int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+    // bf16 hi / lo copies of A in the stream's prefill workspace.
+    const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
+    void* ws = nullptr;
+    cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes, &ws);
+    if (err != cudaSuccess) return err;
+    auto* a_hi = static_cast<uint8_t*>(ws);
+    auto* a_lo = a_hi + piece_bytes;
+    const int64_t n4 = M * K / 4;
+    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8);
+    split_bf16<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
+        reinterpret_cast<uint2*>(a_lo), n4);
+    note_launch();
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    CUtensorMap map_ahi, map_alo, map_w;
+    const int64_t adims[2] = {K, M};
+    const int64_t astrides[1] = {K * 2};
+    const int abox[2] = {BK, BM};
+    err = encode_tiled(&map_ahi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a_hi, 2, adims, astrides, abox,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    err = encode_tiled(&map_alo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a_lo, 2, adims, astrides, abox,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (err != cudaSuccess) return err;
+    const int64_t units = K / 256;
+    const int64_t wdims[3] = {144, units, N};
+    const int64_t wstrides[2] = {144, units * 144};
+    const int wbox[3] = {144, 1, BN};
+    err = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, wdims, wstrides, wbox);
+    if (err != cudaSuccess) return err;
+
+    static int configured[64] = {0};
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
+        err = cudaFuncSetAttribute(gemm_q4_0_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kSmemBytes);
+        if (err != cudaSuccess) return err;
+        __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
+    }
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
+    gemm_q4_0_tc<<<grid, kThreads, kSmemBytes, stream>>>(map_ahi, map_alo, map_w, A, wq, C,
+                                                         static_cast<int>(M), static_cast<int>(N),
+                                                         static_cast<int>(K));
+    note_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t gemm_tc_read_device_error(unsigned int* bits, bool clear) {
+    unsigned int v = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(&v, g_gemm_error, sizeof(v));
+    if (err != cudaSuccess) return err;
+    *bits |= v;
+    if (clear && v != 0) {
+        const unsigned int zero = 0;
+        err = cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero));
+    }
+    return err;
+}
+
+}  // namespace qm

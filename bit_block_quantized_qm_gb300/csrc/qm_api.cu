@@ -32,6 +32,14 @@ struct WorkspaceEntry {
 std::vector<WorkspaceEntry> g_workspaces;
 std::mutex g_ws_mutex;
 
+struct PrefillEntry {
+    int device;
+    cudaStream_t stream;
+    void* ptr;
+    size_t bytes;
+};
+std::vector<PrefillEntry> g_prefill;
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 uint64_t g_launches = 0;
 std::once_flag g_encode_once;
@@ -62,6 +70,37 @@ cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspa
     }
     g_workspaces.push_back({dev.device, stream, ws});
     *out = ws;
+    return cudaSuccess;
+}
+
+cudaError_t prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    PrefillEntry* e = nullptr;
+    for (PrefillEntry& x : g_prefill) {
+        if (x.device == dev.device && x.stream == stream) e = &x;
+    }
+    if (e && e->bytes >= bytes) {
+        *out = e->ptr;
+        return cudaSuccess;
+    }
+    if (e) {
+        // Earlier work on this stream may still read the old buffer.
+        cudaError_t err = cudaStreamSynchronize(stream);
+        if (err != cudaSuccess) return err;
+        cudaFree(e->ptr);
+        e->ptr = nullptr;
+        e->bytes = 0;
+    }
+    void* p = nullptr;
+    cudaError_t err = cudaMalloc(&p, bytes);
+    if (err != cudaSuccess) return err;
+    if (e) {
+        e->ptr = p;
+        e->bytes = bytes;
+    } else {
+        g_prefill.push_back({dev.device, stream, p, bytes});
+    }
+    *out = p;
     return cudaSuccess;
 }
 
@@ -110,7 +149,8 @@ cudaError_t current_device_info(DeviceInfo* out) {
 // first), the byte strides of dimensions 1..rank-1 (multiples of 16), a box
 // of box[d] elements, zero fill outside the tensor.
 cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
-                         const int64_t* dims, const int64_t* strides, const int* box) {
+                         const int64_t* dims, const int64_t* strides, const int* box,
+                         CUtensorMapSwizzle swizzle) {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -131,7 +171,7 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void
         if (i > 0) st[i - 1] = static_cast<cuuint64_t>(strides[i - 1]);
     }
     CUresult r = g_encode_tiled(map, dtype, rank, const_cast<void*>(base), d,
-                                st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -181,7 +221,7 @@ int from_cuda(cudaError_t err) { return err == cudaSuccess ? QM_OK : QM_ERR_CUDA
 int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
                 int algo, void* stream) {
     if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QM_ERR_SHAPE;
-    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMV_SIMT) return QM_ERR_SHAPE;
+    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMM_TC) return QM_ERR_SHAPE;
     int64_t a_elems, c_elems, w_elems, a_bytes, c_bytes, w_bytes;
     if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, &a_bytes) || !mul_ok(M, N, &c_elems) ||
         !mul_ok(c_elems, 4, &c_bytes) || !mul_ok(N, K / 32, &w_elems) ||
@@ -210,11 +250,19 @@ int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, 
     const uint8_t* w = static_cast<const uint8_t*>(wq);
     // Measured on GB300: at M = 1 the FP32 decode issues fewer instructions
     // per weight than the tensor-core one; from M = 2 on, tensor cores win.
-    if (algo == QM_ALGO_AUTO)
-        algo = (M == 1) ? QM_ALGO_GEMV_SIMT : (M <= 8 ? QM_ALGO_GEMV : QM_ALGO_GEMM_SIMT);
+    const bool tc_ok = qm::gemm_tc_supported(A, w, M, N, K);
+    if (algo == QM_ALGO_AUTO) {
+        if (M == 1) algo = QM_ALGO_GEMV_SIMT;
+        else if (M <= 8) algo = QM_ALGO_GEMV;
+        else algo = tc_ok ? QM_ALGO_GEMM_TC : QM_ALGO_GEMM_SIMT;
+    }
     if (algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT)
         return from_cuda(qm::launch_gemv_q4_0(A, w, C, static_cast<int>(M), N, K, s, dev,
                                               algo == QM_ALGO_GEMV));
+    if (algo == QM_ALGO_GEMM_TC) {
+        if (!tc_ok) return QM_ERR_UNSUPPORTED;
+        return from_cuda(qm::launch_gemm_q4_0_tc(A, w, C, M, N, K, s, dev));
+    }
     return from_cuda(qm::launch_gemm_q4_0_simt(A, w, C, M, N, K, s, dev));
 }
 
@@ -306,6 +354,7 @@ int qm_device_status(void* stream, int clear) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QM_ERR_CUDA;
     unsigned int bits = 0;
     if (qm::gemv_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
+    if (qm::gemm_tc_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (bits && clear) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || qm::reset_workspaces(dev) != cudaSuccess)

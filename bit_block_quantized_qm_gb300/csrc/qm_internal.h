@@ -33,7 +33,8 @@ cudaError_t current_device_info(DeviceInfo* out);
 // first), the byte strides of dimensions 1..rank-1 (multiples of 16), a box
 // of box[d] elements, zero fill outside the tensor.
 cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, int rank,
-                         const int64_t* dims, const int64_t* strides, const int* box);
+                         const int64_t* dims, const int64_t* strides, const int* box,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE);
 
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
@@ -49,6 +50,17 @@ cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M,
 // array's address.
 cudaError_t launch_gemv_q4_0_noalloc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                      int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+
+// Growable scratch of the prefill GEMM (bf16 pieces of A), one per (device,
+// stream).  Growing it synchronizes the stream first (the old buffer may
+// still be in use by earlier work on it).
+cudaError_t prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out);
+
+// Prefill GEMM on tcgen05 tensor cores: K % 256 == 0, 16-byte aligned A and wq.
+bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
+                                int64_t K, cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t gemm_tc_read_device_error(unsigned int* bits, bool clear);
 
 // Prefill GEMM on FP32 FMA, any M >= 1.
 cudaError_t launch_gemm_q4_0_simt(const float* A, const uint8_t* wq, float* C, int64_t M,

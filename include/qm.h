@@ -26,6 +26,9 @@
  *     stream) on the current device, and results are visible once that
  *     stream has been synchronized; no entry point but qm_device_status
  *     synchronizes.  Calls are thread-safe.
+ *   - Memory: the prefill GEMM on tensor cores keeps bf16 copies of A (4 bytes
+ *     per element of A) in a per-(device, stream) buffer that grows with
+ *     cudaMalloc as needed (growing synchronizes that stream once).
  *   - Memory: the GEMV (M <= 8) splits K over several CTAs when the matrix
  *     has few rows; their partial sums go through a workspace of about 8 MB
  *     that the library allocates with cudaMalloc on the first such call on
@@ -74,6 +77,8 @@ extern "C" {
 #define QM_ALGO_GEMV 1      /* decode-regime GEMV, decode on tensor cores; M 1..8 */
 #define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
 #define QM_ALGO_GEMV_SIMT 3 /* decode-regime GEMV on FP32 FMA; M 1..8             */
+#define QM_ALGO_GEMM_TC 4   /* prefill GEMM on tcgen05 tensor cores (split bf16);
+                               needs K % 256 == 0 and 16-byte aligned A and wq  */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 QM_API int qm_version(void);

@@ -195,9 +195,35 @@ def test_gemv_misaligned_takes_generic_path(env, offs):
                  C_ref, S_ref)
 
 
+# Prefill GEMM on tcgen05 tensor cores: K % 256 == 0; M and N ragged against
+# the 128 x 128 tiles; K up to 14336 (long accumulations in TMEM).
+GEMM_TC = [(9, 7, 256), (128, 128, 256), (130, 257, 512), (1, 300, 768), (200, 130, 1024),
+           (64, 1000, 2048), (257, 129, 4096), (96, 64, 14336)]
+
+
+@pytest.mark.parametrize("shape", GEMM_TC, ids=lambda s: "x".join(map(str, s)))
+def test_gemm_tensor_cores(env, shape):
+    qm, o = env
+    M, N, K = shape
+    blob = synth.q4_0_weights(N, K, 3 * M + N)
+    A = synth.activations(M, K, 5 * M + K, dist="outliers")
+    C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC), C_ref, S_ref, "tcgen05")
+
+
+def test_gemm_tensor_cores_unsupported_layouts(env):
+    qm, o = env
+    A = torch.zeros((16, 96), device="cuda")
+    wq = torch.zeros(8 * 3 * 18, dtype=torch.uint8, device="cuda")
+    C = torch.zeros((16, 8), device="cuda")
+    rc = qm.qm_matmul_q4_0_algo_ptr(A.data_ptr(), wq.data_ptr(), C.data_ptr(), 16, 8, 96,
+                                    qm.QM_ALGO_GEMM_TC, 0)
+    assert rc == qm.QM_ERR_UNSUPPORTED  # K % 256 != 0
+
+
 def test_deterministic_repeat(env):
     qm, o = env
-    for (M, N, K) in ((1, 4096, 4096), (8, 1000, 14336), (64, 300, 2048)):
+    for (M, N, K) in ((1, 4096, 4096), (8, 1000, 14336), (64, 300, 2048), (300, 500, 4096)):
         blob = synth.q4_0_weights(N, K, 41)
         A = synth.activations(M, K, 42)
         C1 = matmul_gpu(qm, A, blob, N)
@@ -225,7 +251,7 @@ def test_nonfinite_scales(env):
     blob = blob.ravel()
     A = synth.activations(M, K, 52)
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
-    for algo in (qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT, qm.QM_ALGO_GEMM_SIMT):
+    for algo in (qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT, qm.QM_ALGO_GEMM_SIMT, qm.QM_ALGO_GEMM_TC):
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
 
 
