@@ -18,7 +18,7 @@
 //   * warp 0 (one thread) streams, with TMA, the hi / lo activation tiles
 //     (128 rows x 64 k, 128-byte swizzle, 3 stages) and the weight's raw
 //     Q4_0 units (128 rows x 8 blocks, 2 stages);
-//   * warps 2..9 decode each 128 x 64 weight tile into W_hi / W_lo, written
+//   * warps 2..17 decode each 128 x 64 weight tile into W_hi / W_lo, written
 //     in the same swizzled K-major layout (2 stages), then run the epilogue;
 //   * warp 1 owns the TMEM accumulator (128 lanes x 128 f32 columns) and one
 //     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16) per k-step,
@@ -45,7 +45,7 @@ constexpr int BK = 64;
 constexpr int kAStages = 3;
 constexpr int kWStages = 2;
 constexpr int kRawStages = 2;
-constexpr int kDecodeWarps = 8;
+constexpr int kDecodeWarps = 16;
 constexpr int kThreads = (2 + kDecodeWarps) * 32;
 constexpr int kTile = BM * BK * 2;    // one bf16 operand tile: 16 KB (BM == BN)
 constexpr int kRawBytes = BN * 144;   // one Q4_0 unit (8 blocks) of BN rows
@@ -115,38 +115,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
            (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
 }
 
-// Decode one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared memory)
-// into 32 weights, split them into bf16 hi / lo pieces and store both as
-// row n, k = 32 * half .. 32 * half + 31 of a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void decode_block_to_tiles(const uint8_t* blk, int n, int half,
-                                                      uint8_t* tile_hi, uint8_t* tile_lo) {
+// Decode half of one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared
+// memory): quant bytes 8p .. 8p+7, i.e. elements 8p .. 8p+7 (low nibbles) and
+// 16+8p .. 16+8p+7 (high nibbles).  Each weight (q - 8) * d is split into
+// bf16 hi = bf16(w) and lo = bf16(w - hi), an exact two-piece sum; both are
+// stored as row n of 128-byte-swizzled K-major tiles at k = 32 * half + j.
+// Non-finite scales need no care here: they make the output entry non-finite
+// and the epilogue recomputes it element by element.
+__device__ __forceinline__ void decode_half_block(const uint8_t* blk, int p, int n, int half,
+                                                  uint8_t* tile_hi, uint8_t* tile_lo) {
     const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
     const float d = f16_bits_to_float(h[0]);
-    uint32_t qb[4];  // quant bytes 0..15, four per word
+    const uint32_t w0 = static_cast<uint32_t>(h[1 + 4 * p]) | (static_cast<uint32_t>(h[2 + 4 * p]) << 16);
+    const uint32_t w1 = static_cast<uint32_t>(h[3 + 4 * p]) | (static_cast<uint32_t>(h[4 + 4 * p]) << 16);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        qb[i] = static_cast<uint32_t>(h[1 + 2 * i]) | (static_cast<uint32_t>(h[2 + 2 * i]) << 16);
+    for (int side = 0; side < 2; ++side) {  // 0: low nibbles, 1: high nibbles
+        const uint32_t v0 = (side ? (w0 >> 4) : w0) & 0x0F0F0F0Fu;
+        const uint32_t v1 = (side ? (w1 >> 4) : w1) & 0x0F0F0F0Fu;
+        float x[8];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {  // 16-byte chunk c of this block's 64 bytes: k = 8c .. 8c+7
-        float w[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * c + e;  // element of the block
-            const int byte = j & 15;
-            const uint32_t b = (qb[byte >> 2] >> (8 * (byte & 3))) & 0xFFu;
-            const uint32_t nib = (j < 16) ? (b & 0xFu) : (b >> 4);
-            w[e] = magic_minus8(nib | kMagicBits) * d;
+        for (int e = 0; e < 4; ++e) {
+            x[e] = magic_minus8(__byte_perm(v0, kMagicBits, 0x7540u + e)) * d;
+            x[4 + e] = magic_minus8(__byte_perm(v1, kMagicBits, 0x7540u + e)) * d;
         }
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float h0 = __bfloat162float(__float2bfloat16_rn(w[2 * e]));
-            const float h1 = __bfloat162float(__float2bfloat16_rn(w[2 * e + 1]));
-            hi[e] = pack_bf16(h0, h1);
-            const float r0 = w[2 * e] - h0, r1 = w[2 * e + 1] - h1;
-            lo[e] = pack_bf16(isfinite(r0) ? r0 : 0.f, isfinite(r1) ? r1 : 0.f);
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hb);
+            const float r0 = x[2 * e] - __uint_as_float(hw << 16);
+            const float r1 = x[2 * e + 1] - __uint_as_float(hw & 0xFFFF0000u);
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(r0, r1);
+            hi[e] = hw;
+            lo[e] = *reinterpret_cast<const uint32_t*>(&lb);
         }
-        const int chunk = 4 * half + c;
+        // Element 8p + e (side 0) or 16 + 8p + e (side 1) of the block sits in
+        // 16-byte chunk 4 * half + p + 2 * side of the 128-byte tile row.
+        const int chunk = 4 * half + p + 2 * side;
         const int off = n * 128 + ((chunk ^ (n & 7)) << 4);
         *reinterpret_cast<uint4*>(tile_hi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(tile_lo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -179,9 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_alo,
                  const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles, by indexing the shared array
+    // itself so the compiler keeps every access below in the shared space.
+    uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* a_st = base;                                // [kAStages][hi, lo][16 KB]
     uint8_t* w_st = a_st + kAStages * 2 * kTile;         // [kWStages][hi, lo][16 KB]
     uint8_t* raw = w_st + kWStages * 2 * kTile;          // [kRawStages][128 rows][144 B]
@@ -283,11 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(acc_full);
         }
     } else {
-        // Decode warps: thread t of 256 owns weight row t / 2 and block half t % 2
-        // of each 64-wide k-step.
+        // Decode warps: thread t of 512 owns weight row t / 4, block (t / 2) % 2
+        // of the 64-wide k-step and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
         const int dt = threadIdx.x - 64;
-        const int n = dt >> 1;
-        const int half = dt & 1;
+        const int n = dt >> 2;
+        const int half = (dt >> 1) & 1;
+        const int part = dt & 1;
         bool ok = true;
         for (int kt = 0; kt < KT && ok; ++kt) {
             const int u = kt >> 2;
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait_bounded(&w_empty[ws], ((kt / kWStages) - 1) & 1, &g_gemm_error);
             if (!ok) break;
             const uint8_t* blk = raw + rs * kRawBytes + n * 144 + (2 * sub + half) * kBlockBytes;
-            decode_block_to_tiles(blk, n, half, w_st + (2 * ws) * kTile, w_st + (2 * ws + 1) * kTile);
+            decode_half_block(blk, part, n, half, w_st + (2 * ws) * kTile, w_st + (2 * ws + 1) * kTile);
             fence_proxy_async_shared();  // make the tiles visible to the tensor cores
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_full[ws]);
@@ -308,15 +315,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
         }
-        // Epilogue: TMEM lane quarter = warp % 4, column half = (warp - 2) / 4.
+        // Epilogue: TMEM lane quarter = warp % 4, 32 columns per warp.
         if (mbar_wait_bounded(acc_full, 0, &g_gemm_error)) {
             tc_fence_after();
             const int q = warp & 3;
-            const int ch = (warp - 2) >> 2;
+            const int cq = (warp - 2) >> 2;  // 0..3
             const int m = m0 + 32 * q + lane;
 #pragma unroll
-            for (int cb = 0; cb < 2; ++cb) {
-                const int col = 64 * ch + 32 * cb;
+            for (int cb = 0; cb < (BN / 32) / (kDecodeWarps / 4); ++cb) {
+                const int col = 32 * (cq * ((BN / 32) / (kDecodeWarps / 4)) + cb);
                 float v[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
                 if (m < M) {
