@@ -4,6 +4,8 @@
 // contracts"; element j < 16 of a block is the low nibble of quant byte j,
 // element j + 16 its high nibble, value (nibble - 8) * d).
 //
+// This file holds the FP32 FMA kernels; the tensor-core GEMV is in gemv_tc.cu.
+//
 // Persistent kernel (K % 256 == 0, 16-byte aligned wq and A):
 //   * A "unit" is 8 consecutive blocks of one weight row: 144 bytes = 9
 //     aligned 16-byte words covering 256 k.  A "row group" is 32 rows.  The
@@ -45,11 +47,11 @@ constexpr int kUnitElems = 256;
 constexpr int kRowsPerTile = 32;  // one row per lane
 constexpr int kTileBytes = kUnitBytes * kRowsPerTile;
 // Consumer warps per CTA: as many as the registers of one CTA per SM allow.
-template <int M, bool kTC>
-__host__ __device__ constexpr int consumer_warps() { return M <= 4 ? 16 : (kTC ? 12 : 8); }
-template <int M, bool kTC>
+template <int M>
+__host__ __device__ constexpr int consumer_warps() { return M <= 4 ? 16 : 8; }
+template <int M>
 __host__ __device__ constexpr int cta_threads() {
-    return (consumer_warps<M, kTC>() + 1) * 32;  // + producer warp
+    return (consumer_warps<M>() + 1) * 32;  // + producer warp
 }
 constexpr int kMaxSplits = 16;  // at most 16 K ranges
 constexpr int kMaxRowGroupsPerCta = 16;
@@ -190,239 +192,6 @@ __device__ __forceinline__ void unit_dot(const uint8_t* tile_row, const float* _
     }
 }
 
-// ---------------------------------------------------------------------------
-// Tensor-core decode (mma.sync m16n8k16, bf16 operands, f32 accumulators).
-//
-// A (16 x 16, row-major) = weights: 16 rows of the tile x 16 k.  (q - 8) is
-// exact in bf16.  B (16 x 8) = activations: column c is a bf16 piece of one
-// activation row, hi = bf16(a) or lo = bf16(a - hi), so a - hi - lo is at
-// most 2^-18 |a| and every product is exact in f32.  Each lane scales its own
-// weight rows' accumulators by d once per block.
-//
-// Fragment layout (lane = 4 g + t): A regs {row g, k 2t..2t+1}, {row g+8, k
-// 2t..2t+1}, {row g, k 2t+8..2t+9}, {row g+8, k 2t+8..2t+9}; B regs {k
-// 2t..2t+1, col g}, {k 2t+8..2t+9, col g}; D {row g, col 2t}, {row g, col
-// 2t+1}, {row g+8, col 2t}, {row g+8, col 2t+1}.  The k order inside a block
-// is free as long as A and B agree: lane t takes quant bytes 4t..4t+3 of the
-// block, so for the block's two k-steps the fragment k pairs map to elements
-//   step 0: (4t, 4t+2) and (16+4t, 18+4t);  step 1: (4t+1, 4t+3) and (17+4t, 19+4t).
-//
-// Columns: for M <= 4 one MMA per k-step carries both pieces (column m = hi
-// of row m, column 4 + m = lo of row m); for M > 4 two MMAs per k-step, the
-// first with the hi pieces in columns 0..M-1 and the second with the lo pieces,
-// both into the same accumulators.
-
-template <int M>
-__host__ __device__ constexpr int tc_sets() { return M <= 4 ? 1 : 2; }
-
-__device__ __forceinline__ void mma_bf16_16816(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-        "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// (q - 8) as bf16 pairs from quant bytes 4t..4t+3 (Q, byte 4t lowest):
-// R0 = elements (4t, 4t+2), R1 = (16+4t, 18+4t), R2 = (4t+1, 4t+3), R3 = (17+4t, 19+4t).
-// A nibble under the bf16 exponent of 128 reads as 128 + q; subtracting 136
-// leaves q - 8, both steps exact.
-__device__ __forceinline__ void decode_bf16(uint32_t Q, uint32_t R[4]) {
-    constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
-    constexpr uint32_t kOne = 0x3F803F80u;    // bf16 1.0
-    constexpr uint32_t kBias = 0xC308C308u;   // bf16 -136.0
-    const uint32_t r[4] = {(Q & 0x000F000Fu) | kMagic, ((Q >> 4) & 0x000F000Fu) | kMagic,
-                           ((Q >> 8) & 0x000F000Fu) | kMagic, ((Q >> 12) & 0x000F000Fu) | kMagic};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(R[i]) : "r"(r[i]), "r"(kOne), "r"(kBias));
-}
-
-// Element indices (within a block) of the four fragment k values a lane with
-// quarter t holds at k-step h: pairs (e[0], e[1]) and (e[2], e[3]).
-__device__ __forceinline__ void step_elems(int t, int h, int e[4]) {
-    e[0] = 4 * t + h;
-    e[1] = 4 * t + 2 + h;
-    e[2] = 16 + 4 * t + h;
-    e[3] = 18 + 4 * t + h;
-}
-
-// Quant bytes 4t..4t+3 of a block at byte offset `off` of a 16-byte-aligned
-// row unit (off = 18 b): aligned for odd b, two halves for even b.
-__device__ __forceinline__ uint32_t quant_word(const uint8_t* unit, int b, int t) {
-    const uint8_t* p = unit + 18 * b + 2 + 4 * t;
-    if (b & 1) return *reinterpret_cast<const uint32_t*>(p);
-    return static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) |
-           (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p + 2)) << 16);
-}
-
-// B-fragment slot of column c for set p (NS = 2M slots per (k-step, t)); -1
-// when the column carries no activation row.
-template <int M>
-__device__ __forceinline__ int tc_slot(int c, int p) {
-    if constexpr (tc_sets<M>() == 1) {
-        if (c < 4) return c < M ? c : -1;
-        return (c - 4) < M ? M + (c - 4) : -1;
-    } else {
-        return c < M ? p * M + c : -1;
-    }
-}
-
-// (piece, activation row) of D column c in set p: piece 0 = hi, 1 = lo.
-template <int M>
-__device__ __forceinline__ void tc_col(int c, int& piece, int& m) {
-    if constexpr (tc_sets<M>() == 1) {
-        piece = c >= 4 ? 1 : 0;
-        m = c & 3;
-    } else {
-        piece = 0;  // both pieces accumulate into the same column
-        m = c;
-    }
-}
-
-// Turn one unit of staged activations, f32 [M][256] (as a TMA box of the
-// activation matrix lands), into that unit's B fragments in place:
-// entry (s * 2M + slot) * 4 + t = {b0, b1} for k-step s (16 k), lane quarter t
-// and slot (hi pieces of rows 0..M-1, then lo pieces).  The f32 values and the
-// fragments take the same 1 KB * M, so a warp reads everything into registers,
-// syncs, and overwrites.  Lanes of a half-warp later read 16 distinct 8-byte
-// entries: no bank conflicts.
-template <int M>
-__device__ __forceinline__ void convert_unit_inplace(uint8_t* unit, int lane) {
-    constexpr int kPerLane = 2 * M;  // (k-step, row, quarter) triples per lane
-    const float* f = reinterpret_cast<const float*>(unit);
-    float x[kPerLane][4];
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int tr = lane + 32 * i;
-        const int t = tr & 3;
-        const int m = (tr >> 2) % M;
-        const int s = tr / (4 * M);
-        int e[4];
-        step_elems(t, s & 1, e);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) x[i][q] = f[m * 256 + 32 * (s >> 1) + e[q]];
-    }
-    __syncwarp();
-    uint2* out = reinterpret_cast<uint2*>(unit);
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) {
-        const int tr = lane + 32 * i;
-        const int t = tr & 3;
-        const int m = (tr >> 2) % M;
-        const int s = tr / (4 * M);
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat16 h = __float2bfloat16_rn(x[i][q]);
-            const float rest = x[i][q] - __bfloat162float(h);
-            hi[q] = __bfloat16_as_ushort(h);
-            lo[q] = __bfloat16_as_ushort(__float2bfloat16_rn(isfinite(rest) ? rest : 0.f));
-        }
-        out[(s * 2 * M + m) * 4 + t] = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-        out[(s * 2 * M + M + m) * 4 + t] = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
-    }
-}
-
-// Exact sum over units [u0, u0 + nu) of one weight row for activation row
-// `a_m` (global, at the range's first k): sum_k A[m][k] * ((q_k - 8) * d),
-// element by element.  Taken for a row whose block-scaled sum came out
-// infinite or NaN: there a non-finite d times a zero weight (q = 8), or
-// infinities of both signs, must give NaN exactly as the definition does.
-__device__ __noinline__ float row_range_exact(const uint8_t* row_blocks, int nblocks,
-                                              const float* a_m) {
-    float s = 0.f;
-    for (int b = 0; b < nblocks; ++b) {
-        const uint8_t* blk = row_blocks + 18 * b;
-        const float d = f16_bits_to_float(static_cast<uint32_t>(blk[0]) |
-                                          (static_cast<uint32_t>(blk[1]) << 8));
-        for (int j = 0; j < 32; ++j) {
-            const uint32_t byte = blk[2 + (j & 15)];
-            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
-            s = fmaf(__ldg(a_m + 32 * b + j), magic_minus8(nib | kMagicBits) * d, s);
-        }
-    }
-    return s;
-}
-
-// One tile (32 rows x 1 unit) on tensor cores.  rows[i] points at the unit
-// of tile rows g, g+8, 16+g, 24+g; bfr at the unit's B fragments; a_unit at
-// the unit's first activation in global memory, rows lda apart (read only
-// for blocks whose scale is not finite).
-template <int M>
-__device__ __forceinline__ void unit_mma(const uint8_t* const rows[4], const uint2* bfr,
-                                         const float* a_unit, int64_t lda, int lane,
-                                         float acc[2][4]) {
-    constexpr int P = tc_sets<M>();
-    const int g = lane >> 2;
-    const int t = lane & 3;
-    int slot[P];
-#pragma unroll
-    for (int p = 0; p < P; ++p) slot[p] = tc_slot<M>(g, p);
-#pragma unroll 2
-    for (int b = 0; b < 8; ++b) {
-        uint32_t bb[2][P][2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint2* f = bfr + (2 * b + h) * (2 * M) * 4 + t;
-#pragma unroll
-            for (int p = 0; p < P; ++p) {
-                const uint2 v = slot[p] >= 0 ? f[slot[p] * 4] : make_uint2(0u, 0u);
-                bb[h][p][0] = v.x;
-                bb[h][p][1] = v.y;
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const uint8_t* u0 = rows[2 * hh];
-            const uint8_t* u1 = rows[2 * hh + 1];
-            uint32_t r0[4], r1[4];
-            decode_bf16(quant_word(u0, b, t), r0);
-            decode_bf16(quant_word(u1, b, t), r1);
-            float D[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int p = 0; p < P; ++p)
-                mma_bf16_16816(D, r0[0], r1[0], r0[1], r1[1], bb[0][p][0], bb[0][p][1]);
-#pragma unroll
-            for (int p = 0; p < P; ++p)
-                mma_bf16_16816(D, r0[2], r1[2], r0[3], r1[3], bb[1][p][0], bb[1][p][1]);
-            // Scales of this lane's D rows: tile rows g (u0) and g + 8 (u1).
-            const float d0 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u0 + 18 * b));
-            const float d1 = f16_bits_to_float(*reinterpret_cast<const uint16_t*>(u1 + 18 * b));
-            // A non-finite d makes this row's sum non-finite; the row-group
-            // total then recomputes that row element by element.
-            acc[hh][0] = fmaf(d0, D[0], acc[hh][0]);
-            acc[hh][1] = fmaf(d0, D[1], acc[hh][1]);
-            acc[hh][2] = fmaf(d1, D[2], acc[hh][2]);
-            acc[hh][3] = fmaf(d1, D[3], acc[hh][3]);
-        }
-    }
-}
-
-// Add a tile's accumulators into partial[m][row] (row within the 32-row tile).
-template <int M>
-__device__ __forceinline__ void flush_mma(const float acc[2][4], float* partial_w, int lane) {
-    const int g = lane >> 2;
-    const int t = lane & 3;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float v = acc[hh][i];
-            const int row = 16 * hh + g + ((i >= 2) ? 8 : 0);
-            if constexpr (tc_sets<M>() == 1) {
-                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);  // hi (t) + lo (t ^ 2) pieces
-                const int m = 2 * t + (i & 1);
-                if (t < 2 && m < M) partial_w[m * 32 + row] += v;
-            } else {
-                const int m = 2 * t + (i & 1);
-                if (m < M) partial_w[m * 32 + row] += v;
-            }
-        }
-    }
-}
-
 // Work decomposition of one persistent launch.
 struct GemvGrid {
     const uint8_t* wq;  // the weight stream (read directly only by the exact fix-up)
@@ -440,22 +209,19 @@ struct GemvGrid {
     unsigned* ctr;  // [RG] arrival counters (S > 1), zero between launches
 };
 
-template <int M, bool kTC>
-__global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
+template <int M>
+__global__ void __launch_bounds__(cta_threads<M>(), 1)
     gemv_q4_0_persistent(const __grid_constant__ CUtensorMap map0,
-                         const __grid_constant__ CUtensorMap map1,
-                         const __grid_constant__ CUtensorMap amap, const float* __restrict__ A,
+                         const __grid_constant__ CUtensorMap map1, const float* __restrict__ A,
                          float* __restrict__ C, const GemvGrid g) {
-    constexpr int W = consumer_warps<M, kTC>();
+    constexpr int W = consumer_warps<M>();
     extern __shared__ __align__(128) uint8_t smem[];
     // ring [stages][32 rows x nu units x 144 B] (first box0 units of every row,
-    // then the rest) | activations: f32 [M][nu * 256] (FP32 FMA decode) or B
-    // fragments [nu * 16 k-steps][2M][4] (tensor cores) | partial sums
+    // then the rest) | activations f32 [M][nu * 256] | partial sums
     // [rpg][slots][M][32] | full[stages] | empty[stages] | a_bar | seq[stages]
     const int stage_bytes = kTileBytes * g.uc;
     uint8_t* ring = smem;
     float* a_s = reinterpret_cast<float*>(smem + g.stages * stage_bytes);
-    uint2* bfrag = reinterpret_cast<uint2*>(a_s);
     const int lda = g.nu * kUnitElems;
     // Row group r's tiles go to warps (r * nu + j) % W, j < nu: min(nu, W)
     // distinct warps, each with its own partial-sum slot.
@@ -498,21 +264,11 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
         if (lane == 0 && items > 0) {
             prefetch_tensormap(&map0);
             if (box1 > 0) prefetch_tensormap(&map1);
-            if constexpr (kTC) {
-                // One [M][256] f32 box per unit, landing where the unit's B
-                // fragments will be built.
-                prefetch_tensormap(&amap);
-                mbar_arrive_expect_tx(a_bar, static_cast<uint32_t>(nu) * M * 1024);
-                for (int j = 0; j < nu; ++j)
-                    tma_load_2d(reinterpret_cast<uint8_t*>(bfrag) + j * M * 1024, &amap,
-                                (u0 + j) * kUnitElems, 0, a_bar);
-            } else {
-                const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
-                mbar_arrive_expect_tx(a_bar, a_bytes * M);
-                for (int m = 0; m < M; ++m)
-                    bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
-                                 a_bytes, a_bar);
-            }
+            const uint32_t a_bytes = static_cast<uint32_t>(nu) * kUnitElems * 4;
+            mbar_arrive_expect_tx(a_bar, a_bytes * M);
+            for (int m = 0; m < M; ++m)
+                bulk_load_1d(a_s + m * lda, A + m * g.K + static_cast<int64_t>(u0) * kUnitElems,
+                             a_bytes, a_bar);
             // Chunk c = (row group c / chunks, units [(c % chunks) * uc, +uc)).
             for (int c = 0; c < nrg * chunks; ++c) {
                 const int st = c % g.stages;
@@ -530,25 +286,14 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
             }
         }
     } else if (items > 0 && mbar_wait_bounded(a_bar, 0, &g_gemv_error)) {
-        const float* a_cta = A + static_cast<int64_t>(u0) * kUnitElems;  // CTA's first k
-        if constexpr (kTC) {
-            // B fragments of the CTA's k-range: one warp per unit, in place.
-            for (int j = warp; j < nu; j += W)
-                convert_unit_inplace<M>(reinterpret_cast<uint8_t*>(bfrag) + j * M * 1024, lane);
-            asm volatile("bar.sync 1, %0;" ::"r"(W * 32) : "memory");
-        }
         // Consumers: tile i (row group i / nu, unit i % nu) goes to warp i % W.
-        float acc[kTC ? 8 : M];
+        float acc[M];
         int cur = -1;
         auto flush = [&](int r) {
             const int slot = (g.nu >= W) ? warp : ((warp - (r * g.nu) % W) + W) % W;
             float* pw = partial + (r * slots + slot) * M * 32;
-            if constexpr (kTC) {
-                flush_mma<M>(reinterpret_cast<const float(*)[4]>(acc), pw, lane);
-            } else {
 #pragma unroll
-                for (int m = 0; m < M; ++m) pw[m * 32 + lane] += acc[m];
-            }
+            for (int m = 0; m < M; ++m) pw[m * 32 + lane] += acc[m];
         };
         for (int i = warp; i < items; i += W) {
             const int r = i / nu;
@@ -556,7 +301,7 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
             if (r != cur) {
                 if (cur >= 0) flush(cur);
 #pragma unroll
-                for (int q = 0; q < (kTC ? 8 : M); ++q) acc[q] = 0.f;
+                for (int q = 0; q < M; ++q) acc[q] = 0.f;
                 cur = r;
             }
             const int c = i / uc;  // chunk (items of a chunk are consecutive)
@@ -579,15 +324,7 @@ __global__ void __launch_bounds__(cta_threads<M, kTC>(), 1)
                                ? base + (row * g.box0 + jc) * kUnitBytes
                                : base + kTileBytes * g.box0 + (row * box1 + (jc - g.box0)) * kUnitBytes;
                 };
-                if constexpr (kTC) {
-                    const int gq = lane >> 2;
-                    const uint8_t* const rows[4] = {row_unit(gq), row_unit(gq + 8), row_unit(gq + 16),
-                                                    row_unit(gq + 24)};
-                    unit_mma<M>(rows, bfrag + j * 16 * 4 * 2 * M, a_cta + j * kUnitElems, g.K, lane,
-                                reinterpret_cast<float(*)[4]>(acc));
-                } else {
-                    unit_dot<M>(row_unit(lane), a_s, lda, j * kUnitElems, acc);
-                }
+                unit_dot<M>(row_unit(lane), a_s, lda, j * kUnitElems, acc);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -687,13 +424,13 @@ __global__ void __launch_bounds__(256)
 }
 
 // Per-device one-time opt-in to large dynamic shared memory.
-template <int M, bool kTC>
+template <int M>
 cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
     if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_persistent<M, kTC>,
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_persistent<M>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            dev.max_smem_optin);
     if (err != cudaSuccess) return err;
@@ -701,8 +438,7 @@ cudaError_t ensure_smem_attr(const DeviceInfo& dev, int bytes) {
     return cudaSuccess;
 }
 
-int64_t smem_bytes(int M, bool tc, int W, int stages, int uc, int nu, int rpg) {
-    (void)tc;  // f32 activations and B fragments take the same space
+int64_t smem_bytes(int M, int W, int stages, int uc, int nu, int rpg) {
     return static_cast<int64_t>(stages) * kTileBytes * uc +
            static_cast<int64_t>(M) * nu * kUnitElems * 4 +
            static_cast<int64_t>(rpg) * std::min(nu, W) * M * 32 * 4 + (2 * stages + 1) * 8 +
@@ -723,7 +459,7 @@ int first_box(int nu) {
 // poorly), the cheapest wins, fewer splits breaking ties.
 constexpr int64_t kMinStageBytes = 16 * 1024;
 
-bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& dev,
+bool plan_grid(int M, int W, int64_t N, int64_t K, const DeviceInfo& dev,
                const Workspace& ws, GemvGrid* g, int* grid, int* smem) {
     const int U = static_cast<int>(K / kUnitElems);
     const int64_t RG = (N + kRowsPerTile - 1) / kRowsPerTile;
@@ -744,9 +480,9 @@ bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& de
         int uc = nu;
         auto fit = [&](int u) {
             int st = 8;
-            while (st > 1 && smem_bytes(M, tc, W, st, u, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
+            while (st > 1 && smem_bytes(M, W, st, u, nu, static_cast<int>(rpg)) > dev.max_smem_optin)
                 --st;
-            return smem_bytes(M, tc, W, st, u, nu, static_cast<int>(rpg)) <= dev.max_smem_optin ? st : 0;
+            return smem_bytes(M, W, st, u, nu, static_cast<int>(rpg)) <= dev.max_smem_optin ? st : 0;
         };
         int stages = fit(uc);
         while (uc % 2 == 0 && static_cast<int64_t>(kTileBytes) * (uc / 2) >= kMinStageBytes &&
@@ -779,7 +515,7 @@ bool plan_grid(int M, bool tc, int W, int64_t N, int64_t K, const DeviceInfo& de
             c.part = ws.part;
             c.ctr = ws.ctr;
             cgrid[big] = static_cast<int>(g_used * S);
-            csmem[big] = static_cast<int>(smem_bytes(M, tc, W, stages, uc, nu, static_cast<int>(rpg)));
+            csmem[big] = static_cast<int>(smem_bytes(M, W, stages, uc, nu, static_cast<int>(rpg)));
         }
     }
     const int pick = (best[1] != INT64_MAX) ? 1 : 0;
@@ -801,17 +537,17 @@ bool persistent_ok(const float* A, const uint8_t* wq, int64_t N, int64_t K) {
 // Plan and launch the persistent kernel with split-K scratch `ws`.  Sets
 // *launched = false (and launches nothing) when no plan fits.  With
 // clear_counters the row-group counters are zeroed on the stream first.
-template <int M, bool kTC>
+template <int M>
 cudaError_t launch_persistent(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
                               cudaStream_t stream, const DeviceInfo& dev, const Workspace& ws,
                               bool clear_counters, bool* launched) {
     *launched = false;
     GemvGrid g;
     int grid = 0, smem = 0;
-    if (!plan_grid(M, kTC, consumer_warps<M, kTC>(), N, K, dev, ws, &g, &grid, &smem))
+    if (!plan_grid(M, consumer_warps<M>(), N, K, dev, ws, &g, &grid, &smem))
         return cudaSuccess;
     g.wq = wq;
-    cudaError_t err = ensure_smem_attr<M, kTC>(dev, smem);
+    cudaError_t err = ensure_smem_attr<M>(dev, smem);
     if (err != cudaSuccess) return err;
     if (clear_counters && g.S > 1) {
         err = cudaMemsetAsync(g.ctr, 0, static_cast<size_t>(g.RG) * sizeof(unsigned), stream);
@@ -832,17 +568,7 @@ cudaError_t launch_persistent(const float* A, const uint8_t* wq, float* C, int64
         err = encode_tiled(&map1, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, dims, strides, box_b);
         if (err != cudaSuccess) return err;
     }
-    CUtensorMap amap = map0;
-    if constexpr (kTC) {
-        // The activations as f32 [M][K]; boxes of M rows x 256 k.
-        const int64_t adims[2] = {K, M};
-        const int64_t astrides[1] = {K * 4};
-        const int abox[2] = {kUnitElems, M};
-        err = encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
-        if (err != cudaSuccess) return err;
-    }
-    gemv_q4_0_persistent<M, kTC><<<grid, cta_threads<M, kTC>(), smem, stream>>>(map0, map1, amap, A,
-                                                                                 C, g);
+    gemv_q4_0_persistent<M><<<grid, cta_threads<M>(), smem, stream>>>(map0, map1, A, C, g);
     note_launch();
     *launched = true;
     return cudaGetLastError();
@@ -867,8 +593,8 @@ cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int
         cudaError_t err = stream_workspace(dev, stream, &ws);
         if (err != cudaSuccess) return err;
         bool launched = false;
-        err = tc ? launch_persistent<M, true>(A, wq, C, N, K, stream, dev, ws, false, &launched)
-                 : launch_persistent<M, false>(A, wq, C, N, K, stream, dev, ws, false, &launched);
+        err = tc ? launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws, false, &launched)
+                 : launch_persistent<M>(A, wq, C, N, K, stream, dev, ws, false, &launched);
         if (err != cudaSuccess || launched) return err;
     }
     return launch_generic<M>(A, wq, C, N, K, stream, dev);
@@ -949,7 +675,7 @@ cudaError_t launch_m_noalloc(const float* A, const uint8_t* wq, float* C, int64_
         // The arrival counters must start at zero; the array keeps whatever
         // the previous call (or an abandoned one) left, so clear them first.
         bool launched = false;
-        err = launch_persistent<M, true>(A, wq, C, N, K, stream, dev, ws, true, &launched);
+        err = launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws, true, &launched);
         if (err != cudaSuccess || launched) return err;
     }
     return launch_generic<M>(A, wq, C, N, K, stream, dev);

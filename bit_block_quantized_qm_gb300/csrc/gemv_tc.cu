@@ -1,0 +1,629 @@
+// Decode-regime GEMV on tensor cores: C[m][n] = sum_k A[m][k] * W[n][k] for
+// M = 1..8 rows of f32 activations against a Q4_0 weight stream (sections
+// "qmatvec_q4_0" and "matmul_q4_0_tiled" of "fuel-vulkan-kernels — quantized
+// (GGML) kernel contracts": element j < 16 of a block is the low nibble of
+// quant byte j, element j + 16 its high nibble, value (nibble - 8) * d).
+//
+// Arithmetic.  Each block's 32 products go through mma.sync m16n8k16 with
+// bf16 operands and f32 accumulation:
+//   * A operand (16 x 16) = 16 weight rows x 16 k of (q - 8), exact in bf16.
+//   * B operand (16 x 8) = activation pieces: hi = bf16(a), lo = bf16(a - hi),
+//     so |a - hi - lo| <= 2^-17 |a| and every product is exact in f32.  For
+//     M <= 4 one MMA per k-step carries hi pieces in columns 0..M-1 and lo
+//     pieces in columns M..2M-1; for M > 4 a second MMA adds the lo pieces.
+//   * The block's MMA result is scaled once by its row's d in f32.  A row
+//     whose total comes out infinite or NaN is recomputed element by element
+//     (a non-finite d times q = 8 must give NaN, as the definition does).
+//
+// Data movement.  A "unit" is 8 blocks of one row (144 bytes, 256 k); a "row
+// group" is 16 rows (one MMA tile); a "row block" is rps row groups.  A CTA
+// (one per SM) owns a range of row blocks for one range of units (a K split).
+// A producer warp streams stages through a ring in shared memory with TMA: a
+// stage is one row block x c consecutive units, as c boxes of [16 rps rows]
+// [144 B] (the 144-byte row stride keeps the per-lane 4-byte loads on
+// distinct banks).  The W = rps * c consumer warps take one tile (16 rows x 1
+// unit) each from every stage, in stage order, so a warp can never run two
+// phases ahead of a stage's barrier.  Warp w always takes row group w % rps
+// and unit column w / rps, so it accumulates its rows over every c-th unit of
+// the row block; the c partial sums of a row group meet in shared memory
+// (fixed column order) when the row block ends.  Consecutive stages walk a
+// row block's units in order, so each row's bytes are read front to back by
+// one CTA.  The activations of the CTA's K range arrive once (TMA, f32) and
+// are rewritten in place as B fragments.
+//
+// Loads.  Lane (g, t) of a warp holds rows g and g + 8 of the tile and needs 4
+// quant bytes of each per block.  A block pair is 36 bytes = 9 aligned words:
+// the odd block's quants are words 5..8 (lane t takes word 5 + t); the even
+// block's are misaligned by 2, so lanes t < 3 take words 1..3 (quant bytes
+// 2..13) and lane 3 joins the halves of words 0 and 4 (bytes 0, 1, 14, 15).
+// The order of k inside an MMA is free as long as A and B agree, so the B
+// fragments are built in that same lane order.  Word 0 carries the even
+// block's d, word 4 the odd block's.
+//
+// Launch.  Launched with programmatic stream serialization: the kernel lets
+// its dependents start at once, and before its own wait it only initialises
+// barriers and asks L2 for its first stages of weights (a hint that cannot
+// return stale data); every read of A or the weights into the SM, and every
+// write, comes after griddepcontrol.wait.
+//
+// Split K.  With S > 1 ranges a row group's partial sums go to a workspace;
+// the last of the S CTAs to arrive adds them in range order and writes C, so
+// results do not depend on timing.  Counters are left at zero.
+#include <algorithm>
+#include <mutex>
+
+#include "qm_device.cuh"
+#include "qm_internal.h"
+
+namespace qm {
+
+__device__ unsigned int g_gemv_tc_error = 0;
+
+namespace {
+
+constexpr int kUnitBytes = 144;
+constexpr int kUnitElems = 256;
+constexpr int kGroupRows = 16;
+constexpr int kGroupBytes = kGroupRows * kUnitBytes;  // one tile: 2304 bytes
+constexpr int kMaxWarps = 16;                         // consumer warps
+constexpr int kThreadsMax = (kMaxWarps + 1) * 32;     // + producer warp
+constexpr int kMaxStages = 8;
+constexpr int kMaxSplits = 16;
+constexpr int kSlotFloats = kGroupRows * 8;  // one warp's D tile, 16 rows x 8 columns
+
+struct TcPlan {
+    const uint8_t* wq;  // the weight stream (read directly only by the exact fix-up)
+    int N;
+    int64_t K;
+    int U;          // units per row
+    int RG;         // row groups, ceil(N / 16)
+    int S;          // K ranges; range s is units [s U / S, (s + 1) U / S)
+    int rps;        // row groups per row block
+    int c;          // units per stage; rps * c consumer warps
+    int rbpc;       // row blocks per CTA
+    int nu_max;     // units in the largest K range
+    int stages;     // ring depth
+    float* part;    // [RG][S][M][16] split partial sums (S > 1)
+    unsigned* ctr;  // [RG] arrival counters (S > 1), zero between launches
+};
+
+__device__ __forceinline__ uint32_t lds_u32(const uint8_t* p) {
+    return *reinterpret_cast<const uint32_t*>(p);
+}
+
+// D = A x B (C = 0) and D += A x B, m16n8k16, bf16 in, f32 out.
+__device__ __forceinline__ void mma_first(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ void mma_acc(float d[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (q - 8) as bf16 pairs from a quant word Q holding quant bytes (b0, b1, b2,
+// b3), b0 lowest: R0 = low nibbles of (b0, b2), R1 = high nibbles of (b0, b2),
+// R2 = low nibbles of (b1, b3), R3 = high nibbles of (b1, b3), the first of
+// each pair in the low half.  A nibble under the bf16 exponent of 128 reads as
+// 128 + q; subtracting 136 leaves q - 8, both steps exact.
+__device__ __forceinline__ void decode_bf16(uint32_t Q, uint32_t R[4]) {
+    constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
+    constexpr uint32_t kOne = 0x3F803F80u;    // bf16 1.0
+    constexpr uint32_t kBias = 0xC308C308u;   // bf16 -136.0
+    const uint32_t r[4] = {(Q & 0x000F000Fu) | kMagic, ((Q >> 4) & 0x000F000Fu) | kMagic,
+                           ((Q >> 8) & 0x000F000Fu) | kMagic, ((Q >> 12) & 0x000F000Fu) | kMagic};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(R[i]) : "r"(r[i]), "r"(kOne), "r"(kBias));
+}
+
+// Quant bytes (b0, b2) of lane quarter t in a block of the given parity (the
+// word layout above); k-step h of the block pairs elements (b0 + h, b2 + h)
+// in the fragment's first k pair and (b0 + h + 16, b2 + h + 16) in its second.
+__device__ __forceinline__ void lane_bytes(int t, int odd, int& b0, int& b2) {
+    if (odd) {
+        b0 = 4 * t;
+        b2 = 4 * t + 2;
+    } else if (t < 3) {
+        b0 = 4 * t + 2;
+        b2 = 4 * t + 4;
+    } else {
+        b0 = 0;
+        b2 = 14;
+    }
+}
+
+template <int M>
+__host__ __device__ constexpr int tc_sets() { return M <= 4 ? 1 : 2; }
+
+// Fragment columns a lane group reads: 2M (one set) or M per set.
+template <int M>
+__host__ __device__ constexpr int frag_cols() { return tc_sets<M>() == 1 ? 2 * M : M; }
+
+// Rewrite one unit of staged activations, f32 [M][256] as the TMA box lands,
+// into the unit's B fragments in place (the two take the same M KB).  Entry
+// (uint2) for block kb, k-step h, set p, column col < frag_cols, quarter t:
+// ((((kb * 2 + h) * P + p) * frag_cols + col) * 4 + t).  One set: columns
+// 0..M-1 = hi pieces of rows 0..M-1, M..2M-1 = lo pieces.  Two sets: set 0 hi,
+// set 1 lo, column = row.  A warp reads its 2M (hi, lo) groups of 4 values
+// into registers, syncs, and overwrites.
+template <int M>
+__device__ __forceinline__ void build_fragments(uint8_t* unit, int lane) {
+    constexpr int kPer = 2 * M;  // (kb, h, row, t) groups per lane
+    const float* f = reinterpret_cast<const float*>(unit);
+    float x[kPer][4];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int idx = lane + 32 * i;
+        const int t = idx & 3;
+        const int m = (idx >> 2) % M;
+        const int kbh = idx / (4 * M);
+        const int kb = kbh >> 1;
+        const int h = kbh & 1;
+        int b0, b2;
+        lane_bytes(t, kb & 1, b0, b2);
+        const float* row = f + m * kUnitElems + kb * kBlockElems;
+        x[i][0] = row[b0 + h];
+        x[i][1] = row[b2 + h];
+        x[i][2] = row[b0 + h + 16];
+        x[i][3] = row[b2 + h + 16];
+    }
+    __syncwarp();
+    uint2* out = reinterpret_cast<uint2*>(unit);
+    constexpr int P = tc_sets<M>();
+    constexpr int NC = frag_cols<M>();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int idx = lane + 32 * i;
+        const int t = idx & 3;
+        const int m = (idx >> 2) % M;
+        const int kbh = idx / (4 * M);
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat16 hb = __float2bfloat16_rn(x[i][q]);
+            const float rest = x[i][q] - __bfloat162float(hb);
+            hi[q] = __bfloat16_as_ushort(hb);
+            lo[q] = __bfloat16_as_ushort(__float2bfloat16_rn(isfinite(rest) ? rest : 0.f));
+        }
+        const uint2 vh = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+        const uint2 vl = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+        if constexpr (P == 1) {
+            out[(kbh * NC + m) * 4 + t] = vh;
+            out[(kbh * NC + M + m) * 4 + t] = vl;
+        } else {
+            out[((kbh * 2 + 0) * NC + m) * 4 + t] = vh;
+            out[((kbh * 2 + 1) * NC + m) * 4 + t] = vl;
+        }
+    }
+}
+
+// One block of a tile: quant words Qa (row g) and Qb (row g + 8), scales da,
+// db, fragments F of block kb (entries of k-step 0 first).  Lane group g
+// reads fragment column gc = g mod frag_cols: columns past frag_cols only
+// repeat earlier ones, and their results are never read.
+template <int M>
+__device__ __forceinline__ void block_mma(uint32_t Qa, uint32_t Qb, float da, float db,
+                                          const uint2* F, int gc, int t, float acc[4]) {
+    constexpr int P = tc_sets<M>();
+    constexpr int NC = frag_cols<M>();
+    uint32_t ra[4], rb[4];
+    decode_bf16(Qa, ra);
+    decode_bf16(Qb, rb);
+    uint2 b[2][P];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int p = 0; p < P; ++p)
+            b[h][p] = F[((h * P + p) * NC + gc) * 4 + t];
+    float D[4];
+    mma_first(D, ra[0], rb[0], ra[1], rb[1], b[0][0].x, b[0][0].y);
+    if constexpr (P == 2) mma_acc(D, ra[0], rb[0], ra[1], rb[1], b[0][1].x, b[0][1].y);
+    mma_acc(D, ra[2], rb[2], ra[3], rb[3], b[1][0].x, b[1][0].y);
+    if constexpr (P == 2) mma_acc(D, ra[2], rb[2], ra[3], rb[3], b[1][1].x, b[1][1].y);
+    acc[0] = fmaf(da, D[0], acc[0]);
+    acc[1] = fmaf(da, D[1], acc[1]);
+    acc[2] = fmaf(db, D[2], acc[2]);
+    acc[3] = fmaf(db, D[3], acc[3]);
+}
+
+// One tile: rows r0 (row g) and r1 (row g + 8) of a unit in shared memory, the
+// unit's fragments F.
+template <int M>
+__device__ __forceinline__ void tile_mma(const uint8_t* r0, const uint8_t* r1, const uint2* F,
+                                         int gc, int t, uint32_t xoff, uint32_t sel, float acc[4]) {
+    constexpr int kEntriesPerBlock = 2 * tc_sets<M>() * frag_cols<M>() * 4;
+    const uint32_t yoff = 20 + 4 * t;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+        const uint8_t* a = r0 + 36 * pp;
+        const uint8_t* b = r1 + 36 * pp;
+        const uint32_t w0a = lds_u32(a), w4a = lds_u32(a + 16), xa = lds_u32(a + xoff),
+                       ya = lds_u32(a + yoff);
+        const uint32_t w0b = lds_u32(b), w4b = lds_u32(b + 16), xb = lds_u32(b + xoff),
+                       yb = lds_u32(b + yoff);
+        const float dea = f16_bits_to_float(w0a & 0xFFFFu), doa = f16_bits_to_float(w4a >> 16);
+        const float deb = f16_bits_to_float(w0b & 0xFFFFu), dob = f16_bits_to_float(w4b >> 16);
+        block_mma<M>(__byte_perm(xa, w4a, sel), __byte_perm(xb, w4b, sel), dea, deb,
+                     F + (2 * pp) * kEntriesPerBlock, gc, t, acc);
+        block_mma<M>(ya, yb, doa, dob, F + (2 * pp + 1) * kEntriesPerBlock, gc, t, acc);
+    }
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreadsMax, 1)
+    gemv_q4_0_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
+                 const float* __restrict__ A, float* __restrict__ C, const TcPlan p) {
+    const int W = p.rps * p.c;
+    extern __shared__ __align__(128) uint8_t smem[];
+    // ring [stages][c boxes][16 rps rows][144 B] | B fragments [nu_max][M KB] |
+    // D-tile slots [2][W][16][8] f32 | full[stages] | empty[stages] | a_bar
+    const int box_bytes = p.rps * kGroupBytes;
+    const int stage_bytes = p.c * box_bytes;
+    uint8_t* ring = smem;
+    uint8_t* frag = smem + p.stages * stage_bytes;
+    float* slots = reinterpret_cast<float*>(frag + p.nu_max * M * 1024);
+    uint64_t* full = reinterpret_cast<uint64_t*>(slots + 2 * W * kSlotFloats);
+    uint64_t* empty = full + p.stages;
+    uint64_t* a_bar = empty + p.stages;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int split = static_cast<int>(blockIdx.x) % p.S;
+    const int u0 = static_cast<int>(static_cast<int64_t>(split) * p.U / p.S);
+    const int nu = static_cast<int>(static_cast<int64_t>(split + 1) * p.U / p.S) - u0;
+    const int RB = (p.RG + p.rps - 1) / p.rps;
+    const int rb0 = (static_cast<int>(blockIdx.x) / p.S) * p.rbpc;
+    const int nrb = max(0, min(p.rbpc, RB - rb0));
+    const int spr = (nu + p.c - 1) / p.c;  // stages per row block
+    const int nst = nrb * spr;
+
+    grid_launch_dependents();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], W);  // every consumer warp, once per stage
+        }
+        mbar_init(a_bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == W) {
+        if (lane == 0 && nst > 0) {
+            prefetch_tensormap(&wmap);
+            prefetch_tensormap(&amap);
+            const int rows_per_block = p.rps * kGroupRows;
+            // Warm L2 with the first stages (about 64 KB) before waiting on
+            // earlier kernels; more would compete with their last reads.
+            {
+                const int warm = min(min(p.stages, nst), max(1, 65536 / stage_bytes + 1));
+                int sc = 0, row = rb0 * rows_per_block;
+                for (int s = 0; s < warm; ++s) {
+                    for (int ul = 0; ul < p.c; ++ul) {
+                        const int j = sc * p.c + ul;
+                        if (j < nu) tma_prefetch_l2_3d(&wmap, 0, u0 + j, row);
+                    }
+                    if (++sc == spr) {
+                        sc = 0;
+                        row += rows_per_block;
+                    }
+                }
+            }
+            grid_dependency_wait();
+            // The CTA's activations: one [M][256] f32 box per unit.
+            mbar_arrive_expect_tx(a_bar, static_cast<uint32_t>(nu) * M * 1024);
+            for (int j = 0; j < nu; ++j)
+                tma_load_2d(frag + j * M * 1024, &amap, (u0 + j) * kUnitElems, 0, a_bar);
+            int sc = 0, row = rb0 * rows_per_block, st = 0;
+            uint32_t phase = 0;
+            for (int s = 0; s < nst; ++s) {
+                if (s >= p.stages && !mbar_wait_bounded(&empty[st], phase ^ 1u, &g_gemv_tc_error))
+                    break;
+                const int nbox = min(p.c, nu - sc * p.c);
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(nbox * box_bytes));
+                for (int ul = 0; ul < nbox; ++ul)
+                    tma_load_3d(ring + st * stage_bytes + ul * box_bytes, &wmap, 0,
+                                u0 + sc * p.c + ul, row, &full[st]);
+                if (++sc == spr) {
+                    sc = 0;
+                    row += rows_per_block;
+                }
+                if (++st == p.stages) {
+                    st = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        return;
+    }
+
+    grid_dependency_wait();
+    if (nst == 0) return;  // no consumer of this CTA reaches a barrier
+    bool ok = mbar_wait_bounded(a_bar, 0, &g_gemv_tc_error);
+    if (ok) {
+        for (int j = warp; j < nu; j += W) build_fragments<M>(frag + j * M * 1024, lane);
+    }
+    named_barrier_sync(1, W * 32);
+
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int gc = g % frag_cols<M>();
+    const int rgl = warp % p.rps;  // row group within the row block
+    const int ul = warp / p.rps;   // unit column within a stage
+    const uint32_t xoff = (t < 3) ? 4u + 4u * t : 0u;
+    const uint32_t sel = (t < 3) ? 0x3210u : 0x5432u;
+    const uint2* F = reinterpret_cast<const uint2*>(frag);
+    const uint8_t* tile0 = ring + ul * box_bytes + (rgl * kGroupRows + g) * kUnitBytes;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    int st = 0;
+    uint32_t phase = 0;
+
+    for (int rbi = 0; rbi < nrb; ++rbi) {
+        for (int sc = 0; sc < spr; ++sc) {
+            const int j = sc * p.c + ul;  // unit within the CTA's K range
+            if (ok) ok = mbar_wait_bounded(&full[st], phase, &g_gemv_tc_error);
+            if (ok && j < nu) {
+                const uint8_t* r0 = tile0 + st * stage_bytes;
+                tile_mma<M>(r0, r0 + 8 * kUnitBytes, F + j * (M * 128), gc, t, xoff, sel, acc);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+            if (++st == p.stages) {
+                st = 0;
+                phase ^= 1u;
+            }
+        }
+
+        // Row block done: D tiles to shared memory; the warp of unit column 0
+        // adds its row group's c tiles (column order) and takes one row per
+        // lane 0..15.  Slots alternate between row blocks, so one barrier per
+        // row block keeps a slot from being rewritten before it is read.
+        float* slot = slots + ((rbi & 1) * W + warp) * kSlotFloats;
+        reinterpret_cast<float2*>(slot)[g * 4 + t] = make_float2(acc[0], acc[1]);
+        reinterpret_cast<float2*>(slot)[(g + 8) * 4 + t] = make_float2(acc[2], acc[3]);
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+        if (p.c > 1) {
+            named_barrier_sync(1, W * 32);
+        } else {
+            __syncwarp();
+        }
+        if (ul != 0) continue;
+        const int rg = (rb0 + rbi) * p.rps + rgl;
+        const int r = lane & 15;
+        const int row = rg * kGroupRows + r;
+        float tot[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) tot[m] = 0.f;
+        for (int u = 0; u < p.c; ++u) {
+            const float* su = slots + ((rbi & 1) * W + rgl + u * p.rps) * kSlotFloats + r * 8;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                tot[m] += su[m];
+                if constexpr (tc_sets<M>() == 1) tot[m] += su[M + m];
+            }
+        }
+        if (rg >= p.RG) continue;  // whole warp: a row group past the matrix
+        const bool mine = lane < 16 && row < p.N;
+        if (mine) {
+            const uint8_t* row_blocks =
+                p.wq + (static_cast<int64_t>(row) * p.U + u0) * kUnitBytes;
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                if (!isfinite(tot[m]))
+                    tot[m] = row_range_exact(row_blocks, nu * 8,
+                                             A + m * p.K + static_cast<int64_t>(u0) * kUnitElems);
+            }
+        }
+        if (p.S == 1) {
+            if (mine) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) C[static_cast<int64_t>(m) * p.N + row] = tot[m];
+            }
+        } else if (lane < 16) {
+            float* part = p.part + (static_cast<int64_t>(rg) * p.S + split) * (M * kGroupRows);
+#pragma unroll
+            for (int m = 0; m < M; ++m) part[m * kGroupRows + lane] = tot[m];
+        }
+    }
+    if (p.S == 1 || ul != 0) return;
+
+    // Split K: one fence for all of this warp's partial sums, then its
+    // arrivals; the last of the S arrivals at a row group adds the partials
+    // in range order.  (Fencing once here rather than after every row block
+    // keeps the fence's wait out of the streaming loop.)
+    __threadfence();
+    __syncwarp();
+    for (int rbi = 0; rbi < nrb; ++rbi) {
+        const int rg = (rb0 + rbi) * p.rps + rgl;
+        if (rg >= p.RG) break;
+        unsigned old = 0;
+        if (lane == 0) old = atomicAdd(&p.ctr[rg], 1u);
+        old = __shfl_sync(0xFFFFFFFFu, old, 0);
+        if (old != static_cast<unsigned>(p.S - 1)) continue;
+        __threadfence();
+        const int row = rg * kGroupRows + lane;
+        if (lane < 16 && row < p.N) {
+            const float* base = p.part + static_cast<int64_t>(rg) * p.S * (M * kGroupRows);
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float v = 0.f;
+                for (int q = 0; q < p.S; ++q)
+                    v += __ldcg(base + q * (M * kGroupRows) + m * kGroupRows + lane);
+                C[static_cast<int64_t>(m) * p.N + row] = v;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) atomicExch(&p.ctr[rg], 0u);
+    }
+}
+
+// Shared memory of one CTA.
+int64_t tc_smem_bytes(int M, int W, int stages, int nu_max) {
+    return static_cast<int64_t>(stages) * W * kGroupBytes + static_cast<int64_t>(nu_max) * M * 1024 +
+           2LL * W * kSlotFloats * 4 + (2LL * stages + 1) * 8;
+}
+
+// Relative rate of one SM with W consumer warps (more warps hide more of the
+// shared-memory and MMA latency).
+double warp_efficiency(int W) {
+    return W >= 16 ? 1.0 : W >= 14 ? 0.96 : W >= 12 ? 0.92 : W >= 10 ? 0.86 : 0.8;
+}
+
+// Choose the stage shape (rps row groups x c units, W = rps c consumer warps)
+// and S (K ranges) for one CTA per SM.  The cost is the largest per-CTA tile
+// count (idle tile slots included) over the warp efficiency, with charges for
+// split-K partial sums (their bytes against the weight bytes, plus a little
+// per split), for short K ranges (a CTA that reads few bytes of each row
+// leaves DRAM pages to be reopened by others), for a shallow ring, and for
+// cross-warp reductions (c > 1) at more than one row block per CTA.
+bool plan_tc(int M, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws, TcPlan* out,
+             int* grid, int* smem) {
+    const int U = static_cast<int>(K / kUnitElems);
+    const int64_t RG = (N + kGroupRows - 1) / kGroupRows;
+    const int P = dev.sm_count;
+    double best = 1e300;
+    bool found = false;
+    for (int W = kMaxWarps; W >= 8; --W) {
+        for (int c = 1; c <= W; ++c) {
+            if (W % c != 0) continue;
+            const int rps = W / c;
+            if (rps * kGroupRows > 256) continue;  // TMA box height
+            const int64_t RB = (RG + rps - 1) / rps;
+            for (int S = 1; S <= kMaxSplits && S <= U; ++S) {
+                if (S > 1 && (RG * S * M * kGroupRows > static_cast<int64_t>(ws.part_floats) ||
+                              RG > static_cast<int64_t>(ws.ctr_count)))
+                    continue;
+                const int nu_max = (U + S - 1) / S;
+                const int64_t Gs = std::max(1, P / S);
+                const int64_t rbpc = (RB + Gs - 1) / Gs;
+                const int64_t g_used = (RB + rbpc - 1) / rbpc;
+                const int64_t spr = (nu_max + c - 1) / c;
+                const int64_t fixed = tc_smem_bytes(M, W, 0, nu_max);
+                int stages = static_cast<int>((dev.max_smem_optin - fixed) /
+                                              (static_cast<int64_t>(W) * kGroupBytes + 16));
+                stages = std::min(stages, kMaxStages);
+                if (stages < 2) continue;
+                const double split_bytes =
+                    (S > 1) ? 8.0 * M * S / (kBlockBytes * static_cast<double>(K) / kBlockElems)
+                            : 0.0;
+                const double short_rows =
+                    0.3 * std::max(0.0, 1.0 - nu_max * static_cast<double>(kUnitBytes) / 2048.0);
+                const double cost = static_cast<double>(rbpc * spr * W) / warp_efficiency(W) *
+                                    (1.0 + split_bytes + 0.01 * (S - 1) + short_rows) *
+                                    (stages < 3 ? 1.1 : 1.0) *
+                                    ((c > 1 && rbpc > 1) ? 1.0 + 0.05 * rbpc : 1.0);
+                if (cost < best) {
+                    best = cost;
+                    found = true;
+                    TcPlan& q = *out;
+                    q.wq = nullptr;
+                    q.N = static_cast<int>(N);
+                    q.K = K;
+                    q.U = U;
+                    q.RG = static_cast<int>(RG);
+                    q.S = S;
+                    q.rps = rps;
+                    q.c = c;
+                    q.rbpc = static_cast<int>(rbpc);
+                    q.nu_max = nu_max;
+                    q.stages = stages;
+                    q.part = ws.part;
+                    q.ctr = ws.ctr;
+                    *grid = static_cast<int>(g_used * S);
+                    *smem = static_cast<int>(tc_smem_bytes(M, W, stages, nu_max));
+                }
+            }
+        }
+    }
+    return found;
+}
+
+template <int M>
+cudaError_t ensure_tc_smem_attr(const DeviceInfo& dev, int bytes) {
+    static int configured[64] = {0};
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
+    if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_tc<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           dev.max_smem_optin);
+    if (err != cudaSuccess) return err;
+    __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
+    return cudaSuccess;
+}
+
+template <int M>
+cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
+                      cudaStream_t stream, const DeviceInfo& dev, const Workspace& ws,
+                      bool clear_counters, bool* launched) {
+    *launched = false;
+    TcPlan p;
+    int grid = 0, smem = 0;
+    if (!plan_tc(M, N, K, dev, ws, &p, &grid, &smem)) return cudaSuccess;
+    p.wq = wq;
+    cudaError_t err = ensure_tc_smem_attr<M>(dev, smem);
+    if (err != cudaSuccess) return err;
+    if (clear_counters && p.S > 1) {
+        err = cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(p.RG) * sizeof(unsigned), stream);
+        if (err != cudaSuccess) return err;
+    }
+    // Weights as bytes [N rows][U units][144 B]; boxes of 16 rps rows x 1 unit.
+    const int64_t dims[3] = {kUnitBytes, p.U, N};
+    const int64_t strides[2] = {kUnitBytes, static_cast<int64_t>(p.U) * kUnitBytes};
+    const int box[3] = {kUnitBytes, 1, p.rps * kGroupRows};
+    CUtensorMap wmap, amap;
+    err = encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, dims, strides, box);
+    if (err != cudaSuccess) return err;
+    // Activations as f32 [M][K]; boxes of M rows x 256 k.
+    const int64_t adims[2] = {K, M};
+    const int64_t astrides[1] = {K * 4};
+    const int abox[2] = {kUnitElems, M};
+    err = encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(gemv_q4_0_tc<M>, dim3(grid), dim3((p.rps * p.c + 1) * 32), smem, stream, wmap, amap,
+                     A, C, p);
+    if (err != cudaSuccess) return err;
+    note_launch();
+    *launched = true;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                int64_t K, cudaStream_t stream, const DeviceInfo& dev,
+                                const Workspace& ws, bool clear_counters, bool* launched) {
+    switch (M) {
+        case 1: return launch_tc<1>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 2: return launch_tc<2>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 3: return launch_tc<3>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 4: return launch_tc<4>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 5: return launch_tc<5>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 6: return launch_tc<6>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 7: return launch_tc<7>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 8: return launch_tc<8>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear) {
+    unsigned int v = 0;
+    cudaError_t err = cudaMemcpyFromSymbol(&v, g_gemv_tc_error, sizeof(v));
+    if (err != cudaSuccess) return err;
+    *bits |= v;
+    if (clear && v != 0) {
+        const unsigned int zero = 0;
+        err = cudaMemcpyToSymbol(g_gemv_tc_error, &zero, sizeof(zero));
+    }
+    return err;
+}
+
+}  // namespace qm

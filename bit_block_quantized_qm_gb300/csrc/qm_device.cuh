@@ -123,6 +123,33 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Hint: bring a 3-D TMA box into L2 without copying it anywhere.  L2 is the
+// device's point of coherence, so a line fetched early is still updated by
+// any later write; only a load into shared memory or registers must wait.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (when launched with programmatic serialization) start its
+// prologue while this one runs; wait blocks until every kernel this one
+// depends on has finished and its writes are visible.  Both are no-ops for
+// a kernel launched the ordinary way.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Named barrier over the first `threads` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // 16-byte streaming store (output written once, not re-read by this kernel).
 __device__ __forceinline__ void st_global_cs_v4(float* p, float a, float b, float c, float d) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
@@ -137,6 +164,27 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
+}
+
+// Exact sum over `nblocks` consecutive Q4_0 blocks of one weight row against
+// one activation row a_m: sum_k a_m[k] * ((q_k - 8) * d), element by element.
+// Taken for a row whose block-scaled sum came out infinite or NaN: there a
+// non-finite d times a zero weight (q = 8), or infinities of both signs, must
+// give NaN exactly as the definition does.
+static __device__ __noinline__ float row_range_exact(const uint8_t* row_blocks, int nblocks,
+                                                     const float* a_m) {
+    float s = 0.f;
+    for (int b = 0; b < nblocks; ++b) {
+        const uint8_t* blk = row_blocks + kBlockBytes * b;
+        const float d = f16_bits_to_float(static_cast<uint32_t>(blk[0]) |
+                                          (static_cast<uint32_t>(blk[1]) << 8));
+        for (int j = 0; j < kBlockElems; ++j) {
+            const uint32_t byte = blk[2 + (j & 15)];
+            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+            s = fmaf(__ldg(a_m + kBlockElems * b + j), magic_minus8(nib | kMagicBits) * d, s);
+        }
+    }
+    return s;
 }
 
 }  // namespace qm

@@ -39,11 +39,20 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
 
-// Decode-regime GEMV, M = 1..8.  Picks the persistent TMA-fed kernel (its
-// decode on tensor cores when tc, else on FP32 FMA) when wq and A are 16-byte
-// aligned and K % 256 == 0, else the generic kernel.
+// Decode-regime GEMV, M = 1..8.  When wq and A are 16-byte aligned and
+// K % 256 == 0: the tensor-core GEMV (gemv_tc.cu) when tc, else the
+// persistent FP32 FMA kernel; otherwise the generic kernel.
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                              int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool tc);
+
+// The tensor-core GEMV (mma.sync on bf16 pieces) for M = 1..8, K % 256 == 0 and
+// 16-byte aligned A and wq, with split-K scratch `ws` (counters zeroed on the
+// stream first when clear_counters).  Sets *launched = false and enqueues
+// nothing when no launch plan fits.
+cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                int64_t K, cudaStream_t stream, const DeviceInfo& dev,
+                                const Workspace& ws, bool clear_counters, bool* launched);
+cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 
 // The same GEMV with its split-K scratch in a fixed device array instead of
 // a workspace (no allocation).  The first call on a device looks up the
@@ -69,6 +78,26 @@ cudaError_t launch_gemm_q4_0_simt(const float* A, const uint8_t* wq, float* C, i
 
 // Count one kernel enqueued by the library.
 void note_launch();
+
+// Launch `kernel` with programmatic stream serialization: it may start while
+// the previous kernel on the stream is still running, as far as that kernel
+// allows (griddepcontrol.launch_dependents), and must itself execute
+// griddepcontrol.wait before touching memory that earlier work writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Read (and optionally clear) the device error words of the kernel files
 // that wait on asynchronous copies; ORs them into *bits.

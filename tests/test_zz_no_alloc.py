@@ -33,8 +33,8 @@ def env():
     return qm, oracle.load()
 
 
-# (M, N, K): K split 4 ways (M=1), 8 ways (M=8, filling the 1 MB scratch
-# exactly), and a ragged shape.
+# (M, N, K): shapes whose launch plan splits K on GB300 (152 SMs), so the
+# fixed scratch holds partial sums and arrival counters; the last is ragged.
 SHAPES = [(1, 1024, 4096), (8, 4096, 14336), (3, 300, 3840)]
 
 
