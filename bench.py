@@ -14,6 +14,12 @@ timed with CUDA events over --steps steps after --warmup steps.  ``e2e``
 repeats the step with host operands: pinned host -> device copies of every
 input and device -> host copies of every output inside the timed region.
 
+Beside the step, the line reports (keys ``m1_gemv``, ``decode_sweep``,
+``prefill``): back-to-back M=1 GEMVs at K=N=4096, the 32-layer decoder sweep
+at M=1 and M=8 replayed from a CUDA graph (weight GB/s against HBM), and the
+same sweep at M=512 (TFLOP/s against the tensor-core bound of the 3-MMA
+split).
+
 ``--impl reference`` times the CPU oracle instead (on a bounded sample of the
 same step, extrapolated per column), on the same metric.
 """
@@ -56,7 +62,8 @@ def measured_peaks() -> dict:
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-KERNEL_SOURCES = {"dequant_q4_0": "dequant.cu", "gemv_q4_0": "gemv.cu"}
+KERNEL_SOURCES = {"dequant_q4_0": "dequant.cu", "gemv_q4_0_tc": "gemv_tc.cu",
+                  "gemm_q4_0_tc": "gemm_tc.cu"}
 
 
 def source_digest(kernel: str) -> str:
@@ -334,14 +341,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = qm.qm_launch_count()
     barrier()
     t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        step(reps[i % REPLICAS], evs[i])
+        step(reps[i % REPLICAS])
     end.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -372,6 +378,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     else:
         ms_step = ms_local
 
+    # Per-kernel split, from a separate pass with events between the kernels
+    # (an event between two kernels also ends their programmatic overlap, so
+    # these times are slightly longer than their share of the timed step).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(reps[i % REPLICAS], evs[i])
+    torch.cuda.synchronize()
     per_op = {"gemv_up": [], "gemv_down": [], "dequant": []}
     for ev in evs:
         per_op["gemv_up"].append(ev[0].elapsed_time(ev[1]))
@@ -427,12 +440,12 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         ms = avg[key]
         flops = 2.0 * c.M * c.N * c.K
         paths[key] = {
+            "kernel": "gemv_q4_0_tc (mma.sync bf16 split, f32 accumulation)",
             "ms": ms, "weight_gbs": c.weight_bytes / (ms * 1e-3) / 1e9,
             "alg_gbs": gemv_bytes(c) / (ms * 1e-3) / 1e9,
             "hbm_frac": gemv_bytes(c) / (ms * 1e-3) / 1e9 / hbm,
             "tflops": flops / (ms * 1e-3) / 1e12,
-            "fp32_frac_max_clock": flops / (ms * 1e-3) / 1e12 / fp32_peak_max,
-            "bound_time_ms": max(gemv_bytes(c) / (hbm * 1e9), flops / (fp32_peak_max * 1e12)) * 1e3,
+            "bound_time_ms": gemv_bytes(c) / (hbm * 1e9) * 1e3,
         }
     paths["dequant"] = {"ms": avg["dequant"],
                         "alg_gbs": dequant_bytes(deq) / (avg["dequant"] * 1e-3) / 1e9,
@@ -448,17 +461,15 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     else:
         c = up if dominant == "gemv_up" else down
         achieved = paths[dominant]["alg_gbs"]
-        roofline = {"bound": "hbm", "kernel": "gemv_q4_0 (" + dominant + ")",
+        roofline = {"bound": "hbm", "kernel": "gemv_q4_0_tc (" + dominant + ")",
                     "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": measured_traffic("gemv_q4_0", c.name),
+                    "frac": achieved / hbm, "traffic": measured_traffic("gemv_q4_0_tc", c.name),
                     "peak_source": peaks["source"],
-                    "algorithmic_bytes_per_launch": gemv_bytes(c),
-                    "alu_tflops": paths[dominant]["tflops"], "fp32_peak_tflops_max_clock":
-                    fp32_peak_max, "fp32_peak_tflops_live_clock": fp32_peak_live}
+                    "algorithmic_bytes_per_launch": gemv_bytes(c)}
 
-    prefill = None
-    if not args.no_prefill:
-        prefill = prefill_leg(qm, dev, stream, fp32_peak_max, fp32_peak_live, peaks)
+    sweep = None
+    if not args.no_sweep:
+        sweep = sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -475,7 +486,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
-        "prefill": prefill,
+        "m1_gemv": sweep["m1_gemv"] if sweep else None,
+        "decode_sweep": sweep["decode"] if sweep else None,
+        "prefill": sweep["prefill"] if sweep else None,
         "clocks": clocks,
         "hbm_peak_gbs": hbm, "peak_source": peaks["source"],
     }
@@ -487,45 +500,125 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         dist.destroy_process_group()
 
 
-def prefill_leg(qm, dev, stream, fp32_peak_max, fp32_peak_live, peaks) -> dict:
-    """Prefill throughput: one decoder layer's seven projections (hidden 4096,
-    grouped-query attention) at M = 512, through qm_matmul_q4_0, timed with
-    CUDA events over several passes after warm-up.  Reported as TFLOP/s
-    (2*M*N*K) and as a fraction of the FP32 FMA peak at the maximum and at
-    the sampled SM clock."""
-    import torch
-    cases = [c for c in synth.workload(4, layers=1, sweep_m=(512,))]
-    sh = int(stream.cuda_stream)
-    bufs = []
-    for c in cases:
-        bufs.append((torch.from_numpy(c.acts()).to(dev), torch.from_numpy(c.weights()).to(dev),
-                     torch.empty((c.M, c.N), dtype=torch.float32, device=dev), c))
-    flops = sum(2.0 * c.M * c.N * c.K for c in cases)
-
-    def one_pass():
-        for a, w, o, c in bufs:
-            rc = qm.qm_matmul_q4_0_ptr(a.data_ptr(), w.data_ptr(), o.data_ptr(), c.M, c.N, c.K, sh)
-            if rc != qm.QM_OK:
-                raise RuntimeError(f"prefill {c.name}: {qm.qm_status_string(rc)}")
-
-    for _ in range(3):
-        one_pass()
+def graph_ms(torch, fn, passes: int = 5) -> float:
+    """Capture fn() (launches on the current stream) into a CUDA graph after two
+    eager warm-up calls, replay it, and return the best per-replay time (ms)."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+        fn()
     torch.cuda.synchronize()
-    passes = 5
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    g.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    best = float("inf")
     for _ in range(passes):
-        one_pass()
-    e1.record(stream)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return best
+
+
+def sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live) -> dict:
+    """The decoder sweep (32 layers of q, k, v, o, gate, up, down; hidden 4096,
+    grouped-query attention) at M = 1, 8 and 512 through qm_matmul_q4_0, plus
+    back-to-back M = 1 GEMVs at K = N = 4096.  Weights: all 32 layers resident
+    (3.93 GB, far beyond L2).  Activations: one synthetic A per (M, K), shared
+    by the layers (the projections are not chained: no attention and no
+    activation functions).  M = 1 and 8 replay a CUDA graph of the 224 launches
+    (what a decode loop does); M = 512 is launched eagerly."""
+    import torch
+    hbm = peaks["hbm_gbs"]
+    cases = synth.workload(4, layers=32, sweep_m=(1,))
+    weights = [torch.from_numpy(c.weights()).to(dev) for c in cases]
+    wbytes = sum(c.weight_bytes for c in cases)
+    layer_shapes = [(c.N, c.K) for c in cases[:7]]
+    sh = lambda: int(torch.cuda.current_stream().cuda_stream)  # noqa: E731
+
+    def sweep_fn(M, A, outs):
+        def fn():
+            s = sh()
+            for i, c in enumerate(cases):
+                o = outs[i % 7]
+                rc = qm.qm_matmul_q4_0_ptr(A[c.K].data_ptr(), weights[i].data_ptr(),
+                                           o.data_ptr(), M, c.N, c.K, s)
+                if rc != qm.QM_OK:
+                    raise RuntimeError(f"sweep {c.name} M={M}: {qm.qm_status_string(rc)}")
+        return fn
+
+    def acts(M):
+        return {K: torch.from_numpy(synth.activations(M, K, 5, key=(2, M, K))).to(dev)
+                for K in (4096, 14336)}
+
+    decode = {}
+    for M in (1, 8):
+        A = acts(M)
+        outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in layer_shapes]
+        ms = graph_ms(torch, sweep_fn(M, A, outs))
+        decode[f"m{M}"] = {"ms_per_pass": ms, "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+                           "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / hbm,
+                           "launches_per_pass": len(cases)}
+    decode["workload"] = ("32-layer decoder sweep (q,k,v,o,gate,up,down; hidden 4096, GQA), "
+                          "3.93 GB of Q4_0 weights per pass, CUDA graph of 224 GEMV launches")
+
+    # Back-to-back M = 1 GEMVs at K = N = 4096 (16 weight replicas > L2).
+    c0 = synth.workload(0)[0]
+    w0 = [torch.from_numpy(c0.weights()).to(dev) for _ in range(16)]
+    a0 = torch.from_numpy(c0.acts()).to(dev)
+    o0 = torch.empty((1, c0.N), dtype=torch.float32, device=dev)
+
+    def m1_fn():
+        s = sh()
+        for w in w0:
+            rc = qm.qm_matmul_q4_0_ptr(a0.data_ptr(), w.data_ptr(), o0.data_ptr(), 1, c0.N, c0.K, s)
+            if rc != qm.QM_OK:
+                raise RuntimeError(f"m1 gemv: {qm.qm_status_string(rc)}")
+    ms0 = graph_ms(torch, m1_fn) / len(w0)
+    m1 = {"workload": "GEMV M=1, K=N=4096 (9.44 MB of weights), 16 replicas back to back "
+                      "in a CUDA graph",
+          "us_per_gemv": ms0 * 1e3, "weight_gbs": c0.weight_bytes / (ms0 * 1e-3) / 1e9,
+          "hbm_frac": c0.weight_bytes / (ms0 * 1e-3) / 1e9 / hbm}
+    del w0
+
+    # Prefill: the same sweep at M = 512, eager launches.
+    A = acts(512)
+    outs = [torch.empty((512, N), dtype=torch.float32, device=dev) for (N, K) in layer_shapes]
+    fn = sweep_fn(512, A, outs)
+    fn()
+    torch.cuda.synchronize()
+    passes = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(passes):
+        fn()
+    e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / passes
+    flops = sum(2.0 * 512 * c.N * c.K for c in cases)
     tflops = flops / (ms * 1e-3) / 1e12
-    return {"workload": "decoder layer (q,k,v,o,gate,up,down) at M=512, hidden 4096",
-            "ms_per_layer": ms, "tflops": tflops, "roofline": {
-                "bound": "fp32_fma", "peak_tflops_max_clock": fp32_peak_max,
-                "frac_max_clock": tflops / fp32_peak_max,
-                "peak_tflops_live_clock": fp32_peak_live,
-                "frac_live_clock": (tflops / fp32_peak_live) if fp32_peak_live else None}}
+    bf16 = peaks["bf16_tflops"]
+    prefill = {
+        "workload": "32-layer decoder sweep at M=512 (7.15 TFLOP per pass), eager launches",
+        "kernel": "gemm_q4_0_tc (tcgen05, A split into bf16 hi+lo, W exact as two bf16 "
+                  "pieces, 3 MMAs per product, f32 accumulation in TMEM)",
+        "ms_per_pass": ms, "tflops": tflops,
+        "roofline": {
+            "bound": "tensor", "achieved": tflops, "peak": bf16 / 3.0, "unit": "TFLOP/s",
+            "frac": tflops / (bf16 / 3.0),
+            "peak_note": "measured bf16 dense peak / 3 MMAs per useful product",
+            "mma_tflops_issued": 3.0 * tflops, "bf16_peak_tflops": bf16,
+            "fp32_fma_peak_tflops_max_clock": fp32_peak_max,
+            "vs_fp32_fma_peak_max_clock": tflops / fp32_peak_max,
+            "fp32_fma_peak_tflops_live_clock": fp32_peak_live}}
+    del weights
+    torch.cuda.empty_cache()
+    return {"decode": decode, "m1_gemv": m1, "prefill": prefill}
 
 
 def main(argv=None) -> None:
@@ -536,8 +629,8 @@ def main(argv=None) -> None:
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true",
                    help="skip the CPU oracle timing (for profiler runs)")
-    p.add_argument("--no-prefill", action="store_true",
-                   help="skip the M=512 prefill report (for profiler runs)")
+    p.add_argument("--no-sweep", action="store_true",
+                   help="skip the M=1 GEMV, decoder-sweep and prefill reports (profiler runs)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -13,6 +13,11 @@
 // as 256 coalesced 16-byte streaming stores, prefetching the next step's
 // input while it writes.  A generic kernel (2-byte loads, 4- or 16-byte
 // stores) covers misaligned pointers and the last partial group.
+//
+// The fast kernel is launched with programmatic stream serialization: it lets
+// the next kernel start its prologue at once and, before waiting for the
+// kernels it depends on, only asks L2 for its first group (a hint that cannot
+// return stale data); every load and store comes after griddepcontrol.wait.
 #include "qm_device.cuh"
 #include "qm_internal.h"
 
@@ -44,6 +49,11 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32)
     uint8_t* buf = stage[warp];
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarpsPerCta;
     int64_t g = static_cast<int64_t>(blockIdx.x) * kWarpsPerCta + warp;
+
+    grid_launch_dependents();
+    if (g < n_groups && lane < 5)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(wq + g * kGroupInBytes + lane * 128));
+    grid_dependency_wait();
 
     uint4 r0 = make_uint4(0, 0, 0, 0), r1 = make_uint4(0, 0, 0, 0);
     if (g < n_groups) {
@@ -116,10 +126,10 @@ cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
         const int64_t ctas_needed = (n_groups + kWarpsPerCta - 1) / kWarpsPerCta;
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
         const int grid = static_cast<int>(ctas_needed < cap ? ctas_needed : cap);
-        dequant_q4_0_fast<<<grid, kWarpsPerCta * 32, 0, stream>>>(wq, n_groups, out);
-        note_launch();
-        cudaError_t err = cudaGetLastError();
+        cudaError_t err = launch_pdl(dequant_q4_0_fast, dim3(grid), dim3(kWarpsPerCta * 32), 0,
+                                     stream, wq, n_groups, out);
         if (err != cudaSuccess) return err;
+        note_launch();
     }
     const int64_t b_begin = n_groups * kGroupBlocks;
     const int64_t rest = n_blocks - b_begin;
