@@ -23,10 +23,20 @@
 //   * warp 1 owns the TMEM accumulator (128 lanes x 128 f32 columns) and one
 //     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16) per k-step,
 //     committing completion to the stages' "empty" barriers;
-//   * the epilogue reads TMEM with tcgen05.ld (each warp its 32-lane quarter)
-//     and writes C.  An entry that comes out infinite or NaN is recomputed
+//   * the epilogue reads TMEM with tcgen05.ld (each warp a 32 x 32 block of
+//     its 32-lane quarter), stages the block in shared memory (the freed
+//     activation stages) and writes C row by row, 16-byte stores when C's
+//     rows allow;
+//   * when there are fewer output tiles than SMs, K is split into S ranges
+//     (grid z): each CTA writes its partial tile to a workspace and the last
+//     of a tile's S CTAs to arrive adds the partials in range order, so the
+//     result does not depend on timing.  The arrival counters are zeroed by
+//     the A-split kernel that runs before every GEMM.  An entry that comes out infinite or NaN is recomputed
 //     element by element from A and the Q4_0 stream, so non-finite scales
 //     keep the per-element semantics.
+// Both kernels are launched with programmatic stream serialization: they let
+// the next kernel start its prologue early and wait (griddepcontrol.wait)
+// before touching global memory.
 // Every wait is bounded; a wait that gives up sets the device error word.
 #include <algorithm>
 
@@ -183,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_ahi,
                  const __grid_constant__ CUtensorMap map_alo,
                  const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
-                 const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K) {
+                 const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
+                 int c_vec, int S, float* __restrict__ partial, unsigned* __restrict__ ctr) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles, by indexing the shared array
     // itself so the compiler keeps every access below in the shared space.
@@ -205,8 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int m0 = static_cast<int>(blockIdx.y) * BM;
     const int n0 = static_cast<int>(blockIdx.x) * BN;
-    const int KT = K / BK;
+    const int KT = K / BK / S;  // k-steps of this CTA's K range (a multiple of 4)
+    const int split = static_cast<int>(blockIdx.z);
+    const int kt0 = split * KT;
 
+    grid_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAStages; ++s) {
             mbar_init(&a_full[s], 1);
@@ -235,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // A's pieces come from the split kernel before this one
 
     if (warp == 0) {
         if (lane == 0) {
@@ -250,15 +265,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         !mbar_wait_bounded(&raw_empty[rs], ((u / kRawStages) - 1) & 1, &g_gemm_error))
                         break;
                     mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
-                    tma_load_3d(raw + rs * kRawBytes, &map_w, 0, u, n0, &raw_full[rs]);
+                    tma_load_3d(raw + rs * kRawBytes, &map_w, 0, (kt0 >> 2) + u, n0, &raw_full[rs]);
                 }
                 const int as = kt % kAStages;
                 if (kt >= kAStages &&
                     !mbar_wait_bounded(&a_empty[as], ((kt / kAStages) - 1) & 1, &g_gemm_error))
                     break;
                 mbar_arrive_expect_tx(&a_full[as], 2 * kTile);
-                tma_load_2d(a_st + (2 * as) * kTile, &map_ahi, kt * BK, m0, &a_full[as]);
-                tma_load_2d(a_st + (2 * as + 1) * kTile, &map_alo, kt * BK, m0, &a_full[as]);
+                tma_load_2d(a_st + (2 * as) * kTile, &map_ahi, (kt0 + kt) * BK, m0, &a_full[as]);
+                tma_load_2d(a_st + (2 * as + 1) * kTile, &map_alo, (kt0 + kt) * BK, m0, &a_full[as]);
             }
         }
     } else if (warp == 1) {
@@ -315,27 +330,91 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) mbar_arrive(&raw_empty[rs]);
             }
         }
-        // Epilogue: TMEM lane quarter = warp % 4, 32 columns per warp.
-        if (mbar_wait_bounded(acc_full, 0, &g_gemm_error)) {
+        // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns the 32 x 32
+        // block of rows 32 q .. 32 q + 31 and columns 32 cq .. 32 cq + 31.  Lane
+        // i holds row i of the block; the block goes through shared memory (rows
+        // 36 floats apart: conflict-free 16-byte writes and reads) so that C is
+        // written a row at a time.  All MMAs have completed when acc_full fires,
+        // so the activation stages are free.
+        // (Warp-uniform decision: tcgen05.ld below is a warp-wide instruction.)
+        const bool acc_ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(acc_full, 0, &g_gemm_error));
+        static_assert(BN == 32 * (kDecodeWarps / 4), "one 32-column block per warp");
+        static_assert(kDecodeWarps * 32 * 36 * 4 <= kAStages * 2 * kTile, "staging space");
+        const int q = warp & 3;
+        const int cq = (warp - 2) >> 2;
+        const int col = 32 * cq;
+        const int mrow = m0 + 32 * q;
+        float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        if (acc_ok) {
             tc_fence_after();
-            const int q = warp & 3;
-            const int cq = (warp - 2) >> 2;  // 0..3
-            const int m = m0 + 32 * q + lane;
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+        }
+        // v[i]: row mrow + lane, column n0 + col + i.  Staged so that lane i
+        // then holds column i of every row.
 #pragma unroll
-            for (int cb = 0; cb < (BN / 32) / (kDecodeWarps / 4); ++cb) {
-                const int col = 32 * (cq * ((BN / 32) / (kDecodeWarps / 4)) + cb);
-                float v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
-                if (m < M) {
+        for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(stg + lane * 36 + 4 * j) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        __syncwarp();
+        const int nn = n0 + col + lane;  // this lane's column in the row-wise passes
+        if (S == 1) {
+            if (acc_ok) {
+                // Entries that came out non-finite: recompute element by element.
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int nn = n0 + col + i;
-                        if (nn < N) {
-                            float x = v[i];
-                            if (!isfinite(x)) x = entry_exact(A, wq, K, m, nn);
-                            C[static_cast<int64_t>(m) * N + nn] = x;
-                        }
+                for (int i = 0; i < 32; ++i) {
+                    if (!isfinite(v[i]) && mrow + lane < M && n0 + col + i < N)
+                        stg[lane * 36 + i] = entry_exact(A, wq, K, mrow + lane, n0 + col + i);
+                }
+                __syncwarp();
+                if (c_vec) {
+                    // 8 lanes per row, 16 bytes each: 4 rows per store instruction.
+                    const int c4 = lane & 7;
+                    const int n4 = n0 + col + 4 * c4;
+#pragma unroll
+                    for (int r4 = 0; r4 < 8; ++r4) {
+                        const int row = 4 * r4 + (lane >> 3);
+                        const float4 x = *reinterpret_cast<const float4*>(stg + row * 36 + 4 * c4);
+                        if (mrow + row < M && n4 < N)
+                            *reinterpret_cast<float4*>(C + static_cast<int64_t>(mrow + row) * N + n4) = x;
                     }
+                } else {
+                    for (int row = 0; row < 32; ++row) {
+                        if (mrow + row < M && nn < N)
+                            C[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
+                    }
+                }
+            }
+        } else {
+            // Split K: the partial tile to the workspace [S][M][N]; every decode
+            // warp reaches both barriers, whatever its waits returned.
+            float* pw = partial + static_cast<int64_t>(split) * M * N;
+            for (int row = 0; row < 32; ++row) {
+                if (mrow + row < M && nn < N)
+                    pw[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
+            }
+            __threadfence();
+            named_barrier_sync(1, kDecodeWarps * 32);
+            uint32_t* last = tmem_slot + 1;  // CTA-local broadcast of the arrival
+            if (threadIdx.x == 64) {
+                const int tile = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+                const unsigned old = atomicAdd(&ctr[tile], 1u);
+                *last = (old == static_cast<unsigned>(S - 1)) ? 1u : 0u;
+            }
+            named_barrier_sync(1, kDecodeWarps * 32);
+            if (*last != 0) {
+                // The last of the tile's S CTAs: add the partials in range order.
+                __threadfence();
+                for (int row = 0; row < 32; ++row) {
+                    const int m = mrow + row;
+                    if (m >= M || nn >= N) continue;
+                    float x = 0.f;
+                    for (int q2 = 0; q2 < S; ++q2)
+                        x += __ldcg(partial + (static_cast<int64_t>(q2) * M + m) * N + nn);
+                    if (!isfinite(x)) x = entry_exact(A, wq, K, m, nn);
+                    C[static_cast<int64_t>(m) * N + nn] = x;
                 }
             }
         }
@@ -352,9 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // A f32 -> bf16 hi = bf16(a), lo = bf16(a - hi) (lo = 0 where a - hi is not finite).
+// Also zeroes the split-K arrival counters of the GEMM that follows.
 __global__ void __launch_bounds__(256)
     split_bf16(const float4* __restrict__ a, uint2* __restrict__ hi, uint2* __restrict__ lo,
-               int64_t n4) {
+               int64_t n4, unsigned* __restrict__ ctr, int n_ctr) {
+    grid_launch_dependents();
+    grid_dependency_wait();  // the workspace may still be in use by an earlier GEMM
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0u;
+    }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const float4 v = __ldg(a + i);
@@ -381,21 +466,32 @@ bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, 
 
 cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
-    // bf16 hi / lo copies of A in the stream's prefill workspace.
+    // Split K when the output has fewer tiles than SMs: S ranges of whole
+    // 256-wide units, as many as fit one wave.
+    const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
+    int S = 1;
+    for (int c = 2; c <= 16; ++c) {
+        if ((K / 256) % c == 0 && tiles * c <= dev.sm_count) S = c;
+    }
+    // Workspace: bf16 hi / lo copies of A, then (S > 1) the partial tiles
+    // [S][M][N] and one arrival counter per tile.
     const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
+    const size_t part_bytes = (S > 1) ? static_cast<size_t>(S) * M * N * 4 : 0;
+    const size_t ctr_bytes = (S > 1) ? static_cast<size_t>(tiles) * 4 : 0;
     void* ws = nullptr;
-    cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes, &ws);
+    cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes + part_bytes + ctr_bytes, &ws);
     if (err != cudaSuccess) return err;
     auto* a_hi = static_cast<uint8_t*>(ws);
     auto* a_lo = a_hi + piece_bytes;
+    float* part = reinterpret_cast<float*>(a_lo + piece_bytes);
+    unsigned* ctr = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(part) + part_bytes);
     const int64_t n4 = M * K / 4;
     const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8);
-    split_bf16<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
-        reinterpret_cast<uint2*>(a_lo), n4);
-    note_launch();
-    err = cudaGetLastError();
+    err = launch_pdl(split_bf16, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                     reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
+                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(S > 1 ? tiles : 0));
     if (err != cudaSuccess) return err;
+    note_launch();
 
     CUtensorMap map_ahi, map_alo, map_w;
     const int64_t adims[2] = {K, M};
@@ -422,12 +518,15 @@ cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
         if (err != cudaSuccess) return err;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM));
-    gemm_q4_0_tc<<<grid, kThreads, kSmemBytes, stream>>>(map_ahi, map_alo, map_w, A, wq, C,
-                                                         static_cast<int>(M), static_cast<int>(N),
-                                                         static_cast<int>(K));
+    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM),
+                    static_cast<unsigned>(S));
+    const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
+    err = launch_pdl(gemm_q4_0_tc, grid, dim3(kThreads), kSmemBytes, stream, map_ahi, map_alo,
+                     map_w, A, wq, C, static_cast<int>(M), static_cast<int>(N),
+                     static_cast<int>(K), c_vec, S, part, ctr);
+    if (err != cudaSuccess) return err;
     note_launch();
-    return cudaGetLastError();
+    return cudaSuccess;
 }
 
 cudaError_t gemm_tc_read_device_error(unsigned int* bits, bool clear) {

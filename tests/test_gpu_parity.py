@@ -68,15 +68,16 @@ def assert_bits_equal(got, want):
     assert not bad.any(), f"{bad.sum()} elements differ, first at {np.argwhere(bad)[:4].ravel()}"
 
 
-def matmul_gpu(qm, A, blob, N, algo=0, a_off=0, w_off=0):
+def matmul_gpu(qm, A, blob, N, algo=0, a_off=0, w_off=0, c_off=0):
     """C through the C ABI with guard words around C; A and wq may sit at byte
-    offsets (multiples of 4 and 2) inside larger buffers."""
+    offsets (multiples of 4 and 2) inside larger buffers, and C c_off floats
+    past a 16-byte boundary."""
     M, K = A.shape
     a_raw = torch.zeros(A.size * 4 + 64, dtype=torch.uint8, device="cuda")
     a_raw[a_off:a_off + A.size * 4] = dev(A.view(np.uint8).ravel())
     w_raw = torch.zeros(blob.size + 64, dtype=torch.uint8, device="cuda")
     w_raw[w_off:w_off + blob.size] = dev(blob)
-    guard = 32
+    guard = 32 + c_off
     c_buf = torch.empty(M * N + 2 * guard, dtype=torch.int32, device="cuda")
     c_buf.fill_(GUARD_BITS)
     rc = qm.qm_matmul_q4_0_algo_ptr(a_raw.data_ptr() + a_off, w_raw.data_ptr() + w_off,
@@ -209,6 +210,19 @@ def test_gemm_tensor_cores(env, shape):
     A = synth.activations(M, K, 5 * M + K, dist="outliers")
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC), C_ref, S_ref, "tcgen05")
+
+
+@pytest.mark.parametrize("c_off", [1, 2])
+def test_gemm_tensor_cores_misaligned_c(env, c_off):
+    # C off a 16-byte boundary (N % 4 == 0): the epilogue's row stores fall
+    # back from 16-byte to 4-byte stores.
+    qm, o = env
+    M, N, K = 130, 256, 512
+    blob = synth.q4_0_weights(N, K, 90 + c_off)
+    A = synth.activations(M, K, 91 + c_off)
+    C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC, c_off=c_off), C_ref, S_ref,
+                 "tcgen05, misaligned C")
 
 
 def test_gemm_tensor_cores_unsupported_layouts(env):
