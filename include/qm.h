@@ -28,7 +28,13 @@
  *     synchronizes.  Calls are thread-safe.
  *   - Memory: the prefill GEMM on tensor cores keeps bf16 copies of A (4 bytes
  *     per element of A) in a per-(device, stream) buffer that grows with
- *     cudaMalloc as needed (growing synchronizes that stream once).
+ *     cudaMalloc as needed (growing synchronizes that stream once).  When it
+ *     splits K (outputs with fewer 128 x 128 tiles than SMs) the same buffer
+ *     also holds S x M x N floats of partial sums and one counter per tile.
+ *   - Launch: the fast kernels are launched with programmatic dependent
+ *     launch, so one may start its prologue while the previous kernel on the
+ *     stream finishes; it reads and writes memory only after that kernel has
+ *     completed, so stream order is kept exactly as for ordinary launches.
  *   - Memory: the GEMV (M <= 8) splits K over several CTAs when the matrix
  *     has few rows; their partial sums go through a workspace of about 8 MB
  *     that the library allocates with cudaMalloc on the first such call on
@@ -74,7 +80,8 @@ extern "C" {
 
 /* Algorithms for qm_matmul_q4_0_algo. */
 #define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks                          */
-#define QM_ALGO_GEMV 1      /* decode-regime GEMV, decode on tensor cores; M 1..8 */
+#define QM_ALGO_GEMV 1      /* decode-regime GEMV on tensor cores (mma.sync, bf16
+                               pieces, f32 sums); M 1..8                         */
 #define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
 #define QM_ALGO_GEMV_SIMT 3 /* decode-regime GEMV on FP32 FMA; M 1..8             */
 #define QM_ALGO_GEMM_TC 4   /* prefill GEMM on tcgen05 tensor cores (split bf16);
