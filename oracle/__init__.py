@@ -1,4 +1,5 @@
-"""CPU oracle for the GGML Q4_0 x f32 quantized matmul — TEST INFRASTRUCTURE ONLY.
+"""CPU oracle for the GGML Q4_0 x f32 quantized matmul and the Q8_0 dequant and
+quantize — TEST INFRASTRUCTURE ONLY.
 
 The arithmetic lives in ``qm_oracle.c`` (plain C99, fp64, single-threaded);
 this module compiles it with gcc and exposes it to numpy through ctypes.
@@ -7,15 +8,19 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 package imports nothing from it.
 
 Functions (all follow "fuel-vulkan-kernels — quantized (GGML) kernel
-contracts", sections ``dequant_q4_0``, ``qmatvec_q4_0`` and
-``matmul_q4_0_tiled``):
+contracts", sections ``dequant_q4_0``, ``qmatvec_q4_0``, ``matmul_q4_0_tiled``,
+``dequant_q8_0`` and ``quantize_q8_0``):
 
 * ``f16_to_double(bits)``      — binary16 decode, elementwise;
 * ``dequant_q4_0(blob)``       — block stream -> f32, ``(nibble - 8) * d``;
 * ``matmul_q4_0(A, blob, N, K)`` -> ``(C, S)`` in fp64, with
   ``S = sum_k |A[m,k] * W[n,k]|`` for the tolerance;
 * ``matmul_q4_0_entries(A, blob, N, K, m_idx, n_idx)`` — the same for chosen
-  entries only (sampled checks at full size).
+  entries only (sampled checks at full size);
+* ``float_to_f16(x)``          — f32 -> binary16 bits, round to nearest even;
+* ``dequant_q8_0(blob)``       — Q8_0 block stream -> f32, ``qs * d``;
+* ``quantize_q8_0(x)``         — f32 (a multiple of 32 elements) -> Q8_0 blocks,
+  with the readings stated in ``qm_oracle.h``.
 
 Every function is pinned by ``tests/test_oracle_pins.py``.
 """
@@ -35,6 +40,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32
+Q8_0_BLOCK_BYTES = 34
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +78,12 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_matmul_q4_0.restype = ctypes.c_int
     lib.oracle_matmul_q4_0_entries.argtypes = [p, p, i64, i64, i64, p, p, i64, p, p]
     lib.oracle_matmul_q4_0_entries.restype = ctypes.c_int
+    lib.oracle_float_to_f16_array.argtypes = [p, i64, p]
+    lib.oracle_float_to_f16_array.restype = None
+    lib.oracle_dequant_q8_0.argtypes = [p, i64, p]
+    lib.oracle_dequant_q8_0.restype = None
+    lib.oracle_quantize_q8_0.argtypes = [p, i64, p]
+    lib.oracle_quantize_q8_0.restype = None
     return lib
 
 
@@ -149,6 +161,31 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle rejected the sizes or indices")
         return C, S
+
+
+    def float_to_f16(self, x) -> np.ndarray:
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float32).ravel())
+        out = np.empty(x.size, dtype=np.uint16)
+        self.lib.oracle_float_to_f16_array(_ptr(x), x.size, _ptr(out))
+        return out
+
+    def dequant_q8_0(self, blob: np.ndarray) -> np.ndarray:
+        blob = np.ascontiguousarray(blob, dtype=np.uint8).ravel()
+        if blob.size % Q8_0_BLOCK_BYTES:
+            raise ValueError("blob length is not a multiple of 34 bytes")
+        n_blocks = blob.size // Q8_0_BLOCK_BYTES
+        out = np.empty(n_blocks * BLOCK_ELEMS, dtype=np.float32)
+        self.lib.oracle_dequant_q8_0(_ptr(blob), n_blocks, _ptr(out))
+        return out
+
+    def quantize_q8_0(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(np.asarray(x, dtype=np.float32).ravel())
+        if x.size % BLOCK_ELEMS:
+            raise ValueError("element count is not a multiple of 32")
+        n_blocks = x.size // BLOCK_ELEMS
+        blob = np.empty(n_blocks * Q8_0_BLOCK_BYTES, dtype=np.uint8)
+        self.lib.oracle_quantize_q8_0(_ptr(x), n_blocks, _ptr(blob))
+        return blob
 
 
 def within_tolerance(C_test, C_ref, S_ref, rel=1e-5, abs_=1e-7):

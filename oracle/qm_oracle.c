@@ -1,5 +1,6 @@
 /*
- * Oracle for the GGML Q4_0 x f32 quantized matmul — TEST INFRASTRUCTURE ONLY.
+ * Oracle for the GGML Q4_0 x f32 quantized matmul and the Q8_0 dequant and
+ * quantize — TEST INFRASTRUCTURE ONLY.
  * See qm_oracle.h for what it follows and who may use it.  Plain loops, fp64,
  * single-threaded, no blocking or reordering: a reader can check each line
  * against the definitions in the kernel-contract page
@@ -34,6 +35,40 @@ double oracle_f16_to_double(uint16_t h)
 void oracle_f16_to_double_array(const uint16_t* h, int64_t n, double* out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f16_to_double(h[i]);
+}
+
+/* binary16 from a value, by the definition: find the power of two 2^e below
+ * |x|; normals (e >= -14) keep 11 significant bits, i.e. a quantum of
+ * 2^(e-10); smaller values are multiples of 2^-24.  |x| / quantum is exact in
+ * double, and nearbyint rounds it to the nearest integer, ties to even (the
+ * default rounding mode).  Rounding up to 2^11 quanta moves to the next
+ * exponent.  The largest finite binary16 is 65504; halfway to the next step
+ * (65520) and beyond round to infinity. */
+static uint16_t float_to_f16(float xf)
+{
+    double x = (double)xf;
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    double a = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7E00u);
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7C00u);
+    if (a < ldexp(1.0, -14)) {
+        double m = nearbyint(a / ldexp(1.0, -24));  /* 0 .. 1024; 1024 is 2^-14 */
+        return (uint16_t)(sign | (uint16_t)m);
+    }
+    int e = 0;
+    frexp(a, &e);
+    e -= 1;  /* a in [2^e, 2^(e+1)) */
+    double m = nearbyint(a / ldexp(1.0, e - 10));  /* 1024 .. 2048 */
+    if (m == 2048.0) {
+        m = 1024.0;
+        e += 1;
+    }
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(m - 1024.0));
+}
+
+void oracle_float_to_f16_array(const float* x, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = float_to_f16(x[i]);
 }
 
 /* The block's scale d: bytes 0 and 1, little-endian binary16. */
@@ -72,6 +107,52 @@ void oracle_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out)
         for (int j = 0; j < ORACLE_Q4_0_BLOCK_ELEMS; ++j) {
             double x = (double)(block_nibble(block, j) - 8) * d;
             out[b * ORACLE_Q4_0_BLOCK_ELEMS + j] = (float)x;
+        }
+    }
+}
+
+/* Q8_0 dequant: quant j is the signed byte at block offset 2 + j. */
+void oracle_dequant_q8_0(const uint8_t* blob, int64_t n_blocks, float* out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const uint8_t* block = blob + b * ORACLE_Q8_0_BLOCK_BYTES;
+        double d = block_scale(block);
+        for (int j = 0; j < ORACLE_Q4_0_BLOCK_ELEMS; ++j) {
+            int qs = (int)(int8_t)block[2 + j];
+            out[b * ORACLE_Q4_0_BLOCK_ELEMS + j] = (float)((double)qs * d);
+        }
+    }
+}
+
+/* Q8_0 quantize, one block at a time, in the steps of the quantize section
+ * (readings in qm_oracle.h). */
+void oracle_quantize_q8_0(const float* x, int64_t n_blocks, uint8_t* blob)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        const float* xb = x + b * ORACLE_Q4_0_BLOCK_ELEMS;
+        uint8_t* block = blob + b * ORACLE_Q8_0_BLOCK_BYTES;
+        /* max |x| over the block; a NaN never compares greater */
+        float amax = 0.0f;
+        for (int j = 0; j < ORACLE_Q4_0_BLOCK_ELEMS; ++j) {
+            float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        uint16_t bits = float_to_f16(d);
+        block[0] = (uint8_t)(bits & 0xFF);
+        block[1] = (uint8_t)(bits >> 8);
+        for (int j = 0; j < ORACLE_Q4_0_BLOCK_ELEMS; ++j) {
+            int q = 0;
+            if (d != 0.0f) {
+                float t = xb[j] / d;
+                if (!isnan(t)) {
+                    double r = round((double)t);  /* halfway cases away from zero */
+                    if (r > 127.0) r = 127.0;
+                    if (r < -127.0) r = -127.0;
+                    q = (int)r;
+                }
+            }
+            block[2 + j] = (uint8_t)(int8_t)q;
         }
     }
 }

@@ -10,7 +10,12 @@ oracle disagrees with a fact that the kernel-contract page ("fuel-vulkan-kernels
 * closed forms (all-8 nibbles, zero scale, one-hot and all-ones activations);
 * agreement with an independent dense fp64 product (numpy) on dequantized
   weights, row-independence (M=1 against a row of M=8) and invariance under a
-  joint permutation of K-blocks.
+  joint permutation of K-blocks;
+* for Q8_0 (sections ``dequant_q8_0`` and ``quantize_q8_0``): hand-built
+  blocks and hand-worked quantizations (``tests/golden/``), numpy's own
+  float -> binary16 narrowing, an int8 x binary16 dequant written with numpy
+  views, the round-trip bound |qs d - x| <= d / 2, sign symmetry and
+  invariance of the quants under power-of-two scaling.
 
 The same functions run against copies of the oracle with a planted mistake
 (``test_oracle_mutants.py``); every such copy must fail at least one pin.
@@ -77,6 +82,47 @@ def load_golden_matmul():
 
 
 # ---------------------------------------------------------------- binary16
+
+def _parse_float(tok: str) -> float:
+    t = tok.lower()
+    if t.startswith("0x") or t.startswith("-0x"):
+        return float.fromhex(t)
+    return float(t)
+
+
+def load_golden_q8_0_blocks():
+    blocks, values = [], []
+    with open(os.path.join(GOLDEN, "q8_0_hand_blocks.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "block":
+                blocks.append(bytes(int(x, 16) for x in parts[1:]))
+                assert len(blocks[-1]) == 34
+            elif parts[0] == "values":
+                values.append(np.array([float(x) for x in parts[1:]], dtype=np.float32))
+                assert values[-1].size == 32
+    assert len(blocks) == len(values) and blocks
+    return blocks, values
+
+
+def load_golden_q8_0_quantize():
+    xs, blocks = [], []
+    with open(os.path.join(GOLDEN, "q8_0_hand_quantize.txt")) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#"):
+                continue
+            if parts[0] == "x":
+                xs.append(np.array([_parse_float(t) for t in parts[1:]], dtype=np.float32))
+                assert xs[-1].size == 32
+            elif parts[0] == "block":
+                blocks.append(bytes(int(x, 16) for x in parts[1:]))
+                assert len(blocks[-1]) == 34
+    assert len(xs) == len(blocks) and xs
+    return xs, blocks
+
 
 def pin_f16_exhaustive(o):
     bits = np.arange(65536, dtype=np.uint16)
@@ -213,7 +259,105 @@ def pin_entries_match_full(o):
     assert np.array_equal(Ce, C[mi, ni]) and np.array_equal(Se, S[mi, ni])
 
 
+# ---------------------------------------------------------------- Q8_0
+
+def pin_f16_narrowing_vs_numpy(o):
+    """f32 -> binary16 against numpy's conversion (round to nearest even):
+    every binary16 value, every midpoint between neighbours (the ties), values
+    just around the overflow threshold, and random floats over the range."""
+    h = np.arange(0x7C00, dtype=np.uint16)  # +0 .. largest finite
+    v = h.view(np.float16).astype(np.float32)
+    mids = ((v[:-1].astype(np.float64) + v[1:].astype(np.float64)) / 2).astype(np.float32)
+    g = synth.rng(13, (0,))
+    rnd = (g.standard_normal(20000) * np.exp(g.uniform(-25, 12, 20000))).astype(np.float32)
+    edge = np.float32([65504, 65510, 65519.996, 65520, 65536, 1e9, 2.0**-24, 2.0**-25,
+                       2.0**-25 * 1.0000001, 3 * 2.0**-26, 2.0**-14, 2.0**-14 * 0.99999994])
+    x = np.concatenate([v, -v, mids, -mids, rnd, edge, -edge, np.float32([np.inf, -np.inf])])
+    with np.errstate(over="ignore"):
+        want = x.astype(np.float16).view(np.uint16)
+    got = o.float_to_f16(x)
+    bad = got != want
+    assert not bad.any(), f"{bad.sum()} narrowings differ, e.g. x={x[bad][:3]}"
+    nan = o.float_to_f16(np.float32([np.nan]))[0]
+    assert (nan & 0x7C00) == 0x7C00 and (nan & 0x3FF) != 0, "NaN must stay NaN"
+
+
+def pin_q8_0_golden_blocks(o):
+    blocks, values = load_golden_q8_0_blocks()
+    got = o.dequant_q8_0(np.frombuffer(b"".join(blocks), dtype=np.uint8))
+    want = np.concatenate(values)
+    for i in range(len(blocks)):
+        sl = slice(32 * i, 32 * i + 32)
+        assert _same_bits_or_nan(got[sl], want[sl]), f"hand-built Q8_0 block {i} differs"
+
+
+def pin_q8_0_dequant_numpy(o):
+    """qs * d with numpy: the quants as an int8 view, d as a float16 view."""
+    g = synth.rng(14, (0,))
+    nb = 256
+    raw = g.integers(0, 256, size=(nb, 34), dtype=np.uint8)
+    d = (g.standard_normal(nb) * np.exp(g.uniform(-12, 8, nb))).astype(np.float16)
+    raw[:, 0:2] = d.view(np.uint8).reshape(nb, 2)
+    want = (raw[:, 2:].view(np.int8).astype(np.float64) *
+            raw[:, 0:2].copy().view(np.float16).astype(np.float64)).astype(np.float32)
+    got = o.dequant_q8_0(raw.ravel()).reshape(nb, 32)
+    assert _same_bits_or_nan(got, want), "Q8_0 dequant differs from qs * d"
+
+
+def pin_q8_0_golden_quantize(o):
+    xs, blocks = load_golden_q8_0_quantize()
+    got = o.quantize_q8_0(np.concatenate(xs)).reshape(len(xs), 34)
+    for i, b in enumerate(blocks):
+        want = np.frombuffer(b, dtype=np.uint8)
+        assert np.array_equal(got[i], want), f"hand-worked quantization {i} differs: {got[i][:8]}"
+
+
+def _q8_blocks(o, x):
+    blob = o.quantize_q8_0(x).reshape(-1, 34)
+    scale = blob[:, 0:2].copy().view(np.float16).ravel()
+    qs = blob[:, 2:].view(np.int8)
+    return blob, scale, qs
+
+
+def pin_q8_0_roundtrip_bound(o):
+    """For finite blocks whose scale stays in binary16's normal range: the
+    largest |x| gets |qs| = 127, every |qs d - x| <= d / 2 (d = max|x| / 127,
+    up to the f32 rounding of the quotient), and the stored scale is within
+    half a binary16 step of d."""
+    g = synth.rng(15, (0,))
+    nb = 4096
+    x = (g.standard_normal((nb, 32)) * np.exp(g.uniform(-4, 9, (nb, 1)))).astype(np.float32)
+    x[::7, 5] *= 40.0  # some outliers
+    _, scale, qs = _q8_blocks(o, x)
+    amax = np.max(np.abs(x).astype(np.float64), axis=1)
+    d = amax / 127.0
+    err = np.abs(qs.astype(np.float64) * d[:, None] - x.astype(np.float64))
+    assert np.all(err <= d[:, None] * (0.5 + 1e-6)), "a quant is more than d/2 off"
+    imax = np.argmax(np.abs(x), axis=1)
+    assert np.all(np.abs(qs[np.arange(nb), imax]) == 127), "the largest element must map to 127"
+    assert np.all(np.abs(scale.astype(np.float64) - d) <= d * 2.0**-11), "scale not near d"
+
+
+def pin_q8_0_symmetry_and_scaling(o):
+    """quantize(-x): same scale, negated quants; quantize(x * 2^k): same quants,
+    scale times 2^k (all in binary16's normal range)."""
+    g = synth.rng(16, (0,))
+    nb = 512
+    x = (g.standard_normal((nb, 32)) * np.exp(g.uniform(-2, 3, (nb, 1)))).astype(np.float32)
+    b0, s0, q0 = _q8_blocks(o, x)
+    b1, s1, q1 = _q8_blocks(o, -x)
+    assert np.array_equal(b0[:, 0:2], b1[:, 0:2]), "scale depends on the sign of x"
+    assert np.array_equal(q0.astype(np.int16), -q1.astype(np.int16)), "quants not odd in x"
+    for k in (-3, 5):
+        _, s2, q2 = _q8_blocks(o, x * np.float32(2.0**k))
+        assert np.array_equal(q0, q2), f"quants change under scaling by 2^{k}"
+        assert np.array_equal(s0.astype(np.float64) * 2.0**k, s2.astype(np.float64)), \
+            f"scale does not scale by 2^{k}"
+
+
 ALL_PINS = (pin_f16_exhaustive, pin_golden_blocks, pin_all8_and_zero_scale,
             pin_extreme_nibbles, pin_golden_matmul, pin_one_hot,
             pin_ones_closed_form, pin_dense_equivalence, pin_rows_independent,
-            pin_block_permutation, pin_entries_match_full)
+            pin_block_permutation, pin_entries_match_full,
+            pin_f16_narrowing_vs_numpy, pin_q8_0_golden_blocks, pin_q8_0_dequant_numpy,
+            pin_q8_0_golden_quantize, pin_q8_0_roundtrip_bound, pin_q8_0_symmetry_and_scaling)

@@ -47,6 +47,25 @@ MUTANTS = {
                                "double product = (double)A[k] * weight_at(wq, K, n, k);"),
     "weight_row_ignored": ("double product = (double)A[m * K + k] * weight_at(wq, K, n, k);",
                            "double product = (double)A[m * K + k] * weight_at(wq, K, 0, k);"),
+    # Q8_0 dequant and quantize, and the binary16 narrowing
+    "q8_dequant_unsigned": ("int qs = (int)(int8_t)block[2 + j];", "int qs = (int)block[2 + j];"),
+    "q8_dequant_stride_33": ("const uint8_t* block = blob + b * ORACLE_Q8_0_BLOCK_BYTES;",
+                             "const uint8_t* block = blob + b * 33;"),
+    "q8_divisor_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q8_ties_to_even": ("double r = round((double)t);", "double r = nearbyint((double)t);"),
+    "q8_divides_by_narrowed_d": ("float t = xb[j] / d;",
+                                 "float t = xb[j] / (float)oracle_f16_to_double(bits);"),
+    "q8_scale_big_endian": ("block[0] = (uint8_t)(bits & 0xFF);\n        block[1] = (uint8_t)(bits >> 8);",
+                            "block[1] = (uint8_t)(bits & 0xFF);\n        block[0] = (uint8_t)(bits >> 8);"),
+    "q8_max_without_abs": ("float a = fabsf(xb[j]);", "float a = xb[j];"),
+    "q8_quants_offset_128": ("block[2 + j] = (uint8_t)(int8_t)q;", "block[2 + j] = (uint8_t)(q + 128);"),
+    "q8_no_zero_scale_guard": ("if (d != 0.0f) {", "if (1) {"),
+    "q8_no_clamp": ("if (r > 127.0) r = 127.0;", ""),
+    "f16_narrow_truncates": ("double m = nearbyint(a / ldexp(1.0, e - 10));",
+                             "double m = floor(a / ldexp(1.0, e - 10));"),
+    "f16_narrow_overflow_early": ("if (a >= 65520.0)", "if (a > 65504.0)"),
+    "f16_narrow_subnormal_shift": ("double m = nearbyint(a / ldexp(1.0, -24));",
+                                   "double m = nearbyint(a / ldexp(1.0, -25));"),
 }
 
 
