@@ -1,4 +1,5 @@
-"""GGML Q4_0 x f32 quantized matmul and Q4_0 dequant on GB300 (sm_103a).
+"""GGML Q4_0 x f32 quantized matmul, Q4_0 dequant and Q8_0 dequant/quantize on
+GB300 (sm_103a).
 
 A thin Python binding over the C ABI of ``libqm.so`` (``include/qm.h``): it
 only marshals arguments.  Every step of the computation runs in the library's
@@ -8,6 +9,8 @@ library has not been built.  PyTorch supplies device memory and streams.
 Entry points (same names as the C ABI):
 
 * ``qm_dequant_q4_0(wq, out=None, stream=None)`` -> f32 tensor ``[n_blocks*32]``
+* ``qm_dequant_q8_0(wq, out=None, stream=None)`` -> f32 tensor ``[n_blocks*32]``
+* ``qm_quantize_q8_0(x, out=None, stream=None)`` -> uint8 tensor ``[n/32*34]``
 * ``qm_matmul_q4_0(A, wq, N, out=None, stream=None)`` -> f32 tensor ``[M, N]``
 * ``qm_matmul_q4_0_algo(A, wq, N, algo, out=None, stream=None)``
 * ``qm_device_status(stream=None, clear=True)``, ``qm_status_string(code)``,
@@ -26,6 +29,7 @@ __all__ = [
     "qm_dequant_q4_0", "qm_matmul_q4_0", "qm_matmul_q4_0_algo", "qm_device_status",
     "qm_launch_count",
     "qm_dequant_q4_0_ptr", "qm_matmul_q4_0_ptr", "qm_matmul_q4_0_algo_ptr",
+    "qm_dequant_q8_0", "qm_quantize_q8_0", "qm_dequant_q8_0_ptr", "qm_quantize_q8_0_ptr",
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
@@ -52,11 +56,12 @@ QM_ALGO_GEMM_TC = 4
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32
+Q8_0_BLOCK_BYTES = 34
 
 # Every symbol include/qm.h declares.
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
                     "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count",
-                    "qm_matmul_q4_0_noalloc")
+                    "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
@@ -101,6 +106,10 @@ def load_library() -> ctypes.CDLL:
             lib.qm_device_status.restype = i32
             lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
             lib.qm_matmul_q4_0_noalloc.restype = i32
+            lib.qm_dequant_q8_0.argtypes = [p, i64, p, p]
+            lib.qm_dequant_q8_0.restype = i32
+            lib.qm_quantize_q8_0.argtypes = [p, i64, p, p]
+            lib.qm_quantize_q8_0.restype = i32
             lib.qm_launch_count.argtypes = []
             lib.qm_launch_count.restype = ctypes.c_uint64
             _lib = lib
@@ -125,6 +134,14 @@ def _check(code: int, where: str) -> int:
 
 def qm_dequant_q4_0_ptr(wq: int, n_blocks: int, out: int, stream: int = 0) -> int:
     return load_library().qm_dequant_q4_0(wq, n_blocks, out, stream)
+
+
+def qm_dequant_q8_0_ptr(wq: int, n_blocks: int, out: int, stream: int = 0) -> int:
+    return load_library().qm_dequant_q8_0(wq, n_blocks, out, stream)
+
+
+def qm_quantize_q8_0_ptr(x: int, n_elements: int, out: int, stream: int = 0) -> int:
+    return load_library().qm_quantize_q8_0(x, n_elements, out, stream)
 
 
 def qm_matmul_q4_0_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, stream: int = 0) -> int:
@@ -178,6 +195,42 @@ def qm_dequant_q4_0(wq, out=None, stream=None):
         raise ValueError("out has the wrong number of elements")
     _check(qm_dequant_q4_0_ptr(wq.data_ptr(), n_blocks, out.data_ptr(), _stream_handle(stream)),
            "qm_dequant_q4_0")
+    return out
+
+
+def qm_dequant_q8_0(wq, out=None, stream=None):
+    """Dequantize a Q8_0 block stream (uint8 CUDA tensor, n_blocks*34 bytes)
+    into f32 ``[n_blocks*32]``."""
+    import torch
+    _require(wq, torch.uint8, "wq")
+    if wq.numel() % Q8_0_BLOCK_BYTES:
+        raise ValueError("wq length is not a multiple of 34 bytes")
+    n_blocks = wq.numel() // Q8_0_BLOCK_BYTES
+    if out is None:
+        out = torch.empty(n_blocks * BLOCK_ELEMS, dtype=torch.float32, device=wq.device)
+    _require(out, torch.float32, "out")
+    if out.numel() != n_blocks * BLOCK_ELEMS:
+        raise ValueError("out has the wrong number of elements")
+    _check(qm_dequant_q8_0_ptr(wq.data_ptr(), n_blocks, out.data_ptr(), _stream_handle(stream)),
+           "qm_dequant_q8_0")
+    return out
+
+
+def qm_quantize_q8_0(x, out=None, stream=None):
+    """Quantize f32 (a CUDA tensor of a multiple of 32 elements) into a Q8_0
+    block stream (uint8 ``[n/32*34]``)."""
+    import torch
+    _require(x, torch.float32, "x")
+    if x.numel() % BLOCK_ELEMS:
+        raise ValueError("x has a number of elements that is not a multiple of 32")
+    n_out = x.numel() // BLOCK_ELEMS * Q8_0_BLOCK_BYTES
+    if out is None:
+        out = torch.empty(n_out, dtype=torch.uint8, device=x.device)
+    _require(out, torch.uint8, "out")
+    if out.numel() != n_out:
+        raise ValueError("out has the wrong number of bytes")
+    _check(qm_quantize_q8_0_ptr(x.data_ptr(), x.numel(), out.data_ptr(), _stream_handle(stream)),
+           "qm_quantize_q8_0")
     return out
 
 

@@ -305,6 +305,41 @@ int qm_dequant_q4_0(const void* wq, int64_t n_blocks, float* out, void* stream) 
                                              static_cast<cudaStream_t>(stream), dev));
 }
 
+int qm_dequant_q8_0(const void* wq, int64_t n_blocks, float* out, void* stream) {
+    if (n_blocks < 0) return QM_ERR_SHAPE;
+    int64_t in_bytes, out_bytes;
+    if (!mul_ok(n_blocks, 34, &in_bytes) || !mul_ok(n_blocks, 128, &out_bytes)) return QM_ERR_SHAPE;
+    if (n_blocks == 0) return QM_OK;
+    if (!wq || !out) return QM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) != 0) return QM_ERR_ALIGN;
+    if (overlaps(out, out_bytes, wq, in_bytes)) return QM_ERR_ALIAS;
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    int rc = check_pointer(wq, dev.device);
+    if (rc == QM_OK) rc = check_pointer(out, dev.device);
+    if (rc != QM_OK) return rc;
+    return from_cuda(qm::launch_dequant_q8_0(static_cast<const uint8_t*>(wq), n_blocks, out,
+                                             static_cast<cudaStream_t>(stream), dev));
+}
+
+int qm_quantize_q8_0(const float* x, int64_t n_elements, void* out, void* stream) {
+    if (n_elements < 0 || (n_elements % 32) != 0) return QM_ERR_SHAPE;
+    const int64_t n_blocks = n_elements / 32;
+    int64_t in_bytes, out_bytes;
+    if (!mul_ok(n_elements, 4, &in_bytes) || !mul_ok(n_blocks, 34, &out_bytes)) return QM_ERR_SHAPE;
+    if (n_blocks == 0) return QM_OK;
+    if (!x || !out) return QM_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(x) & 3u) != 0) return QM_ERR_ALIGN;
+    if (overlaps(out, out_bytes, x, in_bytes)) return QM_ERR_ALIAS;
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    int rc = check_pointer(x, dev.device);
+    if (rc == QM_OK) rc = check_pointer(out, dev.device);
+    if (rc != QM_OK) return rc;
+    return from_cuda(qm::launch_quantize_q8_0(x, n_blocks, static_cast<uint8_t*>(out),
+                                              static_cast<cudaStream_t>(stream), dev));
+}
+
 int qm_matmul_q4_0(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
                    void* stream) {
     return matmul_impl(A, wq, C, M, N, K, QM_ALGO_AUTO, stream);

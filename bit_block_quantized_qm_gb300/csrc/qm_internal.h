@@ -39,6 +39,12 @@ cudaError_t encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, const void
 cudaError_t launch_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out,
                                 cudaStream_t stream, const DeviceInfo& dev);
 
+// Q8_0 block stream <-> f32 (q8_0.cu).
+cudaError_t launch_dequant_q8_0(const uint8_t* wq, int64_t n_blocks, float* out,
+                                cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t launch_quantize_q8_0(const float* x, int64_t n_blocks, uint8_t* out,
+                                 cudaStream_t stream, const DeviceInfo& dev);
+
 // Decode-regime GEMV, M = 1..8.  When wq and A are 16-byte aligned and
 // K % 256 == 0: the tensor-core GEMV (gemv_tc.cu) when tc, else the
 // persistent FP32 FMA kernel; otherwise the generic kernel.

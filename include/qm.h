@@ -1,6 +1,7 @@
 /*
- * qm.h — C ABI of libqm: the GGML Q4_0 x f32 quantized matmul and the Q4_0
- * dequant, as hand-written CUDA kernels for sm_103a (GB300).
+ * qm.h — C ABI of libqm: the GGML Q4_0 x f32 quantized matmul, the Q4_0
+ * dequant and the Q8_0 dequant and quantize, as hand-written CUDA kernels for
+ * sm_103a (GB300).
  *
  * Operations (defined in "fuel-vulkan-kernels — quantized (GGML) kernel
  * contracts", fuel-dispatch 0.20.71, kernel-contracts/vulkan/quantized.fkc.md):
@@ -108,6 +109,42 @@ QM_API const char* qm_status_string(int status);
  * Returns QM_OK or a negative status.
  */
 QM_API int qm_dequant_q4_0(const void* wq, int64_t n_blocks, float* out, void* stream);
+
+/*
+ * qm_dequant_q8_0 — section "dequant_q8_0": out[32*b + j] = qs_j(b) * d(b)
+ * for every block b < n_blocks and j < 32.  A Q8_0 block is 34 bytes: the
+ * scale d (IEEE binary16, little-endian) in bytes 0-1, then 32 signed 8-bit
+ * quants qs_0 .. qs_31.
+ *   wq       : n_blocks * 34 bytes, any alignment (16-byte aligned, with a
+ *              16-byte aligned out, takes the fast path).
+ *   n_blocks : number of blocks, >= 0.  0 enqueues nothing.
+ *   out      : n_blocks * 32 floats, 4-byte aligned; must not overlap wq.
+ * Exact: an 8-bit integer times a binary16 scale is representable in f32, so
+ * the result is bit-identical to the definition, including the sign of zero,
+ * infinities and NaN.  Returns QM_OK or a negative status.
+ */
+QM_API int qm_dequant_q8_0(const void* wq, int64_t n_blocks, float* out, void* stream);
+
+/*
+ * qm_quantize_q8_0 — section "quantize_q8_0": each block of 32 consecutive
+ * elements of x becomes one 34-byte Q8_0 block with d = max|x| / 127 and
+ * qs = round(x / d).  Where the section is silent this library takes:
+ *   - f32 arithmetic; d = max|x| / 127 and each x / d are single correctly
+ *     rounded f32 divisions; NaN elements do not raise the max;
+ *   - the stored scale is d narrowed to binary16, round to nearest even
+ *     (values from 65520 up become infinity);
+ *   - round() takes halfway cases away from zero; qs is clamped to
+ *     [-127, 127] (this binds only when d is an f32 subnormal);
+ *   - qs = 0 where d is 0 or x / d is NaN.
+ *   x          : n_elements floats, 4-byte aligned (16-byte aligned, with a
+ *                16-byte aligned out, takes the fast path).
+ *   n_elements : >= 0 and a multiple of 32, else QM_ERR_SHAPE.  0 enqueues
+ *                nothing.
+ *   out        : n_elements / 32 * 34 bytes, any alignment; must not overlap x.
+ * Deterministic: every block depends only on its own 32 inputs.
+ * Returns QM_OK or a negative status.
+ */
+QM_API int qm_quantize_q8_0(const float* x, int64_t n_elements, void* out, void* stream);
 
 /*
  * qm_matmul_q4_0 — C = A x dequant(W)^T (see the header comment).

@@ -106,3 +106,42 @@ def test_python_wrappers_validate_tensors():
         qm.qm_dequant_q4_0(torch.zeros(18, dtype=torch.float32))
     with pytest.raises(ValueError):
         qm.qm_dequant_q4_0(torch.zeros(18, dtype=torch.uint8))  # not a CUDA tensor
+
+
+def test_q8_0_argument_errors(lib):
+    # shapes: negative counts, quantize element counts not a multiple of 32,
+    # byte counts that overflow
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, -1, C_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, 1 << 62, C_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, -32, W_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, 33, W_ADDR) == qm.QM_ERR_SHAPE
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, 1 << 62, W_ADDR) == qm.QM_ERR_SHAPE
+    # empty inputs enqueue nothing
+    assert qm.qm_dequant_q8_0_ptr(0, 0, 0) == qm.QM_OK
+    assert qm.qm_quantize_q8_0_ptr(0, 0, 0) == qm.QM_OK
+    # null pointers
+    assert qm.qm_dequant_q8_0_ptr(0, 3, C_ADDR) == qm.QM_ERR_NULL
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, 3, 0) == qm.QM_ERR_NULL
+    assert qm.qm_quantize_q8_0_ptr(0, 64, W_ADDR) == qm.QM_ERR_NULL
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, 64, 0) == qm.QM_ERR_NULL
+    # alignment: dequant output and quantize input need 4 bytes; the block
+    # streams take any alignment
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, 3, C_ADDR + 2) == qm.QM_ERR_ALIGN
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR + 2, 64, W_ADDR) == qm.QM_ERR_ALIGN
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR + 1, 3, C_ADDR) in (qm.QM_ERR_CUDA, qm.QM_ERR_POINTER)
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, 64, W_ADDR + 1) in (qm.QM_ERR_CUDA, qm.QM_ERR_POINTER)
+    # aliasing: 4 blocks = 136 bytes in, 512 bytes out; 64 floats = 256 bytes
+    # in, 68 bytes out
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, 4, W_ADDR + 132) == qm.QM_ERR_ALIAS
+    assert qm.qm_quantize_q8_0_ptr(A_ADDR, 64, A_ADDR + 252) == qm.QM_ERR_ALIAS
+    assert qm.qm_dequant_q8_0_ptr(W_ADDR, 4, W_ADDR + 136) in (qm.QM_ERR_CUDA, qm.QM_ERR_POINTER)
+
+
+def test_q8_0_python_wrappers_validate_tensors():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(TypeError):
+        qm.qm_dequant_q8_0(torch.zeros(34, dtype=torch.float32))
+    with pytest.raises(ValueError):
+        qm.qm_dequant_q8_0(torch.zeros(34, dtype=torch.uint8))  # not a CUDA tensor
+    with pytest.raises(TypeError):
+        qm.qm_quantize_q8_0(torch.zeros(32, dtype=torch.float64))
