@@ -15,10 +15,11 @@ repeats the step with host operands: pinned host -> device copies of every
 input and device -> host copies of every output inside the timed region.
 
 Beside the step, the line reports (keys ``m1_gemv``, ``decode_sweep``,
-``prefill``): back-to-back M=1 GEMVs at K=N=4096, the 32-layer decoder sweep
-at M=1 and M=8 replayed from a CUDA graph (weight GB/s against HBM), and the
-same sweep at M=512 (TFLOP/s against the tensor-core bound of the 3-MMA
-split).
+``prefill``, ``q8_0``): back-to-back M=1 GEMVs at K=N=4096, the 32-layer
+decoder sweep at M=1 and M=8 replayed from a CUDA graph (weight GB/s against
+HBM), the same sweep at M=512 (TFLOP/s against the tensor-core bound of the
+3-MMA split), and the Q8_0 quantize and dequant of a 14336 x 4096 tensor (GB/s
+against HBM).
 
 ``--impl reference`` times the CPU oracle instead (on a bounded sample of the
 same step, extrapolated per column), on the same metric.
@@ -489,6 +490,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "m1_gemv": sweep["m1_gemv"] if sweep else None,
         "decode_sweep": sweep["decode"] if sweep else None,
         "prefill": sweep["prefill"] if sweep else None,
+        "q8_0": sweep["q8_0"] if sweep else None,
         "clocks": clocks,
         "hbm_peak_gbs": hbm, "peak_source": peaks["source"],
     }
@@ -618,7 +620,57 @@ def sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live) -> dict:
             "fp32_fma_peak_tflops_live_clock": fp32_peak_live}}
     del weights
     torch.cuda.empty_cache()
-    return {"decode": decode, "m1_gemv": m1, "prefill": prefill}
+    return {"decode": decode, "m1_gemv": m1, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks)}
+
+
+def q8_0_leg(qm, dev, peaks) -> dict:
+    """Q8_0 quantize and dequant of a 14336 x 4096 tensor (58.7 M elements),
+    4 rotating replicas (> L2), CUDA events over 20 calls each after warm-up.
+    Algorithmic bytes per call (the page's cost model): n * 4 + n * 1.0625."""
+    import torch
+    n = 14336 * 4096
+    reps = 4
+    g = synth.rng(6, (0,))
+    x_host = g.standard_normal(n).astype(np.float32)
+    xs = [torch.from_numpy(x_host).to(dev) for _ in range(reps)]
+    qs = [torch.empty(n // 32 * 34, dtype=torch.uint8, device=dev) for _ in range(reps)]
+    ys = [torch.empty(n, dtype=torch.float32, device=dev) for _ in range(reps)]
+    sh = int(torch.cuda.current_stream().cuda_stream)
+
+    def timed(fn, calls=20):
+        for i in range(4):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(calls):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / calls
+
+    def quant(i):
+        rc = qm.qm_quantize_q8_0_ptr(xs[i % reps].data_ptr(), n, qs[i % reps].data_ptr(), sh)
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"quantize_q8_0: {qm.qm_status_string(rc)}")
+
+    def deq(i):
+        rc = qm.qm_dequant_q8_0_ptr(qs[i % reps].data_ptr(), n // 32, ys[i % reps].data_ptr(), sh)
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"dequant_q8_0: {qm.qm_status_string(rc)}")
+
+    nbytes = n * 4 + n // 32 * 34
+    hbm = peaks["hbm_gbs"]
+    out = {"workload": "Q8_0 quantize and dequant of 14336 x 4096 f32 (58.7 M elements), "
+                       "4 rotating replicas",
+           "algorithmic_bytes_per_call": nbytes}
+    for name, fn in (("quantize", quant), ("dequant", deq)):
+        ms = timed(fn)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "gbs": gbs, "hbm_frac": gbs / hbm}
+    del xs, qs, ys
+    torch.cuda.empty_cache()
+    return out
 
 
 def main(argv=None) -> None:

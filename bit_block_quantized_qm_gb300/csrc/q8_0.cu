@@ -133,15 +133,33 @@ __device__ __forceinline__ int q8_quant(float x, float d) {
     return static_cast<int>(fminf(fmaxf(roundf(t), -127.f), 127.f));
 }
 
-__device__ __forceinline__ uint32_t pack_q4(int a, int b, int c, int d) {
-    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
-           ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
+// The quant byte of x, as q8_quant gives it, without a division in the
+// common case.  With r = 1/d correctly rounded and t' = x * r rounded,
+// t' = (x/d)(1 + e1)(1 + e2) and fl(x/d) = (x/d)(1 + e3), |e_i| <= 2^-24, so
+// |t' - fl(x/d)| <= 127.5 * (3 * 2^-24 + 2^-48) < 2.3e-5 when |t'| < 127.4.
+// Rounding t' to the nearest integer (adding 1.5 * 2^23 leaves it in the low
+// mantissa bits, two's complement for negatives) then gives the same integer
+// as rounding fl(x/d), half away from zero, unless t' is within 1e-4 of a
+// half-integer; those, and every t' out of range or not finite (d = 0, a
+// subnormal d whose reciprocal overflows, NaN or infinite x), take q8_quant.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ uint32_t q8_quant_byte(float x, float d, float r) {
+    const float t = __fmul_rn(x, r);
+    const float m = __fadd_rn(t, kRoundMagic);
+    const float ri = __fsub_rn(m, kRoundMagic);  // t rounded to an integer, exactly
+    if (fabsf(t) < 127.4f && fabsf(__fsub_rn(t, ri)) < 0.4999f) return __float_as_uint(m) & 0xFFu;
+    return static_cast<uint32_t>(q8_quant(x, d)) & 0xFFu;
+}
+
+__device__ __forceinline__ uint32_t pack_q4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    return a | (b << 8) | (c << 16) | (d << 24);
 }
 
 // 32 blocks per warp step: lane l loads float4 (32 i + l), i < 8, which holds
 // elements 4 (l % 8) .. +3 of block 4 i + l / 8; the 8 lanes of a block share
-// its max by shuffles, each quantizes its 4 elements, and the 34-byte blocks
-// are assembled in shared memory and written as 68 16-byte words.
+// its max by shuffles, each quantizes its 4 elements (q8_quant_byte), and the
+// 34-byte blocks are assembled in shared memory and written as 68 16-byte
+// words.
 __global__ void __launch_bounds__(kWarps * 32)
     quantize_q8_0_fast(const float* __restrict__ x, int64_t n_groups, uint8_t* __restrict__ out) {
     __shared__ __align__(16) uint8_t stage[kWarps][kGroupBytes];
@@ -159,6 +177,9 @@ __global__ void __launch_bounds__(kWarps * 32)
         float4 v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = __ldcs(src + 32 * i + lane);
+        // The max of block 4 i + l / 8 over its 8 lanes, then gathered so that
+        // lane l holds block l's: one division and one reciprocal per block.
+        float mine = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float m = fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w)));
@@ -166,15 +187,23 @@ __global__ void __launch_bounds__(kWarps * 32)
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-            const float d = __fdiv_rn(m, 127.f);
+            const float mb = __shfl_sync(0xFFFFFFFFu, m, 8 * (lane & 3));  // block 4 i + (lane & 3)
+            if ((lane >> 2) == i) mine = mb;
+        }
+        const float d_mine = __fdiv_rn(mine, 127.f);
+        const float r_mine = __frcp_rn(d_mine);
+        *reinterpret_cast<uint16_t*>(buf + lane * kQ8Bytes) = static_cast<uint16_t>(f16_bits_rn(d_mine));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
             const int b = 4 * i + (lane >> 3);
+            const float d = __shfl_sync(0xFFFFFFFFu, d_mine, b);
+            const float r = __shfl_sync(0xFFFFFFFFu, r_mine, b);
             uint8_t* blk = buf + b * kQ8Bytes;
-            const uint32_t w = pack_q4(q8_quant(v[i].x, d), q8_quant(v[i].y, d),
-                                       q8_quant(v[i].z, d), q8_quant(v[i].w, d));
+            const uint32_t w = pack_q4(q8_quant_byte(v[i].x, d, r), q8_quant_byte(v[i].y, d, r),
+                                       q8_quant_byte(v[i].z, d, r), q8_quant_byte(v[i].w, d, r));
             // Quant bytes 4 sub .. 4 sub + 3 at block offset 2 + 4 sub (2-byte aligned).
             *reinterpret_cast<uint16_t*>(blk + 2 + 4 * sub) = static_cast<uint16_t>(w & 0xFFFFu);
             *reinterpret_cast<uint16_t*>(blk + 4 + 4 * sub) = static_cast<uint16_t>(w >> 16);
-            if (sub == 0) *reinterpret_cast<uint16_t*>(blk) = static_cast<uint16_t>(f16_bits_rn(d));
         }
         __syncwarp();
         uint8_t* dst = out + g * kGroupBytes;
