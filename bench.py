@@ -673,6 +673,40 @@ def q8_0_leg(qm, dev, peaks) -> dict:
     return out
 
 
+def profile_case(args) -> None:
+    """Run one operation a few times on cuda:0 and exit, for profiler captures
+    (``--profile-case gemm --M .. --N .. --K ..`` or ``--profile-case q8_0``).
+    Prints a one-line note, not a bench line."""
+    import torch
+    import bit_block_quantized_qm_gb300 as qm
+    qm.load_library()
+    dev = torch.device("cuda", 0)
+    sh = int(torch.cuda.current_stream().cuda_stream)
+    if args.profile_case == "gemm":
+        M, N, K = args.M, args.N, args.K
+        blob = synth.q4_0_weights(N, K, 1)
+        A = synth.activations(M, K, 2)
+        w = torch.from_numpy(blob).to(dev)
+        a = torch.from_numpy(A).to(dev)
+        c = torch.empty((M, N), dtype=torch.float32, device=dev)
+        for _ in range(args.calls):
+            rc = qm.qm_matmul_q4_0_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, sh)
+            if rc != qm.QM_OK:
+                raise RuntimeError(qm.qm_status_string(rc))
+    else:
+        n = 14336 * 4096
+        x = torch.from_numpy(synth.rng(6, (0,)).standard_normal(n).astype(np.float32)).to(dev)
+        q = torch.empty(n // 32 * 34, dtype=torch.uint8, device=dev)
+        y = torch.empty(n, dtype=torch.float32, device=dev)
+        for _ in range(args.calls):
+            for rc in (qm.qm_quantize_q8_0_ptr(x.data_ptr(), n, q.data_ptr(), sh),
+                       qm.qm_dequant_q8_0_ptr(q.data_ptr(), n // 32, y.data_ptr(), sh)):
+                if rc != qm.QM_OK:
+                    raise RuntimeError(qm.qm_status_string(rc))
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_case": args.profile_case, "calls": args.calls}), flush=True)
+
+
 def main(argv=None) -> None:
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -683,7 +717,16 @@ def main(argv=None) -> None:
                    help="skip the CPU oracle timing (for profiler runs)")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the M=1 GEMV, decoder-sweep and prefill reports (profiler runs)")
+    p.add_argument("--profile-case", choices=("gemm", "q8_0"), default=None,
+                   help="run one operation a few times and exit (profiler captures)")
+    p.add_argument("--M", type=int, default=512)
+    p.add_argument("--N", type=int, default=4096)
+    p.add_argument("--K", type=int, default=4096)
+    p.add_argument("--calls", type=int, default=3)
     args = p.parse_args(argv)
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
     rank = int(os.environ.get("RANK", "0"))

@@ -180,3 +180,26 @@ def test_q8_0_deterministic(env):
     a = quantize_gpu(qm, x)
     b = quantize_gpu(qm, x)
     assert np.array_equal(a, b)
+
+
+def test_quantize_q8_0_near_half_integers(env):
+    # Elements within a few ulp of (k + 1/2) * d for random block scales: the
+    # quotient x / d sits at a rounding boundary, where the kernel must decide
+    # exactly as rounding the correctly rounded quotient does.
+    qm, o = env
+    g = synth.rng(10, (83,))
+    nb = 8192
+    amax = np.exp(g.uniform(-20, 20, nb)).astype(np.float32)
+    d = (amax / np.float32(127)).astype(np.float32)
+    k = g.integers(-126, 126, size=(nb, 31)).astype(np.float32)
+    x = ((k + np.float32(0.5)) * d[:, None]).astype(np.float32)
+    steps = g.integers(-3, 4, size=(nb, 31))
+    x = np.nextafter(x, np.where(steps >= 0, np.inf, -np.inf).astype(np.float32)) * (steps != 0) + x * (steps == 0)
+    for s in range(2, 4):
+        far = np.abs(steps) >= s
+        x[far] = np.nextafter(x[far], np.where(steps[far] > 0, np.inf, -np.inf).astype(np.float32))
+    blocks = np.concatenate([amax[:, None], x.astype(np.float32)], axis=1).astype(np.float32)
+    got = quantize_gpu(qm, blocks)
+    want = o.quantize_q8_0(blocks)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, f"{bad.size} bytes differ; first block {bad[0] // 34}"
