@@ -405,16 +405,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_barrier_sync(1, kDecodeWarps * 32);
             if (*last != 0) {
-                // The last of the tile's S CTAs: add the partials in range order.
+                // The last of the tile's S CTAs: add the partials in range
+                // order, 8 rows at a time so that 8 * S loads are in flight
+                // together (one row at a time would serialise 32 L2 round trips).
                 __threadfence();
-                for (int row = 0; row < 32; ++row) {
-                    const int m = mrow + row;
-                    if (m >= M || nn >= N) continue;
-                    float x = 0.f;
-                    for (int q2 = 0; q2 < S; ++q2)
-                        x += __ldcg(partial + (static_cast<int64_t>(q2) * M + m) * N + nn);
-                    if (!isfinite(x)) x = entry_exact(A, wq, K, m, nn);
-                    C[static_cast<int64_t>(m) * N + nn] = x;
+                for (int r0 = 0; r0 < 32; r0 += 8) {
+                    float x[8];
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
+                    for (int q2 = 0; q2 < S; ++q2) {
+                        const float* pq = partial + static_cast<int64_t>(q2) * M * N;
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr) {
+                            const int m = mrow + r0 + rr;
+                            if (m < M && nn < N) x[rr] += __ldcg(pq + static_cast<int64_t>(m) * N + nn);
+                        }
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr) {
+                        const int m = mrow + r0 + rr;
+                        if (m >= M || nn >= N) continue;
+                        float v = x[rr];
+                        if (!isfinite(v)) v = entry_exact(A, wq, K, m, nn);
+                        C[static_cast<int64_t>(m) * N + nn] = v;
+                    }
                 }
             }
         }
