@@ -569,6 +569,32 @@ def sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live) -> dict:
     decode["workload"] = ("32-layer decoder sweep (q,k,v,o,gate,up,down; hidden 4096, GQA), "
                           "3.93 GB of Q4_0 weights per pass, CUDA graph of 224 GEMV launches")
 
+    # The same weights with q|k|v and gate|up stacked by rows (one row-major
+    # block stream each, as an engine with fused projections stores them):
+    # 4 GEMVs per layer, 128 launches per pass.
+    fused, fused_shapes = [], []
+    for layer in range(32):
+        w = weights[7 * layer:7 * layer + 7]
+        fused += [torch.cat([w[0], w[1], w[2]]), w[3], torch.cat([w[4], w[5]]), w[6]]
+    fused_shapes = [(4096 + 1024 + 1024, 4096), (4096, 4096), (2 * 14336, 4096), (4096, 14336)]
+    for M in (1, 8):
+        A = acts(M)
+        outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in fused_shapes]
+
+        def fused_fn(M=M, A=A, outs=outs):
+            s = sh()
+            for i, wf in enumerate(fused):
+                N, K = fused_shapes[i % 4]
+                rc = qm.qm_matmul_q4_0_ptr(A[K].data_ptr(), wf.data_ptr(), outs[i % 4].data_ptr(),
+                                           M, N, K, s)
+                if rc != qm.QM_OK:
+                    raise RuntimeError(f"fused sweep M={M}: {qm.qm_status_string(rc)}")
+        ms = graph_ms(torch, fused_fn)
+        decode[f"m{M}_fused_layout"] = {"ms_per_pass": ms, "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
+                                        "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / hbm,
+                                        "launches_per_pass": len(fused)}
+    del fused
+
     # Back-to-back M = 1 GEMVs at K = N = 4096 (16 weight replicas > L2).
     c0 = synth.workload(0)[0]
     w0 = [torch.from_numpy(c0.weights()).to(dev) for _ in range(16)]
