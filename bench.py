@@ -701,7 +701,8 @@ def q8_0_leg(qm, dev, peaks) -> dict:
 
 def profile_case(args) -> None:
     """Run one operation a few times on cuda:0 and exit, for profiler captures
-    (``--profile-case gemm --M .. --N .. --K ..`` or ``--profile-case q8_0``).
+    (``--profile-case gemm --M .. --N .. --K .. [--algo QM_ALGO_*]``, any M,
+    or ``--profile-case q8_0``).
     Prints a one-line note, not a bench line."""
     import torch
     import bit_block_quantized_qm_gb300 as qm
@@ -716,7 +717,8 @@ def profile_case(args) -> None:
         a = torch.from_numpy(A).to(dev)
         c = torch.empty((M, N), dtype=torch.float32, device=dev)
         for _ in range(args.calls):
-            rc = qm.qm_matmul_q4_0_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, sh)
+            rc = qm.qm_matmul_q4_0_algo_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K,
+                                            args.algo, sh)
             if rc != qm.QM_OK:
                 raise RuntimeError(qm.qm_status_string(rc))
     else:
@@ -749,6 +751,8 @@ def main(argv=None) -> None:
     p.add_argument("--N", type=int, default=4096)
     p.add_argument("--K", type=int, default=4096)
     p.add_argument("--calls", type=int, default=3)
+    p.add_argument("--algo", type=int, default=0,
+                   help="QM_ALGO_* value for --profile-case gemm (0: automatic choice)")
     args = p.parse_args(argv)
     if args.profile_case:
         profile_case(args)

@@ -34,6 +34,7 @@ __all__ = [
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
+    "QM_ALGO_GEMV_PK",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -53,6 +54,7 @@ QM_ALGO_GEMV = 1
 QM_ALGO_GEMM_SIMT = 2
 QM_ALGO_GEMV_SIMT = 3
 QM_ALGO_GEMM_TC = 4
+QM_ALGO_GEMV_PK = 5
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32

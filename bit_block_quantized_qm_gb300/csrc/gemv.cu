@@ -587,14 +587,16 @@ cudaError_t launch_generic(const float* A, const uint8_t* wq, float* C, int64_t 
 
 template <int M>
 cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
-                     cudaStream_t stream, const DeviceInfo& dev, bool tc) {
+                     cudaStream_t stream, const DeviceInfo& dev, GemvKind kind) {
     if (persistent_ok(A, wq, N, K)) {
         Workspace ws;
         cudaError_t err = stream_workspace(dev, stream, &ws);
         if (err != cudaSuccess) return err;
         bool launched = false;
-        err = tc ? launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws, false, &launched)
-                 : launch_persistent<M>(A, wq, C, N, K, stream, dev, ws, false, &launched);
+        err = kind == GemvKind::kSimt
+                  ? launch_persistent<M>(A, wq, C, N, K, stream, dev, ws, false, &launched)
+                  : launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws,
+                                        kind == GemvKind::kPacked, false, &launched);
         if (err != cudaSuccess || launched) return err;
     }
     return launch_generic<M>(A, wq, C, N, K, stream, dev);
@@ -603,16 +605,16 @@ cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int
 }  // namespace
 
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
-                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool tc) {
+                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, GemvKind kind) {
     switch (M) {
-        case 1: return launch_m<1>(A, wq, C, N, K, stream, dev, tc);
-        case 2: return launch_m<2>(A, wq, C, N, K, stream, dev, tc);
-        case 3: return launch_m<3>(A, wq, C, N, K, stream, dev, tc);
-        case 4: return launch_m<4>(A, wq, C, N, K, stream, dev, tc);
-        case 5: return launch_m<5>(A, wq, C, N, K, stream, dev, tc);
-        case 6: return launch_m<6>(A, wq, C, N, K, stream, dev, tc);
-        case 7: return launch_m<7>(A, wq, C, N, K, stream, dev, tc);
-        case 8: return launch_m<8>(A, wq, C, N, K, stream, dev, tc);
+        case 1: return launch_m<1>(A, wq, C, N, K, stream, dev, kind);
+        case 2: return launch_m<2>(A, wq, C, N, K, stream, dev, kind);
+        case 3: return launch_m<3>(A, wq, C, N, K, stream, dev, kind);
+        case 4: return launch_m<4>(A, wq, C, N, K, stream, dev, kind);
+        case 5: return launch_m<5>(A, wq, C, N, K, stream, dev, kind);
+        case 6: return launch_m<6>(A, wq, C, N, K, stream, dev, kind);
+        case 7: return launch_m<7>(A, wq, C, N, K, stream, dev, kind);
+        case 8: return launch_m<8>(A, wq, C, N, K, stream, dev, kind);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -675,7 +677,8 @@ cudaError_t launch_m_noalloc(const float* A, const uint8_t* wq, float* C, int64_
         // The arrival counters must start at zero; the array keeps whatever
         // the previous call (or an abandoned one) left, so clear them first.
         bool launched = false;
-        err = launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws, true, &launched);
+        err = launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws,
+                                  gemv_auto_kind(M, N, K) == GemvKind::kPacked, true, &launched);
         if (err != cudaSuccess || launched) return err;
     }
     return launch_generic<M>(A, wq, C, N, K, stream, dev);

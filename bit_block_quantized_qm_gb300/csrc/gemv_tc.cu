@@ -63,13 +63,17 @@ namespace {
 
 constexpr int kUnitBytes = 144;
 constexpr int kUnitElems = 256;
-constexpr int kGroupRows = 16;
-constexpr int kGroupBytes = kGroupRows * kUnitBytes;  // one tile: 2304 bytes
-constexpr int kMaxWarps = 16;                         // consumer warps
-constexpr int kThreadsMax = (kMaxWarps + 1) * 32;     // + producer warp
-constexpr int kMaxStages = 8;
+// Rows of one warp tile: 16 for the MMA consumer, 32 (one per lane) for the
+// packed FP32 consumer.
+__host__ __device__ constexpr int group_rows(bool packed) { return packed ? 32 : 16; }
+// Consumer warps at most (the MMA consumer needs more registers per thread).
+__host__ __device__ constexpr int max_warps(bool packed) { return packed ? 24 : 16; }
+// Threads of a CTA at most: the consumers and the producer warp.
+__host__ __device__ constexpr int max_threads(bool packed) { return (max_warps(packed) + 1) * 32; }
+constexpr int kMaxStages = 12;
 constexpr int kMaxSplits = 16;
-constexpr int kSlotFloats = kGroupRows * 8;  // one warp's D tile, 16 rows x 8 columns
+// One warp's partial sums at the end of a row block: group rows x 8 columns.
+__host__ __device__ constexpr int slot_floats(bool packed) { return group_rows(packed) * 8; }
 
 struct TcPlan {
     const uint8_t* wq;  // the weight stream (read directly only by the exact fix-up)
@@ -79,7 +83,8 @@ struct TcPlan {
     int RG;         // row groups, ceil(N / 16)
     int S;          // K ranges; range s is units [s U / S, (s + 1) U / S)
     int rps;        // row groups per row block
-    int c;          // units per stage; rps * c consumer warps
+    int c;          // units per stage (rps * c tiles)
+    int hs;         // warps per tile: 1 (whole unit) or 2 (half a unit each)
     int rbpc;       // row blocks per CTA
     int nu_max;     // units in the largest K range
     int stages;     // ring depth
@@ -235,15 +240,17 @@ __device__ __forceinline__ void block_mma(uint32_t Qa, uint32_t Qb, float da, fl
     acc[3] = fmaf(db, D[3], acc[3]);
 }
 
-// One tile: rows r0 (row g) and r1 (row g + 8) of a unit in shared memory, the
-// unit's fragments F.
-template <int M>
-__device__ __forceinline__ void tile_mma(const uint8_t* r0, const uint8_t* r1, const uint2* F,
-                                         int gc, int t, uint32_t xoff, uint32_t sel, float acc[4]) {
+// NP block pairs of a tile from pair pp0 on (a whole unit: NP = 4, pp0 = 0;
+// half h of it: NP = 2, pp0 = 2h): rows r0 (row g) and r1 (row g + 8) of a
+// unit in shared memory, the unit's fragments F.
+template <int M, int NP>
+__device__ __forceinline__ void pairs_mma(const uint8_t* r0, const uint8_t* r1, const uint2* F, int pp0,
+                                          int gc, int t, uint32_t xoff, uint32_t sel, float acc[4]) {
     constexpr int kEntriesPerBlock = 2 * tc_sets<M>() * frag_cols<M>() * 4;
     const uint32_t yoff = 20 + 4 * t;
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
+    for (int i = 0; i < NP; ++i) {
+        const int pp = pp0 + i;
         const uint8_t* a = r0 + 36 * pp;
         const uint8_t* b = r1 + 36 * pp;
         const uint32_t w0a = lds_u32(a), w4a = lds_u32(a + 16), xa = lds_u32(a + xoff),
@@ -258,20 +265,177 @@ __device__ __forceinline__ void tile_mma(const uint8_t* r0, const uint8_t* r1, c
     }
 }
 
+// ---------------------------------------------------------------------------
+// Packed FP32 consumer (lane = row): a lane reads half of its row's 144-byte
+// unit (72 bytes, two block pairs) with four 16-byte loads and one 8-byte load
+// (rows 144 bytes apart put the 8 lanes of a quarter-warp on distinct bank
+// quads) and realigns the even blocks' quants with byte permutes.  Each nibble
+// q goes into bits 16..19 of a word whose top byte is 0x43, which reads as the
+// float 128 + q; one packed FMA per pair, x * d - 136 d, then gives (q - 8) * d
+// exactly (136 d and (q - 8) d have at most 19 significant bits), and a second
+// packed FMA (fma.rn.f32x2) adds its product with the activation into the
+// row's sums.  A non-finite d makes the row's total non-finite, which the
+// epilogue recomputes element by element.
+
+// Selectors of __byte_perm(v, 0x43000000, s): byte i of v into bits 16..23,
+// 0x43 into the top byte, zeros below.
+constexpr uint32_t kPkHigh = 0x43000000u;
+__host__ __device__ constexpr uint32_t pk_sel(int i) { return 0x7044u | (static_cast<uint32_t>(i) << 8); }
+
+// One block: quant words q (elements j and j + 16 in byte j of the 16), its
+// d pair and bias pair (-136 d), activations a (f32 [M][256] at the block).
 template <int M>
-__global__ void __launch_bounds__(kThreadsMax, 1)
+__device__ __forceinline__ void block_dot_pk(const float* a, const uint32_t q[4], float2 d2, float2 b2,
+                                             float2 (&s)[M][2]) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const uint32_t lo = q[w] & 0x0F0F0F0Fu;         // elements 4w .. 4w+3
+        const uint32_t hi = (q[w] >> 4) & 0x0F0F0F0Fu;  // elements 16+4w .. 16+4w+3
+        float2 v[4];
+        v[0] = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(lo, kPkHigh, pk_sel(0))),
+                                      __uint_as_float(__byte_perm(lo, kPkHigh, pk_sel(1)))), d2, b2);
+        v[1] = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(lo, kPkHigh, pk_sel(2))),
+                                      __uint_as_float(__byte_perm(lo, kPkHigh, pk_sel(3)))), d2, b2);
+        v[2] = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(hi, kPkHigh, pk_sel(0))),
+                                      __uint_as_float(__byte_perm(hi, kPkHigh, pk_sel(1)))), d2, b2);
+        v[3] = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(hi, kPkHigh, pk_sel(2))),
+                                      __uint_as_float(__byte_perm(hi, kPkHigh, pk_sel(3)))), d2, b2);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const float4 al = *reinterpret_cast<const float4*>(a + m * kUnitElems + 4 * w);
+            const float4 ah = *reinterpret_cast<const float4*>(a + m * kUnitElems + 16 + 4 * w);
+            s[m][0] = __ffma2_rn(make_float2(al.x, al.y), v[0], s[m][0]);
+            s[m][1] = __ffma2_rn(make_float2(al.z, al.w), v[1], s[m][1]);
+            s[m][0] = __ffma2_rn(make_float2(ah.x, ah.y), v[2], s[m][0]);
+            s[m][1] = __ffma2_rn(make_float2(ah.z, ah.w), v[3], s[m][1]);
+        }
+    }
+}
+
+__device__ __forceinline__ void pk_scale(uint32_t bits16, float2& d2, float2& b2) {
+    const float d = f16_bits_to_float(bits16);
+    const float b = -136.0f * d;
+    d2 = make_float2(d, d);
+    b2 = make_float2(b, b);
+}
+
+// A whole unit (8 blocks, nine 16-byte loads) of this lane's row against the
+// unit's activations a (f32 [M][256] in shared memory).  acc holds the row's
+// sums as two float pairs per activation row.
+template <int M>
+__device__ __forceinline__ void unit_dot_pk(const uint8_t* row, const float* a, float (&acc)[4 * M]) {
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+        w[4 * i + 0] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    float2 s[M][2];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        s[m][0] = make_float2(acc[4 * m + 0], acc[4 * m + 1]);
+        s[m][1] = make_float2(acc[4 * m + 2], acc[4 * m + 3]);
+    }
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) {
+        const uint32_t* Wp = w + 9 * pp;
+        float2 d2, b2;
+        const uint32_t qa[4] = {__byte_perm(Wp[0], Wp[1], 0x5432u), __byte_perm(Wp[1], Wp[2], 0x5432u),
+                                __byte_perm(Wp[2], Wp[3], 0x5432u), __byte_perm(Wp[3], Wp[4], 0x5432u)};
+        pk_scale(Wp[0] & 0xFFFFu, d2, b2);
+        block_dot_pk<M>(a + 64 * pp, qa, d2, b2, s);
+        const uint32_t qb[4] = {Wp[5], Wp[6], Wp[7], Wp[8]};
+        pk_scale(Wp[4] >> 16, d2, b2);
+        block_dot_pk<M>(a + 64 * pp + 32, qb, d2, b2, s);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        acc[4 * m + 0] = s[m][0].x;
+        acc[4 * m + 1] = s[m][0].y;
+        acc[4 * m + 2] = s[m][1].x;
+        acc[4 * m + 3] = s[m][1].y;
+    }
+}
+
+// Half h of a unit (blocks 4h .. 4h + 3), as above.
+template <int M>
+__device__ __forceinline__ void half_dot_pk(const uint8_t* row, int h, const float* a, float (&acc)[4 * M]) {
+    uint32_t w[18];
+    if (h == 0) {  // bytes 0 .. 71: 16-byte loads first
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+            w[4 * i + 0] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 64);
+        w[16] = v.x;
+        w[17] = v.y;
+    } else {  // bytes 72 .. 143: 16-byte loads from byte 80
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 72);
+        w[0] = v.x;
+        w[1] = v.y;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = reinterpret_cast<const uint4*>(row + 80)[i];
+            w[2 + 4 * i + 0] = u.x;
+            w[2 + 4 * i + 1] = u.y;
+            w[2 + 4 * i + 2] = u.z;
+            w[2 + 4 * i + 3] = u.w;
+        }
+    }
+    float2 s[M][2];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        s[m][0] = make_float2(acc[4 * m + 0], acc[4 * m + 1]);
+        s[m][1] = make_float2(acc[4 * m + 2], acc[4 * m + 3]);
+    }
+    const float* ah = a + 128 * h;
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        const uint32_t* Wp = w + 9 * pp;
+        float2 d2, b2;
+        // Even block: d in the low half of word 0, quants at bytes 2..17.
+        const uint32_t qa[4] = {__byte_perm(Wp[0], Wp[1], 0x5432u), __byte_perm(Wp[1], Wp[2], 0x5432u),
+                                __byte_perm(Wp[2], Wp[3], 0x5432u), __byte_perm(Wp[3], Wp[4], 0x5432u)};
+        pk_scale(Wp[0] & 0xFFFFu, d2, b2);
+        block_dot_pk<M>(ah + 64 * pp, qa, d2, b2, s);
+        // Odd block: d in the high half of word 4, quants in words 5..8.
+        const uint32_t qb[4] = {Wp[5], Wp[6], Wp[7], Wp[8]};
+        pk_scale(Wp[4] >> 16, d2, b2);
+        block_dot_pk<M>(ah + 64 * pp + 32, qb, d2, b2, s);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        acc[4 * m + 0] = s[m][0].x;
+        acc[4 * m + 1] = s[m][0].y;
+        acc[4 * m + 2] = s[m][1].x;
+        acc[4 * m + 3] = s[m][1].y;
+    }
+}
+
+template <int M, bool kPk>
+__global__ void __launch_bounds__(max_threads(kPk), 1)
     gemv_q4_0_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                  const float* __restrict__ A, float* __restrict__ C, const TcPlan p) {
-    const int W = p.rps * p.c;
+    constexpr int kRows = group_rows(kPk);
+    constexpr int kSlot = slot_floats(kPk);
+    const int W = p.rps * p.c * p.hs;
     extern __shared__ __align__(128) uint8_t smem[];
-    // ring [stages][c boxes][16 rps rows][144 B] | B fragments [nu_max][M KB] |
-    // D-tile slots [2][W][16][8] f32 | full[stages] | empty[stages] | a_bar
-    const int box_bytes = p.rps * kGroupBytes;
+    // ring [stages][c boxes][kRows rps rows][144 B] | activations [nu_max][M KB]
+    // (B fragments for the MMA consumer, f32 for the packed one) | partial-sum
+    // slots [2][W][kRows][8] f32 | full[stages] | empty[stages] | a_bar
+    const int box_bytes = p.rps * kRows * kUnitBytes;
     const int stage_bytes = p.c * box_bytes;
     uint8_t* ring = smem;
     uint8_t* frag = smem + p.stages * stage_bytes;
     float* slots = reinterpret_cast<float*>(frag + p.nu_max * M * 1024);
-    uint64_t* full = reinterpret_cast<uint64_t*>(slots + 2 * W * kSlotFloats);
+    uint64_t* full = reinterpret_cast<uint64_t*>(slots + 2 * W * kSlot);
     uint64_t* empty = full + p.stages;
     uint64_t* a_bar = empty + p.stages;
 
@@ -301,11 +465,12 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
         if (lane == 0 && nst > 0) {
             prefetch_tensormap(&wmap);
             prefetch_tensormap(&amap);
-            const int rows_per_block = p.rps * kGroupRows;
-            // Warm L2 with the first stages (about 64 KB) before waiting on
-            // earlier kernels; more would compete with their last reads.
+            const int rows_per_block = p.rps * kRows;
+            // Warm L2 with the first stage before waiting on earlier kernels;
+            // more would compete with their last reads and with the
+            // activations, which can only be read after the wait.
+            const int warm = 1;
             {
-                const int warm = min(min(p.stages, nst), max(1, 65536 / stage_bytes + 1));
                 int sc = 0, row = rb0 * rows_per_block;
                 for (int s = 0; s < warm; ++s) {
                     for (int ul = 0; ul < p.c; ++ul) {
@@ -349,21 +514,30 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
     grid_dependency_wait();
     if (nst == 0) return;  // no consumer of this CTA reaches a barrier
     bool ok = mbar_wait_bounded(a_bar, 0, &g_gemv_tc_error);
-    if (ok) {
-        for (int j = warp; j < nu; j += W) build_fragments<M>(frag + j * M * 1024, lane);
+    if constexpr (!kPk) {
+        if (ok) {
+            for (int j = warp; j < nu; j += W) build_fragments<M>(frag + j * M * 1024, lane);
+        }
     }
     named_barrier_sync(1, W * 32);
 
     const int g = lane >> 2;
     const int t = lane & 3;
     const int gc = g % frag_cols<M>();
-    const int rgl = warp % p.rps;  // row group within the row block
-    const int ul = warp / p.rps;   // unit column within a stage
+    // Warp (ul * rps + rgl) * hs + h takes half h of its tile when hs = 2.
+    const int h = warp % p.hs;
+    const int rgl = (warp / p.hs) % p.rps;  // row group within the row block
+    const int ul = warp / (p.hs * p.rps);   // unit column within a stage
     const uint32_t xoff = (t < 3) ? 4u + 4u * t : 0u;
     const uint32_t sel = (t < 3) ? 0x3210u : 0x5432u;
     const uint2* F = reinterpret_cast<const uint2*>(frag);
-    const uint8_t* tile0 = ring + ul * box_bytes + (rgl * kGroupRows + g) * kUnitBytes;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // MMA consumer: rows g and g + 8 of the 16-row tile; packed consumer: row lane.
+    const uint8_t* tile0 =
+        ring + ul * box_bytes + (rgl * kRows + (kPk ? lane : g)) * kUnitBytes;
+    constexpr int kAcc = 4 * (kPk ? M : 1);
+    float acc[kAcc];
+#pragma unroll
+    for (int i = 0; i < kAcc; ++i) acc[i] = 0.f;
     int st = 0;
     uint32_t phase = 0;
 
@@ -373,7 +547,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
             if (ok) ok = mbar_wait_bounded(&full[st], phase, &g_gemv_tc_error);
             if (ok && j < nu) {
                 const uint8_t* r0 = tile0 + st * stage_bytes;
-                tile_mma<M>(r0, r0 + 8 * kUnitBytes, F + j * (M * 128), gc, t, xoff, sel, acc);
+                const float* aj = reinterpret_cast<const float*>(frag + j * M * 1024);
+                const uint2* Fj = F + j * (M * 128);
+                if constexpr (kPk) {
+                    if (p.hs == 1) unit_dot_pk<M>(r0, aj, acc);
+                    else half_dot_pk<M>(r0, h, aj, acc);
+                } else {
+                    pairs_mma<M, 4>(r0, r0 + 8 * kUnitBytes, Fj, 0, gc, t, xoff, sel, acc);  // hs = 1
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
@@ -383,36 +564,47 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
             }
         }
 
-        // Row block done: D tiles to shared memory; the warp of unit column 0
-        // adds its row group's c tiles (column order) and takes one row per
-        // lane 0..15.  Slots alternate between row blocks, so one barrier per
-        // row block keeps a slot from being rewritten before it is read.
-        float* slot = slots + ((rbi & 1) * W + warp) * kSlotFloats;
-        reinterpret_cast<float2*>(slot)[g * 4 + t] = make_float2(acc[0], acc[1]);
-        reinterpret_cast<float2*>(slot)[(g + 8) * 4 + t] = make_float2(acc[2], acc[3]);
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-        if (p.c > 1) {
+        // Row block done: partial sums to shared memory; the warp of unit
+        // column 0 (half 0) adds its row group's c * hs slots (column order)
+        // and takes one row per lane.  Slots alternate between row blocks, so
+        // one barrier per row block keeps a slot from being rewritten before
+        // it is read.
+        float* slot = slots + ((rbi & 1) * W + warp) * kSlot;
+        if constexpr (kPk) {
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+                slot[lane * 8 + m] = (acc[4 * m] + acc[4 * m + 1]) + (acc[4 * m + 2] + acc[4 * m + 3]);
+        } else {
+            reinterpret_cast<float2*>(slot)[g * 4 + t] = make_float2(acc[0], acc[1]);
+            reinterpret_cast<float2*>(slot)[(g + 8) * 4 + t] = make_float2(acc[2], acc[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < kAcc; ++i) acc[i] = 0.f;
+        if (W > p.rps) {
             named_barrier_sync(1, W * 32);
         } else {
             __syncwarp();
         }
-        if (ul != 0) continue;
+        if (ul != 0 || h != 0) continue;
         const int rg = (rb0 + rbi) * p.rps + rgl;
-        const int r = lane & 15;
-        const int row = rg * kGroupRows + r;
+        const int r = lane & (kRows - 1);
+        const int row = rg * kRows + r;
         float tot[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) tot[m] = 0.f;
         for (int u = 0; u < p.c; ++u) {
-            const float* su = slots + ((rbi & 1) * W + rgl + u * p.rps) * kSlotFloats + r * 8;
+            for (int hh = 0; hh < p.hs; ++hh) {
+                const float* su =
+                    slots + ((rbi & 1) * W + (u * p.rps + rgl) * p.hs + hh) * kSlot + r * 8;
 #pragma unroll
-            for (int m = 0; m < M; ++m) {
-                tot[m] += su[m];
-                if constexpr (tc_sets<M>() == 1) tot[m] += su[M + m];
+                for (int m = 0; m < M; ++m) {
+                    tot[m] += su[m];
+                    if constexpr (!kPk && tc_sets<M>() == 1) tot[m] += su[M + m];
+                }
             }
         }
         if (rg >= p.RG) continue;  // whole warp: a row group past the matrix
-        const bool mine = lane < 16 && row < p.N;
+        const bool mine = lane < kRows && row < p.N;
         if (mine) {
             const uint8_t* row_blocks =
                 p.wq + (static_cast<int64_t>(row) * p.U + u0) * kUnitBytes;
@@ -428,13 +620,13 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
 #pragma unroll
                 for (int m = 0; m < M; ++m) C[static_cast<int64_t>(m) * p.N + row] = tot[m];
             }
-        } else if (lane < 16) {
-            float* part = p.part + (static_cast<int64_t>(rg) * p.S + split) * (M * kGroupRows);
+        } else if (lane < kRows) {
+            float* part = p.part + (static_cast<int64_t>(rg) * p.S + split) * (M * kRows);
 #pragma unroll
-            for (int m = 0; m < M; ++m) part[m * kGroupRows + lane] = tot[m];
+            for (int m = 0; m < M; ++m) part[m * kRows + lane] = tot[m];
         }
     }
-    if (p.S == 1 || ul != 0) return;
+    if (p.S == 1 || ul != 0 || h != 0) return;
 
     // Split K: one fence for all of this warp's partial sums, then its
     // arrivals; the last of the S arrivals at a row group adds the partials
@@ -450,14 +642,14 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
         old = __shfl_sync(0xFFFFFFFFu, old, 0);
         if (old != static_cast<unsigned>(p.S - 1)) continue;
         __threadfence();
-        const int row = rg * kGroupRows + lane;
-        if (lane < 16 && row < p.N) {
-            const float* base = p.part + static_cast<int64_t>(rg) * p.S * (M * kGroupRows);
+        const int row = rg * kRows + lane;
+        if (lane < kRows && row < p.N) {
+            const float* base = p.part + static_cast<int64_t>(rg) * p.S * (M * kRows);
 #pragma unroll
             for (int m = 0; m < M; ++m) {
                 float v = 0.f;
                 for (int q = 0; q < p.S; ++q)
-                    v += __ldcg(base + q * (M * kGroupRows) + m * kGroupRows + lane);
+                    v += __ldcg(base + q * (M * kRows) + m * kRows + lane);
                 C[static_cast<int64_t>(m) * p.N + row] = v;
             }
         }
@@ -466,40 +658,44 @@ __global__ void __launch_bounds__(kThreadsMax, 1)
     }
 }
 
-// Shared memory of one CTA.
-int64_t tc_smem_bytes(int M, int W, int stages, int nu_max) {
-    return static_cast<int64_t>(stages) * W * kGroupBytes + static_cast<int64_t>(nu_max) * M * 1024 +
-           2LL * W * kSlotFloats * 4 + (2LL * stages + 1) * 8;
+// Shared memory of one CTA: W consumer warps, stages of `tiles` tiles.
+int64_t tc_smem_bytes(int M, bool packed, int W, int tiles, int stages, int nu_max) {
+    return static_cast<int64_t>(stages) * tiles * group_rows(packed) * kUnitBytes +
+           static_cast<int64_t>(nu_max) * M * 1024 + 2LL * W * slot_floats(packed) * 4 +
+           (2LL * stages + 1) * 8;
 }
 
 // Relative rate of one SM with W consumer warps (more warps hide more of the
-// shared-memory and MMA latency).
+// shared-memory, barrier and arithmetic latency; past 16 measured no gain).
 double warp_efficiency(int W) {
     return W >= 16 ? 1.0 : W >= 14 ? 0.96 : W >= 12 ? 0.92 : W >= 10 ? 0.86 : 0.8;
 }
 
-// Choose the stage shape (rps row groups x c units, W = rps c consumer warps)
-// and S (K ranges) for one CTA per SM.  The cost is the largest per-CTA tile
-// count (idle tile slots included) over the warp efficiency, with charges for
-// split-K partial sums (their bytes against the weight bytes, plus a little
-// per split), for short K ranges (a CTA that reads few bytes of each row
-// leaves DRAM pages to be reopened by others), for a shallow ring, and for
-// cross-warp reductions (c > 1) at more than one row block per CTA.
-bool plan_tc(int M, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws, TcPlan* out,
-             int* grid, int* smem) {
+// Best stage shape with hs warps a tile (rps row groups x c units, W = rps c
+// hs consumer warps) and S (K ranges) for one CTA per SM.  The cost is the
+// largest per-CTA tile count (idle tile slots included) over the warp
+// efficiency, with charges for split-K partial sums (their bytes against the
+// weight bytes, plus a little per split), for short K ranges (a CTA that reads
+// few bytes of each row leaves DRAM pages to be reopened by others), for a
+// shallow ring, and for cross-warp reductions at more than one row block per
+// CTA.  Returns the cost (infinite when nothing fits).
+double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const DeviceInfo& dev,
+                  const Workspace& ws, TcPlan* out, int* grid, int* smem) {
+    const int kRows = group_rows(packed);
     const int U = static_cast<int>(K / kUnitElems);
-    const int64_t RG = (N + kGroupRows - 1) / kGroupRows;
+    const int64_t RG = (N + kRows - 1) / kRows;
     const int P = dev.sm_count;
     double best = 1e300;
-    bool found = false;
-    for (int W = kMaxWarps; W >= 8; --W) {
-        for (int c = 1; c <= W; ++c) {
-            if (W % c != 0) continue;
-            const int rps = W / c;
-            if (rps * kGroupRows > 256) continue;  // TMA box height
+    for (int W = std::min(max_warps(packed), 16 * hs); W >= 8; --W) {
+        if (W % hs != 0) continue;
+        const int tiles = W / hs;
+        for (int c = 1; c <= tiles; ++c) {
+            if (tiles % c != 0) continue;
+            const int rps = tiles / c;
+            if (rps * kRows > 256) continue;  // TMA box height
             const int64_t RB = (RG + rps - 1) / rps;
             for (int S = 1; S <= kMaxSplits && S <= U; ++S) {
-                if (S > 1 && (RG * S * M * kGroupRows > static_cast<int64_t>(ws.part_floats) ||
+                if (S > 1 && (RG * S * M * kRows > static_cast<int64_t>(ws.part_floats) ||
                               RG > static_cast<int64_t>(ws.ctr_count)))
                     continue;
                 const int nu_max = (U + S - 1) / S;
@@ -507,9 +703,10 @@ bool plan_tc(int M, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace
                 const int64_t rbpc = (RB + Gs - 1) / Gs;
                 const int64_t g_used = (RB + rbpc - 1) / rbpc;
                 const int64_t spr = (nu_max + c - 1) / c;
-                const int64_t fixed = tc_smem_bytes(M, W, 0, nu_max);
-                int stages = static_cast<int>((dev.max_smem_optin - fixed) /
-                                              (static_cast<int64_t>(W) * kGroupBytes + 16));
+                const int64_t fixed = tc_smem_bytes(M, packed, W, tiles, 0, nu_max);
+                int stages = static_cast<int>(
+                    (dev.max_smem_optin - fixed) /
+                    (static_cast<int64_t>(tiles) * kRows * kUnitBytes + 16));
                 stages = std::min(stages, kMaxStages);
                 if (stages < 2) continue;
                 const double split_bytes =
@@ -517,13 +714,12 @@ bool plan_tc(int M, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace
                             : 0.0;
                 const double short_rows =
                     0.3 * std::max(0.0, 1.0 - nu_max * static_cast<double>(kUnitBytes) / 2048.0);
-                const double cost = static_cast<double>(rbpc * spr * W) / warp_efficiency(W) *
+                const double cost = static_cast<double>(rbpc * spr * tiles) / warp_efficiency(W) *
                                     (1.0 + split_bytes + 0.01 * (S - 1) + short_rows) *
                                     (stages < 3 ? 1.1 : 1.0) *
-                                    ((c > 1 && rbpc > 1) ? 1.0 + 0.05 * rbpc : 1.0);
+                                    ((W > rps && rbpc > 1) ? 1.0 + 0.05 * rbpc : 1.0);
                 if (cost < best) {
                     best = cost;
-                    found = true;
                     TcPlan& q = *out;
                     q.wq = nullptr;
                     q.N = static_cast<int>(N);
@@ -533,52 +729,61 @@ bool plan_tc(int M, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace
                     q.S = S;
                     q.rps = rps;
                     q.c = c;
+                    q.hs = hs;
                     q.rbpc = static_cast<int>(rbpc);
                     q.nu_max = nu_max;
                     q.stages = stages;
                     q.part = ws.part;
                     q.ctr = ws.ctr;
                     *grid = static_cast<int>(g_used * S);
-                    *smem = static_cast<int>(tc_smem_bytes(M, W, stages, nu_max));
+                    *smem = static_cast<int>(tc_smem_bytes(M, packed, W, tiles, stages, nu_max));
                 }
             }
         }
     }
-    return found;
+    return best;
 }
 
-template <int M>
+// The launch plan: whole-unit tiles for the MMA consumer, half-unit warps
+// for the packed one (measured on GB300: half units lose with the MMA
+// consumer, and give the packed one twice the warps on the same stages).
+bool plan_tc(int M, bool packed, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws,
+             TcPlan* out, int* grid, int* smem) {
+    return plan_tc_hs(M, packed, packed ? 2 : 1, N, K, dev, ws, out, grid, smem) < 1e300;
+}
+
+template <int M, bool kPk>
 cudaError_t ensure_tc_smem_attr(const DeviceInfo& dev, int bytes) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
     if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_tc<M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_tc<M, kPk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            dev.max_smem_optin);
     if (err != cudaSuccess) return err;
     __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     return cudaSuccess;
 }
 
-template <int M>
+template <int M, bool kPk>
 cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
                       cudaStream_t stream, const DeviceInfo& dev, const Workspace& ws,
                       bool clear_counters, bool* launched) {
     *launched = false;
     TcPlan p;
     int grid = 0, smem = 0;
-    if (!plan_tc(M, N, K, dev, ws, &p, &grid, &smem)) return cudaSuccess;
+    if (!plan_tc(M, kPk, N, K, dev, ws, &p, &grid, &smem)) return cudaSuccess;
     p.wq = wq;
-    cudaError_t err = ensure_tc_smem_attr<M>(dev, smem);
+    cudaError_t err = ensure_tc_smem_attr<M, kPk>(dev, smem);
     if (err != cudaSuccess) return err;
     if (clear_counters && p.S > 1) {
         err = cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(p.RG) * sizeof(unsigned), stream);
         if (err != cudaSuccess) return err;
     }
-    // Weights as bytes [N rows][U units][144 B]; boxes of 16 rps rows x 1 unit.
+    // Weights as bytes [N rows][U units][144 B]; boxes of (group rows) rps rows x 1 unit.
     const int64_t dims[3] = {kUnitBytes, p.U, N};
     const int64_t strides[2] = {kUnitBytes, static_cast<int64_t>(p.U) * kUnitBytes};
-    const int box[3] = {kUnitBytes, 1, p.rps * kGroupRows};
+    const int box[3] = {kUnitBytes, 1, p.rps * group_rows(kPk)};
     CUtensorMap wmap, amap;
     err = encode_tiled(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, dims, strides, box);
     if (err != cudaSuccess) return err;
@@ -588,8 +793,8 @@ cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, in
     const int abox[2] = {kUnitElems, M};
     err = encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(gemv_q4_0_tc<M>, dim3(grid), dim3((p.rps * p.c + 1) * 32), smem, stream, wmap, amap,
-                     A, C, p);
+    err = launch_pdl(gemv_q4_0_tc<M, kPk>, dim3(grid), dim3((p.rps * p.c * p.hs + 1) * 32), smem,
+                     stream, wmap, amap, A, C, p);
     if (err != cudaSuccess) return err;
     note_launch();
     *launched = true;
@@ -600,16 +805,24 @@ cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, in
 
 cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                                const Workspace& ws, bool clear_counters, bool* launched) {
+                                const Workspace& ws, bool packed, bool clear_counters,
+                                bool* launched) {
+    if (packed) {
+        switch (M) {
+            case 1: return launch_tc<1, true>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+            case 2: return launch_tc<2, true>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (M) {
-        case 1: return launch_tc<1>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 2: return launch_tc<2>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 3: return launch_tc<3>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 4: return launch_tc<4>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 5: return launch_tc<5>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 6: return launch_tc<6>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 7: return launch_tc<7>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
-        case 8: return launch_tc<8>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 1: return launch_tc<1, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 2: return launch_tc<2, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 3: return launch_tc<3, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 4: return launch_tc<4, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 5: return launch_tc<5, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 6: return launch_tc<6, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 7: return launch_tc<7, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        case 8: return launch_tc<8, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
         default: return cudaErrorInvalidValue;
     }
 }

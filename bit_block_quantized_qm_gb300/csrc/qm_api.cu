@@ -221,13 +221,14 @@ int from_cuda(cudaError_t err) { return err == cudaSuccess ? QM_OK : QM_ERR_CUDA
 int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
                 int algo, void* stream) {
     if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QM_ERR_SHAPE;
-    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMM_TC) return QM_ERR_SHAPE;
+    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMV_PK) return QM_ERR_SHAPE;
     int64_t a_elems, c_elems, w_elems, a_bytes, c_bytes, w_bytes;
     if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, &a_bytes) || !mul_ok(M, N, &c_elems) ||
         !mul_ok(c_elems, 4, &c_bytes) || !mul_ok(N, K / 32, &w_elems) ||
         !mul_ok(w_elems, 18, &w_bytes))
         return QM_ERR_SHAPE;
     if ((algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT) && M > 8) return QM_ERR_UNSUPPORTED;
+    if (algo == QM_ALGO_GEMV_PK && M > 2) return QM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return QM_OK;
     if (!C) return QM_ERR_NULL;
     if (K > 0 && (!A || !wq)) return QM_ERR_NULL;
@@ -248,16 +249,18 @@ int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(c_bytes), s));
     const uint8_t* w = static_cast<const uint8_t*>(wq);
-    // Measured on GB300: the tensor-core GEMV is the faster decode for every
-    // M = 1..8 shape timed (back-to-back launches of 1024..14336 x 4096..14336).
     const bool tc_ok = qm::gemm_tc_supported(A, w, M, N, K);
     if (algo == QM_ALGO_AUTO) {
-        if (M <= 8) algo = QM_ALGO_GEMV;
+        if (M <= 8)
+            algo = qm::gemv_auto_kind(M, N, K) == qm::GemvKind::kPacked ? QM_ALGO_GEMV_PK : QM_ALGO_GEMV;
         else algo = tc_ok ? QM_ALGO_GEMM_TC : QM_ALGO_GEMM_SIMT;
     }
-    if (algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT)
-        return from_cuda(qm::launch_gemv_q4_0(A, w, C, static_cast<int>(M), N, K, s, dev,
-                                              algo == QM_ALGO_GEMV));
+    if (algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT || algo == QM_ALGO_GEMV_PK) {
+        const qm::GemvKind kind = algo == QM_ALGO_GEMV      ? qm::GemvKind::kMma
+                                  : algo == QM_ALGO_GEMV_PK ? qm::GemvKind::kPacked
+                                                            : qm::GemvKind::kSimt;
+        return from_cuda(qm::launch_gemv_q4_0(A, w, C, static_cast<int>(M), N, K, s, dev, kind));
+    }
     if (algo == QM_ALGO_GEMM_TC) {
         if (!tc_ok) return QM_ERR_UNSUPPORTED;
         return from_cuda(qm::launch_gemm_q4_0_tc(A, w, C, M, N, K, s, dev));

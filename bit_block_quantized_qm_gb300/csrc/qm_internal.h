@@ -45,19 +45,35 @@ cudaError_t launch_dequant_q8_0(const uint8_t* wq, int64_t n_blocks, float* out,
 cudaError_t launch_quantize_q8_0(const float* x, int64_t n_blocks, uint8_t* out,
                                  cudaStream_t stream, const DeviceInfo& dev);
 
-// Decode-regime GEMV, M = 1..8.  When wq and A are 16-byte aligned and
-// K % 256 == 0: the tensor-core GEMV (gemv_tc.cu) when tc, else the
-// persistent FP32 FMA kernel; otherwise the generic kernel.
-cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
-                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool tc);
+// Consumers of the decode-regime GEMV.
+enum class GemvKind { kSimt, kMma, kPacked };
 
-// The tensor-core GEMV (mma.sync on bf16 pieces) for M = 1..8, K % 256 == 0 and
-// 16-byte aligned A and wq, with split-K scratch `ws` (counters zeroed on the
-// stream first when clear_counters).  Sets *launched = false and enqueues
-// nothing when no launch plan fits.
+// The automatic choice between the GEMV consumers.  Measured on GB300
+// (back-to-back launches): at M = 1 the packed FP32 consumer is faster up to
+// 4096 x 4096 weights (1024 x 4096: 5.2 against 6.0 us; 4096 x 4096: 6.4
+// against 6.6 us) and the tensor-core consumer beyond (14336 x 4096: 11.7
+// against 12.0 us); for M = 2..8 the tensor-core consumer is faster for every
+// shape timed.
+inline GemvKind gemv_auto_kind(int64_t M, int64_t N, int64_t K) {
+    return (M == 1 && N * K <= 4096LL * 4096) ? GemvKind::kPacked : GemvKind::kMma;
+}
+
+// Decode-regime GEMV, M = 1..8.  When wq and A are 16-byte aligned and
+// K % 256 == 0: the staged GEMV (gemv_tc.cu) on tensor cores (kMma) or on
+// packed FP32 FMAs (kPacked, M <= 2), else the persistent FP32 FMA kernel
+// (kSimt); otherwise the generic kernel.
+cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                             int64_t K, cudaStream_t stream, const DeviceInfo& dev, GemvKind kind);
+
+// The staged GEMV for K % 256 == 0 and 16-byte aligned A and wq, with split-K
+// scratch `ws` (counters zeroed on the stream first when clear_counters): on
+// tensor cores (mma.sync on bf16 pieces) for M = 1..8, or with packed FP32
+// FMAs (fma.rn.f32x2, one row per lane) for M = 1..2 when `packed`.  Sets
+// *launched = false and enqueues nothing when no launch plan fits.
 cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                                const Workspace& ws, bool clear_counters, bool* launched);
+                                const Workspace& ws, bool packed, bool clear_counters,
+                                bool* launched);
 cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 
 // The same GEMV with its split-K scratch in a fixed device array instead of

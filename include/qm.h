@@ -80,13 +80,17 @@ extern "C" {
                                    qm_matmul_q4_0_noalloc (M > 8)               */
 
 /* Algorithms for qm_matmul_q4_0_algo. */
-#define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks                          */
+#define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks: GEMV_PK for M == 1 and
+                               N*K <= 4096*4096, GEMV for M <= 8, otherwise
+                               GEMM_TC where it applies, else GEMM_SIMT      */
 #define QM_ALGO_GEMV 1      /* decode-regime GEMV on tensor cores (mma.sync, bf16
                                pieces, f32 sums); M 1..8                         */
 #define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
 #define QM_ALGO_GEMV_SIMT 3 /* decode-regime GEMV on FP32 FMA; M 1..8             */
 #define QM_ALGO_GEMM_TC 4   /* prefill GEMM on tcgen05 tensor cores (split bf16);
                                needs K % 256 == 0 and 16-byte aligned A and wq  */
+#define QM_ALGO_GEMV_PK 5   /* decode-regime GEMV on packed FP32 FMA
+                               (fma.rn.f32x2), one weight row per lane; M 1..2 */
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 QM_API int qm_version(void);

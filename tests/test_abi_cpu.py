@@ -98,6 +98,9 @@ def test_aliasing(lib):
 def test_forced_algorithm_limits(lib):
     assert qm.qm_matmul_q4_0_algo_ptr(A_ADDR, W_ADDR, C_ADDR, 9, 4, 32,
                                       qm.QM_ALGO_GEMV) == qm.QM_ERR_UNSUPPORTED
+    assert qm.qm_matmul_q4_0_algo_ptr(A_ADDR, W_ADDR, C_ADDR, 3, 4, 32,
+                                      qm.QM_ALGO_GEMV_PK) == qm.QM_ERR_UNSUPPORTED
+    assert qm.qm_matmul_q4_0_algo_ptr(A_ADDR, W_ADDR, C_ADDR, 1, 4, 32, 6) == qm.QM_ERR_SHAPE
 
 
 def test_python_wrappers_validate_tensors():

@@ -158,7 +158,8 @@ def test_matmul_tail_shapes(env, shape):
     A = synth.activations(M, K, K + M, dist="outliers")
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     algos = [qm.QM_ALGO_AUTO, qm.QM_ALGO_GEMM_SIMT] + \
-        ([qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT] if M <= 8 else [])
+        ([qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT] if M <= 8 else []) + \
+        ([qm.QM_ALGO_GEMV_PK] if M <= 2 else [])
     for algo in algos:
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
 
@@ -169,7 +170,8 @@ def test_matmul_tail_shapes(env, shape):
 GEMV_FAST = [(M, N, K) for M in (1, 2, 4, 7, 8)
              for (N, K) in ((1, 256), (31, 512), (33, 768), (100, 2048), (1000, 256),
                             (64, 14336), (4096, 512), (1024, 4096), (300, 3840))] + \
-            [(1, 80000, 256), (3, 4096, 4096), (8, 4096, 4096)]
+            [(1, 80000, 256), (3, 4096, 4096), (8, 4096, 4096), (1, 14336, 4096),
+             (1, 4096, 14336), (2, 6144, 4096), (1, 28672, 4096)]
 
 
 @pytest.mark.parametrize("shape", GEMV_FAST, ids=lambda s: "x".join(map(str, s)))
@@ -181,6 +183,8 @@ def test_gemv_tma_path(env, shape):
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV), C_ref, S_ref, "tensor cores")
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV_SIMT), C_ref, S_ref, "fp32 fma")
+    if M <= 2:
+        assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMV_PK), C_ref, S_ref, "packed fp32")
 
 
 @pytest.mark.parametrize("offs", [(4, 0), (0, 2), (0, 18), (8, 8)])
@@ -267,6 +271,9 @@ def test_nonfinite_scales(env):
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     for algo in (qm.QM_ALGO_GEMV, qm.QM_ALGO_GEMV_SIMT, qm.QM_ALGO_GEMM_SIMT, qm.QM_ALGO_GEMM_TC):
         assert_close(matmul_gpu(qm, A, blob, N, algo), C_ref, S_ref, f"algo {algo}")
+    for m in (1, 2):
+        C_ref, S_ref = o.matmul_q4_0(A[:m], blob, N, K)
+        assert_close(matmul_gpu(qm, A[:m], blob, N, qm.QM_ALGO_GEMV_PK), C_ref, S_ref, "packed fp32")
 
 
 def test_m1_matches_rows_of_m8(env):
