@@ -13,20 +13,25 @@
 //     terms are at most 2^-17 |a W| together.  bf16 x bf16 products are exact
 //     in the f32 accumulator.
 //
-// Structure (one 128 x 128 output tile per CTA, K in 64-wide steps):
+// Structure (one 128 x 256 output tile per CTA, K in 64-wide steps):
 //   * a pre-pass splits A once into bf16 hi / lo matrices (workspace);
 //   * warp 0 (one thread) streams, with TMA, the hi / lo activation tiles
-//     (128 rows x 64 k, 128-byte swizzle, 3 stages) and the weight's raw
-//     Q4_0 units (128 rows x 8 blocks, 2 stages);
-//   * warps 2..17 decode each 128 x 64 weight tile into W_hi / W_lo, written
+//     (128 rows x 64 k, 128-byte swizzle, 2 stages) and the weight's raw
+//     Q4_0 bytes of each k-step (256 rows x the 48-byte, 16-byte aligned
+//     span that holds the step's 36-byte block pair, 2 stages);
+//   * warps 2..17 decode each 256 x 64 weight tile into W_hi / W_lo, written
 //     in the same swizzled K-major layout (2 stages), then run the epilogue;
-//   * warp 1 owns the TMEM accumulator (128 lanes x 128 f32 columns) and one
-//     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16) per k-step,
-//     committing completion to the stages' "empty" barriers;
-//   * the epilogue reads TMEM with tcgen05.ld (each warp a 32 x 32 block of
-//     its 32-lane quarter), stages the block in shared memory (the freed
-//     activation stages) and writes C row by row, 16-byte stores when C's
-//     rows allow;
+//   * warp 1 owns the TMEM accumulator (128 lanes x 256 f32 columns) and one
+//     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16, each
+//     128 x 256 x 16) per k-step, committing completion to the stages'
+//     "empty" barriers;
+//   * the epilogue reads TMEM with tcgen05.ld (each warp two 32 x 32 blocks
+//     of its 32-lane quarter), stages a block in shared memory (the freed
+//     weight stages) and writes C row by row, 16-byte stores when C's rows
+//     allow;
+// The 256-wide tile reads each activation tile once per 256 output columns
+// and keeps the operand reads of one MMA at 12 KB per 2^20 flops, which the
+// shared-memory bandwidth sustains together with the decode's stores.
 //   * when there are fewer output tiles than SMs, K is split into S ranges
 //     (grid z): each CTA writes its partial tile to a workspace and the last
 //     of a tile's S CTAs to arrive adds the partials in range order, so the
@@ -50,24 +55,30 @@ __device__ unsigned int g_gemm_error = 0;
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 128;
 constexpr int BK = 64;
-constexpr int kAStages = 3;
 constexpr int kWStages = 2;
 constexpr int kRawStages = 2;
 constexpr int kDecodeWarps = 16;
 constexpr int kThreads = (2 + kDecodeWarps) * 32;
-constexpr int kTile = BM * BK * 2;    // one bf16 operand tile: 16 KB (BM == BN)
-constexpr int kRawBytes = BN * 144;   // one Q4_0 unit (8 blocks) of BN rows
-constexpr int kTmemCols = BN;         // f32 accumulator columns
-constexpr int kSmemBytes = (kAStages * 2 + kWStages * 2) * kTile + kRawStages * kRawBytes +
-                           16 * 8 + 1024;  // + barriers, TMEM slot, alignment slack
+constexpr int kTileA = BM * BK * 2;   // one bf16 activation tile: 16 KB
+constexpr int kRawRow = 48;           // raw bytes of one row per k-step (3 x 16 B)
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
-// N = BN, M = BM.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
+// Tiles of BN = 128 or 256 output columns.
+template <int BN>
+struct Tile {
+    static constexpr int kAStages = BN == 128 ? 3 : 2;
+    static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
+    static constexpr int kRawBytes = BN * kRawRow;
+    static constexpr int kTmemCols = BN;        // f32 accumulator columns
+    static constexpr int kSmemBytes = kAStages * 2 * kTileA + kWStages * 2 * kTileW +
+                                      kRawStages * kRawBytes + 16 * 8 + 1024;  // + barriers, slack
+    // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
+    // N = BN, M = BM.
+    static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                       (static_cast<uint32_t>(BN >> 3) << 17) |
+                                       (static_cast<uint32_t>(BM >> 4) << 24);
+    static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
+};
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle (rows of 128 B,
 // 8-row atoms 1024 B apart), start address in 16-byte units.
@@ -80,12 +91,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t acc) {
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
+                                        uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(da), "l"(db), "r"(kIdesc), "r"(acc));
+        ::"r"(tmem_d), "l"(da), "l"(db), "r"(idesc), "r"(acc));
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -189,19 +201,24 @@ __device__ __noinline__ float entry_exact(const float* __restrict__ A, const uin
     return s;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_ahi,
                  const __grid_constant__ CUtensorMap map_alo,
                  const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
                  int c_vec, int S, float* __restrict__ partial, unsigned* __restrict__ ctr) {
+    using T = Tile<BN>;
+    constexpr int kAStages = T::kAStages;
+    constexpr int kTileW = T::kTileW;
+    constexpr int kRawBytes = T::kRawBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles, by indexing the shared array
     // itself so the compiler keeps every access below in the shared space.
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* a_st = base;                                // [kAStages][hi, lo][16 KB]
-    uint8_t* w_st = a_st + kAStages * 2 * kTile;         // [kWStages][hi, lo][16 KB]
-    uint8_t* raw = w_st + kWStages * 2 * kTile;          // [kRawStages][128 rows][144 B]
+    uint8_t* w_st = a_st + kAStages * 2 * kTileA;        // [kWStages][hi, lo][BN rows][128 B]
+    uint8_t* raw = w_st + kWStages * 2 * kTileW;         // [kRawStages][BN rows][48 B]
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRawBytes);
     uint64_t* a_full = bars;
     uint64_t* a_empty = bars + kAStages;
@@ -216,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     const int m0 = static_cast<int>(blockIdx.y) * BM;
     const int n0 = static_cast<int>(blockIdx.x) * BN;
-    const int KT = K / BK / S;  // k-steps of this CTA's K range (a multiple of 4)
+    const int KT = K / BK / S;  // k-steps of this CTA's K range
     const int split = static_cast<int>(blockIdx.z);
     const int kt0 = split * KT;
 
@@ -241,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile(
             "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                 smem_addr(tmem_slot)),
-            "r"(kTmemCols)
+            "r"(T::kTmemCols)
             : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -253,27 +270,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // Producer: raw weight units (one per 4 k-steps) and activation tiles.
+            // Producer: the raw weight bytes and the activation tiles of each
+            // k-step.  The step's block pair is bytes 36 j .. 36 j + 35 of each
+            // row (j = k-step); the 48-byte box starts at the 16-byte boundary
+            // below it, which TMA requires, and still covers the pair.
             prefetch_tensormap(&map_ahi);
             prefetch_tensormap(&map_alo);
             prefetch_tensormap(&map_w);
             for (int kt = 0; kt < KT; ++kt) {
-                if ((kt & 3) == 0) {
-                    const int u = kt >> 2;
-                    const int rs = u % kRawStages;
-                    if (u >= kRawStages &&
-                        !mbar_wait_bounded(&raw_empty[rs], ((u / kRawStages) - 1) & 1, &g_gemm_error))
-                        break;
-                    mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
-                    tma_load_3d(raw + rs * kRawBytes, &map_w, 0, (kt0 >> 2) + u, n0, &raw_full[rs]);
-                }
+                const int rs = kt % kRawStages;
+                if (kt >= kRawStages &&
+                    !mbar_wait_bounded(&raw_empty[rs], ((kt / kRawStages) - 1) & 1, &g_gemm_error))
+                    break;
+                mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
+                tma_load_2d(raw + rs * kRawBytes, &map_w, (36 * (kt0 + kt)) & ~15, n0, &raw_full[rs]);
                 const int as = kt % kAStages;
                 if (kt >= kAStages &&
                     !mbar_wait_bounded(&a_empty[as], ((kt / kAStages) - 1) & 1, &g_gemm_error))
                     break;
-                mbar_arrive_expect_tx(&a_full[as], 2 * kTile);
-                tma_load_2d(a_st + (2 * as) * kTile, &map_ahi, (kt0 + kt) * BK, m0, &a_full[as]);
-                tma_load_2d(a_st + (2 * as + 1) * kTile, &map_alo, (kt0 + kt) * BK, m0, &a_full[as]);
+                mbar_arrive_expect_tx(&a_full[as], 2 * kTileA);
+                tma_load_2d(a_st + (2 * as) * kTileA, &map_ahi, (kt0 + kt) * BK, m0, &a_full[as]);
+                tma_load_2d(a_st + (2 * as + 1) * kTileA, &map_alo, (kt0 + kt) * BK, m0, &a_full[as]);
             }
         }
     } else if (warp == 1) {
@@ -287,16 +304,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      mbar_wait_bounded(&w_full[ws], (kt / kWStages) & 1, &g_gemm_error);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t ahi = smem_addr(a_st + (2 * as) * kTile);
-                const uint32_t alo = ahi + kTile;
-                const uint32_t whi = smem_addr(w_st + (2 * ws) * kTile);
-                const uint32_t wlo = whi + kTile;
+                const uint32_t ahi = smem_addr(a_st + (2 * as) * kTileA);
+                const uint32_t alo = ahi + kTileA;
+                const uint32_t whi = smem_addr(w_st + (2 * ws) * kTileW);
+                const uint32_t wlo = whi + kTileW;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint32_t off = kk * 32;  // 16 bf16 along K
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), (kt | kk) != 0);
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), 1u);
-                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), 1u);
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), T::kIdesc, (kt | kk) != 0);
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), T::kIdesc, 1u);
+                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), T::kIdesc, 1u);
                 }
                 mma_commit(&a_empty[as]);
                 mma_commit(&w_empty[ws]);
@@ -304,64 +321,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(acc_full);
         }
     } else {
-        // Decode warps: thread t of 512 owns weight row t / 4, block (t / 2) % 2
-        // of the 64-wide k-step and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
+        // Decode warps: kTpr threads per weight row.  With 2 (BN = 256) thread
+        // t of 512 owns row t / 2 and block t % 2 of the 64-wide k-step, both
+        // halves of its quant bytes; with 4 (BN = 128) it owns row t / 4,
+        // block (t / 2) % 2 and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
+        constexpr int kTpr = kDecodeWarps * 32 / BN;
+        static_assert(kTpr == 2 || kTpr == 4, "threads per weight row");
         const int dt = threadIdx.x - 64;
-        const int n = dt >> 2;
-        const int half = (dt >> 1) & 1;
-        const int part = dt & 1;
+        const int n = dt / kTpr;
+        const int half = (kTpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
         bool ok = true;
         for (int kt = 0; kt < KT && ok; ++kt) {
-            const int u = kt >> 2;
-            const int sub = kt & 3;
-            const int rs = u % kRawStages;
+            const int rs = kt % kRawStages;
             const int ws = kt % kWStages;
-            if (sub == 0) ok = mbar_wait_bounded(&raw_full[rs], (u / kRawStages) & 1, &g_gemm_error);
+            ok = mbar_wait_bounded(&raw_full[rs], (kt / kRawStages) & 1, &g_gemm_error);
             if (ok && kt >= kWStages)
                 ok = mbar_wait_bounded(&w_empty[ws], ((kt / kWStages) - 1) & 1, &g_gemm_error);
             if (!ok) break;
-            const uint8_t* blk = raw + rs * kRawBytes + n * 144 + (2 * sub + half) * kBlockBytes;
-            decode_half_block(blk, part, n, half, w_st + (2 * ws) * kTile, w_st + (2 * ws + 1) * kTile);
+            const uint8_t* blk =
+                raw + rs * kRawBytes + n * kRawRow + ((36 * (kt0 + kt)) & 15) + half * kBlockBytes;
+            uint8_t* thi = w_st + (2 * ws) * kTileW;
+            if constexpr (kTpr == 2) {
+                decode_half_block(blk, 0, n, half, thi, thi + kTileW);
+                decode_half_block(blk, 1, n, half, thi, thi + kTileW);
+            } else {
+                decode_half_block(blk, dt & 1, n, half, thi, thi + kTileW);
+            }
             fence_proxy_async_shared();  // make the tiles visible to the tensor cores
             __syncwarp();
-            if (lane == 0) mbar_arrive(&w_full[ws]);
-            if (sub == 3) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[rs]);
+            if (lane == 0) {
+                mbar_arrive(&w_full[ws]);
+                mbar_arrive(&raw_empty[rs]);
             }
         }
-        // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns the 32 x 32
-        // block of rows 32 q .. 32 q + 31 and columns 32 cq .. 32 cq + 31.  Lane
-        // i holds row i of the block; the block goes through shared memory (rows
-        // 36 floats apart: conflict-free 16-byte writes and reads) so that C is
-        // written a row at a time.  All MMAs have completed when acc_full fires,
-        // so the activation stages are free.
+        // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns rows
+        // 32 q .. 32 q + 31 and columns BN/4 cq .. BN/4 cq + BN/4 - 1, as
+        // BN/128 blocks of 32 x 32.  Lane i holds row i of a block; the block
+        // goes through shared memory (rows 36 floats apart: conflict-free
+        // 16-byte writes and reads) so that C is written a row at a time.  All
+        // MMAs have completed when acc_full fires, and it fires only after
+        // every decode warp has left its loop, so the activation and weight
+        // stages are free.
         // (Warp-uniform decision: tcgen05.ld below is a warp-wide instruction.)
         const bool acc_ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(acc_full, 0, &g_gemm_error));
-        static_assert(BN == 32 * (kDecodeWarps / 4), "one 32-column block per warp");
-        static_assert(kDecodeWarps * 32 * 36 * 4 <= kAStages * 2 * kTile, "staging space");
+        constexpr int kColBlocks = BN / 128;  // 32-column blocks per warp
+        static_assert(BN == 32 * kColBlocks * (kDecodeWarps / 4), "column blocks");
+        static_assert(kDecodeWarps * 32 * 36 * 4 <= kAStages * 2 * kTileA + kWStages * 2 * kTileW,
+                      "staging space");
         const int q = warp & 3;
         const int cq = (warp - 2) >> 2;
-        const int col = 32 * cq;
         const int mrow = m0 + 32 * q;
         float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
-        float v[32];
+        for (int jb = 0; jb < kColBlocks; ++jb) {
+            const int col = (BN / 4) * cq + 32 * jb;
+            float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        if (acc_ok) {
-            tc_fence_after();
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
-        }
-        // v[i]: row mrow + lane, column n0 + col + i.  Staged so that lane i
-        // then holds column i of every row.
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(stg + lane * 36 + 4 * j) =
-                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-        __syncwarp();
-        const int nn = n0 + col + lane;  // this lane's column in the row-wise passes
-        if (S == 1) {
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
             if (acc_ok) {
+                tc_fence_after();
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+            }
+            __syncwarp();  // the previous block's reads of the staging rows are done
+            // v[i]: row mrow + lane, column n0 + col + i.  Staged so that lane i
+            // then holds column i of every row.
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<float4*>(stg + lane * 36 + 4 * j) =
+                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            __syncwarp();
+            const int nn = n0 + col + lane;  // this lane's column in the row-wise passes
+            if (S == 1) {
+                if (!acc_ok) continue;
                 // Entries that came out non-finite: recompute element by element.
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -386,15 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                             C[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
                     }
                 }
+            } else {
+                // Split K: the partial block to the workspace [S][M][N].
+                float* pw = partial + static_cast<int64_t>(split) * M * N;
+                for (int row = 0; row < 32; ++row) {
+                    if (mrow + row < M && nn < N)
+                        pw[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
+                }
             }
-        } else {
-            // Split K: the partial tile to the workspace [S][M][N]; every decode
-            // warp reaches both barriers, whatever its waits returned.
-            float* pw = partial + static_cast<int64_t>(split) * M * N;
-            for (int row = 0; row < 32; ++row) {
-                if (mrow + row < M && nn < N)
-                    pw[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
-            }
+        }
+        if (S > 1) {
+            // Every decode warp reaches both barriers, whatever its waits returned.
             __threadfence();
             named_barrier_sync(1, kDecodeWarps * 32);
             uint32_t* last = tmem_slot + 1;  // CTA-local broadcast of the arrival
@@ -409,25 +441,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // order, 8 rows at a time so that 8 * S loads are in flight
                 // together (one row at a time would serialise 32 L2 round trips).
                 __threadfence();
-                for (int r0 = 0; r0 < 32; r0 += 8) {
-                    float x[8];
+                for (int jb = 0; jb < kColBlocks; ++jb) {
+                    const int nn = n0 + (BN / 4) * cq + 32 * jb + lane;
+                    for (int r0 = 0; r0 < 32; r0 += 8) {
+                        float x[8];
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
-                    for (int q2 = 0; q2 < S; ++q2) {
-                        const float* pq = partial + static_cast<int64_t>(q2) * M * N;
+                        for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
+                        for (int q2 = 0; q2 < S; ++q2) {
+                            const float* pq = partial + static_cast<int64_t>(q2) * M * N;
+#pragma unroll
+                            for (int rr = 0; rr < 8; ++rr) {
+                                const int m = mrow + r0 + rr;
+                                if (m < M && nn < N) x[rr] += __ldcg(pq + static_cast<int64_t>(m) * N + nn);
+                            }
+                        }
 #pragma unroll
                         for (int rr = 0; rr < 8; ++rr) {
                             const int m = mrow + r0 + rr;
-                            if (m < M && nn < N) x[rr] += __ldcg(pq + static_cast<int64_t>(m) * N + nn);
+                            if (m >= M || nn >= N) continue;
+                            float v = x[rr];
+                            if (!isfinite(v)) v = entry_exact(A, wq, K, m, nn);
+                            C[static_cast<int64_t>(m) * N + nn] = v;
                         }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 8; ++rr) {
-                        const int m = mrow + r0 + rr;
-                        if (m >= M || nn >= N) continue;
-                        float v = x[rr];
-                        if (!isfinite(v)) v = entry_exact(A, wq, K, m, nn);
-                        C[static_cast<int64_t>(m) * N + nn] = v;
                     }
                 }
             }
@@ -439,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols)
+                     "r"(T::kTmemCols)
                      : "memory");
     }
 }
@@ -478,8 +513,24 @@ bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, 
            (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
 }
 
-cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
-                                int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+namespace {
+
+// Tile width: 256 columns where the output has enough of them to fill the
+// GPU without splitting K, or K is long, and M is at least 256; 128 columns
+// otherwise.  Measured on GB300 (CUDA-graph replay): 256 columns run 512 x
+// 14336 x 4096 in 164 against 178 us, 512 x 4096 x 14336 in 166 against
+// 202 us and 1024 x 14336 x 4096 in 257 against 348 us; 128 columns run
+// 512 x 4096 x 4096 in 62 against 66 us, 256 x 4096 x 4096 in 43 against
+// 55 us and 32 x 4096 x 4096 in 33 against 62 us (wide tiles decode twice
+// the weight rows for the same few activation rows).
+int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
+    const int64_t tiles256 = ((N + 255) / 256) * ((M + BM - 1) / BM);
+    return (M >= 256 && (4 * tiles256 >= 3 * dev.sm_count || K >= 8192)) ? 256 : 128;
+}
+
+template <int BN>
+cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t stream, const DeviceInfo& dev) {
     // Split K when the output has fewer tiles than SMs: S ranges of whole
     // 256-wide units, as many as fit one wave.
     const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
@@ -517,30 +568,40 @@ cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
     err = encode_tiled(&map_alo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a_lo, 2, adims, astrides, abox,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (err != cudaSuccess) return err;
-    const int64_t units = K / 256;
-    const int64_t wdims[3] = {144, units, N};
-    const int64_t wstrides[2] = {144, units * 144};
-    const int wbox[3] = {144, 1, BN};
-    err = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 3, wdims, wstrides, wbox);
+    // Weights as bytes [N rows][K/32 * 18 B] (a row is a multiple of 144 B,
+    // so of 16 B); boxes of BN rows x 48 B, bytes past a row's end read as 0.
+    const int64_t row_bytes = K / kBlockElems * kBlockBytes;
+    const int64_t wdims[2] = {row_bytes, N};
+    const int64_t wstrides[1] = {row_bytes};
+    const int wbox[2] = {kRawRow, BN};
+    err = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 2, wdims, wstrides, wbox);
     if (err != cudaSuccess) return err;
 
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
-        err = cudaFuncSetAttribute(gemm_q4_0_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kSmemBytes);
+        err = cudaFuncSetAttribute(gemm_q4_0_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   Tile<BN>::kSmemBytes);
         if (err != cudaSuccess) return err;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
     const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM),
                     static_cast<unsigned>(S));
     const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
-    err = launch_pdl(gemm_q4_0_tc, grid, dim3(kThreads), kSmemBytes, stream, map_ahi, map_alo,
-                     map_w, A, wq, C, static_cast<int>(M), static_cast<int>(N),
+    err = launch_pdl(gemm_q4_0_tc<BN>, grid, dim3(kThreads), Tile<BN>::kSmemBytes, stream, map_ahi,
+                     map_alo, map_w, A, wq, C, static_cast<int>(M), static_cast<int>(N),
                      static_cast<int>(K), c_vec, S, part, ctr);
     if (err != cudaSuccess) return err;
     note_launch();
     return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
+                                int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
+    return choose_bn(M, N, K, dev) == 256 ? launch_bn<256>(A, wq, C, M, N, K, stream, dev)
+                                          : launch_bn<128>(A, wq, C, M, N, K, stream, dev);
 }
 
 cudaError_t gemm_tc_read_device_error(unsigned int* bits, bool clear) {

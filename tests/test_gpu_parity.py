@@ -201,7 +201,8 @@ def test_gemv_misaligned_takes_generic_path(env, offs):
 
 
 # Prefill GEMM on tcgen05 tensor cores: K % 256 == 0; M and N ragged against
-# the 128 x 128 tiles; K up to 14336 (long accumulations in TMEM).
+# the 128 x 128 tiles; K up to 14336 (long accumulations in TMEM).  These
+# shapes take the 128-column tiles.
 GEMM_TC = [(9, 7, 256), (128, 128, 256), (130, 257, 512), (1, 300, 768), (200, 130, 1024),
            (64, 1000, 2048), (257, 129, 4096), (96, 64, 14336)]
 
@@ -214,6 +215,26 @@ def test_gemm_tensor_cores(env, shape):
     A = synth.activations(M, K, 5 * M + K, dist="outliers")
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC), C_ref, S_ref, "tcgen05")
+
+
+# Shapes that take the 256-column tiles (M >= 256 and either enough 128 x 256
+# tiles to fill the GPU or K >= 8192): ragged M and N, a 16-way K split, a
+# misaligned C, and non-finite scales in both the split and the unsplit path.
+GEMM_WIDE = [(260, 300, 8192, 0), (300, 9800, 512, 0), (300, 9800, 512, 1)]
+
+
+@pytest.mark.parametrize("shape", GEMM_WIDE, ids=lambda s: "x".join(map(str, s)))
+def test_gemm_tensor_cores_wide_tiles(env, shape):
+    qm, o = env
+    M, N, K, c_off = shape
+    blob = synth.q4_0_weights(N, K, 7 * M + N).reshape(N, K // 32, 18).copy()
+    blob[N - 1, 3, 0:2] = np.frombuffer(np.float16(np.inf).tobytes(), np.uint8)
+    blob[N // 2, K // 64, 0:2] = np.frombuffer(np.float16(np.nan).tobytes(), np.uint8)
+    blob = blob.ravel()
+    A = synth.activations(M, K, 11 * M + K, dist="outliers")
+    C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC, c_off=c_off), C_ref, S_ref,
+                 "tcgen05, 256-column tiles")
 
 
 @pytest.mark.parametrize("c_off", [1, 2])
