@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_alo,
                  const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
-                 int c_vec, int S, float* __restrict__ partial, unsigned* __restrict__ ctr) {
+                 int c_vec, int nt, int n_full, int s_rem, float* __restrict__ partial,
+                 unsigned* __restrict__ ctr) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
     constexpr int kTileW = T::kTileW;
@@ -231,10 +232,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = static_cast<int>(blockIdx.y) * BM;
-    const int n0 = static_cast<int>(blockIdx.x) * BN;
+    // Work item: CTAs below n_full take whole tiles; each later tile is split
+    // into s_rem K ranges, one per CTA.  Tiles are numbered m-tile major.
+    const int b = static_cast<int>(blockIdx.x);
+    const int tile = (b < n_full) ? b : n_full + (b - n_full) / s_rem;
+    const int split = (b < n_full) ? 0 : (b - n_full) % s_rem;
+    const int S = (b < n_full) ? 1 : s_rem;
+    const int m0 = (tile / nt) * BM;
+    const int n0 = (tile % nt) * BN;
     const int KT = K / BK / S;  // k-steps of this CTA's K range
-    const int split = static_cast<int>(blockIdx.z);
     const int kt0 = split * KT;
 
     grid_launch_dependents();
@@ -431,7 +437,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_barrier_sync(1, kDecodeWarps * 32);
             uint32_t* last = tmem_slot + 1;  // CTA-local broadcast of the arrival
             if (threadIdx.x == 64) {
-                const int tile = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
                 const unsigned old = atomicAdd(&ctr[tile], 1u);
                 *last = (old == static_cast<unsigned>(S - 1)) ? 1u : 0u;
             }
@@ -508,8 +513,10 @@ __global__ void __launch_bounds__(256)
 }  // namespace
 
 bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, int64_t K) {
+    // (Work items are numbered in one int: at most 2^26 tiles of 128 x 128.)
     return M >= 1 && N >= 1 && (K % 256) == 0 && K > 0 && K <= (int64_t(1) << 24) &&
-           M <= (int64_t(65535) * BM) && N <= (int64_t(1) << 30) &&
+           M <= (int64_t(1) << 30) && N <= (int64_t(1) << 30) &&
+           ((M + BM - 1) / BM) * ((N + 127) / 128) <= (int64_t(1) << 26) &&
            (reinterpret_cast<uintptr_t>(wq) & 15u) == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
 }
 
@@ -531,18 +538,25 @@ int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 template <int BN>
 cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
                       cudaStream_t stream, const DeviceInfo& dev) {
-    // Split K when the output has fewer tiles than SMs: S ranges of whole
-    // 256-wide units, as many as fit one wave.
-    const int64_t tiles = ((N + BN - 1) / BN) * ((M + BM - 1) / BM);
-    int S = 1;
+    // Work items for one CTA per SM.  Whole tiles fill as many full waves as
+    // they can; the tiles of the last, partial wave (all tiles when there are
+    // fewer than SMs) are split into s_rem K ranges of whole 256-wide units,
+    // as many as fit the SMs, so the last wave is not left mostly idle.
+    const int64_t nt = (N + BN - 1) / BN;
+    const int64_t tiles = nt * ((M + BM - 1) / BM);
+    const int64_t P = dev.sm_count;
+    const int64_t rem = tiles % P;
+    int s_rem = 1;
     for (int c = 2; c <= 16; ++c) {
-        if ((K / 256) % c == 0 && tiles * c <= dev.sm_count) S = c;
+        if ((K / 256) % c == 0 && rem * c <= P) s_rem = c;
     }
-    // Workspace: bf16 hi / lo copies of A, then (S > 1) the partial tiles
-    // [S][M][N] and one arrival counter per tile.
+    const int64_t n_full = (s_rem > 1) ? tiles - rem : tiles;
+    const int64_t items = n_full + (tiles - n_full) * s_rem;
+    // Workspace: bf16 hi / lo copies of A, then (split tiles) the partial
+    // tiles [s_rem][M][N] and one arrival counter per tile.
     const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
-    const size_t part_bytes = (S > 1) ? static_cast<size_t>(S) * M * N * 4 : 0;
-    const size_t ctr_bytes = (S > 1) ? static_cast<size_t>(tiles) * 4 : 0;
+    const size_t part_bytes = (s_rem > 1) ? static_cast<size_t>(s_rem) * M * N * 4 : 0;
+    const size_t ctr_bytes = (s_rem > 1) ? static_cast<size_t>(tiles) * 4 : 0;
     void* ws = nullptr;
     cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes + part_bytes + ctr_bytes, &ws);
     if (err != cudaSuccess) return err;
@@ -554,7 +568,7 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8);
     err = launch_pdl(split_bf16, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                      reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
-                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(S > 1 ? tiles : 0));
+                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(s_rem > 1 ? tiles : 0));
     if (err != cudaSuccess) return err;
     note_launch();
 
@@ -585,12 +599,11 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
         if (err != cudaSuccess) return err;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
-    const dim3 grid(static_cast<unsigned>((N + BN - 1) / BN), static_cast<unsigned>((M + BM - 1) / BM),
-                    static_cast<unsigned>(S));
     const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
-    err = launch_pdl(gemm_q4_0_tc<BN>, grid, dim3(kThreads), Tile<BN>::kSmemBytes, stream, map_ahi,
-                     map_alo, map_w, A, wq, C, static_cast<int>(M), static_cast<int>(N),
-                     static_cast<int>(K), c_vec, S, part, ctr);
+    err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
+                     Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, A, wq, C,
+                     static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec,
+                     static_cast<int>(nt), static_cast<int>(n_full), s_rem, part, ctr);
     if (err != cudaSuccess) return err;
     note_launch();
     return cudaSuccess;

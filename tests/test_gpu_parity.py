@@ -204,7 +204,8 @@ def test_gemv_misaligned_takes_generic_path(env, offs):
 # the 128 x 128 tiles; K up to 14336 (long accumulations in TMEM).  These
 # shapes take the 128-column tiles.
 GEMM_TC = [(9, 7, 256), (128, 128, 256), (130, 257, 512), (1, 300, 768), (200, 130, 1024),
-           (64, 1000, 2048), (257, 129, 4096), (96, 64, 14336)]
+           (64, 1000, 2048), (257, 129, 4096), (96, 64, 14336),
+           (130, 10200, 1024)]  # 160 tiles: 152 whole, the last 8 split in 4 K ranges
 
 
 @pytest.mark.parametrize("shape", GEMM_TC, ids=lambda s: "x".join(map(str, s)))
@@ -235,6 +236,23 @@ def test_gemm_tensor_cores_wide_tiles(env, shape):
     C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC, c_off=c_off), C_ref, S_ref,
                  "tcgen05, 256-column tiles")
+
+
+def test_gemm_tensor_cores_wide_tiles_last_wave_split(env):
+    # 154 tiles of 128 x 256 on 152 SMs: 152 whole tiles, the last 2 split in
+    # 2 K ranges.  Checked on all columns of 3 rows (first, last, one of the
+    # split tiles' rows) and 1024 random entries.
+    qm, o = env
+    M, N, K = 256, 19500, 512
+    blob = synth.q4_0_weights(N, K, 77)
+    A = synth.activations(M, K, 78, dist="outliers")
+    C = matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC)
+    g = synth.rng(79, (M, N, K))
+    rows = np.array([0, 200, M - 1])
+    mi = np.concatenate([np.repeat(rows, N), g.integers(0, M, 1024)])
+    ni = np.concatenate([np.tile(np.arange(N), rows.size), g.integers(0, N, 1024)])
+    C_ref, S_ref = o.matmul_q4_0_entries(A, blob, N, K, mi, ni)
+    assert_close(C[mi, ni], C_ref, S_ref, "tcgen05, last wave split")
 
 
 @pytest.mark.parametrize("c_off", [1, 2])
