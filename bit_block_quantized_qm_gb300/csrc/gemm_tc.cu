@@ -139,35 +139,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Decode half of one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared
 // memory): quant bytes 8p .. 8p+7, i.e. elements 8p .. 8p+7 (low nibbles) and
-// 16+8p .. 16+8p+7 (high nibbles).  Each weight (q - 8) * d is split into
-// bf16 hi = bf16(w) and lo = bf16(w - hi), an exact two-piece sum; both are
-// stored as row n of 128-byte-swizzled K-major tiles at k = 32 * half + j.
-// Non-finite scales need no care here: they make the output entry non-finite
-// and the epilogue recomputes it element by element.
+// 16+8p .. 16+8p+7 (high nibbles).  A byte permute puts each nibble q in bits
+// 16..19 under the byte 0x43, which reads as the float 128 + q; one packed FMA
+// per pair, x d - 136 d, gives w = (q - 8) d exactly (136 d and (q - 8) d have
+// at most 19 significant bits).  w is then split into bf16 hi = bf16(w) and
+// lo = bf16(w - hi), an exact two-piece sum (w - hi has at most 7 significant
+// bits); both are stored as row n of 128-byte-swizzled K-major tiles at
+// k = 32 * half + j.  Non-finite scales need no care here: they make the
+// output entry non-finite and the epilogue recomputes it element by element.
 __device__ __forceinline__ void decode_half_block(const uint8_t* blk, int p, int n, int half,
                                                   uint8_t* tile_hi, uint8_t* tile_lo) {
+    constexpr uint32_t kHigh = 0x43000000u;
     const uint16_t* h = reinterpret_cast<const uint16_t*>(blk);
     const float d = f16_bits_to_float(h[0]);
+    const float2 d2 = make_float2(d, d);
+    const float2 b2 = make_float2(-136.0f * d, -136.0f * d);
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
     const uint32_t w0 = static_cast<uint32_t>(h[1 + 4 * p]) | (static_cast<uint32_t>(h[2 + 4 * p]) << 16);
     const uint32_t w1 = static_cast<uint32_t>(h[3 + 4 * p]) | (static_cast<uint32_t>(h[4 + 4 * p]) << 16);
 #pragma unroll
     for (int side = 0; side < 2; ++side) {  // 0: low nibbles, 1: high nibbles
         const uint32_t v0 = (side ? (w0 >> 4) : w0) & 0x0F0F0F0Fu;
         const uint32_t v1 = (side ? (w1 >> 4) : w1) & 0x0F0F0F0Fu;
-        float x[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            x[e] = magic_minus8(__byte_perm(v0, kMagicBits, 0x7540u + e)) * d;
-            x[4 + e] = magic_minus8(__byte_perm(v1, kMagicBits, 0x7540u + e)) * d;
-        }
+        const uint32_t src[4] = {v0, v0, v1, v1};
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+            // Elements 2e and 2e + 1 of the eight: bytes (2e) % 4 and (2e) % 4 + 1.
+            const uint32_t sel0 = 0x7044u | (static_cast<uint32_t>((2 * e) & 3) << 8);
+            const uint32_t sel1 = 0x7044u | (static_cast<uint32_t>((2 * e + 1) & 3) << 8);
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(src[e], kHigh, sel0)),
+                                                    __uint_as_float(__byte_perm(src[e], kHigh, sel1))),
+                                        d2, b2);
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(x.x, x.y);
             const uint32_t hw = *reinterpret_cast<const uint32_t*>(&hb);
-            const float r0 = x[2 * e] - __uint_as_float(hw << 16);
-            const float r1 = x[2 * e + 1] - __uint_as_float(hw & 0xFFFF0000u);
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(r0, r1);
+            const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw << 16), __uint_as_float(hw & 0xFFFF0000u)),
+                                        neg1, x);
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
             hi[e] = hw;
             lo[e] = *reinterpret_cast<const uint32_t*>(&lb);
         }
