@@ -56,7 +56,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kWStages = 2;
 constexpr int kRawStages = 2;
 constexpr int kDecodeWarps = 16;
 constexpr int kThreads = (2 + kDecodeWarps) * 32;
@@ -67,11 +66,15 @@ constexpr int kRawRow = 48;           // raw bytes of one row per k-step (3 x 16
 template <int BN>
 struct Tile {
     static constexpr int kAStages = BN == 128 ? 3 : 2;
+    static constexpr int kWStages = 2;
     static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
     static constexpr int kRawBytes = BN * kRawRow;
     static constexpr int kTmemCols = BN;        // f32 accumulator columns
+    // Barriers (full and empty per stage, acc_full), then the TMEM address and
+    // the split-K arrival flag, rounded up to 16 bytes.
+    static constexpr int kBarBytes = ((2 * (kAStages + kWStages + kRawStages) + 1) * 8 + 8 + 15) / 16 * 16;
     static constexpr int kSmemBytes = kAStages * 2 * kTileA + kWStages * 2 * kTileW +
-                                      kRawStages * kRawBytes + 16 * 8 + 1024;  // + barriers, slack
+                                      kRawStages * kRawBytes + kBarBytes + 1024;  // + alignment slack
     // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
     // N = BN, M = BM.
     static constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -219,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  unsigned* __restrict__ ctr) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
+    constexpr int kWStages = T::kWStages;
     constexpr int kTileW = T::kTileW;
     constexpr int kRawBytes = T::kRawBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
