@@ -216,9 +216,10 @@ template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_ahi,
                  const __grid_constant__ CUtensorMap map_alo,
-                 const __grid_constant__ CUtensorMap map_w, const float* __restrict__ A,
+                 const __grid_constant__ CUtensorMap map_w,
+                 const __grid_constant__ CUtensorMap map_w2, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
-                 int c_vec, int nt, int n_full, int s_rem, float* __restrict__ partial,
+                 int c_vec, int nt, int n_full, int s_rem, int hw, float* __restrict__ partial,
                  unsigned* __restrict__ ctr) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
@@ -244,14 +245,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Work item: CTAs below n_full take whole tiles; each later tile is split
-    // into s_rem K ranges, one per CTA.  Tiles are numbered m-tile major.
+    // Work item: CTAs below n_full take whole tiles.  Each later tile is
+    // either split into s_rem K ranges, one per CTA, or (hw, BN = 256 only)
+    // into two 128-column halves, one per CTA.  Tiles are numbered m-tile
+    // major.
     const int b = static_cast<int>(blockIdx.x);
-    const int tile = (b < n_full) ? b : n_full + (b - n_full) / s_rem;
-    const int split = (b < n_full) ? 0 : (b - n_full) % s_rem;
-    const int S = (b < n_full) ? 1 : s_rem;
+    const bool half_item = (BN == 256) && hw != 0 && b >= n_full;
+    const int tile = (b < n_full) ? b : n_full + (b - n_full) / (hw ? 2 : s_rem);
+    const int split = (b < n_full || hw) ? 0 : (b - n_full) % s_rem;
+    const int S = (b < n_full || hw) ? 1 : s_rem;
+    const int wn = half_item ? BN / 2 : BN;  // columns of this item
     const int m0 = (tile / nt) * BM;
-    const int n0 = (tile % nt) * BN;
+    const int n0 = (tile % nt) * BN + (half_item ? ((b - n_full) & 1) * (BN / 2) : 0);
     const int KT = K / BK / S;  // k-steps of this CTA's K range
     const int kt0 = split * KT;
 
@@ -294,14 +299,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // below it, which TMA requires, and still covers the pair.
             prefetch_tensormap(&map_ahi);
             prefetch_tensormap(&map_alo);
-            prefetch_tensormap(&map_w);
+            const CUtensorMap* mw = half_item ? &map_w2 : &map_w;
+            prefetch_tensormap(mw);
             for (int kt = 0; kt < KT; ++kt) {
                 const int rs = kt % kRawStages;
                 if (kt >= kRawStages &&
                     !mbar_wait_bounded(&raw_empty[rs], ((kt / kRawStages) - 1) & 1, &g_gemm_error))
                     break;
-                mbar_arrive_expect_tx(&raw_full[rs], kRawBytes);
-                tma_load_2d(raw + rs * kRawBytes, &map_w, (36 * (kt0 + kt)) & ~15, n0, &raw_full[rs]);
+                mbar_arrive_expect_tx(&raw_full[rs], static_cast<uint32_t>(wn * kRawRow));
+                tma_load_2d(raw + rs * kRawBytes, mw, (36 * (kt0 + kt)) & ~15, n0, &raw_full[rs]);
                 const int as = kt % kAStages;
                 if (kt >= kAStages &&
                     !mbar_wait_bounded(&a_empty[as], ((kt / kAStages) - 1) & 1, &g_gemm_error))
@@ -313,7 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // MMA issuer: 3 pieces x 4 k-steps of 16 per 64-wide k-step.
+            // MMA issuer: 3 pieces x 4 k-steps of 16 per 64-wide k-step, N = wn.
+            const uint32_t idesc =
+                (T::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(wn >> 3) << 17);
             bool ok = true;
             for (int kt = 0; kt < KT && ok; ++kt) {
                 const int as = kt % kAStages;
@@ -329,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint32_t off = kk * 32;  // 16 bf16 along K
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), T::kIdesc, (kt | kk) != 0);
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), T::kIdesc, 1u);
-                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), T::kIdesc, 1u);
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), idesc, (kt | kk) != 0);
+                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), idesc, 1u);
+                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), idesc, 1u);
                 }
                 mma_commit(&a_empty[as]);
                 mma_commit(&w_empty[ws]);
@@ -339,15 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(acc_full);
         }
     } else {
-        // Decode warps: kTpr threads per weight row.  With 2 (BN = 256) thread
-        // t of 512 owns row t / 2 and block t % 2 of the 64-wide k-step, both
-        // halves of its quant bytes; with 4 (BN = 128) it owns row t / 4,
-        // block (t / 2) % 2 and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
-        constexpr int kTpr = kDecodeWarps * 32 / BN;
-        static_assert(kTpr == 2 || kTpr == 4, "threads per weight row");
+        // Decode warps: tpr threads per weight row.  With 2 (256 columns)
+        // thread t of 512 owns row t / 2 and block t % 2 of the 64-wide k-step,
+        // both halves of its quant bytes; with 4 (128 columns) it owns row
+        // t / 4, block (t / 2) % 2 and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
+        const int tpr = kDecodeWarps * 32 / wn;
         const int dt = threadIdx.x - 64;
-        const int n = dt / kTpr;
-        const int half = (kTpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
+        const int n = dt / tpr;
+        const int half = (tpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
         bool ok = true;
         for (int kt = 0; kt < KT && ok; ++kt) {
             const int rs = kt % kRawStages;
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* blk =
                 raw + rs * kRawBytes + n * kRawRow + ((36 * (kt0 + kt)) & 15) + half * kBlockBytes;
             uint8_t* thi = w_st + (2 * ws) * kTileW;
-            if constexpr (kTpr == 2) {
+            if (tpr == 2) {
                 decode_half_block(blk, 0, n, half, thi, thi + kTileW);
                 decode_half_block(blk, 1, n, half, thi, thi + kTileW);
             } else {
@@ -373,8 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns rows
-        // 32 q .. 32 q + 31 and columns BN/4 cq .. BN/4 cq + BN/4 - 1, as
-        // BN/128 blocks of 32 x 32.  Lane i holds row i of a block; the block
+        // 32 q .. 32 q + 31 and columns wn/4 cq .. wn/4 cq + wn/4 - 1, as
+        // wn/128 blocks of 32 x 32.  Lane i holds row i of a block; the block
         // goes through shared memory (rows 36 floats apart: conflict-free
         // 16-byte writes and reads) so that C is written a row at a time.  All
         // MMAs have completed when acc_full fires, and it fires only after
@@ -390,8 +397,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cq = (warp - 2) >> 2;
         const int mrow = m0 + 32 * q;
         float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
-        for (int jb = 0; jb < kColBlocks; ++jb) {
-            const int col = (BN / 4) * cq + 32 * jb;
+        const int ncb = wn / 128;  // 32-column blocks of this warp
+        for (int jb = 0; jb < ncb; ++jb) {
+            const int col = (wn / 4) * cq + 32 * jb;
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -458,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // order, 8 rows at a time so that 8 * S loads are in flight
                 // together (one row at a time would serialise 32 L2 round trips).
                 __threadfence();
-                for (int jb = 0; jb < kColBlocks; ++jb) {
-                    const int nn = n0 + (BN / 4) * cq + 32 * jb + lane;
+                for (int jb = 0; jb < ncb; ++jb) {
+                    const int nn = n0 + (wn / 4) * cq + 32 * jb + lane;
                     for (int r0 = 0; r0 < 32; r0 += 8) {
                         float x[8];
 #pragma unroll
@@ -552,18 +560,21 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
                       cudaStream_t stream, const DeviceInfo& dev) {
     // Work items for one CTA per SM.  Whole tiles fill as many full waves as
     // they can; the tiles of the last, partial wave (all tiles when there are
-    // fewer than SMs) are split into s_rem K ranges of whole 256-wide units,
-    // as many as fit the SMs, so the last wave is not left mostly idle.
+    // fewer than SMs) are split so that the last wave is not left mostly
+    // idle: 256-column tiles after a full wave into two 128-column halves
+    // when those fit the SMs (no partial sums to add), otherwise into s_rem
+    // K ranges of whole 256-wide units, as many as fit the SMs.
     const int64_t nt = (N + BN - 1) / BN;
     const int64_t tiles = nt * ((M + BM - 1) / BM);
     const int64_t P = dev.sm_count;
     const int64_t rem = tiles % P;
+    const int hw = (BN == 256 && tiles >= P && rem > 0 && 2 * rem <= P) ? 1 : 0;
     int s_rem = 1;
-    for (int c = 2; c <= 16; ++c) {
+    for (int c = 2; c <= 16 && !hw; ++c) {
         if ((K / 256) % c == 0 && rem * c <= P) s_rem = c;
     }
-    const int64_t n_full = (s_rem > 1) ? tiles - rem : tiles;
-    const int64_t items = n_full + (tiles - n_full) * s_rem;
+    const int64_t n_full = (s_rem > 1 || hw) ? tiles - rem : tiles;
+    const int64_t items = n_full + (tiles - n_full) * (hw ? 2 : s_rem);
     // Workspace: bf16 hi / lo copies of A, then (split tiles) the partial
     // tiles [s_rem][M][N] and one arrival counter per tile.
     const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
@@ -584,7 +595,7 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     if (err != cudaSuccess) return err;
     note_launch();
 
-    CUtensorMap map_ahi, map_alo, map_w;
+    CUtensorMap map_ahi, map_alo, map_w, map_w2;
     const int64_t adims[2] = {K, M};
     const int64_t astrides[1] = {K * 2};
     const int abox[2] = {BK, BM};
@@ -602,6 +613,9 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     const int wbox[2] = {kRawRow, BN};
     err = encode_tiled(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 2, wdims, wstrides, wbox);
     if (err != cudaSuccess) return err;
+    const int wbox2[2] = {kRawRow, BN / 2};  // half-width items
+    err = encode_tiled(&map_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 2, wdims, wstrides, wbox2);
+    if (err != cudaSuccess) return err;
 
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
@@ -613,9 +627,9 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     }
     const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
     err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
-                     Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, A, wq, C,
+                     Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, map_w2, A, wq, C,
                      static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec,
-                     static_cast<int>(nt), static_cast<int>(n_full), s_rem, part, ctr);
+                     static_cast<int>(nt), static_cast<int>(n_full), s_rem, hw, part, ctr);
     if (err != cudaSuccess) return err;
     note_launch();
     return cudaSuccess;

@@ -239,9 +239,10 @@ def test_gemm_tensor_cores_wide_tiles(env, shape):
 
 
 def test_gemm_tensor_cores_wide_tiles_last_wave_split(env):
-    # 154 tiles of 128 x 256 on 152 SMs: 152 whole tiles, the last 2 split in
-    # 2 K ranges.  Checked on all columns of 3 rows (first, last, one of the
-    # split tiles' rows) and 1024 random entries.
+    # 154 tiles of 128 x 256 on 152 SMs: 152 whole tiles, the last 2 split
+    # into 128-column halves (one of them wholly past N = 19500).  Checked on
+    # all columns of 3 rows (first, last, one of the split tiles' rows) and
+    # 1024 random entries.
     qm, o = env
     M, N, K = 256, 19500, 512
     blob = synth.q4_0_weights(N, K, 77)
