@@ -70,9 +70,10 @@ struct Tile {
     static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
     static constexpr int kRawBytes = BN * kRawRow;
     static constexpr int kTmemCols = BN;        // f32 accumulator columns
-    // Barriers (full and empty per stage, acc_full), then the TMEM address and
-    // the split-K arrival flag, rounded up to 16 bytes.
-    static constexpr int kBarBytes = ((2 * (kAStages + kWStages + kRawStages) + 1) * 8 + 8 + 15) / 16 * 16;
+    // Barriers (full and empty per stage, acc_full, two cluster-reduction
+    // barriers), then the TMEM address and the split-K arrival flag, rounded
+    // up to 16 bytes.
+    static constexpr int kBarBytes = ((2 * (kAStages + kWStages + kRawStages) + 3) * 8 + 8 + 15) / 16 * 16;
     static constexpr int kSmemBytes = kAStages * 2 * kTileA + kWStages * 2 * kTileW +
                                       kRawStages * kRawBytes + kBarBytes + 1024;  // + alignment slack
     // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_w,
                  const __grid_constant__ CUtensorMap map_w2, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
-                 int c_vec, int nt, int n_full, int s_rem, int hw, float* __restrict__ partial,
+                 int c_vec, int nt, int n_full, int s_rem, int hw, int cl, float* __restrict__ partial,
                  unsigned* __restrict__ ctr) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* raw_full = w_empty + kWStages;
     uint64_t* raw_empty = raw_full + kRawStages;
     uint64_t* acc_full = raw_empty + kRawStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+    uint64_t* red_bar = acc_full + 1;  // [2]: partial tiles written, partial tiles read
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -275,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&raw_empty[s], kDecodeWarps);
         }
         mbar_init(acc_full, 1);
+        mbar_init(&red_bar[0], cl ? s_rem : 1);  // one arrival per CTA of the cluster
+        mbar_init(&red_bar[1], cl ? s_rem : 1);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -288,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Cluster launches: every CTA's barriers are initialised before any CTA
+    // can arrive on them remotely.
+    if (cl) cluster_sync_all();
     const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();  // A's pieces come from the split kernel before this one
 
@@ -398,6 +405,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mrow = m0 + 32 * q;
         float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
         const int ncb = wn / 128;  // 32-column blocks of this warp
+        if (S > 1 && cl) {
+            // Split K through the cluster (the S CTAs of this tile, ranks in
+            // range order): each CTA leaves its partial tile in its own shared
+            // memory, [128 rows][wn + 4] f32, then adds rows r 128/S ..
+            // (r + 1) 128/S - 1 of all S tiles in rank order, reading the
+            // others' through distributed shared memory, and writes C.  The
+            // arrivals come on every path, whatever the waits returned.
+            const int ld = wn + 4;  // row stride: 16-byte stores of 8 lanes hit distinct banks
+            float* ptile = reinterpret_cast<float*>(a_st);
+            for (int jb = 0; jb < ncb; ++jb) {
+                const int col = (wn / 4) * cq + 32 * jb;
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                if (acc_ok) {
+                    tc_fence_after();
+                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+                }
+                float* dst = ptile + (32 * q + lane) * ld + col;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(dst + 4 * j) =
+                        make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
+            asm volatile("fence.acq_rel.cluster;" ::: "memory");
+            named_barrier_sync(1, kDecodeWarps * 32);
+            const uint32_t rank = cluster_ctarank();
+            if (threadIdx.x == 64) {
+                for (int r = 0; r < S; ++r)
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&red_bar[0]), static_cast<uint32_t>(r)));
+            }
+            if (mbar_wait_cluster_bounded(&red_bar[0], 0, &g_gemm_error)) {
+                const int rows = BM / S;
+                const int c4n = wn / 4;
+                const uint32_t tbase = smem_addr(ptile);
+                for (int it = threadIdx.x - 64; it < rows * c4n; it += kDecodeWarps * 32) {
+                    const int rl = static_cast<int>(rank) * rows + it / c4n;  // row in the tile
+                    const int c4 = it % c4n;
+                    const uint32_t off = static_cast<uint32_t>((rl * ld + 4 * c4) * 4);
+                    float4 acc4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int r = 0; r < S; ++r) {
+                        const float4 x = ld_dsmem_f4(mapa_shared(tbase + off, static_cast<uint32_t>(r)));
+                        acc4.x += x.x;
+                        acc4.y += x.y;
+                        acc4.z += x.z;
+                        acc4.w += x.w;
+                    }
+                    const int m = m0 + rl;
+                    const int n = n0 + 4 * c4;
+                    if (m >= M || n >= N) continue;
+                    float o[4] = {acc4.x, acc4.y, acc4.z, acc4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (n + e < N && !isfinite(o[e])) o[e] = entry_exact(A, wq, K, m, n + e);
+                    }
+                    float* crow = C + static_cast<int64_t>(m) * N;
+                    if (c_vec) {
+                        *reinterpret_cast<float4*>(crow + n) = make_float4(o[0], o[1], o[2], o[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (n + e < N) crow[n + e] = o[e];
+                    }
+                }
+            }
+            // No CTA leaves while another may still read its partial tile.
+            named_barrier_sync(1, kDecodeWarps * 32);
+            if (threadIdx.x == 64) {
+                for (int r = 0; r < S; ++r)
+                    mbar_arrive_cluster(mapa_shared(smem_addr(&red_bar[1]), static_cast<uint32_t>(r)));
+            }
+            mbar_wait_cluster_bounded(&red_bar[1], 0, &g_gemm_error);
+        } else {
         for (int jb = 0; jb < ncb; ++jb) {
             const int col = (wn / 4) * cq + 32 * jb;
             float v[32];
@@ -492,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        }  // global split-K path
     }
 
     tc_fence_before();
@@ -558,6 +639,14 @@ int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 template <int BN>
 cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
                       cudaStream_t stream, const DeviceInfo& dev) {
+    static int configured[64] = {0};
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_q4_0_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Tile<BN>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
+    }
     // Work items for one CTA per SM.  Whole tiles fill as many full waves as
     // they can; the tiles of the last, partial wave (all tiles when there are
     // fewer than SMs) are split so that the last wave is not left mostly
@@ -575,11 +664,30 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     }
     const int64_t n_full = (s_rem > 1 || hw) ? tiles - rem : tiles;
     const int64_t items = n_full + (tiles - n_full) * (hw ? 2 : s_rem);
-    // Workspace: bf16 hi / lo copies of A, then (split tiles) the partial
-    // tiles [s_rem][M][N] and one arrival counter per tile.
+    // A tile split over K is added up through a cluster of its s_rem CTAs
+    // (distributed shared memory) when s_rem is 2, 4 or 8, whole tiles come
+    // in whole clusters, and all of the split tiles' clusters fit on the GPU
+    // at once; otherwise through the workspace by the last CTA to arrive.
+    int cl = 0;
+    if ((s_rem == 2 || s_rem == 4 || s_rem == 8) && n_full % s_rem == 0) {
+        // Resident clusters per device and size, queried once.
+        static int fit[64][4] = {};  // 0: not queried; else 1 + the count
+        const int si = s_rem == 2 ? 1 : s_rem == 4 ? 2 : 3;
+        int f = __atomic_load_n(&fit[dev.device][si], __ATOMIC_ACQUIRE);
+        if (f == 0) {
+            f = 1 + max_active_clusters(gemm_q4_0_tc<BN>, dim3(kThreads), Tile<BN>::kSmemBytes,
+                                        static_cast<unsigned>(s_rem));
+            __atomic_store_n(&fit[dev.device][si], f, __ATOMIC_RELEASE);
+        }
+        if (f - 1 >= rem) cl = 1;
+    }
+    // Workspace: bf16 hi / lo copies of A, then (tiles split through the
+    // workspace) the partial tiles [s_rem][M][N] and one arrival counter per
+    // tile.
+    const bool ws_split = s_rem > 1 && !cl;
     const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
-    const size_t part_bytes = (s_rem > 1) ? static_cast<size_t>(s_rem) * M * N * 4 : 0;
-    const size_t ctr_bytes = (s_rem > 1) ? static_cast<size_t>(tiles) * 4 : 0;
+    const size_t part_bytes = ws_split ? static_cast<size_t>(s_rem) * M * N * 4 : 0;
+    const size_t ctr_bytes = ws_split ? static_cast<size_t>(tiles) * 4 : 0;
     void* ws = nullptr;
     cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes + part_bytes + ctr_bytes, &ws);
     if (err != cudaSuccess) return err;
@@ -591,7 +699,7 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8);
     err = launch_pdl(split_bf16, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
                      reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
-                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(s_rem > 1 ? tiles : 0));
+                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(ws_split ? tiles : 0));
     if (err != cudaSuccess) return err;
     note_launch();
 
@@ -617,19 +725,19 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     err = encode_tiled(&map_w2, CU_TENSOR_MAP_DATA_TYPE_UINT8, wq, 2, wdims, wstrides, wbox2);
     if (err != cudaSuccess) return err;
 
-    static int configured[64] = {0};
-    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-    if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
-        err = cudaFuncSetAttribute(gemm_q4_0_tc<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   Tile<BN>::kSmemBytes);
-        if (err != cudaSuccess) return err;
-        __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
-    }
     const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
-    err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
-                     Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, map_w2, A, wq, C,
-                     static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec,
-                     static_cast<int>(nt), static_cast<int>(n_full), s_rem, hw, part, ctr);
+    if (cl) {
+        err = launch_pdl_cluster(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
+                                 Tile<BN>::kSmemBytes, stream, static_cast<unsigned>(s_rem), map_ahi,
+                                 map_alo, map_w, map_w2, A, wq, C, static_cast<int>(M),
+                                 static_cast<int>(N), static_cast<int>(K), c_vec, static_cast<int>(nt),
+                                 static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
+    } else {
+        err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
+                         Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, map_w2, A, wq, C,
+                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec,
+                         static_cast<int>(nt), static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
+    }
     if (err != cudaSuccess) return err;
     note_launch();
     return cudaSuccess;

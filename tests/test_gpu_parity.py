@@ -238,6 +238,32 @@ def test_gemm_tensor_cores_wide_tiles(env, shape):
                  "tcgen05, 256-column tiles")
 
 
+@pytest.mark.parametrize("shape", [(200, 130, 1024), (64, 1000, 2048), (130, 10200, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_gemm_cluster_split_nonfinite_scales(env, shape):
+    # Tiles split over 4 or 8 K ranges whose sums meet through a thread-block
+    # cluster (the last shape: after 152 whole tiles); non-finite scales in
+    # rows of split tiles go through the element-by-element recomputation.
+    qm, o = env
+    M, N, K = shape
+    blob = synth.q4_0_weights(N, K, 13 * M + N).reshape(N, K // 32, 18).copy()
+    blob[N - 1, 1, 0:2] = np.frombuffer(np.float16(-np.inf).tobytes(), np.uint8)
+    blob[N // 3, K // 64, 0:2] = np.frombuffer(np.float16(np.nan).tobytes(), np.uint8)
+    blob = blob.ravel()
+    A = synth.activations(M, K, 17 * M + K, dist="outliers")
+    C = matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC)
+    if M * N * K <= 1e9:
+        C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
+        assert_close(C, C_ref, S_ref, "tcgen05, cluster split")
+        return
+    g = synth.rng(80, (M, N, K))
+    rows = np.array([0, M - 1])
+    mi = np.concatenate([np.repeat(rows, N), g.integers(0, M, 1024)])
+    ni = np.concatenate([np.tile(np.arange(N), rows.size), g.integers(0, N, 1024)])
+    C_ref, S_ref = o.matmul_q4_0_entries(A, blob, N, K, mi, ni)
+    assert_close(C[mi, ni], C_ref, S_ref, "tcgen05, cluster split (sampled)")
+
+
 def test_gemm_tensor_cores_wide_tiles_last_wave_split(env):
     # 154 tiles of 128 x 256 on 152 SMs: 152 whole tiles, the last 2 split
     # into 128-column halves (one of them wholly past N = 19500).  Checked on
