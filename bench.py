@@ -12,7 +12,8 @@ several times, so no step finds its inputs in L2.
 value = Q4_0 weight bytes streamed per step / device time per step (GB/s),
 timed with CUDA events over --steps steps after --warmup steps.  ``e2e``
 repeats the step with host operands: pinned host -> device copies of every
-input and device -> host copies of every output inside the timed region.
+input and device -> host copies of every output inside the timed region, the
+copies of neighbouring steps overlapping a step's kernels on separate streams.
 
 Beside the step, the line reports (keys ``m1_gemv``, ``decode_sweep``,
 ``prefill``, ``q8_0``): back-to-back M=1 GEMVs at K=N=4096, the 32-layer
@@ -403,24 +404,50 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                 "down_C": torch.empty(down.M * down.N * 4, dtype=torch.uint8).pin_memory(),
                 "deq_out": torch.empty(n_blocks * 128, dtype=torch.uint8).pin_memory()}
 
-    def e2e_step(rp):
-        for k in host:
-            rp[k].view(torch.uint8).view(-1).copy_(pinned[k], non_blocking=True)
+    # Each step copies its inputs in, runs, and copies its outputs back, as a
+    # serving loop would: inputs on one copy stream, the kernels on the main
+    # stream, outputs on a second copy stream, so that step i + 1's inputs and
+    # step i - 1's outputs move (in opposite directions) while step i
+    # computes.  A replica's buffers are refilled only after its previous
+    # step's outputs have been read back.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    freed = [None] * REPLICAS
+
+    def e2e_step(i):
+        r = i % REPLICAS
+        rp = reps[r]
+        with torch.cuda.stream(s_in):
+            if freed[r] is not None:
+                s_in.wait_event(freed[r])
+            for k in host:
+                rp[k].view(torch.uint8).view(-1).copy_(pinned[k], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        stream.wait_event(ev_in)
         step(rp)
-        for k in out_host:
-            out_host[k].copy_(rp[k].view(torch.uint8).view(-1), non_blocking=True)
+        ev_c = torch.cuda.Event()
+        ev_c.record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c)
+            for k in out_host:
+                out_host[k].copy_(rp[k].view(torch.uint8).view(-1), non_blocking=True)
+            ev_out = torch.cuda.Event()
+            ev_out.record(s_out)
+        freed[r] = ev_out
 
     h2d = sum(v.nbytes for v in host.values())
     d2h = sum(int(v.numel()) for v in out_host.values())
     e2e_steps = max(3, min(args.steps, 50))
-    for i in range(2):
-        e2e_step(reps[i % REPLICAS])
+    for i in range(2 * REPLICAS):
+        e2e_step(i)
+    torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(s_in)
     for i in range(e2e_steps):
-        e2e_step(reps[i % REPLICAS])
-    e1.record(stream)
+        e2e_step(i)
+    e1.record(s_out)
+    torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if dist is not None:
@@ -485,7 +512,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "roofline": roofline,
         "paths": paths,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "overlap": "inputs, kernels and outputs on three streams; step i+1's inputs "
+                           "and step i-1's outputs move while step i computes"},
         "gpu_launches": launches,
         "m1_gemv": sweep["m1_gemv"] if sweep else None,
         "decode_sweep": sweep["decode"] if sweep else None,
