@@ -49,13 +49,14 @@ cudaError_t launch_quantize_q8_0(const float* x, int64_t n_blocks, uint8_t* out,
 enum class GemvKind { kSimt, kMma, kPacked };
 
 // The automatic choice between the GEMV consumers.  Measured on GB300
-// (back-to-back launches): at M = 1 the packed FP32 consumer is faster up to
-// 4096 x 4096 weights (1024 x 4096: 5.2 against 6.0 us; 4096 x 4096: 6.4
-// against 6.6 us) and the tensor-core consumer beyond (14336 x 4096: 11.7
-// against 12.0 us); for M = 2..8 the tensor-core consumer is faster for every
-// shape timed.
-inline GemvKind gemv_auto_kind(int64_t M, int64_t N, int64_t K) {
-    return (M == 1 && N * K <= 4096LL * 4096) ? GemvKind::kPacked : GemvKind::kMma;
+// (back-to-back launches, both consumers in the same run): the packed FP32
+// consumer is faster for M = 1..2 at N = 1024 (M = 1: 5.2 against 6.0 us;
+// M = 2: 5.9 against 6.7 us at K = 4096); from N = 2048 up the tensor-core
+// consumer is as fast or faster (M = 1, 2048 x 4096: 6.1 against 6.7 us;
+// 4096 x 4096: 6.6 against 6.4 us; 14336 x 4096: 11.7 against 12.0 us), and
+// for M = 3..8 it is the only consumer.
+inline GemvKind gemv_auto_kind(int64_t M, int64_t N, int64_t /*K*/) {
+    return (M <= 2 && N <= 1024) ? GemvKind::kPacked : GemvKind::kMma;
 }
 
 // Decode-regime GEMV, M = 1..8.  When wq and A are 16-byte aligned and

@@ -80,9 +80,9 @@ extern "C" {
                                    qm_matmul_q4_0_noalloc (M > 8)               */
 
 /* Algorithms for qm_matmul_q4_0_algo. */
-#define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks: GEMV_PK for M == 1 and
-                               N*K <= 4096*4096, GEMV for M <= 8, otherwise
-                               GEMM_TC where it applies, else GEMM_SIMT      */
+#define QM_ALGO_AUTO 0      /* what qm_matmul_q4_0 picks: GEMV_PK for M <= 2 and
+                               N <= 1024, GEMV for M <= 8, otherwise GEMM_TC
+                               where it applies, else GEMM_SIMT              */
 #define QM_ALGO_GEMV 1      /* decode-regime GEMV on tensor cores (mma.sync, bf16
                                pieces, f32 sums); M 1..8                         */
 #define QM_ALGO_GEMM_SIMT 2 /* prefill GEMM on FP32 FMA; any M >= 1              */
