@@ -56,7 +56,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kRawStages = 2;
 constexpr int kDecodeWarps = 16;
 constexpr int kThreads = (2 + kDecodeWarps) * 32;
 constexpr int kTileA = BM * BK * 2;   // one bf16 activation tile: 16 KB
@@ -67,6 +66,7 @@ template <int BN>
 struct Tile {
     static constexpr int kAStages = BN == 128 ? 3 : 2;
     static constexpr int kWStages = 2;
+    static constexpr int kRawStages = 2;  // raw Q4_0 bytes of one k-step per stage
     static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
     static constexpr int kRawBytes = BN * kRawRow;
     static constexpr int kTmemCols = BN;        // f32 accumulator columns
@@ -225,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
     constexpr int kWStages = T::kWStages;
+    constexpr int kRawStages = T::kRawStages;
     constexpr int kTileW = T::kTileW;
     constexpr int kRawBytes = T::kRawBytes;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -342,11 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t whi = smem_addr(w_st + (2 * ws) * kTileW);
                 const uint32_t wlo = whi + kTileW;
 #pragma unroll
+                // Descriptors once per stage; a k-step of 16 bf16 (32 bytes) is +2
+                // in the start-address field (16-byte units, below 2^14 here).
+                const uint64_t dah = sw128_desc(ahi), dal = sw128_desc(alo);
+                const uint64_t dwh = sw128_desc(whi), dwl = sw128_desc(wlo);
+#pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint32_t off = kk * 32;  // 16 bf16 along K
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(whi + off), idesc, (kt | kk) != 0);
-                    mma_f16(tmem, sw128_desc(ahi + off), sw128_desc(wlo + off), idesc, 1u);
-                    mma_f16(tmem, sw128_desc(alo + off), sw128_desc(whi + off), idesc, 1u);
+                    const uint64_t o = static_cast<uint64_t>(2 * kk);
+                    mma_f16(tmem, dah + o, dwh + o, idesc, (kt | kk) != 0);
+                    mma_f16(tmem, dah + o, dwl + o, idesc, 1u);
+                    mma_f16(tmem, dal + o, dwh + o, idesc, 1u);
                 }
                 mma_commit(&a_empty[as]);
                 mma_commit(&w_empty[ws]);
