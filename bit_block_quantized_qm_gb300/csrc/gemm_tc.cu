@@ -136,10 +136,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
 
 // Decode half of one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared
 // memory): quant bytes 8p .. 8p+7, i.e. elements 8p .. 8p+7 (low nibbles) and
@@ -342,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t alo = ahi + kTileA;
                 const uint32_t whi = smem_addr(w_st + (2 * ws) * kTileW);
                 const uint32_t wlo = whi + kTileW;
-#pragma unroll
                 // Descriptors once per stage; a k-step of 16 bf16 (32 bytes) is +2
                 // in the start-address field (16-byte units, below 2^14 here).
                 const uint64_t dah = sw128_desc(ahi), dal = sw128_desc(alo);
@@ -591,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// A f32 -> bf16 hi = bf16(a), lo = bf16(a - hi) (lo = 0 where a - hi is not finite).
+// A f32 -> bf16 hi = bf16(a), lo = bf16(a - hi).
 // Also zeroes the split-K arrival counters of the GEMM that follows.
 __global__ void __launch_bounds__(256)
     split_bf16(const float4* __restrict__ a, uint2* __restrict__ hi, uint2* __restrict__ lo,
@@ -604,16 +599,23 @@ __global__ void __launch_bounds__(256)
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const float4 v = __ldg(a + i);
-        const float x[4] = {v.x, v.y, v.z, v.w};
-        float h[4], l[4];
+        const float2 x[2] = {make_float2(v.x, v.y), make_float2(v.z, v.w)};
+        uint32_t hw[2], lw[2];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            h[j] = __bfloat162float(__float2bfloat16_rn(x[j]));
-            const float r = x[j] - h[j];
-            l[j] = isfinite(r) ? r : 0.f;
+        for (int e = 0; e < 2; ++e) {
+            // Packed conversions (two values per instruction); lo = x - hi by
+            // one packed FMA, exact.  A non-finite piece makes the entries
+            // that use it non-finite, and the GEMM recomputes those exactly.
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(x[e].x, x[e].y);
+            hw[e] = *reinterpret_cast<const uint32_t*>(&hb);
+            const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw[e] << 16),
+                                                    __uint_as_float(hw[e] & 0xFFFF0000u)),
+                                        make_float2(-1.0f, -1.0f), x[e]);
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
+            lw[e] = *reinterpret_cast<const uint32_t*>(&lb);
         }
-        hi[i] = make_uint2(pack_bf16(h[0], h[1]), pack_bf16(h[2], h[3]));
-        lo[i] = make_uint2(pack_bf16(l[0], l[1]), pack_bf16(l[2], l[3]));
+        hi[i] = make_uint2(hw[0], hw[1]);
+        lo[i] = make_uint2(lw[0], lw[1]);
     }
 }
 

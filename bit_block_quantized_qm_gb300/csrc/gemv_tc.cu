@@ -159,7 +159,11 @@ __host__ __device__ constexpr int frag_cols() { return tc_sets<M>() == 1 ? 2 * M
 // ((((kb * 2 + h) * P + p) * frag_cols + col) * 4 + t).  One set: columns
 // 0..M-1 = hi pieces of rows 0..M-1, M..2M-1 = lo pieces.  Two sets: set 0 hi,
 // set 1 lo, column = row.  A warp reads its 2M (hi, lo) groups of 4 values
-// into registers, syncs, and overwrites.
+// into registers, syncs, and overwrites.  The pieces are formed two at a
+// time (packed bf16x2 conversions; lo from one packed FMA x - hi, exact), which
+// halves the work of the conversion pipe; a value whose hi or lo is not
+// finite makes its rows' totals not finite, and the epilogue recomputes those
+// rows element by element.
 template <int M>
 __device__ __forceinline__ void build_fragments(uint8_t* unit, int lane) {
     constexpr int kPer = 2 * M;  // (kb, h, row, t) groups per lane
@@ -191,16 +195,18 @@ __device__ __forceinline__ void build_fragments(uint8_t* unit, int lane) {
         const int t = idx & 3;
         const int m = (idx >> 2) % M;
         const int kbh = idx / (4 * M);
-        uint32_t hi[4], lo[4];
+        uint32_t hw[2], lw[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const __nv_bfloat16 hb = __float2bfloat16_rn(x[i][q]);
-            const float rest = x[i][q] - __bfloat162float(hb);
-            hi[q] = __bfloat16_as_ushort(hb);
-            lo[q] = __bfloat16_as_ushort(__float2bfloat16_rn(isfinite(rest) ? rest : 0.f));
+        for (int e = 0; e < 2; ++e) {
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(x[i][2 * e], x[i][2 * e + 1]);
+            hw[e] = *reinterpret_cast<const uint32_t*>(&hb);
+            const float2 rest = __ffma2_rn(make_float2(__uint_as_float(hw[e] << 16), __uint_as_float(hw[e] & 0xFFFF0000u)),
+                                           make_float2(-1.0f, -1.0f), make_float2(x[i][2 * e], x[i][2 * e + 1]));
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(rest.x, rest.y);
+            lw[e] = *reinterpret_cast<const uint32_t*>(&lb);
         }
-        const uint2 vh = make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
-        const uint2 vl = make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
+        const uint2 vh = make_uint2(hw[0], hw[1]);
+        const uint2 vl = make_uint2(lw[0], lw[1]);
         if constexpr (P == 1) {
             out[(kbh * NC + m) * 4 + t] = vh;
             out[(kbh * NC + M + m) * 4 + t] = vl;
