@@ -30,7 +30,9 @@
  *   - Memory: the prefill GEMM on tensor cores keeps bf16 copies of A (4 bytes
  *     per element of A) in a per-(device, stream) buffer that grows with
  *     cudaMalloc as needed (growing synchronizes that stream once).  When it
- *     splits K (outputs with fewer 128 x 128 tiles than SMs) the same buffer
+ *     splits K (too few output tiles to fill the SMs), the S CTAs of a tile
+ *     add their partial sums inside a thread-block cluster when S is 2, 4 or
+ *     8 and the clusters fit on the GPU at once; otherwise the same buffer
  *     also holds S x M x N floats of partial sums and one counter per tile.
  *   - Launch: the fast kernels are launched with programmatic dependent
  *     launch, so one may start its prologue while the previous kernel on the
