@@ -34,7 +34,7 @@ __all__ = [
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
-    "QM_ALGO_GEMV_PK",
+    "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -62,7 +62,7 @@ Q8_0_BLOCK_BYTES = 34
 
 # Every symbol include/qm.h declares.
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
-                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count",
+                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan",
                     "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -104,6 +104,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_matmul_q4_0.restype = i32
             lib.qm_matmul_q4_0_algo.argtypes = [p, p, p, i64, i64, i64, i32, p]
             lib.qm_matmul_q4_0_algo.restype = i32
+            lib.qm_gemv_plan.argtypes = [i64, i64, i64, i32, i32, i32, p]
+            lib.qm_gemv_plan.restype = i32
             lib.qm_device_status.argtypes = [p, i32]
             lib.qm_device_status.restype = i32
             lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
@@ -259,6 +261,22 @@ def qm_matmul_q4_0_algo(A, wq, N: int, algo: int, out=None, stream=None):
 def qm_matmul_q4_0(A, wq, N: int, out=None, stream=None):
     """C[M, N] = A[M, K] x dequant(W)^T; GEMV kernels for M <= 8, GEMM above."""
     return qm_matmul_q4_0_algo(A, wq, N, QM_ALGO_AUTO, out=out, stream=stream)
+
+
+GEMV_PLAN_FIELDS = ("RG", "U", "S", "rps", "c", "hs", "rbpc", "nu_max", "stages", "grid", "smem", "W")
+
+
+def qm_gemv_plan(M: int, N: int, K: int, packed: bool = False, sm_count: int = 152,
+                 smem_optin: int = 232448):
+    """The decode GEMV's launch plan (host only, see include/qm.h) as a dict,
+    or None when no plan fits; raises on invalid arguments."""
+    out = (ctypes.c_int64 * 12)()
+    rc = load_library().qm_gemv_plan(M, N, K, 1 if packed else 0, sm_count, smem_optin,
+                                     ctypes.cast(out, ctypes.c_void_p))
+    if rc == QM_ERR_UNSUPPORTED:
+        return None
+    _check(rc, "qm_gemv_plan")
+    return dict(zip(GEMV_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def qm_launch_count() -> int:

@@ -833,6 +833,24 @@ cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
     }
 }
 
+bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, int smem_optin,
+                        int64_t part_floats, int64_t ctr_count, int64_t out[12]) {
+    DeviceInfo dev;
+    dev.device = 0;
+    dev.sm_count = sm_count;
+    dev.max_smem_optin = smem_optin;
+    Workspace ws;
+    ws.part_floats = static_cast<size_t>(part_floats);
+    ws.ctr_count = static_cast<int>(std::min<int64_t>(ctr_count, 0x7FFFFFFF));
+    TcPlan p;
+    int grid = 0, smem = 0;
+    if (!plan_tc(M, packed, N, K, dev, ws, &p, &grid, &smem)) return false;
+    const int64_t v[12] = {p.RG, p.U, p.S, p.rps, p.c, p.hs, p.rbpc, p.nu_max, p.stages, grid, smem,
+                           static_cast<int64_t>(p.rps) * p.c * p.hs};
+    for (int i = 0; i < 12; ++i) out[i] = v[i];
+    return true;
+}
+
 cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear) {
     unsigned int v = 0;
     cudaError_t err = cudaMemcpyFromSymbol(&v, g_gemv_tc_error, sizeof(v));

@@ -387,6 +387,18 @@ int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M, 
 
 uint64_t qm_launch_count(void) { return qm::launch_count(); }
 
+int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin,
+                 int64_t* out) {
+    if (!out) return QM_ERR_NULL;
+    if (M < 1 || M > (packed ? 2 : 8) || N < 1 || N > 0x7FFFFFFF || K < 256 || (K % 256) != 0 ||
+        K > (int64_t(1) << 30) || sm_count < 1 || smem_optin < 1)
+        return QM_ERR_SHAPE;
+    return qm::gemv_tc_plan_query(static_cast<int>(M), packed != 0, N, K, sm_count, smem_optin,
+                                  static_cast<int64_t>(qm::kWorkspacePartFloats), qm::kWorkspaceCounters, out)
+               ? QM_OK
+               : QM_ERR_UNSUPPORTED;
+}
+
 int qm_device_status(void* stream, int clear) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QM_ERR_CUDA;
     unsigned int bits = 0;

@@ -77,6 +77,13 @@ cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
                                 bool* launched);
 cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 
+// The staged GEMV's launch plan for a device with sm_count SMs and smem_optin
+// bytes of opt-in shared memory and a split-K workspace of the given size,
+// without touching a device: {RG, U, S, rps, c, hs, rbpc, nu_max, stages,
+// grid, smem, W}.  False when no plan fits.
+bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, int smem_optin,
+                        int64_t part_floats, int64_t ctr_count, int64_t out[12]);
+
 // The same GEMV with its split-K scratch in a fixed device array instead of
 // a workspace (no allocation).  The first call on a device looks up the
 // array's address.

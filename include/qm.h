@@ -216,6 +216,23 @@ QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int6
                                   int64_t N, int64_t K, void* stream);
 
 /*
+ * qm_gemv_plan — the launch plan the decode GEMV (QM_ALGO_GEMV, packed = 0;
+ * QM_ALGO_GEMV_PK, packed = 1) takes for (M, N, K) on a device with sm_count
+ * SMs and smem_optin bytes of opt-in shared memory per CTA, with the
+ * per-stream split-K workspace.  Host only: touches no device and enqueues
+ * nothing; meant for tests and tuning.
+ *   out: 12 int64 values {RG row groups, U units of 256 k, S K ranges, rps row
+ *        groups per row block, c units per stage, hs warps per tile, rbpc row
+ *        blocks per CTA, nu_max units in the largest K range, stages, grid
+ *        CTAs, dynamic shared memory bytes, W consumer warps}.
+ *   M 1..8 (1..2 when packed), N >= 1, K a positive multiple of 256.
+ * Returns QM_OK, QM_ERR_NULL, QM_ERR_SHAPE, or QM_ERR_UNSUPPORTED when no
+ * plan fits (the library then runs the generic GEMV).
+ */
+QM_API int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin,
+                        int64_t* out);
+
+/*
  * qm_launch_count — the number of kernels this library has enqueued in this
  * process (all devices, all threads), for accounting in benchmarks.
  */
