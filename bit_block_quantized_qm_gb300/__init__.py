@@ -34,7 +34,7 @@ __all__ = [
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
-    "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS",
+    "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -62,7 +62,7 @@ Q8_0_BLOCK_BYTES = 34
 
 # Every symbol include/qm.h declares.
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
-                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan",
+                    "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan", "qm_gemm_plan",
                     "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -106,6 +106,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_matmul_q4_0_algo.restype = i32
             lib.qm_gemv_plan.argtypes = [i64, i64, i64, i32, i32, i32, p]
             lib.qm_gemv_plan.restype = i32
+            lib.qm_gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p]
+            lib.qm_gemm_plan.restype = i32
             lib.qm_device_status.argtypes = [p, i32]
             lib.qm_device_status.restype = i32
             lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
@@ -277,6 +279,18 @@ def qm_gemv_plan(M: int, N: int, K: int, packed: bool = False, sm_count: int = 1
         return None
     _check(rc, "qm_gemv_plan")
     return dict(zip(GEMV_PLAN_FIELDS, (int(v) for v in out)))
+
+
+GEMM_PLAN_FIELDS = ("BN", "nt", "tiles", "n_full", "s_rem", "hw", "items", "cl")
+
+
+def qm_gemm_plan(M: int, N: int, K: int, sm_count: int = 152, fit=(76, 38, 19)):
+    """The prefill GEMM's work items (host only, see include/qm.h) as a dict;
+    `fit` = resident clusters of 2, 4 and 8 CTAs."""
+    out = (ctypes.c_int64 * 8)()
+    _check(load_library().qm_gemm_plan(M, N, K, sm_count, fit[0], fit[1], fit[2],
+                                       ctypes.cast(out, ctypes.c_void_p)), "qm_gemm_plan")
+    return dict(zip(GEMM_PLAN_FIELDS, (int(v) for v in out)))
 
 
 def qm_launch_count() -> int:

@@ -644,6 +644,41 @@ int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
     return (M >= 256 && (4 * tiles256 >= 3 * dev.sm_count || K >= 8192)) ? 256 : 128;
 }
 
+// Work items for one CTA per SM.  Whole tiles fill as many full waves as they
+// can; the tiles of the last, partial wave (all tiles when there are fewer
+// than SMs) are split so that the last wave is not left mostly idle:
+// 256-column tiles after a full wave into two 128-column halves when those fit
+// the SMs (no partial sums to add), otherwise into s_rem K ranges of whole
+// 256-wide units, as many as fit the SMs.
+struct GemmItems {
+    int64_t nt, tiles, rem, n_full, items;
+    int s_rem, hw;
+};
+
+GemmItems plan_gemm_items(int bn, int64_t M, int64_t N, int64_t K, int64_t P) {
+    GemmItems g;
+    g.nt = (N + bn - 1) / bn;
+    g.tiles = g.nt * ((M + BM - 1) / BM);
+    g.rem = g.tiles % P;
+    g.hw = (bn == 256 && g.tiles >= P && g.rem > 0 && 2 * g.rem <= P) ? 1 : 0;
+    g.s_rem = 1;
+    for (int c = 2; c <= 16 && !g.hw; ++c) {
+        if ((K / 256) % c == 0 && g.rem * c <= P) g.s_rem = c;
+    }
+    g.n_full = (g.s_rem > 1 || g.hw) ? g.tiles - g.rem : g.tiles;
+    g.items = g.n_full + (g.tiles - g.n_full) * (g.hw ? 2 : g.s_rem);
+    return g;
+}
+
+// A tile split over K is added up through a cluster of its s_rem CTAs
+// (distributed shared memory) when s_rem is 2, 4 or 8, whole tiles come in
+// whole clusters, and all of the split tiles' clusters fit on the GPU at once
+// (`fit` resident clusters of s_rem CTAs); otherwise through the workspace by
+// the last CTA to arrive.
+bool cluster_split(const GemmItems& g, int fit) {
+    return (g.s_rem == 2 || g.s_rem == 4 || g.s_rem == 8) && g.n_full % g.s_rem == 0 && fit >= g.rem;
+}
+
 template <int BN>
 cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
                       cudaStream_t stream, const DeviceInfo& dev) {
@@ -655,27 +690,9 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
         if (e != cudaSuccess) return e;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
-    // Work items for one CTA per SM.  Whole tiles fill as many full waves as
-    // they can; the tiles of the last, partial wave (all tiles when there are
-    // fewer than SMs) are split so that the last wave is not left mostly
-    // idle: 256-column tiles after a full wave into two 128-column halves
-    // when those fit the SMs (no partial sums to add), otherwise into s_rem
-    // K ranges of whole 256-wide units, as many as fit the SMs.
-    const int64_t nt = (N + BN - 1) / BN;
-    const int64_t tiles = nt * ((M + BM - 1) / BM);
-    const int64_t P = dev.sm_count;
-    const int64_t rem = tiles % P;
-    const int hw = (BN == 256 && tiles >= P && rem > 0 && 2 * rem <= P) ? 1 : 0;
-    int s_rem = 1;
-    for (int c = 2; c <= 16 && !hw; ++c) {
-        if ((K / 256) % c == 0 && rem * c <= P) s_rem = c;
-    }
-    const int64_t n_full = (s_rem > 1 || hw) ? tiles - rem : tiles;
-    const int64_t items = n_full + (tiles - n_full) * (hw ? 2 : s_rem);
-    // A tile split over K is added up through a cluster of its s_rem CTAs
-    // (distributed shared memory) when s_rem is 2, 4 or 8, whole tiles come
-    // in whole clusters, and all of the split tiles' clusters fit on the GPU
-    // at once; otherwise through the workspace by the last CTA to arrive.
+    const GemmItems g = plan_gemm_items(BN, M, N, K, dev.sm_count);
+    const int64_t nt = g.nt, tiles = g.tiles, n_full = g.n_full, items = g.items;
+    const int s_rem = g.s_rem, hw = g.hw;
     int cl = 0;
     if ((s_rem == 2 || s_rem == 4 || s_rem == 8) && n_full % s_rem == 0) {
         // Resident clusters per device and size, queried once.
@@ -687,7 +704,7 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
                                         static_cast<unsigned>(s_rem));
             __atomic_store_n(&fit[dev.device][si], f, __ATOMIC_RELEASE);
         }
-        if (f - 1 >= rem) cl = 1;
+        cl = cluster_split(g, f - 1) ? 1 : 0;
     }
     // Workspace: bf16 hi / lo copies of A, then (tiles split through the
     // workspace) the partial tiles [s_rem][M][N] and one arrival counter per
@@ -757,6 +774,15 @@ cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
     return choose_bn(M, N, K, dev) == 256 ? launch_bn<256>(A, wq, C, M, N, K, stream, dev)
                                           : launch_bn<128>(A, wq, C, M, N, K, stream, dev);
+}
+
+void gemm_tc_plan_query(int64_t M, int64_t N, int64_t K, int sm_count, const int fit[3], int64_t out[8]) {
+    const DeviceInfo dev{0, sm_count, 0};
+    const int bn = choose_bn(M, N, K, dev);
+    const GemmItems g = plan_gemm_items(bn, M, N, K, sm_count);
+    const int f = g.s_rem == 2 ? fit[0] : g.s_rem == 4 ? fit[1] : g.s_rem == 8 ? fit[2] : 0;
+    const int64_t v[8] = {bn, g.nt, g.tiles, g.n_full, g.s_rem, g.hw, g.items, cluster_split(g, f) ? 1 : 0};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
 }
 
 cudaError_t gemm_tc_read_device_error(unsigned int* bits, bool clear) {

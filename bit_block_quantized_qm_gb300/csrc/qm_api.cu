@@ -387,6 +387,18 @@ int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M, 
 
 uint64_t qm_launch_count(void) { return qm::launch_count(); }
 
+int qm_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, int fit2, int fit4, int fit8,
+                 int64_t* out) {
+    if (!out) return QM_ERR_NULL;
+    if (M < 1 || N < 1 || K < 256 || (K % 256) != 0 || sm_count < 1 ||
+        !qm::gemm_tc_supported(reinterpret_cast<const float*>(16), reinterpret_cast<const uint8_t*>(16),
+                               M, N, K))
+        return QM_ERR_SHAPE;
+    const int fit[3] = {fit2, fit4, fit8};
+    qm::gemm_tc_plan_query(M, N, K, sm_count, fit, out);
+    return QM_OK;
+}
+
 int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin,
                  int64_t* out) {
     if (!out) return QM_ERR_NULL;

@@ -84,6 +84,11 @@ cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, int smem_optin,
                         int64_t part_floats, int64_t ctr_count, int64_t out[12]);
 
+// The prefill GEMM's work items for a device with sm_count SMs on which fit[i]
+// clusters of 2, 4, 8 CTAs can be resident at once: {BN, n-tiles, tiles,
+// whole-tile items, s_rem, half-width split, items, cluster split}.
+void gemm_tc_plan_query(int64_t M, int64_t N, int64_t K, int sm_count, const int fit[3], int64_t out[8]);
+
 // The same GEMV with its split-K scratch in a fixed device array instead of
 // a workspace (no allocation).  The first call on a device looks up the
 // array's address.

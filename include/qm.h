@@ -216,6 +216,22 @@ QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int6
                                   int64_t N, int64_t K, void* stream);
 
 /*
+ * qm_gemm_plan — the work items the prefill GEMM on tensor cores
+ * (QM_ALGO_GEMM_TC) takes for (M, N, K) on a device with sm_count SMs on
+ * which fit2, fit4 and fit8 thread-block clusters of 2, 4 and 8 of its CTAs
+ * can be resident at once.  Host only: touches no device and enqueues nothing;
+ * meant for tests and tuning.
+ *   out: 8 int64 values {BN tile width (128 or 256), n-tiles, tiles, whole-tile
+ *        items, s_rem K ranges of each later tile, 1 if the later tiles are
+ *        split into 128-column halves instead, items (= CTAs), 1 if the K
+ *        ranges add up through a cluster}.
+ *   M, N >= 1, K a positive multiple of 256 (the shapes QM_ALGO_GEMM_TC takes).
+ * Returns QM_OK, QM_ERR_NULL or QM_ERR_SHAPE.
+ */
+QM_API int qm_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, int fit2, int fit4, int fit8,
+                        int64_t* out);
+
+/*
  * qm_gemv_plan — the launch plan the decode GEMV (QM_ALGO_GEMV, packed = 0;
  * QM_ALGO_GEMV_PK, packed = 1) takes for (M, N, K) on a device with sm_count
  * SMs and smem_optin bytes of opt-in shared memory per CTA, with the

@@ -1,0 +1,80 @@
+"""The prefill GEMM's work items, checked on the host (qm_gemm_plan).
+
+For a GEMM of M x N x K the library picks a tile width (128 or 256 columns),
+fills whole waves of CTAs with whole tiles and splits the tiles of the last,
+partial wave: into two 128-column halves, or into s_rem K ranges whose sums
+meet through a thread-block cluster or through the workspace.  This test
+replays the kernel's decoding of its 1-D grid for the returned plans and checks
+that every (tile, k-step, column half) is computed exactly once, that K ranges
+are whole 256-wide units, that a cluster never straddles whole and split
+tiles, and that nothing spills into a second wave that a split was meant to
+avoid.
+"""
+import numpy as np
+import pytest
+
+import bit_block_quantized_qm_gb300 as qm
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_block_quantized_qm_gb300 import build as qm_build
+    qm_build.build()
+    return qm.load_library()
+
+
+def replay(plan, M, N, K):
+    """Count visits of each (tile, k-step of 64, column half) by the grid."""
+    bn, nt, tiles, n_full = plan["BN"], plan["nt"], plan["tiles"], plan["n_full"]
+    s_rem, hw, items = plan["s_rem"], plan["hw"], plan["items"]
+    ksteps = K // 64
+    count = np.zeros((tiles, ksteps, 2), dtype=np.int64)
+    for b in range(items):
+        half_item = bn == 256 and hw and b >= n_full
+        tile = b if b < n_full else n_full + (b - n_full) // (2 if hw else s_rem)
+        split = 0 if (b < n_full or hw) else (b - n_full) % s_rem
+        S = 1 if (b < n_full or hw) else s_rem
+        kt = ksteps // S
+        halves = [(b - n_full) & 1] if half_item else [0, 1]
+        for hh in halves:
+            count[tile, split * kt:(split + 1) * kt, hh] += 1
+    return count
+
+
+SHAPES = [(9, 7, 256), (32, 4096, 4096), (130, 257, 512), (200, 130, 1024), (256, 4096, 4096),
+          (260, 300, 8192), (300, 9800, 512), (256, 19500, 512), (512, 1024, 4096),
+          (512, 4096, 4096), (512, 14336, 4096), (512, 4096, 14336), (1024, 14336, 4096),
+          (130, 10200, 1024), (4096, 4096, 256), (96, 64, 14336)]
+
+
+@pytest.mark.parametrize("sm_count", [152, 132, 20])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_work_items_cover_every_tile_once(lib, shape, sm_count):
+    M, N, K = shape
+    plan = qm.qm_gemm_plan(M, N, K, sm_count)
+    bn = plan["BN"]
+    assert bn in (128, 256)
+    assert plan["nt"] == -(-N // bn) and plan["tiles"] == plan["nt"] * -(-M // 128)
+    assert (K // 256) % plan["s_rem"] == 0, "K ranges are whole 256-wide units"
+    assert not (plan["hw"] and plan["s_rem"] > 1)
+    if plan["hw"]:
+        assert bn == 256 and 2 * (plan["tiles"] - plan["n_full"]) <= sm_count
+    if plan["s_rem"] > 1 or plan["hw"]:
+        assert plan["tiles"] - plan["n_full"] == plan["tiles"] % sm_count
+        assert plan["items"] - plan["n_full"] <= sm_count, "the split last wave fits the SMs"
+    if plan["cl"]:
+        assert plan["s_rem"] in (2, 4, 8) and plan["n_full"] % plan["s_rem"] == 0
+    count = replay(plan, M, N, K)
+    assert count.min() == 1 and count.max() == 1
+
+
+def test_cluster_split_needs_resident_clusters(lib):
+    # 32 tiles split 4 ways: clusters only when 32 clusters of 4 fit at once.
+    assert qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 38, 19))["cl"] == 1
+    assert qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 31, 19))["cl"] == 0
+
+
+def test_plan_rejects_unsupported_shapes(lib):
+    for args in ((1, 4096, 4000), (0, 4096, 4096), (1, 0, 4096)):
+        with pytest.raises(qm.QMError):
+            qm.qm_gemm_plan(*args)
