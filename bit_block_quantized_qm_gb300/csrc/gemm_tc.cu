@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const __grid_constant__ CUtensorMap map_w,
                  const __grid_constant__ CUtensorMap map_w2, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
-                 int c_vec, int nt, int n_full, int s_rem, int hw, int cl, float* __restrict__ partial,
+                 int c_vec, int tw, int nt, int n_full, int s_rem, int hw, int cl, float* __restrict__ partial,
                  unsigned* __restrict__ ctr) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
@@ -244,18 +244,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Work item: CTAs below n_full take whole tiles.  Each later tile is
-    // either split into s_rem K ranges, one per CTA, or (hw, BN = 256 only)
-    // into two 128-column halves, one per CTA.  Tiles are numbered m-tile
-    // major.
+    // Work item: CTAs below n_full take whole tiles of tw columns (tw = BN,
+    // or 112 with BN = 128 when 112-column tiles fill the SMs better).  Each
+    // later tile is either split into s_rem K ranges, one per CTA, or (hw,
+    // BN = 256 only) into two 128-column halves, one per CTA.  Tiles are
+    // numbered m-tile major.
     const int b = static_cast<int>(blockIdx.x);
     const bool half_item = (BN == 256) && hw != 0 && b >= n_full;
     const int tile = (b < n_full) ? b : n_full + (b - n_full) / (hw ? 2 : s_rem);
     const int split = (b < n_full || hw) ? 0 : (b - n_full) % s_rem;
     const int S = (b < n_full || hw) ? 1 : s_rem;
-    const int wn = half_item ? BN / 2 : BN;  // columns of this item
+    const int wn = half_item ? BN / 2 : tw;  // columns of this item
     const int m0 = (tile / nt) * BM;
-    const int n0 = (tile % nt) * BN + (half_item ? ((b - n_full) & 1) * (BN / 2) : 0);
+    const int n0 = (tile % nt) * tw + (half_item ? ((b - n_full) & 1) * (BN / 2) : 0);
     const int KT = K / BK / S;  // k-steps of this CTA's K range
     const int kt0 = split * KT;
 
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kt >= kRawStages &&
                     !mbar_wait_bounded(&raw_empty[rs], ((kt / kRawStages) - 1) & 1, &g_gemm_error))
                     break;
-                mbar_arrive_expect_tx(&raw_full[rs], static_cast<uint32_t>(wn * kRawRow));
+                // The box is BN rows (BN / 2 for a half item), whatever wn is.
+                mbar_arrive_expect_tx(&raw_full[rs], static_cast<uint32_t>((half_item ? BN / 2 : BN) * kRawRow));
                 tma_load_2d(raw + rs * kRawBytes, mw, (36 * (kt0 + kt)) & ~15, n0, &raw_full[rs]);
                 const int as = kt % kAStages;
                 if (kt >= kAStages &&
@@ -359,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // thread t of 512 owns row t / 2 and block t % 2 of the 64-wide k-step,
         // both halves of its quant bytes; with 4 (128 columns) it owns row
         // t / 4, block (t / 2) % 2 and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
-        const int tpr = kDecodeWarps * 32 / wn;
+        const int tpr = wn > 128 ? 2 : 4;
         const int dt = threadIdx.x - 64;
         const int n = dt / tpr;
         const int half = (tpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tpr == 2) {
                 decode_half_block(blk, 0, n, half, thi, thi + kTileW);
                 decode_half_block(blk, 1, n, half, thi, thi + kTileW);
-            } else {
+            } else if (n < wn) {  // rows past a 112-column tile are not decoded
                 decode_half_block(blk, dt & 1, n, half, thi, thi + kTileW);
             }
             fence_proxy_async_shared();  // make the tiles visible to the tensor cores
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns rows
         // 32 q .. 32 q + 31 and columns wn/4 cq .. wn/4 cq + wn/4 - 1, as
-        // wn/128 blocks of 32 x 32.  Lane i holds row i of a block; the block
+        // blocks of 32 x 32 (the last one narrower when wn/4 = 28).  Lane i holds row i of a block; the block
         // goes through shared memory (rows 36 floats apart: conflict-free
         // 16-byte writes and reads) so that C is written a row at a time.  All
         // MMAs have completed when acc_full fires, and it fires only after
@@ -397,15 +399,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stages are free.
         // (Warp-uniform decision: tcgen05.ld below is a warp-wide instruction.)
         const bool acc_ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(acc_full, 0, &g_gemm_error));
-        constexpr int kColBlocks = BN / 128;  // 32-column blocks per warp
-        static_assert(BN == 32 * kColBlocks * (kDecodeWarps / 4), "column blocks");
         static_assert(kDecodeWarps * 32 * 36 * 4 <= kAStages * 2 * kTileA + kWStages * 2 * kTileW,
                       "staging space");
         const int q = warp & 3;
         const int cq = (warp - 2) >> 2;
         const int mrow = m0 + 32 * q;
         float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
-        const int ncb = wn / 128;  // 32-column blocks of this warp
+        const int cw = wn / 4;              // columns of this warp (28, 32, 64)
+        const int ncb = (cw + 31) / 32;     // 32-column blocks of this warp
         if (S > 1 && cl) {
             // Split K through the cluster (the S CTAs of this tile, ranks in
             // range order): each CTA leaves its partial tile in its own shared
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ld = wn + 4;  // row stride: 16-byte stores of 8 lanes hit distinct banks
             float* ptile = reinterpret_cast<float*>(a_st);
             for (int jb = 0; jb < ncb; ++jb) {
-                const int col = (wn / 4) * cq + 32 * jb;
+                const int col = cw * cq + 32 * jb;
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -480,7 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait_cluster_bounded(&red_bar[1], 0, &g_gemm_error);
         } else {
         for (int jb = 0; jb < ncb; ++jb) {
-            const int col = (wn / 4) * cq + 32 * jb;
+            const int col = cw * cq + 32 * jb;
+            const int valid = min(32, cw - 32 * jb);  // columns of this block inside the tile
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Entries that came out non-finite: recompute element by element.
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    if (!isfinite(v[i]) && mrow + lane < M && n0 + col + i < N)
+                    if (i < valid && !isfinite(v[i]) && mrow + lane < M && n0 + col + i < N)
                         stg[lane * 36 + i] = entry_exact(A, wq, K, mrow + lane, n0 + col + i);
                 }
                 __syncwarp();
@@ -514,12 +516,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r4 = 0; r4 < 8; ++r4) {
                         const int row = 4 * r4 + (lane >> 3);
                         const float4 x = *reinterpret_cast<const float4*>(stg + row * 36 + 4 * c4);
-                        if (mrow + row < M && n4 < N)
+                        if (mrow + row < M && n4 < N && 4 * c4 < valid)
                             *reinterpret_cast<float4*>(C + static_cast<int64_t>(mrow + row) * N + n4) = x;
                     }
                 } else {
                     for (int row = 0; row < 32; ++row) {
-                        if (mrow + row < M && nn < N)
+                        if (mrow + row < M && nn < N && lane < valid)
                             C[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
                     }
                 }
@@ -527,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Split K: the partial block to the workspace [S][M][N].
                 float* pw = partial + static_cast<int64_t>(split) * M * N;
                 for (int row = 0; row < 32; ++row) {
-                    if (mrow + row < M && nn < N)
+                    if (mrow + row < M && nn < N && lane < valid)
                         pw[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
                 }
             }
@@ -548,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // together (one row at a time would serialise 32 L2 round trips).
                 __threadfence();
                 for (int jb = 0; jb < ncb; ++jb) {
-                    const int nn = n0 + (wn / 4) * cq + 32 * jb + lane;
+                    const int nn = (lane < min(32, cw - 32 * jb)) ? n0 + cw * cq + 32 * jb + lane : N;
                     for (int r0 = 0; r0 < 32; r0 += 8) {
                         float x[8];
 #pragma unroll
@@ -679,9 +681,20 @@ bool cluster_split(const GemmItems& g, int fit) {
     return (g.s_rem == 2 || g.s_rem == 4 || g.s_rem == 8) && g.n_full % g.s_rem == 0 && fit >= g.rem;
 }
 
+// 112-column tiles (with the 128-column kernel) where 128-column tiles leave
+// SMs idle, need no K split, and 112-column ones fill more SMs, still without
+// a split: 512 x 4096 makes 148 tiles of 112 against 128 tiles of 128 on 152
+// SMs, each with 12.5% less work.
+bool narrow_tiles(int64_t M, int64_t N, int64_t K, int64_t P) {
+    const GemmItems g128 = plan_gemm_items(128, M, N, K, P);
+    const GemmItems g112 = plan_gemm_items(112, M, N, K, P);
+    return g128.tiles < P && g128.s_rem == 1 && g112.s_rem == 1 && g112.tiles <= P &&
+           g112.tiles > g128.tiles;
+}
+
 template <int BN>
 cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
-                      cudaStream_t stream, const DeviceInfo& dev) {
+                      cudaStream_t stream, const DeviceInfo& dev, int tw) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
@@ -690,7 +703,7 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
         if (e != cudaSuccess) return e;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
-    const GemmItems g = plan_gemm_items(BN, M, N, K, dev.sm_count);
+    const GemmItems g = plan_gemm_items(tw, M, N, K, dev.sm_count);
     const int64_t nt = g.nt, tiles = g.tiles, n_full = g.n_full, items = g.items;
     const int s_rem = g.s_rem, hw = g.hw;
     int cl = 0;
@@ -755,12 +768,12 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
         err = launch_pdl_cluster(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
                                  Tile<BN>::kSmemBytes, stream, static_cast<unsigned>(s_rem), map_ahi,
                                  map_alo, map_w, map_w2, A, wq, C, static_cast<int>(M),
-                                 static_cast<int>(N), static_cast<int>(K), c_vec, static_cast<int>(nt),
+                                 static_cast<int>(N), static_cast<int>(K), c_vec, tw, static_cast<int>(nt),
                                  static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
     } else {
         err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
                          Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, map_w2, A, wq, C,
-                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec,
+                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec, tw,
                          static_cast<int>(nt), static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
     }
     if (err != cudaSuccess) return err;
@@ -772,13 +785,15 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
 
 cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
-    return choose_bn(M, N, K, dev) == 256 ? launch_bn<256>(A, wq, C, M, N, K, stream, dev)
-                                          : launch_bn<128>(A, wq, C, M, N, K, stream, dev);
+    if (choose_bn(M, N, K, dev) == 256) return launch_bn<256>(A, wq, C, M, N, K, stream, dev, 256);
+    return launch_bn<128>(A, wq, C, M, N, K, stream, dev,
+                          narrow_tiles(M, N, K, dev.sm_count) ? 112 : 128);
 }
 
 void gemm_tc_plan_query(int64_t M, int64_t N, int64_t K, int sm_count, const int fit[3], int64_t out[8]) {
     const DeviceInfo dev{0, sm_count, 0};
-    const int bn = choose_bn(M, N, K, dev);
+    int bn = choose_bn(M, N, K, dev);
+    if (bn == 128 && narrow_tiles(M, N, K, sm_count)) bn = 112;
     const GemmItems g = plan_gemm_items(bn, M, N, K, sm_count);
     const int f = g.s_rem == 2 ? fit[0] : g.s_rem == 4 ? fit[1] : g.s_rem == 8 ? fit[2] : 0;
     const int64_t v[8] = {bn, g.nt, g.tiles, g.n_full, g.s_rem, g.hw, g.items, cluster_split(g, f) ? 1 : 0};

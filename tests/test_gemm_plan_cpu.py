@@ -41,7 +41,7 @@ def replay(plan, M, N, K):
     return count
 
 
-SHAPES = [(9, 7, 256), (32, 4096, 4096), (130, 257, 512), (200, 130, 1024), (256, 4096, 4096),
+SHAPES = [(130, 8000, 512), (9, 7, 256), (32, 4096, 4096), (130, 257, 512), (200, 130, 1024), (256, 4096, 4096),
           (260, 300, 8192), (300, 9800, 512), (256, 19500, 512), (512, 1024, 4096),
           (512, 4096, 4096), (512, 14336, 4096), (512, 4096, 14336), (1024, 14336, 4096),
           (130, 10200, 1024), (4096, 4096, 256), (96, 64, 14336)]
@@ -53,7 +53,7 @@ def test_work_items_cover_every_tile_once(lib, shape, sm_count):
     M, N, K = shape
     plan = qm.qm_gemm_plan(M, N, K, sm_count)
     bn = plan["BN"]
-    assert bn in (128, 256)
+    assert bn in (112, 128, 256)
     assert plan["nt"] == -(-N // bn) and plan["tiles"] == plan["nt"] * -(-M // 128)
     assert (K // 256) % plan["s_rem"] == 0, "K ranges are whole 256-wide units"
     assert not (plan["hw"] and plan["s_rem"] > 1)
@@ -66,6 +66,15 @@ def test_work_items_cover_every_tile_once(lib, shape, sm_count):
         assert plan["s_rem"] in (2, 4, 8) and plan["n_full"] % plan["s_rem"] == 0
     count = replay(plan, M, N, K)
     assert count.min() == 1 and count.max() == 1
+
+
+def test_narrow_tiles_fill_more_sms(lib):
+    # 512 x 4096: 128 tiles of 128 columns, 148 of 112, both without a K split.
+    plan = qm.qm_gemm_plan(512, 4096, 4096, 152)
+    assert plan["BN"] == 112 and plan["tiles"] == 148 and plan["items"] == 148
+    # 1024 x 14336 takes 256-column tiles; 512 x 1024 splits K with 128 columns.
+    assert qm.qm_gemm_plan(1024, 14336, 4096, 152)["BN"] == 256
+    assert qm.qm_gemm_plan(512, 1024, 4096, 152)["BN"] == 128
 
 
 def test_cluster_split_needs_resident_clusters(lib):

@@ -218,6 +218,24 @@ def test_gemm_tensor_cores(env, shape):
     assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC), C_ref, S_ref, "tcgen05")
 
 
+# 112-column tiles (the 128-column kernel with N = 112 MMAs) where they fill
+# more SMs without a K split: 144 tiles of 130 x 8000 against 126 of 128
+# columns; a ragged last tile, a misaligned C, and non-finite scales.
+@pytest.mark.parametrize("c_off", [0, 1])
+def test_gemm_tensor_cores_narrow_tiles(env, c_off):
+    qm, o = env
+    M, N, K = 130, 8000, 512
+    assert qm.qm_gemm_plan(M, N, K)["BN"] == 112
+    blob = synth.q4_0_weights(N, K, 41 + c_off).reshape(N, K // 32, 18).copy()
+    blob[N - 1, 2, 0:2] = np.frombuffer(np.float16(np.inf).tobytes(), np.uint8)
+    blob[115, 9, 0:2] = np.frombuffer(np.float16(np.nan).tobytes(), np.uint8)
+    blob = blob.ravel()
+    A = synth.activations(M, K, 43 + c_off, dist="outliers")
+    C_ref, S_ref = o.matmul_q4_0(A, blob, N, K)
+    assert_close(matmul_gpu(qm, A, blob, N, qm.QM_ALGO_GEMM_TC, c_off=c_off), C_ref, S_ref,
+                 "tcgen05, 112-column tiles")
+
+
 # Shapes that take the 256-column tiles (M >= 256 and either enough 128 x 256
 # tiles to fill the GPU or K >= 8192): ragged M and N, a 16-way K split, a
 # misaligned C, and non-finite scales in both the split and the unsplit path.
