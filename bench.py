@@ -93,6 +93,23 @@ def measured_traffic(kernel: str, workload: str):
     return None
 
 
+def max_over_ranks(x: float, dist, device) -> float:
+    """The largest x over all ranks: a step is as slow as the slowest rank.
+    With one rank (dist None) x itself."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: int, world: int, ms_step: float) -> float:
+    """Whole-job throughput: the bytes every rank streamed in one step over
+    the (slowest rank's) step time."""
+    return bytes_per_rank * world / (ms_step * 1e-3) / 1e9
+
+
 def step_cases():
     cases = synth.workload(1)
     up = next(c for c in cases if c.name == "gemv_m8_k4096_n14336")
@@ -372,13 +389,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     if qm.qm_device_status(clear=True) != qm.QM_OK:
         raise RuntimeError("device error word set during the timed region")
 
-    ms_local = total_ms / args.steps
-    if dist is not None:
-        t = torch.tensor([ms_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    else:
-        ms_step = ms_local
+    ms_step = max_over_ranks(total_ms / args.steps, dist, dev)
 
     # Per-kernel split, from a separate pass with events between the kernels
     # (an event between two kernels also ends their programmatic overlap, so
@@ -395,7 +406,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     avg = {k: statistics.mean(v) for k, v in per_op.items()}
 
     wbytes = up.weight_bytes + down.weight_bytes + deq.weight_bytes
-    value = wbytes * world / (ms_step * 1e-3) / 1e9
+    value = job_gbs(wbytes, world, ms_step)
 
     # ---------------------------------------------------------------- e2e
     pinned = {k: torch.from_numpy(v.view(np.uint8).ravel() if v.dtype != np.uint8 else v)
@@ -449,12 +460,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     e1.record(s_out)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = wbytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
+    e2e_value = job_gbs(wbytes, world, e2e_ms)
 
     # ------------------------------------------------------------ roofline
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
