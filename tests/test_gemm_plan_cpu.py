@@ -87,3 +87,32 @@ def test_plan_rejects_unsupported_shapes(lib):
     for args in ((1, 4096, 4000), (0, 4096, 4096), (1, 0, 4096)):
         with pytest.raises(qm.QMError):
             qm.qm_gemm_plan(*args)
+
+
+def random_shapes(n, seed):
+    g = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(g.choice([int(g.integers(9, 300)), int(g.integers(300, 4100))]))
+        N = int(g.choice([int(g.integers(1, 600)), int(g.integers(600, 30000))]))
+        K = 256 * int(g.integers(1, 65))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("sm_count", [152, 132, 20, 8])
+def test_work_items_random_shapes(lib, sm_count):
+    # Seeded random shapes: the same invariants as above, over ragged M and N,
+    # K from 256 to 16384, and devices of several sizes.
+    for (M, N, K) in random_shapes(40, 1000 + sm_count):
+        plan = qm.qm_gemm_plan(M, N, K, sm_count)
+        bn = plan["BN"]
+        assert bn in (112, 128, 256), (M, N, K)
+        assert plan["nt"] == -(-N // bn) and plan["tiles"] == plan["nt"] * -(-M // 128)
+        assert (K // 256) % plan["s_rem"] == 0, (M, N, K)
+        if plan["s_rem"] > 1 or plan["hw"]:
+            assert plan["items"] - plan["n_full"] <= sm_count, (M, N, K)
+        if plan["cl"]:
+            assert plan["s_rem"] in (2, 4, 8) and plan["n_full"] % plan["s_rem"] == 0
+        count = replay(plan, M, N, K)
+        assert count.min() == 1 and count.max() == 1, (M, N, K, plan)

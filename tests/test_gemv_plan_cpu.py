@@ -96,3 +96,28 @@ def test_plan_rejects_bad_arguments(lib):
         qm.qm_gemv_plan(1, 4096, 4000)
     with pytest.raises(qm.QMError):
         qm.qm_gemv_plan(1, 0, 4096)
+
+
+@pytest.mark.parametrize("dev", DEVICES, ids=lambda d: f"{d[0]}sm")
+def test_plan_invariants_random_shapes(lib, dev):
+    # Seeded random shapes over M = 1..8, ragged N up to 60000 and K up to
+    # 32768, both consumers.
+    sm_count, smem_optin = dev
+    g = np.random.default_rng(7 + sm_count)
+    for _ in range(40):
+        M = int(g.integers(1, 9))
+        N = int(g.choice([int(g.integers(1, 700)), int(g.integers(700, 60000))]))
+        K = 256 * int(g.integers(1, 129))
+        for packed in ((False, True) if M <= 2 else (False,)):
+            plan = qm.qm_gemv_plan(M, N, K, packed, sm_count, smem_optin)
+            if plan is None:
+                continue
+            rows = 32 if packed else 16
+            assert plan["RG"] == -(-N // rows) and plan["U"] == K // UNIT
+            assert plan["W"] == plan["rps"] * plan["c"] * plan["hs"]
+            assert plan["rps"] * rows <= 256 and plan["smem"] <= smem_optin
+            assert plan["grid"] % plan["S"] == 0 and plan["grid"] <= sm_count
+            if plan["S"] > 1:
+                assert plan["RG"] * plan["S"] * M * rows <= PART_FLOATS
+            count = covered(plan, packed)
+            assert count.min() == 1 and count.max() == 1, (M, N, K, packed, plan)
