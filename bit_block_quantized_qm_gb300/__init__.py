@@ -32,7 +32,7 @@ __all__ = [
     "qm_dequant_q8_0", "qm_quantize_q8_0", "qm_dequant_q8_0_ptr", "qm_quantize_q8_0_ptr",
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
-    "qm_matmul_q4_0_noalloc_ptr",
+    "qm_matmul_q4_0_noalloc_ptr", "qm_selftest_wait_timeout",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
     "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
     "EXPORTED_SYMBOLS",
@@ -63,7 +63,8 @@ Q8_0_BLOCK_BYTES = 34
 # Every symbol include/qm.h declares.
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
                     "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan", "qm_gemm_plan",
-                    "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0")
+                    "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0",
+                    "qm_selftest_wait_timeout")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
@@ -109,6 +110,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p]
             lib.qm_gemm_plan.restype = i32
             lib.qm_device_status.argtypes = [p, i32]
+            lib.qm_selftest_wait_timeout.argtypes = [p]
+            lib.qm_selftest_wait_timeout.restype = i32
             lib.qm_device_status.restype = i32
             lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
             lib.qm_matmul_q4_0_noalloc.restype = i32
@@ -157,6 +160,13 @@ def qm_matmul_q4_0_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, stream: 
 def qm_matmul_q4_0_algo_ptr(A: int, wq: int, C: int, M: int, N: int, K: int, algo: int,
                             stream: int = 0) -> int:
     return load_library().qm_matmul_q4_0_algo(A, wq, C, M, N, K, algo, stream)
+
+
+def qm_selftest_wait_timeout(stream=None) -> int:
+    """Enqueue the failure-path self-test kernel (a bounded wait that runs
+    out); the next qm_device_status reports QM_ERR_TIMEOUT.  Returns the C
+    status."""
+    return load_library().qm_selftest_wait_timeout(_stream_handle(stream))
 
 
 def qm_matmul_q4_0_noalloc_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,

@@ -701,4 +701,29 @@ cudaError_t launch_gemv_q4_0_noalloc(const float* A, const uint8_t* wq, float* C
     }
 }
 
+// ---------------------------------------------------------------------------
+// Failure-path self-test (qm_selftest_wait_timeout): one thread waits, with a
+// short bound, on an mbarrier whose phase nothing completes.  The wait gives
+// up, sets the device error word the other kernels use, and the kernel
+// returns: the host then sees QM_ERR_TIMEOUT and the context stays usable.
+// No asynchronous copy is in flight, so returning early leaves nothing behind.
+constexpr uint32_t kSelftestPolls = 1u << 16;
+
+__global__ void wait_timeout_selftest(uint32_t polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    for (uint32_t i = 0; i < polls; ++i) {
+        if (mbar_try_wait(&bar, 0)) return;
+    }
+    atomicOr(&g_gemv_error, kErrWaitTimeout);
+}
+
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream) {
+    wait_timeout_selftest<<<1, 32, 0, stream>>>(kSelftestPolls);
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace qm

@@ -411,6 +411,12 @@ int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int 
                : QM_ERR_UNSUPPORTED;
 }
 
+int qm_selftest_wait_timeout(void* stream) {
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    return from_cuda(qm::launch_wait_timeout_selftest(static_cast<cudaStream_t>(stream)));
+}
+
 int qm_device_status(void* stream, int clear) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QM_ERR_CUDA;
     unsigned int bits = 0;

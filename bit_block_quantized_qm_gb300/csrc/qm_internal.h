@@ -183,4 +183,8 @@ int max_active_clusters(void (*kernel)(KArgs...), dim3 block, size_t smem, unsig
 // that wait on asynchronous copies; ORs them into *bits.
 cudaError_t gemv_read_device_error(unsigned int* bits, bool clear);
 
+// One-thread kernel whose bounded wait on an mbarrier nothing completes runs
+// out and sets the device error word (qm_selftest_wait_timeout).
+cudaError_t launch_wait_timeout_selftest(cudaStream_t stream);
+
 }  // namespace qm

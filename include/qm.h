@@ -187,6 +187,20 @@ QM_API int qm_matmul_q4_0_algo(const float* A, const void* wq, float* C, int64_t
 QM_API int qm_device_status(void* stream, int clear);
 
 /*
+ * qm_selftest_wait_timeout — exercises the failure path of the bounded waits
+ * without faulting or hanging anything.  No counterpart on the kernel-contract
+ * pages; it exists so that tests can check, on a real GPU, that a wait which
+ * runs out is reported and that the context stays usable.  Enqueues on
+ * `stream` one kernel in which a single thread waits on an mbarrier that
+ * nothing completes, giving up after 65536 polls; it then sets the device
+ * error word and returns.  The next qm_device_status on the stream returns
+ * QM_ERR_TIMEOUT (and, with clear != 0, resets the word, after which
+ * qm_device_status returns QM_OK again).  No memory is read or written but the
+ * error word.  Returns QM_OK, or QM_ERR_CUDA if the launch failed.
+ */
+QM_API int qm_selftest_wait_timeout(void* stream);
+
+/*
  * qm_matmul_q4_0_noalloc — the decode-regime product C = A x dequant(W)^T for
  * M = 1..8, for callers that cannot call cudaMalloc.  No counterpart on the
  * kernel-contract pages: it exists for code that must not allocate device
