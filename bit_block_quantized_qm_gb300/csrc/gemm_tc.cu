@@ -13,32 +13,39 @@
 //     terms are at most 2^-17 |a W| together.  bf16 x bf16 products are exact
 //     in the f32 accumulator.
 //
-// Structure (one 128 x 256 output tile per CTA, K in 64-wide steps):
+// Structure (one 128-row output tile of BN = 128 or 256 columns per work
+// item, K in 64-wide steps; BN = 128 also runs 112-column tiles, where those
+// fill more SMs):
 //   * a pre-pass splits A once into bf16 hi / lo matrices (workspace);
 //   * warp 0 (one thread) streams, with TMA, the hi / lo activation tiles
-//     (128 rows x 64 k, 128-byte swizzle, 2 stages) and the weight's raw
-//     Q4_0 bytes of each k-step (256 rows x the 48-byte, 16-byte aligned
-//     span that holds the step's 36-byte block pair, 2 stages);
-//   * warps 2..17 decode each 256 x 64 weight tile into W_hi / W_lo, written
+//     (128 rows x 64 k, 128-byte swizzle) and the weight's raw Q4_0 bytes of
+//     each k-step (BN rows x the 48-byte, 16-byte aligned span that holds the
+//     step's 36-byte block pair);
+//   * warps 2..17 decode each BN x 64 weight tile into W_hi / W_lo, written
 //     in the same swizzled K-major layout (2 stages), then run the epilogue;
-//   * warp 1 owns the TMEM accumulator (128 lanes x 256 f32 columns) and one
+//   * warp 1 owns the TMEM accumulator (128 lanes x BN f32 columns) and one
 //     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16, each
-//     128 x 256 x 16) per k-step, committing completion to the stages'
+//     128 x N x 16) per k-step, committing completion to the stages'
 //     "empty" barriers;
-//   * the epilogue reads TMEM with tcgen05.ld (each warp two 32 x 32 blocks
-//     of its 32-lane quarter), stages a block in shared memory (the freed
-//     weight stages) and writes C row by row, 16-byte stores when C's rows
-//     allow;
+//   * the epilogue reads TMEM with tcgen05.ld (32 x 32 blocks), stages a
+//     block in shared memory (the freed weight stages) and writes C row by
+//     row, 16-byte stores when C's rows allow.
 // The 256-wide tile reads each activation tile once per 256 output columns
 // and keeps the operand reads of one MMA at 12 KB per 2^20 flops, which the
 // shared-memory bandwidth sustains together with the decode's stores.
-//   * when there are fewer output tiles than SMs, K is split into S ranges
-//     (grid z): each CTA writes its partial tile to a workspace and the last
-//     of a tile's S CTAs to arrive adds the partials in range order, so the
-//     result does not depend on timing.  The arrival counters are zeroed by
-//     the A-split kernel that runs before every GEMM.  An entry that comes out infinite or NaN is recomputed
-//     element by element from A and the Q4_0 stream, so non-finite scales
-//     keep the per-element semantics.
+// Work items (a 1-D grid, one per CTA): whole tiles fill as many full waves
+// of SMs as they can; the tiles of a last, partial wave become 128-column
+// halves of 256-column tiles, or are split into s_rem K ranges of whole
+// 256-wide units.  The partial tiles of a K split meet through a thread-block
+// cluster (each CTA keeps its partial tile in shared memory and, after a
+// bounded mbarrier handshake, sums a slice of rows of all of them in rank
+// order over distributed shared memory) when the split tiles' clusters fit
+// on the GPU at once; otherwise each CTA writes its partial tile to the
+// workspace and the last to arrive adds them in range order.  Either way the
+// result does not depend on timing.  The arrival counters are zeroed by the
+// A-split kernel that runs before every GEMM.  An entry that comes out
+// infinite or NaN is recomputed element by element from A and the Q4_0
+// stream, so non-finite scales keep the per-element semantics.
 // Both kernels are launched with programmatic stream serialization: they let
 // the next kernel start its prologue early and wait (griddepcontrol.wait)
 // before touching global memory.
@@ -61,7 +68,7 @@ constexpr int kThreads = (2 + kDecodeWarps) * 32;
 constexpr int kTileA = BM * BK * 2;   // one bf16 activation tile: 16 KB
 constexpr int kRawRow = 48;           // raw bytes of one row per k-step (3 x 16 B)
 
-// Tiles of BN = 128 or 256 output columns.
+// Tiles of BN = 128 (run 128 or 112 columns wide) or 256 output columns.
 template <int BN>
 struct Tile {
     static constexpr int kAStages = BN == 128 ? 3 : 2;

@@ -235,7 +235,7 @@ QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int6
  * which fit2, fit4 and fit8 thread-block clusters of 2, 4 and 8 of its CTAs
  * can be resident at once.  Host only: touches no device and enqueues nothing;
  * meant for tests and tuning.
- *   out: 8 int64 values {BN tile width (128 or 256), n-tiles, tiles, whole-tile
+ *   out: 8 int64 values {tile width (112, 128 or 256), n-tiles, tiles, whole-tile
  *        items, s_rem K ranges of each later tile, 1 if the later tiles are
  *        split into 128-column halves instead, items (= CTAs), 1 if the K
  *        ranges add up through a cluster}.
