@@ -8,10 +8,13 @@
 //   * a weight (q - 8) * d has at most 4 + 11 significant bits, so it is
 //     exactly W_hi + W_lo with W_hi = bf16(W), W_lo = bf16(W - W_hi);
 //   * an activation a is a_hi + a_lo + r with a_hi = bf16(a),
-//     a_lo = bf16(a - a_hi), |r| <= 2^-18 |a|;
-//   * D += a_hi W_hi + a_hi W_lo + a_lo W_hi; the dropped a_lo W_lo and r
-//     terms are at most 2^-17 |a W| together.  bf16 x bf16 products are exact
-//     in the f32 accumulator.
+//     a_lo = bf16(a - a_hi), |r| <= 2^-17 |a|;
+//   * D += a_hi W_hi + a_hi W_lo + a_lo W_hi; the dropped a_lo W_lo term is
+//     at most 2^-16 |a W|, so one product is off by at most
+//     (2^-16 + 2^-17) |a W|.  The dropped terms take both signs and mostly
+//     cancel in a sum over K; on inputs whose products all round the same
+//     way they add up, as the rounding of any f32 sum does.  bf16 x bf16
+//     products are exact in the f32 accumulator.
 //
 // Structure (one 128-row output tile of BN = 128 or 256 columns per work
 // item, K in 64-wide steps; BN = 128 also runs 112-column tiles, where those
