@@ -282,7 +282,7 @@ const char* qm_status_string(int status) {
         case QM_ERR_ALIGN: return "misaligned pointer (wq needs 2 bytes, A/C/out 4 bytes)";
         case QM_ERR_ALIAS: return "an output overlaps an input";
         case QM_ERR_CUDA: return "a CUDA call or kernel launch failed";
-        case QM_ERR_TIMEOUT: return "a kernel gave up waiting for an asynchronous copy";
+        case QM_ERR_TIMEOUT: return "a kernel gave up a bounded wait (an asynchronous copy or a peer that did not arrive)";
         case QM_ERR_UNSUPPORTED: return "the forced algorithm cannot run this shape";
         case QM_ERR_POINTER: return "a pointer is not device memory of the current device";
         case QM_ERR_TOO_LARGE: return "beyond the fixed scratch of qm_matmul_q4_0_noalloc (M > 8)";
