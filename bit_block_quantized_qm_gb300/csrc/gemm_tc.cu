@@ -9,12 +9,13 @@
 //     exactly W_hi + W_lo with W_hi = bf16(W), W_lo = bf16(W - W_hi);
 //   * an activation a is a_hi + a_lo + r with a_hi = bf16(a),
 //     a_lo = bf16(a - a_hi), |r| <= 2^-17 |a|;
-//   * D += a_hi W_hi + a_hi W_lo + a_lo W_hi; the dropped a_lo W_lo term is
-//     at most 2^-16 |a W|, so one product is off by at most
-//     (2^-16 + 2^-17) |a W|.  The dropped terms take both signs and mostly
-//     cancel in a sum over K; on inputs whose products all round the same
-//     way they add up, as the rounding of any f32 sum does.  bf16 x bf16
-//     products are exact in the f32 accumulator.
+//   * all four products a_hi W_hi, a_hi W_lo, a_lo W_hi, a_lo W_lo are taken
+//     (bf16 x bf16 products are exact in the f32 accumulator), so one product
+//     misses a W by the activation residual r W alone, at most 2^-17 |a W|;
+//   * the large products a_hi W_hi accumulate in one TMEM accumulator and the
+//     three small ones (at most 2^-8 of the large one each) in a second one,
+//     added once in the epilogue: the rounding of the small terms then
+//     happens at their own magnitude, not at the running total's.
 //
 // Structure (one 128-row output tile of BN = 128 or 256 columns per work
 // item, K in 64-wide steps; BN = 128 also runs 112-column tiles, where those
@@ -26,13 +27,13 @@
 //     step's 36-byte block pair);
 //   * warps 2..17 decode each BN x 64 weight tile into W_hi / W_lo, written
 //     in the same swizzled K-major layout (2 stages), then run the epilogue;
-//   * warp 1 owns the TMEM accumulator (128 lanes x BN f32 columns) and one
-//     thread issues 12 tcgen05.mma (3 pieces x 4 k-steps of 16, each
-//     128 x N x 16) per k-step, committing completion to the stages'
-//     "empty" barriers;
-//   * the epilogue reads TMEM with tcgen05.ld (32 x 32 blocks), stages a
-//     block in shared memory (the freed weight stages) and writes C row by
-//     row, 16-byte stores when C's rows allow.
+//   * warp 1 owns the two TMEM accumulators (128 lanes x BN f32 columns
+//     each: a_hi W_hi, then the three small products) and one thread issues
+//     16 tcgen05.mma (4 products x 4 k-steps of 16, each 128 x N x 16) per
+//     k-step, committing completion to the stages' "empty" barriers;
+//   * the epilogue reads both accumulators with tcgen05.ld (32 x 32 blocks),
+//     adds them, stages a block in shared memory (the freed weight stages)
+//     and writes C row by row, 16-byte stores when C's rows allow.
 // The 256-wide tile reads each activation tile once per 256 output columns
 // and keeps the operand reads of one MMA at 12 KB per 2^20 flops, which the
 // shared-memory bandwidth sustains together with the decode's stores.
@@ -79,7 +80,7 @@ struct Tile {
     static constexpr int kRawStages = 2;  // raw Q4_0 bytes of one k-step per stage
     static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
     static constexpr int kRawBytes = BN * kRawRow;
-    static constexpr int kTmemCols = BN;        // f32 accumulator columns
+    static constexpr int kTmemCols = 2 * BN;    // two f32 accumulators of BN columns
     // Barriers (full and empty per stage, acc_full, two cluster-reduction
     // barriers), then the TMEM address and the split-K arrival flag, rounded
     // up to 16 bytes.
@@ -146,6 +147,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t r[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// 32 consecutive columns of this thread's TMEM lane in the large-product
+// accumulator plus the same columns of the small-product one, `small_off`
+// columns further on (16 columns of each at a time, to keep registers low).
+__device__ __forceinline__ void tmem_ld_acc(uint32_t taddr, uint32_t small_off, float v[32]) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t a[16], b[16];
+        tmem_ld16(taddr + 16 * h, a);
+        tmem_ld16(taddr + small_off + 16 * h, b);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[16 * h + i] = __uint_as_float(a[i]) + __uint_as_float(b[i]);
+    }
+}
 
 // Decode half of one Q4_0 block (18 bytes at `blk`, 2-byte aligned, shared
 // memory): quant bytes 8p .. 8p+7, i.e. elements 8p .. 8p+7 (low nibbles) and
@@ -335,7 +361,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            // MMA issuer: 3 pieces x 4 k-steps of 16 per 64-wide k-step, N = wn.
+            // MMA issuer: 4 products x 4 k-steps of 16 per 64-wide k-step, N =
+            // wn; the large product into columns 0.., the small ones into
+            // columns BN.. of the TMEM allocation.
             const uint32_t idesc =
                 (T::kIdesc & ~(0x3Fu << 17)) | (static_cast<uint32_t>(wn >> 3) << 17);
             bool ok = true;
@@ -357,9 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint64_t o = static_cast<uint64_t>(2 * kk);
-                    mma_f16(tmem, dah + o, dwh + o, idesc, (kt | kk) != 0);
-                    mma_f16(tmem, dah + o, dwl + o, idesc, 1u);
-                    mma_f16(tmem, dal + o, dwh + o, idesc, 1u);
+                    const uint32_t acc_on = (kt | kk) != 0;
+                    mma_f16(tmem, dah + o, dwh + o, idesc, acc_on);
+                    mma_f16(tmem + BN, dah + o, dwl + o, idesc, acc_on);
+                    mma_f16(tmem + BN, dal + o, dwh + o, idesc, 1u);
+                    mma_f16(tmem + BN, dal + o, dwl + o, idesc, 1u);
                 }
                 mma_commit(&a_empty[as]);
                 mma_commit(&w_empty[ws]);
@@ -433,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 if (acc_ok) {
                     tc_fence_after();
-                    tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+                    tmem_ld_acc(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, BN, v);
                 }
                 float* dst = ptile + (32 * q + lane) * ld + col;
 #pragma unroll
@@ -498,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
             if (acc_ok) {
                 tc_fence_after();
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, v);
+                tmem_ld_acc(tmem + (static_cast<uint32_t>(32 * q) << 16) + col, BN, v);
             }
             __syncwarp();  // the previous block's reads of the staging rows are done
             // v[i]: row mrow + lane, column n0 + col + i.  Staged so that lane i
