@@ -13,6 +13,8 @@ Entry points (same names as the C ABI):
 * ``qm_quantize_q8_0(x, out=None, stream=None)`` -> uint8 tensor ``[n/32*34]``
 * ``qm_matmul_q4_0(A, wq, N, out=None, stream=None)`` -> f32 tensor ``[M, N]``
 * ``qm_matmul_q4_0_algo(A, wq, N, algo, out=None, stream=None)``
+* ``qm_gemv_q4_0_list(problems, M, counters=None, stream=None)``: a list of
+  GEMV problems ``(A, wq, C, N, wait_for)`` in one persistent launch
 * ``qm_device_status(stream=None, clear=True)``, ``qm_status_string(code)``,
   ``qm_version()``
 
@@ -35,7 +37,7 @@ __all__ = [
     "qm_matmul_q4_0_noalloc_ptr", "qm_selftest_wait_timeout",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
     "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
-    "EXPORTED_SYMBOLS",
+    "EXPORTED_SYMBOLS", "QmGemvProblem", "qm_gemv_q4_0_list_ptr", "qm_gemv_q4_0_list",
 ]
 
 QM_OK = 0
@@ -64,12 +66,19 @@ Q8_0_BLOCK_BYTES = 34
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
                     "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan", "qm_gemm_plan",
                     "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0",
-                    "qm_selftest_wait_timeout")
+                    "qm_selftest_wait_timeout", "qm_gemv_q4_0_list")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
 _lock = threading.Lock()
 _lib = None
+
+
+class QmGemvProblem(ctypes.Structure):
+    """One problem of qm_gemv_q4_0_list (the C struct qm_gemv_problem)."""
+    _fields_ = [("A", ctypes.c_void_p), ("wq", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("wait_for", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class QMError(RuntimeError):
@@ -119,6 +128,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_dequant_q8_0.restype = i32
             lib.qm_quantize_q8_0.argtypes = [p, i64, p, p]
             lib.qm_quantize_q8_0.restype = i32
+            lib.qm_gemv_q4_0_list.argtypes = [p, i64, i64, p, p]
+            lib.qm_gemv_q4_0_list.restype = i32
             lib.qm_launch_count.argtypes = []
             lib.qm_launch_count.restype = ctypes.c_uint64
             _lib = lib
@@ -173,6 +184,17 @@ def qm_matmul_q4_0_noalloc_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
                                stream: int = 0) -> int:
     """The allocation-free GEMV (M <= 8); see include/qm.h."""
     return load_library().qm_matmul_q4_0_noalloc(A, wq, C, M, N, K, stream)
+
+
+def qm_gemv_q4_0_list_ptr(problems, M: int, counters: int = 0, stream: int = 0) -> int:
+    """The list GEMV on raw addresses: `problems` is a sequence of (A, wq, C, N,
+    K, wait_for) tuples of ints; `counters` the device address of len(problems)
+    uint32 (0 for none).  Returns the C status."""
+    arr = (QmGemvProblem * max(1, len(problems)))()
+    for i, (A, wq, C, N, K, wait_for) in enumerate(problems):
+        arr[i] = QmGemvProblem(A, wq, C, N, K, wait_for, 0)
+    return load_library().qm_gemv_q4_0_list(ctypes.cast(arr, ctypes.c_void_p), len(problems), M,
+                                            counters or None, stream)
 
 
 # ------------------------------------------------------------ torch tensors
@@ -273,6 +295,31 @@ def qm_matmul_q4_0_algo(A, wq, N: int, algo: int, out=None, stream=None):
 def qm_matmul_q4_0(A, wq, N: int, out=None, stream=None):
     """C[M, N] = A[M, K] x dequant(W)^T; GEMV kernels for M <= 8, GEMM above."""
     return qm_matmul_q4_0_algo(A, wq, N, QM_ALGO_AUTO, out=out, stream=stream)
+
+
+def qm_gemv_q4_0_list(problems, M: int = 1, counters=None, stream=None):
+    """Run a list of GEMV problems ``(A, wq, C, N, wait_for)`` (A f32 [M, K], wq
+    the uint8 block stream of N x K, C f32 [M, N] written in place) in one
+    persistent launch where the shapes allow; ``counters`` is a uint32 or int32
+    CUDA tensor of len(problems) entries, needed for launches in which a
+    problem waits on another (see include/qm.h)."""
+    import torch
+    raw = []
+    for A, wq, C, N, wait_for in problems:
+        _require(A, torch.float32, "A")
+        _require(wq, torch.uint8, "wq")
+        _require(C, torch.float32, "C")
+        K = A.shape[-1]
+        if A.numel() != M * K or C.numel() != M * N or K % BLOCK_ELEMS or \
+                wq.numel() != N * (K // BLOCK_ELEMS) * BLOCK_BYTES:
+            raise ValueError("problem operands do not match M, N, K")
+        raw.append((A.data_ptr(), wq.data_ptr(), C.data_ptr(), N, K, wait_for))
+    ctr = 0
+    if counters is not None:
+        if not counters.is_cuda or counters.element_size() != 4 or counters.numel() < len(problems):
+            raise ValueError("counters must be a CUDA tensor of len(problems) 32-bit entries")
+        ctr = counters.data_ptr()
+    _check(qm_gemv_q4_0_list_ptr(raw, M, ctr, _stream_handle(stream)), "qm_gemv_q4_0_list")
 
 
 GEMV_PLAN_FIELDS = ("RG", "U", "S", "rps", "c", "hs", "rbpc", "nu_max", "stages", "grid", "smem", "W")

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqm.so")
-SOURCES = ("qm_api.cu", "dequant.cu", "q8_0.cu", "gemv.cu", "gemv_tc.cu", "gemm.cu", "gemm_tc.cu")
+SOURCES = ("qm_api.cu", "dequant.cu", "q8_0.cu", "gemv.cu", "gemv_tc.cu", "gemv_list.cu", "gemm.cu",
+           "gemm_tc.cu")
 HEADERS = ("qm_device.cuh", "qm_internal.h")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -121,13 +121,14 @@ __device__ __forceinline__ void mma_acc(float d[4], uint32_t a0, uint32_t a1, ui
 // 128 + q; subtracting 136 leaves q - 8, both steps exact.
 __device__ __forceinline__ void decode_bf16(uint32_t Q, uint32_t R[4]) {
     constexpr uint32_t kMagic = 0x43004300u;  // bf16 128.0 in both halves
-    constexpr uint32_t kOne = 0x3F803F80u;    // bf16 1.0
-    constexpr uint32_t kBias = 0xC308C308u;   // bf16 -136.0
     const uint32_t r[4] = {(Q & 0x000F000Fu) | kMagic, ((Q >> 4) & 0x000F000Fu) | kMagic,
                            ((Q >> 8) & 0x000F000Fu) | kMagic, ((Q >> 12) & 0x000F000Fu) | kMagic};
+    const __nv_bfloat162 bias = __floats2bfloat162_rn(-136.0f, -136.0f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(R[i]) : "r"(r[i]), "r"(kOne), "r"(kBias));
+    for (int i = 0; i < 4; ++i) {
+        const __nv_bfloat162 v = __hadd2(*reinterpret_cast<const __nv_bfloat162*>(&r[i]), bias);
+        R[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
 }
 
 // Quant bytes (b0, b2) of lane quarter t in a block of the given parity (the

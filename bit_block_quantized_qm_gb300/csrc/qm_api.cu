@@ -218,36 +218,53 @@ int check_pointer(const void* p, int device) {
 
 int from_cuda(cudaError_t err) { return err == cudaSuccess ? QM_OK : QM_ERR_CUDA; }
 
-int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
-                int algo, void* stream) {
+int run_matmul(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K, int algo,
+               cudaStream_t s, const qm::DeviceInfo& dev);
+
+// Host checks of one product's operands (the qm_matmul_q4_0 rules); on
+// success the byte counts of A, wq and C.
+int check_matmul(const float* A, const void* wq, const float* C, int64_t M, int64_t N, int64_t K,
+                 int64_t* a_bytes, int64_t* w_bytes, int64_t* c_bytes) {
     if (M < 0 || N < 0 || K < 0 || (K % 32) != 0) return QM_ERR_SHAPE;
-    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMV_PK) return QM_ERR_SHAPE;
-    int64_t a_elems, c_elems, w_elems, a_bytes, c_bytes, w_bytes;
-    if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, &a_bytes) || !mul_ok(M, N, &c_elems) ||
-        !mul_ok(c_elems, 4, &c_bytes) || !mul_ok(N, K / 32, &w_elems) ||
-        !mul_ok(w_elems, 18, &w_bytes))
+    int64_t a_elems, c_elems, w_elems;
+    if (!mul_ok(M, K, &a_elems) || !mul_ok(a_elems, 4, a_bytes) || !mul_ok(M, N, &c_elems) ||
+        !mul_ok(c_elems, 4, c_bytes) || !mul_ok(N, K / 32, &w_elems) || !mul_ok(w_elems, 18, w_bytes))
         return QM_ERR_SHAPE;
-    if ((algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT) && M > 8) return QM_ERR_UNSUPPORTED;
-    if (algo == QM_ALGO_GEMV_PK && M > 2) return QM_ERR_UNSUPPORTED;
     if (M == 0 || N == 0) return QM_OK;
     if (!C) return QM_ERR_NULL;
     if (K > 0 && (!A || !wq)) return QM_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(C) & 3u) != 0) return QM_ERR_ALIGN;
-    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3u) != 0 ||
-                  (reinterpret_cast<uintptr_t>(wq) & 1u) != 0))
+    if (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 3u) != 0 || (reinterpret_cast<uintptr_t>(wq) & 1u) != 0))
         return QM_ERR_ALIGN;
-    if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, wq, w_bytes)) return QM_ERR_ALIAS;
+    if (overlaps(C, *c_bytes, A, *a_bytes) || overlaps(C, *c_bytes, wq, *w_bytes)) return QM_ERR_ALIAS;
     if (M > 0x7FFFFFFF || N > 0x7FFFFFFF) return QM_ERR_SHAPE;
+    return QM_OK;
+}
+
+int matmul_impl(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
+                int algo, void* stream) {
+    if (algo < QM_ALGO_AUTO || algo > QM_ALGO_GEMV_PK) return QM_ERR_SHAPE;
+    int64_t a_bytes = 0, w_bytes = 0, c_bytes = 0;
+    int rc = check_matmul(A, wq, C, M, N, K, &a_bytes, &w_bytes, &c_bytes);
+    if (rc != QM_OK) return rc;
+    if ((algo == QM_ALGO_GEMV || algo == QM_ALGO_GEMV_SIMT) && M > 8) return QM_ERR_UNSUPPORTED;
+    if (algo == QM_ALGO_GEMV_PK && M > 2) return QM_ERR_UNSUPPORTED;
+    if (M == 0 || N == 0) return QM_OK;
 
     qm::DeviceInfo dev;
     if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
-    int rc = check_pointer(C, dev.device);
+    rc = check_pointer(C, dev.device);
     if (rc == QM_OK && K > 0) rc = check_pointer(A, dev.device);
     if (rc == QM_OK && K > 0) rc = check_pointer(wq, dev.device);
     if (rc != QM_OK) return rc;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(c_bytes), s));
+    return run_matmul(A, wq, C, M, N, K, algo, static_cast<cudaStream_t>(stream), dev);
+}
+
+// The launch part of qm_matmul_q4_0 for arguments already checked.
+int run_matmul(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K, int algo,
+               cudaStream_t s, const qm::DeviceInfo& dev) {
+    if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(M * N * 4), s));
     const uint8_t* w = static_cast<const uint8_t*>(wq);
     const bool tc_ok = qm::gemm_tc_supported(A, w, M, N, K);
     if (algo == QM_ALGO_AUTO) {
@@ -385,6 +402,96 @@ int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M, 
                                                   static_cast<int>(M), N, K, s, dev));
 }
 
+// The list GEMV: checks every problem as qm_matmul_q4_0 does, then the
+// ordering rules between problems, then runs maximal runs of problems the
+// persistent kernel takes (M = 1, K % 2048 == 0, K <= 14336, 16-byte aligned
+// A and wq) as launches of up to 128 problems; any other problem runs alone
+// through qm_matmul_q4_0's path, in list order on the same stream.
+int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M, uint32_t* counters,
+                      void* stream) {
+    if (count < 0 || M < 0) return QM_ERR_SHAPE;
+    if (count == 0 || M == 0) return QM_OK;
+    if (!problems) return QM_ERR_NULL;
+    if (count > (int64_t(1) << 24)) return QM_ERR_SHAPE;
+    if (counters && (reinterpret_cast<uintptr_t>(counters) & 3u) != 0) return QM_ERR_ALIGN;
+    std::vector<int64_t> ab(count), wb(count), cb(count);
+    for (int64_t i = 0; i < count; ++i) {
+        const qm_gemv_problem& p = problems[i];
+        if (p.reserved != 0 || p.wait_for < -1 || p.wait_for >= i) return QM_ERR_SHAPE;
+        const int rc = check_matmul(p.A, p.wq, p.C, M, p.N, p.K, &ab[i], &wb[i], &cb[i]);
+        if (rc != QM_OK) return rc;
+        if (p.N == 0) ab[i] = wb[i] = cb[i] = 0;
+        if (p.K == 0) ab[i] = wb[i] = 0;
+    }
+    // Ordering between problems: no output overlaps any weight stream; an
+    // output of problem i that overlaps an operand of a later problem j (or j's
+    // output overlaps i's activations) needs j to wait for i; the counters
+    // overlap nothing.
+    const int64_t ctr_bytes = counters ? count * 4 : 0;
+    for (int64_t i = 0; i < count; ++i) {
+        const qm_gemv_problem& p = problems[i];
+        if (overlaps(counters, ctr_bytes, p.A, ab[i]) || overlaps(counters, ctr_bytes, p.wq, wb[i]) ||
+            overlaps(counters, ctr_bytes, p.C, cb[i]))
+            return QM_ERR_ALIAS;
+        for (int64_t j = 0; j < count; ++j) {
+            if (j != i && overlaps(p.C, cb[i], problems[j].wq, wb[j])) return QM_ERR_ALIAS;
+        }
+        for (int64_t j = i + 1; j < count; ++j) {
+            const qm_gemv_problem& q = problems[j];
+            const bool touch = overlaps(p.C, cb[i], q.A, ab[j]) || overlaps(p.C, cb[i], q.C, cb[j]) ||
+                               overlaps(q.C, cb[j], p.A, ab[i]);
+            if (touch && q.wait_for < i) return QM_ERR_ALIAS;
+        }
+    }
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    for (int64_t i = 0; i < count; ++i) {
+        const qm_gemv_problem& p = problems[i];
+        if (p.N == 0) continue;
+        int rc = check_pointer(p.C, dev.device);
+        if (rc == QM_OK && p.K > 0) rc = check_pointer(p.A, dev.device);
+        if (rc == QM_OK && p.K > 0) rc = check_pointer(p.wq, dev.device);
+        if (rc != QM_OK) return rc;
+    }
+    if (counters && check_pointer(counters, dev.device) != QM_OK) return QM_ERR_POINTER;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto list_ok = [&](const qm_gemv_problem& p) {
+        return M == 1 && p.N > 0 && p.K > 0 && (p.K % 2048) == 0 && p.K <= qm::kListMaxK &&
+               (reinterpret_cast<uintptr_t>(p.A) & 15u) == 0 && (reinterpret_cast<uintptr_t>(p.wq) & 15u) == 0;
+    };
+    std::vector<qm::GemvListItem> items;
+    int64_t i = 0;
+    while (i < count) {
+        const qm_gemv_problem& p = problems[i];
+        if (p.N == 0) {
+            ++i;
+            continue;
+        }
+        if (!list_ok(p)) {
+            const int rc = run_matmul(p.A, p.wq, p.C, M, p.N, p.K, QM_ALGO_AUTO, s, dev);
+            if (rc != QM_OK) return rc;
+            ++i;
+            continue;
+        }
+        // A run of list problems from i: at most kListMaxProblems; without
+        // counters it ends before a problem that waits on one inside it
+        // (the launch boundary then orders them).
+        items.clear();
+        const int64_t start = i;
+        while (i < count && static_cast<int>(items.size()) < qm::kListMaxProblems && list_ok(problems[i])) {
+            const qm_gemv_problem& q = problems[i];
+            const int w = q.wait_for >= start ? static_cast<int>(q.wait_for - start) : -1;
+            if (w >= 0 && !counters) break;
+            items.push_back({q.A, static_cast<const uint8_t*>(q.wq), q.C, q.N, q.K, w});
+            ++i;
+        }
+        const int rc = from_cuda(qm::launch_gemv_q4_0_list(items.data(), static_cast<int>(items.size()),
+                                                           counters ? counters + start : nullptr, s, dev));
+        if (rc != QM_OK) return rc;
+    }
+    return QM_OK;
+}
+
 uint64_t qm_launch_count(void) { return qm::launch_count(); }
 
 int qm_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, int fit2, int fit4, int fit8,
@@ -423,6 +530,7 @@ int qm_device_status(void* stream, int clear) {
     if (qm::gemv_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (qm::gemm_tc_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (qm::gemv_tc_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
+    if (qm::gemv_list_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (bits && clear) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || qm::reset_workspaces(dev) != cudaSuccess)

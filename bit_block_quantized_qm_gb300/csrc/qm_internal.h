@@ -95,6 +95,27 @@ void gemm_tc_plan_query(int64_t M, int64_t N, int64_t K, int sm_count, const int
 cudaError_t launch_gemv_q4_0_noalloc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                      int64_t K, cudaStream_t stream, const DeviceInfo& dev);
 
+// One problem of the persistent list GEMV (gemv_list.cu): M = 1, K % 2048 == 0,
+// K <= kListMaxK, A and W 16-byte aligned; wait_for is -1 or an earlier index
+// of the same launch (A is read once problems 0..wait_for are complete).
+constexpr int kListMaxK = 14336;
+constexpr int kListMaxProblems = 128;
+struct GemvListItem {
+    const float* A;
+    const uint8_t* W;
+    float* C;
+    int64_t N;
+    int64_t K;
+    int wait_for;
+};
+
+// The list GEMV: one persistent launch over `count` (<= kListMaxProblems)
+// problems.  `counters` (count unsigned, device memory) is required when some
+// wait_for >= 0; it is cleared on the stream first.
+cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned* counters,
+                                  cudaStream_t stream, const DeviceInfo& dev);
+cudaError_t gemv_list_read_device_error(unsigned int* bits, bool clear);
+
 // Growable scratch of the prefill GEMM (bf16 pieces of A), one per (device,
 // stream).  Growing it synchronizes the stream first (the old buffer may
 // still be in use by earlier work on it).

@@ -230,6 +230,49 @@ QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int6
                                   int64_t N, int64_t K, void* stream);
 
 /*
+ * qm_gemv_q4_0_list — a list of decode-regime products C_p = A_p x
+ * dequant(W_p)^T (sections "qmatvec_q4_0" and "matmul_q4_0_tiled"; the
+ * GEMV's cost is streaming the weight blocks once), all with the same M, in
+ * one persistent launch where the shapes allow it: a decode step's chain of
+ * projections without a fixed launch price per projection.
+ *   problems : host array of `count` descriptors (read before the call
+ *              returns).  Each problem follows the rules of qm_matmul_q4_0
+ *              (operands, layouts, alignment, no output overlapping its own
+ *              inputs).  wait_for is -1, or an index j below the problem's own:
+ *              the problem's A is read only after problems 0..j have written
+ *              their C (this is how a problem consumes an earlier one's
+ *              output).  reserved must be 0.
+ *   count    : >= 0.  M : >= 0, the rows of every A and C.
+ *   counters : device memory of `count` uint32 (4-byte aligned, overlapping
+ *              no operand) that the launch uses to count finished problems;
+ *              it is cleared on `stream` before each launch that needs it.
+ *              May be NULL: dependencies are then honoured by ending the
+ *              launch before every problem that waits on one inside it.
+ * Results are those of calling qm_matmul_q4_0 on the problems in list order.
+ * Problems that neither wait on one another nor share memory may run in any
+ * order; so no output may overlap another problem's weights, and an output
+ * that overlaps another problem's activations or output (or whose
+ * activations another problem's output overlaps) needs the later of the two
+ * to wait for the earlier (QM_ERR_ALIAS otherwise).  The persistent kernel
+ * takes M = 1, K % 2048 == 0, K <= 14336 and 16-byte aligned A and wq; other
+ * problems run one by one through qm_matmul_q4_0's kernels, in list order on
+ * the same stream.  Deterministic, like qm_matmul_q4_0.
+ * Returns QM_OK or a negative status (nothing is enqueued when a check fails).
+ */
+typedef struct qm_gemv_problem {
+    const float* A;   /* [M][K] f32, row-major                         */
+    const void* wq;   /* [N][K/32] Q4_0 blocks                          */
+    float* C;         /* [M][N] f32, row-major                          */
+    int64_t N;
+    int64_t K;
+    int32_t wait_for; /* -1, or read A after problems 0..wait_for       */
+    int32_t reserved; /* 0                                              */
+} qm_gemv_problem;
+
+QM_API int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M,
+                             uint32_t* counters, void* stream);
+
+/*
  * qm_gemm_plan — the work items the prefill GEMM on tensor cores
  * (QM_ALGO_GEMM_TC) takes for (M, N, K) on a device with sm_count SMs on
  * which fit2, fit4 and fit8 thread-block clusters of 2, 4 and 8 of its CTAs

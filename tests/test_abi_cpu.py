@@ -148,3 +148,55 @@ def test_q8_0_python_wrappers_validate_tensors():
         qm.qm_dequant_q8_0(torch.zeros(34, dtype=torch.uint8))  # not a CUDA tensor
     with pytest.raises(TypeError):
         qm.qm_quantize_q8_0(torch.zeros(32, dtype=torch.float64))
+
+
+# ---------------------------------------------------------- qm_gemv_q4_0_list
+
+def _p(A, W, C, N=64, K=256, wait_for=-1):
+    return (A, W, C, N, K, wait_for)
+
+
+def test_list_empty_and_shape_errors(lib):
+    assert qm.qm_gemv_q4_0_list_ptr([], 1) == qm.QM_OK
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR)], 0) == qm.QM_OK
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR)], -1) == qm.QM_ERR_SHAPE
+    # wait_for must name an earlier problem (or be -1)
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR, wait_for=0)], 1) == qm.QM_ERR_SHAPE
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR, wait_for=-2)], 1) == qm.QM_ERR_SHAPE
+    # each problem follows the qm_matmul_q4_0 rules
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR, K=33)], 1) == qm.QM_ERR_SHAPE
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, 0)], 1) == qm.QM_ERR_NULL
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR + 2)], 1) == qm.QM_ERR_ALIGN
+    assert qm.qm_gemv_q4_0_list_ptr([_p(A_ADDR, W_ADDR, C_ADDR)], 1, counters=0x40000002) == qm.QM_ERR_ALIGN
+
+
+def test_list_reserved_field_must_be_zero(lib):
+    import ctypes
+    arr = (qm.QmGemvProblem * 1)()
+    arr[0] = qm.QmGemvProblem(A_ADDR, W_ADDR, C_ADDR, 64, 256, -1, 7)
+    rc = lib.qm_gemv_q4_0_list(ctypes.cast(arr, ctypes.c_void_p), 1, 1, None, None)
+    assert rc == qm.QM_ERR_SHAPE
+
+
+def test_list_ordering_rules(lib):
+    # Problem 1 reads problem 0's output: allowed only when it waits for 0.
+    p0 = _p(A_ADDR, W_ADDR, C_ADDR, N=256, K=256)
+    p1_nowait = _p(C_ADDR, W_ADDR + 0x100000, C_ADDR + 0x100000, N=64, K=256)
+    assert qm.qm_gemv_q4_0_list_ptr([p0, p1_nowait], 1) == qm.QM_ERR_ALIAS
+    # Problem 1 overwrites what problem 0 reads, without waiting: rejected.
+    p1_war = _p(A_ADDR + 0x100000, W_ADDR + 0x100000, A_ADDR, N=64, K=256)
+    assert qm.qm_gemv_q4_0_list_ptr([p0, p1_war], 1) == qm.QM_ERR_ALIAS
+    # Two outputs on the same bytes without an order: rejected.
+    p1_waw = _p(A_ADDR + 0x100000, W_ADDR + 0x100000, C_ADDR, N=64, K=256)
+    assert qm.qm_gemv_q4_0_list_ptr([p0, p1_waw], 1) == qm.QM_ERR_ALIAS
+    # An output over another problem's weights: always rejected.
+    p1_w = _p(A_ADDR + 0x100000, W_ADDR + 0x100000, W_ADDR, N=64, K=256, wait_for=0)
+    assert qm.qm_gemv_q4_0_list_ptr([p0, p1_w], 1) == qm.QM_ERR_ALIAS
+    # Counters over an operand: rejected.
+    assert qm.qm_gemv_q4_0_list_ptr([p0], 1, counters=C_ADDR) == qm.QM_ERR_ALIAS
+    # With the wait the same list passes the host checks (and then needs a
+    # device, which this machine does not have: the status is not an
+    # argument error).
+    p1_wait = _p(C_ADDR, W_ADDR + 0x100000, C_ADDR + 0x100000, N=64, K=256, wait_for=0)
+    rc = qm.qm_gemv_q4_0_list_ptr([p0, p1_wait], 1)
+    assert rc not in (qm.QM_ERR_ALIAS, qm.QM_ERR_SHAPE, qm.QM_ERR_NULL, qm.QM_ERR_ALIGN)
