@@ -1,29 +1,33 @@
 """Benchmark of the Q4_0 x f32 hot path on GB300 (one JSON line on stdout).
 
-One step = one pass of the whole hot path over the decode-batch workload:
+One step = one pass of the decode-batch GEMV workload, the FFN pair at M=8:
   * GEMV M=8, K=4096,  N=14336 (FFN up projection),
   * GEMV M=8, K=14336, N=4096  (FFN down projection),
-  * dequant_q4_0 of the 14336 x 4096 weight to f32,
-each through libqm's C ABI (qm_matmul_q4_0 / qm_dequant_q4_0) on one stream.
-Inputs are synthetic (seeded generators in ``synth``).  Every step uses a
-different replica of all operands, and the replicas together exceed the L2
-several times, so no step finds its inputs in L2.
+each through libqm's C ABI (qm_matmul_q4_0) on one stream.  Inputs are
+synthetic (seeded generators in ``synth``).  Every step uses a different
+replica of all operands, and the replicas together exceed the L2 several
+times, so no step finds its inputs in L2.
 
-value = Q4_0 weight bytes streamed per step / device time per step (GB/s),
-timed with CUDA events over --steps steps after --warmup steps.  ``e2e``
-repeats the step with host operands: pinned host -> device copies of every
-input and device -> host copies of every output inside the timed region, the
-copies of neighbouring steps overlapping a step's kernels on separate streams.
+value = Q4_0 weight bytes streamed per step / device time per step (GB/s), the
+GEMV weight-stream rate of the metric, timed with CUDA events over --steps
+steps after --warmup steps.  ``roofline`` is the GEMV launch with the longer
+event-timed duration, against the measured HBM copy rate.  ``e2e`` repeats the
+step with host operands: pinned host -> device copies of every input and
+device -> host copies of every output inside the timed region, the copies of
+neighbouring steps overlapping a step's kernels on separate streams.
 
-Beside the step, the line reports (keys ``m1_gemv``, ``decode_sweep``,
-``prefill``, ``q8_0``): back-to-back M=1 GEMVs at K=N=4096, the 32-layer
-decoder sweep at M=1 and M=8 replayed from a CUDA graph (weight GB/s against
-HBM), the same sweep at M=512 (TFLOP/s against the tensor-core bound of the
-3-MMA split), and the Q8_0 quantize and dequant of a 14336 x 4096 tensor (GB/s
-against HBM).
+Every other workload is reported in the same line: ``roofline.per_config``
+holds the GEMV and dequant rows (M=1 at K=N=4096 back to back, the step's two
+GEMVs, the dequant of the 14336 x 4096 weight, the 32-layer decoder sweep at
+M=1 and M=8) as weight GB/s against HBM, and ``prefill`` the GEMM rows (M=32
+and M=256 at 4096 x 4096, M=1024 at both FFN shapes, the decoder sweep at
+M=512) as TFLOP/s against the tensor-core bound.  ``q8_0`` holds the Q8_0
+quantize and dequant.
 
-``--impl reference`` times the CPU oracle instead (on a bounded sample of the
-same step, extrapolated per column), on the same metric.
+``cpu_baseline`` times the oracle (fp64 C) on this host on a bounded column
+sample of the step: one thread, and all cores through OpenMP.  ``--impl
+reference`` runs that oracle as the reference arm, each step a bounded column
+sample of the same workload, on the same metric.
 """
 from __future__ import annotations
 
@@ -45,9 +49,19 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "Q4_0 GEMV weight GB/s (% of HBM peak); prefill TFLOP/s (% of roofline)"
-WORKLOAD = "q4_0_decode_batch_m8_ffn_up_down_plus_dequant"
+WORKLOAD = "q4_0_gemv_decode_batch_m8_ffn_up_down"
 FALLBACK_HBM_GBS = 6800.0
-REPLICAS = 4  # 4 x (99 MB read + 235 MB written) >> 129 MB of L2
+REPLICAS = 4  # 4 x 66 MB of weights (plus activations) > 129 MB of L2
+
+
+def bench_config(world: int) -> dict:
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": WORKLOAD, "M": 8,
+            "shapes": "K=4096,N=14336 (up); K=14336,N=4096 (down)",
+            "seeds": [1, 2],
+            "l2": f"{REPLICAS} rotating operand replicas (> L2) between steps",
+            "parallelism": f"replicas x{world}",
+            "value_definition": "Q4_0 weight bytes streamed per step / step time"}
 
 
 # ------------------------------------------------------------------ helpers
@@ -198,73 +212,80 @@ class ClockSampler:
 
 # ------------------------------------------------------------ reference arm
 
-class OracleStep:
-    """The CPU oracle on one step of the workload, bounded to a time budget:
-    it computes the first `cols` output columns (all M rows) of each GEMV and
-    the first `blocks` blocks of the dequant, and scales each part's time by
-    (total / computed).  With a large enough budget the sample is the whole
-    step.  Single-threaded."""
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
-    def __init__(self, budget_s: float):
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of one step: all M rows of the
+    first `cols` output columns of each GEMV (the rows of W they stream), with
+    `cols` sized so that the sample takes about `budget_s` seconds.  The
+    metric is a rate, weight bytes streamed per second, so the sample's own
+    bytes over its own time need no scaling.  With parallel=True the oracle
+    is the OpenMP build of the same source (entries shared over every core)."""
+
+    def __init__(self, budget_s: float, parallel: bool):
         import oracle
-        self.o = oracle.load()
-        self.up, self.down, self.deq = step_cases()
+        self.parallel = parallel
+        if parallel:
+            os.environ.setdefault("OMP_NUM_THREADS", str(host_cores()))
+            self.threads = int(os.environ["OMP_NUM_THREADS"])
+            self.o = oracle.load_parallel()
+        else:
+            self.threads = 1
+            self.o = oracle.load()
+        self.up, self.down, _ = step_cases()
         self.data = {c.name: (c.acts(), c.weights()) for c in (self.up, self.down)}
-        self.deq_blob = self.deq.weights()
-        # calibrate seconds per multiply-add on a small slice
-        A, blob = self.data[self.up.name]
-        mi, ni = np.repeat(np.arange(8), 16), np.tile(np.arange(16), 8)
-        self.o.matmul_q4_0_entries(A, blob, self.up.N, self.up.K, mi, ni)
+        # Calibrate seconds per column (all M rows of one output column).
+        c = self.up
+        A, blob = self.data[c.name]
+        n0 = 4 * self.threads
+        self._run(c, n0)
         t0 = time.perf_counter()
-        self.o.matmul_q4_0_entries(A, blob, self.up.N, self.up.K, mi, ni)
-        per_mac = (time.perf_counter() - t0) / (8 * 16 * self.up.K)
-        share = budget_s * 0.48
-        self.cols = {c.name: int(max(1, min(c.N, share / (per_mac * c.M * c.K))))
-                     for c in (self.up, self.down)}
-        nb = self.deq.weight_bytes // 18
-        self.blocks = int(max(32, min(nb, budget_s * 0.04 / 1.5e-9 / 32)))
+        self._run(c, n0)
+        per_col_k = (time.perf_counter() - t0) / (n0 * c.K)
+        self.cols = {x.name: int(max(1, min(x.N, budget_s * 0.5 / (per_col_k * x.K))))
+                     for x in (self.up, self.down)}
 
-    def run(self):
-        t = {}
+    def _run(self, c, n):
+        A, blob = self.data[c.name]
+        mi, ni = np.repeat(np.arange(c.M), n), np.tile(np.arange(n), c.M)
+        self.o.matmul_q4_0_entries(A, blob, c.N, c.K, mi, ni)
+
+    def run(self) -> float:
+        """One sampled step; its wall time in seconds."""
+        t0 = time.perf_counter()
         for c in (self.up, self.down):
-            A, blob = self.data[c.name]
-            n = self.cols[c.name]
-            mi, ni = np.repeat(np.arange(c.M), n), np.tile(np.arange(n), c.M)
-            t0 = time.perf_counter()
-            self.o.matmul_q4_0_entries(A, blob, c.N, c.K, mi, ni)
-            t[c.name] = (time.perf_counter() - t0) * c.N / n
-        nb = self.deq.weight_bytes // 18
-        blob = self.deq_blob[: self.blocks * 18]
-        t0 = time.perf_counter()
-        self.o.dequant_q4_0(blob)
-        t["dequant"] = (time.perf_counter() - t0) * nb / self.blocks
-        return sum(t.values()), t
-
-    def describe(self) -> str:
-        nb = self.deq.weight_bytes // 18
-        return (f"per step, one thread: all {self.up.M} rows x first {self.cols[self.up.name]} "
-                f"of {self.up.N} columns of the up GEMV, x first {self.cols[self.down.name]} of "
-                f"{self.down.N} of the down GEMV, and the first {self.blocks} of {nb} blocks of "
-                f"the dequant; each part's time scaled by total/computed")
+            self._run(c, self.cols[c.name])
+        return time.perf_counter() - t0
 
     @property
     def weight_bytes(self) -> int:
-        return self.up.weight_bytes + self.down.weight_bytes + self.deq.weight_bytes
+        """Q4_0 bytes of the sampled columns (each column is one row of W)."""
+        return sum(self.cols[c.name] * (c.K // 32) * 18 for c in (self.up, self.down))
+
+    def describe(self) -> str:
+        return (f"{'OpenMP, ' + str(self.threads) + ' threads' if self.parallel else 'one thread'}: "
+                f"all {self.up.M} rows x the first {self.cols[self.up.name]} of {self.up.N} columns "
+                f"of the up GEMV and the first {self.cols[self.down.name]} of {self.down.N} columns "
+                f"of the down GEMV per step ({self.weight_bytes} weight bytes); value = sampled "
+                f"weight bytes / sample time")
 
 
 def run_reference(args, rank: int, world: int) -> None:
-    """The CPU oracle on the same step (bounded sample, extrapolated)."""
+    """The CPU oracle as the reference arm, each step a bounded sample of the
+    step's workload, timed whole (no extrapolation)."""
     if rank != 0:
         return
-    budget = min(12.0, max(0.05, 75.0 / (args.steps + args.warmup)))
-    st = OracleStep(budget)
+    budget = min(4.0, max(0.05, 100.0 / (args.steps + args.warmup)))
+    st = OracleSample(budget, parallel=True)
     for _ in range(args.warmup):
         st.run()
-    times, parts = [], []
-    for _ in range(args.steps):
-        s, p = st.run()
-        times.append(s)
-        parts.append(p)
+    times = [st.run() for _ in range(args.steps)]
     step_s = statistics.mean(times)
     value = st.weight_bytes / step_s / 1e9
     line = {
@@ -272,23 +293,29 @@ def run_reference(args, rank: int, world: int) -> None:
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 8, "shapes": "K=4096,N=14336; K=14336,N=4096; "
-                   "dequant 14336x4096", "seeds": [1, 2]},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "config": bench_config(world),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": st.threads, "kind": "oracle",
                          "sample": st.describe()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "parts_s": {k: statistics.mean(p[k] for p in parts) for k in parts[0]},
+        "sample_note": "ms_per_step is the measured time of the sampled step, not extrapolated",
     }
     print(json.dumps(line), flush=True)
 
 
 def cpu_baseline_leg() -> dict:
-    """The oracle timed on this host (1 thread) on a ~12 s sample of the step."""
-    st = OracleStep(12.0)
-    total, parts = st.run()
-    return {"value": st.weight_bytes / total / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": st.describe(), "seconds_per_step": total,
-            "parts_s": parts}
+    """The oracle timed on this host on a column sample of the step: one
+    thread (~8 s) and all cores with OpenMP (~8 s)."""
+    out = {}
+    for parallel in (False, True):
+        st = OracleSample(8.0, parallel)
+        t = st.run()
+        out["parallel" if parallel else "single"] = {
+            "value": st.weight_bytes / t / 1e9, "unit": "GB/s", "cores": st.threads,
+            "seconds": t, "sample": st.describe()}
+    par = out["parallel"]
+    return {"value": par["value"], "unit": "GB/s", "cores": par["cores"], "kind": "oracle",
+            "sample": par["sample"], "host_cores": host_cores(),
+            "single_thread": out["single"]}
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -308,10 +335,9 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
 
-    up, down, deq = step_cases()
+    up, down, _ = step_cases()
     host = {"up_A": up.acts(), "up_W": up.weights(), "down_A": down.acts(),
-            "down_W": down.weights(), "deq_W": deq.weights()}
-    n_blocks = deq.weight_bytes // 18
+            "down_W": down.weights()}
     reps = []
     for r in range(REPLICAS):
         reps.append({
@@ -321,8 +347,6 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             "down_A": torch.from_numpy(host["down_A"]).to(dev),
             "down_W": torch.from_numpy(host["down_W"]).to(dev),
             "down_C": torch.empty((down.M, down.N), dtype=torch.float32, device=dev),
-            "deq_W": torch.from_numpy(host["deq_W"]).to(dev),
-            "deq_out": torch.empty(n_blocks * 32, dtype=torch.float32, device=dev),
         })
     torch.cuda.synchronize()
 
@@ -341,10 +365,6 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                                    rp["down_C"].data_ptr(), down.M, down.N, down.K, sh), "down")
         if ev is not None:
             ev[2].record(stream)
-        call(qm.qm_dequant_q4_0_ptr(rp["deq_W"].data_ptr(), n_blocks, rp["deq_out"].data_ptr(),
-                                    sh), "dequant")
-        if ev is not None:
-            ev[3].record(stream)
 
     def barrier():
         if dist is not None:
@@ -394,26 +414,21 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     # Per-kernel split, from a separate pass with events between the kernels
     # (an event between two kernels also ends their programmatic overlap, so
     # these times are slightly longer than their share of the timed step).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for i in range(args.steps):
         step(reps[i % REPLICAS], evs[i])
     torch.cuda.synchronize()
-    per_op = {"gemv_up": [], "gemv_down": [], "dequant": []}
-    for ev in evs:
-        per_op["gemv_up"].append(ev[0].elapsed_time(ev[1]))
-        per_op["gemv_down"].append(ev[1].elapsed_time(ev[2]))
-        per_op["dequant"].append(ev[2].elapsed_time(ev[3]))
-    avg = {k: statistics.mean(v) for k, v in per_op.items()}
+    avg = {"gemv_up": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
+           "gemv_down": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)}
 
-    wbytes = up.weight_bytes + down.weight_bytes + deq.weight_bytes
+    wbytes = up.weight_bytes + down.weight_bytes
     value = job_gbs(wbytes, world, ms_step)
 
     # ---------------------------------------------------------------- e2e
     pinned = {k: torch.from_numpy(v.view(np.uint8).ravel() if v.dtype != np.uint8 else v)
               .pin_memory() for k, v in host.items()}
     out_host = {"up_C": torch.empty(up.M * up.N * 4, dtype=torch.uint8).pin_memory(),
-                "down_C": torch.empty(down.M * down.N * 4, dtype=torch.uint8).pin_memory(),
-                "deq_out": torch.empty(n_blocks * 128, dtype=torch.uint8).pin_memory()}
+                "down_C": torch.empty(down.M * down.N * 4, dtype=torch.uint8).pin_memory()}
 
     # Each step copies its inputs in, runs, and copies its outputs back, as a
     # serving loop would: inputs on one copy stream, the kernels on the main
@@ -462,71 +477,59 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_value = job_gbs(wbytes, world, e2e_ms)
+    del pinned, out_host
 
     # ------------------------------------------------------------ roofline
-    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-    sm_mhz = clocks.get("sm_mhz") or 0.0
-    sm_max = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
-    fp32_peak_max = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
-    fp32_peak_live = sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     hbm = peaks["hbm_gbs"]
     paths = {}
     for key, c in (("gemv_up", up), ("gemv_down", down)):
         ms = avg[key]
-        flops = 2.0 * c.M * c.N * c.K
         paths[key] = {
             "kernel": "gemv_q4_0_tc (mma.sync bf16 split, f32 accumulation)",
-            "ms": ms, "weight_gbs": c.weight_bytes / (ms * 1e-3) / 1e9,
+            "workload": c.name, "ms": ms, "weight_gbs": c.weight_bytes / (ms * 1e-3) / 1e9,
             "alg_gbs": gemv_bytes(c) / (ms * 1e-3) / 1e9,
             "hbm_frac": gemv_bytes(c) / (ms * 1e-3) / 1e9 / hbm,
-            "tflops": flops / (ms * 1e-3) / 1e12,
+            "tflops": 2.0 * c.M * c.N * c.K / (ms * 1e-3) / 1e12,
             "bound_time_ms": gemv_bytes(c) / (hbm * 1e9) * 1e3,
         }
-    paths["dequant"] = {"ms": avg["dequant"],
-                        "alg_gbs": dequant_bytes(deq) / (avg["dequant"] * 1e-3) / 1e9,
-                        "hbm_frac": dequant_bytes(deq) / (avg["dequant"] * 1e-3) / 1e9 / hbm}
     dominant = max(avg, key=avg.get)
-    if dominant == "dequant":
-        achieved = paths["dequant"]["alg_gbs"]
-        roofline = {"bound": "hbm", "kernel": "dequant_q4_0", "achieved": achieved,
-                    "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": measured_traffic("dequant_q4_0", deq.name),
-                    "peak_source": peaks["source"],
-                    "algorithmic_bytes_per_launch": dequant_bytes(deq)}
-    else:
-        c = up if dominant == "gemv_up" else down
-        achieved = paths[dominant]["alg_gbs"]
-        roofline = {"bound": "hbm", "kernel": "gemv_q4_0_tc (" + dominant + ")",
-                    "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                    "frac": achieved / hbm, "traffic": measured_traffic("gemv_q4_0_tc", c.name),
-                    "peak_source": peaks["source"],
-                    "algorithmic_bytes_per_launch": gemv_bytes(c)}
+    c = up if dominant == "gemv_up" else down
+    achieved = paths[dominant]["alg_gbs"]
+    roofline = {"bound": "hbm", "kernel": f"gemv_q4_0_tc ({c.name}, the step's longer launch)",
+                "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": measured_traffic("gemv_q4_0_tc", c.name),
+                "peak_source": peaks["source"],
+                "algorithmic_bytes_per_launch": gemv_bytes(c),
+                "algorithmic_bytes_definition": "N*K*0.5625 weight + M*K*4 A + M*N*4 C",
+                "launch_ms": paths[dominant]["ms"],
+                "per_config": {"cfg1_" + k: {"workload": v["workload"], "ms": v["ms"],
+                                             "weight_gbs": v["weight_gbs"],
+                                             "frac": v["hbm_frac"], "bound": "hbm"}
+                               for k, v in paths.items()}}
 
-    sweep = None
+    prefill = None
+    q8 = None
     if not args.no_sweep:
-        sweep = sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live)
+        legs = configs_leg(qm, dev, peaks, clocks)
+        roofline["per_config"].update(legs["gemv"])
+        prefill = legs["prefill"]
+        q8 = legs["q8_0"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "M": 8,
-                   "shapes": "K=4096,N=14336; K=14336,N=4096; dequant 14336x4096",
-                   "seeds": [1, 2], "l2": f"{REPLICAS} rotating operand replicas (> L2)",
-                   "parallelism": f"replicas x{world}",
-                   "value_definition": "Q4_0 weight bytes streamed per step / step time"},
+        "config": bench_config(world),
         "roofline": roofline,
-        "paths": paths,
+        "prefill": prefill,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "overlap": "inputs, kernels and outputs on three streams; step i+1's inputs "
                            "and step i-1's outputs move while step i computes"},
         "gpu_launches": launches,
-        "m1_gemv": sweep["m1_gemv"] if sweep else None,
-        "decode_sweep": sweep["decode"] if sweep else None,
-        "prefill": sweep["prefill"] if sweep else None,
-        "q8_0": sweep["q8_0"] if sweep else None,
+        "paths": paths,
+        "q8_0": q8,
         "clocks": clocks,
         "hbm_peak_gbs": hbm, "peak_source": peaks["source"],
     }
@@ -563,52 +566,197 @@ def graph_ms(torch, fn, passes: int = 5) -> float:
     return best
 
 
-def sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live) -> dict:
-    """The decoder sweep (32 layers of q, k, v, o, gate, up, down; hidden 4096,
-    grouped-query attention) at M = 1, 8 and 512 through qm_matmul_q4_0, plus
-    back-to-back M = 1 GEMVs at K = N = 4096.  Weights: all 32 layers resident
-    (3.93 GB, far beyond L2).  Activations: one synthetic A per (M, K), shared
-    by the layers (the projections are not chained: no attention and no
-    activation functions).  M = 1 and 8 replay a CUDA graph of the 224 launches
-    (what a decode loop does); M = 512 is launched eagerly."""
+MMAS_PER_PRODUCT = 4  # the tensor-core GEMM takes all four bf16 piece products
+DECODER_PROJS = tuple(p for (p, _, _) in synth.DECODER_LAYER)
+
+
+def timed_loop(torch, fn, calls: int, warm: int = 3) -> float:
+    """Mean ms per call of fn(i) over `calls` calls (events around the loop,
+    none in between), after `warm` untimed calls."""
+    for i in range(warm):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(calls):
+        fn(i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / calls
+
+
+def configs_leg(qm, dev, peaks, clocks) -> dict:
+    """Every other workload, each on its own synthetic inputs:
+
+    GEMV / dequant rows (weight GB/s against HBM):
+      cfg0: GEMV M=1, K=N=4096 (9.44 MB), 16 weight replicas back to back in
+            a CUDA graph (the replicas exceed L2);
+      cfg1_dequant: dequant of the 14336 x 4096 weight, 4 rotating replicas;
+      cfg4 M=1 / M=8: the 32-layer decoder sweep (q, k, v, o, gate, up, down;
+            hidden 4096, GQA; 3.93 GB of weights, all resident), a CUDA graph
+            of its 224 launches, as a decode loop replays it; also with q|k|v
+            and gate|up stacked by rows (128 launches).  Activations: one
+            synthetic A per (M, K), shared by the layers (no attention or
+            activation functions between the projections).
+    GEMM rows (TFLOP/s against the tensor-core bound, bf16 peak / 4 MMAs per
+    product, and against the FP32 FMA peak):
+      cfg2: M=32 and M=256 at K=N=4096 (A with 1% outliers), 16 weight replicas;
+      cfg3: M=1024 at (K=4096, N=14336) and (K=14336, N=4096), 2 replicas;
+      cfg4 M=512: the decoder sweep, eager launches.
+    """
     import torch
     hbm = peaks["hbm_gbs"]
+    bf16 = peaks["bf16_tflops"]
+    tc_bound = bf16 / MMAS_PER_PRODUCT
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    fp32_peak = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
+    sh = lambda: int(torch.cuda.current_stream().cuda_stream)  # noqa: E731
+    gemv, prefill = {}, {}
+
+    def mm(A, W, C, M, N, K, what):
+        rc = qm.qm_matmul_q4_0_ptr(A.data_ptr(), W.data_ptr(), C.data_ptr(), M, N, K, sh())
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"{what}: {qm.qm_status_string(rc)}")
+
+    def gemv_row(workload, kernel, wbytes, ms, launches=1):
+        gbs = wbytes / (ms * 1e-3) / 1e9
+        return {"workload": workload, "kernel": kernel, "ms": ms, "weight_gbs": gbs,
+                "frac": gbs / hbm, "bound": "hbm", "launches": launches}
+
+    def gemm_row(workload, flops, ms):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"workload": workload, "kernel": "gemm_q4_0_tc", "ms": ms, "tflops": tf,
+                "frac": tf / tc_bound, "bound": "tensor", "peak": tc_bound,
+                "vs_fp32_fma_peak": tf / fp32_peak}
+
+    # cfg0: back-to-back M = 1 GEMVs at K = N = 4096.
+    c0 = synth.workload(0)[0]
+    w0 = [torch.from_numpy(c0.weights()).to(dev) for _ in range(16)]
+    a0 = torch.from_numpy(c0.acts()).to(dev)
+    o0 = torch.empty((1, c0.N), dtype=torch.float32, device=dev)
+
+    def m1_fn():
+        for w in w0:
+            mm(a0, w, o0, 1, c0.N, c0.K, "cfg0")
+    ms0 = graph_ms(torch, m1_fn) / len(w0)
+    gemv["cfg0_gemv_m1_k4096_n4096"] = gemv_row(
+        "GEMV M=1, K=N=4096, 16 replicas back to back in a CUDA graph", "gemv_q4_0_tc",
+        c0.weight_bytes, ms0)
+    del w0
+
+    # cfg1 dequant.
+    deq = step_cases()[2]
+    nb = deq.weight_bytes // 18
+    dw = [torch.from_numpy(deq.weights()).to(dev) for _ in range(REPLICAS)]
+    dout = [torch.empty(nb * 32, dtype=torch.float32, device=dev) for _ in range(REPLICAS)]
+
+    def deq_fn(i):
+        rc = qm.qm_dequant_q4_0_ptr(dw[i % REPLICAS].data_ptr(), nb, dout[i % REPLICAS].data_ptr(), sh())
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"dequant: {qm.qm_status_string(rc)}")
+    ms = timed_loop(torch, deq_fn, 20)
+    row = gemv_row("dequant_q4_0 of the 14336 x 4096 weight, 4 rotating replicas",
+                   "dequant_q4_0_fast", deq.weight_bytes, ms)
+    row["alg_gbs"] = dequant_bytes(deq) / (ms * 1e-3) / 1e9
+    row["frac"] = row["alg_gbs"] / hbm
+    row["algorithmic_bytes_per_launch"] = dequant_bytes(deq)
+    row["traffic"] = measured_traffic("dequant_q4_0", deq.name)
+    gemv["cfg1_dequant"] = row
+    del dw, dout
+
+    # cfg2 and cfg3: prefill GEMMs.
+    for c in synth.workload(2) + synth.workload(3):
+        reps = 16 if c.weight_bytes < 16 << 20 else 2
+        ws = [torch.from_numpy(c.weights()).to(dev) for _ in range(reps)]
+        A = torch.from_numpy(c.acts()).to(dev)
+        C = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
+        calls = 32 if c.M < 1024 else 6
+
+        def fn(i, ws=ws, A=A, C=C, c=c):
+            mm(A, ws[i % len(ws)], C, c.M, c.N, c.K, c.name)
+        ms = timed_loop(torch, fn, calls)
+        key = ("cfg2_" if c.M < 1024 else "cfg3_") + c.name
+        prefill[key] = gemm_row(f"{c.name} ({reps} weight replicas)", 2.0 * c.M * c.N * c.K, ms)
+        del ws, A, C
+
+    # cfg4: the 32-layer decoder sweep.
     cases = synth.workload(4, layers=32, sweep_m=(1,))
     weights = [torch.from_numpy(c.weights()).to(dev) for c in cases]
     wbytes = sum(c.weight_bytes for c in cases)
     layer_shapes = [(c.N, c.K) for c in cases[:7]]
-    sh = lambda: int(torch.cuda.current_stream().cuda_stream)  # noqa: E731
-
-    def sweep_fn(M, A, outs):
-        def fn():
-            s = sh()
-            for i, c in enumerate(cases):
-                o = outs[i % 7]
-                rc = qm.qm_matmul_q4_0_ptr(A[c.K].data_ptr(), weights[i].data_ptr(),
-                                           o.data_ptr(), M, c.N, c.K, s)
-                if rc != qm.QM_OK:
-                    raise RuntimeError(f"sweep {c.name} M={M}: {qm.qm_status_string(rc)}")
-        return fn
 
     def acts(M):
         return {K: torch.from_numpy(synth.activations(M, K, 5, key=(2, M, K))).to(dev)
                 for K in (4096, 14336)}
 
-    decode = {}
+    def sweep_fn(M, A, outs):
+        def fn():
+            for i, c in enumerate(cases):
+                mm(A[c.K], weights[i], outs[i % 7], M, c.N, c.K, f"sweep {c.name} M={M}")
+        return fn
+
     for M in (1, 8):
         A = acts(M)
         outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in layer_shapes]
         ms = graph_ms(torch, sweep_fn(M, A, outs))
-        decode[f"m{M}"] = {"ms_per_pass": ms, "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
-                           "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / hbm,
-                           "launches_per_pass": len(cases)}
-    decode["workload"] = ("32-layer decoder sweep (q,k,v,o,gate,up,down; hidden 4096, GQA), "
-                          "3.93 GB of Q4_0 weights per pass, CUDA graph of 224 GEMV launches")
+        gemv[f"cfg4_sweep_m{M}"] = gemv_row(
+            f"32-layer decoder sweep at M={M}: CUDA graph of {len(cases)} GEMV launches, "
+            "3.93 GB of weights per pass", "gemv_q4_0_tc", wbytes, ms, len(cases))
+
+    # M = 1 through the list GEMV (qm_gemv_q4_0_list, one persistent launch
+    # per list), every problem with its own output:
+    #   * per_group: 4 lists per layer, [q, k, v], [o], [gate, up], [down], as an
+    #     engine with attention and activation kernels in between launches them;
+    #   * one_list: all 224 GEMVs of the sweep in one list, independent;
+    #   * chained: the same list with the decoder's ordering (q, k, v wait for the
+    #     previous layer's down; o for v; gate and up for o; down for up): every
+    #     activation read waits for those problems to finish on every SM, as a
+    #     chain of dependent projections would (the activations themselves stay
+    #     the shared synthetic ones, so values do not grow through 224 products).
+    A1 = acts(1)
+    louts = [torch.empty((1, c.N), dtype=torch.float32, device=dev) for c in cases]
+    ctr = torch.zeros(len(cases), dtype=torch.int32, device=dev)
+    # Within a layer: the index of the last problem each projection waits for
+    # (None: the previous layer's down).
+    proj_wait = {"q": None, "k": None, "v": None, "o": 2, "gate": 3, "up": 3, "down": 5}
+
+    def list_problems(chained):
+        out = []
+        for i, c in enumerate(cases):
+            wf = -1
+            if chained:
+                layer, p = divmod(i, 7)
+                rel = proj_wait[DECODER_PROJS[p]]
+                wf = 7 * layer + rel if rel is not None else 7 * layer - 1
+            out.append((A1[c.K].data_ptr(), weights[i].data_ptr(), louts[i].data_ptr(), c.N, c.K, wf))
+        return out
+
+    def run_lists(lists, with_ctr):
+        s = sh()
+        for lst in lists:
+            rc = qm.qm_gemv_q4_0_list_ptr(lst, 1, ctr.data_ptr() if with_ctr else 0, s)
+            if rc != qm.QM_OK:
+                raise RuntimeError(f"gemv list: {qm.qm_status_string(rc)}")
+
+    groups = []
+    for layer in range(32):
+        b = 7 * layer
+        ps = list_problems(False)[b:b + 7]
+        groups += [ps[0:3], ps[3:4], ps[4:6], ps[6:7]]
+    variants = (("per_group", groups, False, len(groups)),
+                ("one_list", [list_problems(False)], False, 1),
+                ("chained", [list_problems(True)], True, 1))
+    for name, lists, with_ctr, nl in variants:
+        ms = graph_ms(torch, lambda lists=lists, with_ctr=with_ctr: run_lists(lists, with_ctr))
+        gemv[f"cfg4_sweep_m1_list_{name}"] = gemv_row(
+            f"32-layer decoder sweep at M=1 through qm_gemv_q4_0_list ({name}): CUDA graph of "
+            f"{nl} list launches", "gemv_q4_0_list", wbytes, ms, nl)
+    del louts
 
     # The same weights with q|k|v and gate|up stacked by rows (one row-major
-    # block stream each, as an engine with fused projections stores them):
-    # 4 GEMVs per layer, 128 launches per pass.
-    fused, fused_shapes = [], []
+    # block stream each, as an engine with fused projections stores them).
+    fused = []
     for layer in range(32):
         w = weights[7 * layer:7 * layer + 7]
         fused += [torch.cat([w[0], w[1], w[2]]), w[3], torch.cat([w[4], w[5]]), w[6]]
@@ -618,71 +766,29 @@ def sweep_leg(qm, dev, peaks, fp32_peak_max, fp32_peak_live) -> dict:
         outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in fused_shapes]
 
         def fused_fn(M=M, A=A, outs=outs):
-            s = sh()
             for i, wf in enumerate(fused):
                 N, K = fused_shapes[i % 4]
-                rc = qm.qm_matmul_q4_0_ptr(A[K].data_ptr(), wf.data_ptr(), outs[i % 4].data_ptr(),
-                                           M, N, K, s)
-                if rc != qm.QM_OK:
-                    raise RuntimeError(f"fused sweep M={M}: {qm.qm_status_string(rc)}")
+                mm(A[K], wf, outs[i % 4], M, N, K, f"stacked sweep M={M}")
         ms = graph_ms(torch, fused_fn)
-        decode[f"m{M}_fused_layout"] = {"ms_per_pass": ms, "weight_gbs": wbytes / (ms * 1e-3) / 1e9,
-                                        "hbm_frac": wbytes / (ms * 1e-3) / 1e9 / hbm,
-                                        "launches_per_pass": len(fused)}
+        gemv[f"cfg4_sweep_m{M}_stacked"] = gemv_row(
+            f"the decoder sweep at M={M} with q|k|v and gate|up stacked by rows: CUDA graph of "
+            f"{len(fused)} GEMV launches", "gemv_q4_0_tc", wbytes, ms, len(fused))
     del fused
 
-    # Back-to-back M = 1 GEMVs at K = N = 4096 (16 weight replicas > L2).
-    c0 = synth.workload(0)[0]
-    w0 = [torch.from_numpy(c0.weights()).to(dev) for _ in range(16)]
-    a0 = torch.from_numpy(c0.acts()).to(dev)
-    o0 = torch.empty((1, c0.N), dtype=torch.float32, device=dev)
-
-    def m1_fn():
-        s = sh()
-        for w in w0:
-            rc = qm.qm_matmul_q4_0_ptr(a0.data_ptr(), w.data_ptr(), o0.data_ptr(), 1, c0.N, c0.K, s)
-            if rc != qm.QM_OK:
-                raise RuntimeError(f"m1 gemv: {qm.qm_status_string(rc)}")
-    ms0 = graph_ms(torch, m1_fn) / len(w0)
-    m1 = {"workload": "GEMV M=1, K=N=4096 (9.44 MB of weights), 16 replicas back to back "
-                      "in a CUDA graph",
-          "us_per_gemv": ms0 * 1e3, "weight_gbs": c0.weight_bytes / (ms0 * 1e-3) / 1e9,
-          "hbm_frac": c0.weight_bytes / (ms0 * 1e-3) / 1e9 / hbm}
-    del w0
-
-    # Prefill: the same sweep at M = 512, eager launches.
+    # The sweep at M = 512, eager launches.
     A = acts(512)
     outs = [torch.empty((512, N), dtype=torch.float32, device=dev) for (N, K) in layer_shapes]
     fn = sweep_fn(512, A, outs)
-    fn()
-    torch.cuda.synchronize()
-    passes = 3
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(passes):
-        fn()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / passes
+    ms = timed_loop(torch, lambda i: fn(), 3, warm=1)
     flops = sum(2.0 * 512 * c.N * c.K for c in cases)
-    tflops = flops / (ms * 1e-3) / 1e12
-    bf16 = peaks["bf16_tflops"]
-    prefill = {
-        "workload": "32-layer decoder sweep at M=512 (7.15 TFLOP per pass), eager launches",
-        "kernel": "gemm_q4_0_tc (tcgen05, A split into bf16 hi+lo, W exact as two bf16 "
-                  "pieces, 3 MMAs per product, f32 accumulation in TMEM)",
-        "ms_per_pass": ms, "tflops": tflops,
-        "roofline": {
-            "bound": "tensor", "achieved": tflops, "peak": bf16 / 3.0, "unit": "TFLOP/s",
-            "frac": tflops / (bf16 / 3.0),
-            "peak_note": "measured bf16 dense peak / 3 MMAs per useful product",
-            "mma_tflops_issued": 3.0 * tflops, "bf16_peak_tflops": bf16,
-            "fp32_fma_peak_tflops_max_clock": fp32_peak_max,
-            "vs_fp32_fma_peak_max_clock": tflops / fp32_peak_max,
-            "fp32_fma_peak_tflops_live_clock": fp32_peak_live}}
+    prefill["cfg4_sweep_m512"] = gemm_row("32-layer decoder sweep at M=512 (7.15 TFLOP per pass), "
+                                          "eager launches", flops, ms)
+    prefill["bound_note"] = (f"tensor-core bound = measured bf16 dense peak {bf16} TFLOP/s / "
+                             f"{MMAS_PER_PRODUCT} bf16 MMAs per useful product; FP32 FMA peak "
+                             f"{fp32_peak:.1f} TFLOP/s at {sm_max} MHz")
     del weights
     torch.cuda.empty_cache()
-    return {"decode": decode, "m1_gemv": m1, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks)}
+    return {"gemv": gemv, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks)}
 
 
 def q8_0_leg(qm, dev, peaks) -> dict:

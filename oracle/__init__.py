@@ -3,6 +3,10 @@ quantize — TEST INFRASTRUCTURE ONLY.
 
 The arithmetic lives in ``qm_oracle.c`` (plain C99, fp64, single-threaded);
 this module compiles it with gcc and exposes it to numpy through ctypes.
+``load_parallel()`` binds a second build of the same source with OpenMP,
+which shares independent output entries (and dequant blocks) out over the
+host's cores for the multi-core CPU baseline; every entry is still one
+ascending-k fp64 sum, so its results are bit-identical to ``load()``'s.
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never does, and this
 package imports nothing from it.
@@ -37,6 +41,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "qm_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_OMP_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_omp.so")
 
 BLOCK_BYTES = 18
 BLOCK_ELEMS = 32
@@ -44,6 +49,7 @@ Q8_0_BLOCK_BYTES = 34
 
 _lock = threading.Lock()
 _lib = None
+_omp_lib = None
 
 # Plain IEEE arithmetic: no contraction into fused multiply-adds, no fast-math.
 _CFLAGS = ["-std=c99", "-O2", "-fPIC", "-shared", "-ffp-contract=off",
@@ -56,6 +62,12 @@ def build(src: str = _SRC, out: str = _LIB_PATH, extra_flags=()) -> str:
     cmd = ["gcc", *_CFLAGS, *extra_flags, "-o", out, src, "-lm"]
     subprocess.run(cmd, check=True, capture_output=True, text=True)
     return out
+
+
+def build_all() -> None:
+    """Compile both builds of the oracle: plain, and with OpenMP."""
+    build()
+    build(out=_OMP_LIB_PATH, extra_flags=("-fopenmp",))
 
 
 def _needs_build(path: str) -> bool:
@@ -99,6 +111,18 @@ def load(path: str | None = None) -> "Oracle":
                 build()
             _lib = Oracle(_bind(ctypes.CDLL(_LIB_PATH)))
     return _lib
+
+
+def load_parallel() -> "Oracle":
+    """The oracle built with OpenMP (threads: OMP_NUM_THREADS, else every
+    core the process may run on)."""
+    global _omp_lib
+    with _lock:
+        if _omp_lib is None:
+            if _needs_build(_OMP_LIB_PATH):
+                build(out=_OMP_LIB_PATH, extra_flags=("-fopenmp",))
+            _omp_lib = Oracle(_bind(ctypes.CDLL(_OMP_LIB_PATH)))
+    return _omp_lib
 
 
 def _ptr(a: np.ndarray) -> int:

@@ -101,6 +101,9 @@ static double weight_at(const uint8_t* wq, int64_t K, int64_t n, int64_t k)
 
 void oracle_dequant_q4_0(const uint8_t* wq, int64_t n_blocks, float* out)
 {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t b = 0; b < n_blocks; ++b) {
         const uint8_t* block = wq + b * ORACLE_Q4_0_BLOCK_BYTES;
         double d = block_scale(block);
@@ -181,6 +184,12 @@ int oracle_matmul_q4_0(const float* A, const uint8_t* wq, int64_t M, int64_t N,
                        int64_t K, double* C, double* S)
 {
     if (!sizes_ok(M, N, K)) return -1;
+    /* Entries are independent; a build with OpenMP (the multi-core CPU
+     * baseline) shares them out over threads, each still summed by entry()
+     * alone, so the result is the same bit for bit. */
+#ifdef _OPENMP
+#pragma omp parallel for collapse(2) schedule(static)
+#endif
     for (int64_t m = 0; m < M; ++m) {
         for (int64_t n = 0; n < N; ++n) {
             entry(A, wq, K, m, n, &C[m * N + n], S ? &S[m * N + n] : NULL);
@@ -198,6 +207,9 @@ int oracle_matmul_q4_0_entries(const float* A, const uint8_t* wq, int64_t M,
     for (int64_t i = 0; i < count; ++i) {
         if (m_idx[i] < 0 || m_idx[i] >= M || n_idx[i] < 0 || n_idx[i] >= N) return -1;
     }
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
     for (int64_t i = 0; i < count; ++i) {
         entry(A, wq, K, m_idx[i], n_idx[i], &C[i], S ? &S[i] : NULL);
     }

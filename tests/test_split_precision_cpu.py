@@ -12,9 +12,11 @@ code and no oracle involved).
 * Activation split (GEMV and GEMM): |a - hi - lo| <= 2^-17 |a| for normal f32
   a, with hi = bf16(a), lo = bf16(a - hi).  The GEMV keeps both pieces against
   the exact (q - 8), so 2^-17 is its whole per-product error.
-* GEMM products: the three bf16 products the GEMM keeps (hi W_hi + hi W_lo +
-  lo W_hi) miss a * W by at most (2^-16 + 2^-17) |a W|, the dropped lo W_lo
-  term being up to 2^-16 |a W|, and the bound is nearly reached.
+* GEMM products: the GEMM takes all four bf16 piece products (hi W_hi +
+  hi W_lo + lo W_hi + lo W_lo), which miss a * W by the activation residual
+  alone, at most 2^-17 |a W|.  Three products (dropping lo W_lo, up to 2^-16
+  |a W|) would miss by up to (2^-16 + 2^-17) |a W|, more than the 1e-5
+  tolerance, and that bound is nearly reached.
 * Accumulation: on a constant input (every product the same, so every
   rounding error has the same sign) f32 sums over K = 4096 miss the 1e-5
   relative tolerance whichever way they are formed, including the plain
@@ -102,7 +104,7 @@ def test_activation_split_bound():
 
 
 def gemm_kept(a, W):
-    """The three products the GEMM keeps for activation a and weight W."""
+    """Three of the four piece products (lo W_lo dropped), for activation a and weight W."""
     hi = bf16_rne(a).astype(np.float64)
     lo = bf16_rne((np.float64(a) - hi).astype(np.float32)).astype(np.float64)
     W_hi = bf16_rne(W).astype(np.float64)
@@ -126,6 +128,31 @@ def test_gemm_three_product_bound():
     W1 = np.float32(np.float16(1.0029296875))      # q = 9
     e1 = abs(gemm_kept(a1, W1) - np.float64(a1) * np.float64(W1)) / (np.float64(a1) * np.float64(W1))
     assert 1.1e-5 < e1 <= 2.0 ** -16 + 2.0 ** -17
+
+
+def gemm_four(a, W):
+    """The four products the GEMM takes for activation a and weight W."""
+    hi = bf16_rne(a).astype(np.float64)
+    lo = bf16_rne((np.float64(a) - hi).astype(np.float32)).astype(np.float64)
+    W_hi = bf16_rne(W).astype(np.float64)
+    W_lo = bf16_rne((np.float64(W) - W_hi).astype(np.float32)).astype(np.float64)
+    return hi * W_hi + hi * W_lo + lo * W_hi + lo * W_lo
+
+
+def test_gemm_four_product_bound():
+    g = np.random.default_rng(2)
+    a = g.standard_normal(200_000).astype(np.float32) * np.float32(3.0)
+    d = g.choice(finite_f16()[finite_f16() > 0], 200_000).astype(np.float32)
+    W = (g.integers(0, 16, 200_000) - 8).astype(np.float32) * d
+    keep = (a != 0) & (W != 0)
+    a, W = a[keep], W[keep]
+    exact = a.astype(np.float64) * W.astype(np.float64)
+    assert (np.abs(gemm_four(a, W) - exact) <= 2.0 ** -17 * np.abs(exact)).all()
+    # The input that defeats three products is exact to 2^-23 with four.
+    a1 = np.float32(1 + 2 ** -8 - 2 ** -23)
+    W1 = np.float32(np.float16(1.0029296875))
+    p1 = np.float64(a1) * np.float64(W1)
+    assert abs(gemm_four(a1, W1) - p1) / p1 <= 2.0 ** -22
 
 
 def test_constant_inputs_defeat_any_f32_sum():
