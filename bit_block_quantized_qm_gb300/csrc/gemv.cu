@@ -646,18 +646,40 @@ static __device__ __align__(256) float g_noalloc_scratch[kStaticPartFloats + kSt
 namespace {
 
 // Device address of g_noalloc_scratch, found once per device with that device
-// current.  (In host code the array's name is only a host-side stand-in.)
+// current.  (In host code the array's name is only a host-side stand-in.)  The
+// address belongs to the device's context: after cudaDeviceReset the next call
+// gets a new context, with the module loaded anew, so the address is looked
+// up again when the current context is not the one it was found in.
 void* g_noalloc_addr[64] = {nullptr};
+CUcontext g_noalloc_ctx[64] = {nullptr};
 std::mutex g_noalloc_mutex;
+
+using CtxGetCurrent = CUresult (*)(CUcontext*);
+
+CUcontext current_context() {
+    static CtxGetCurrent fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<CtxGetCurrent>(nullptr);
+        return reinterpret_cast<CtxGetCurrent>(f);
+    }();
+    CUcontext ctx = nullptr;
+    if (fn) fn(&ctx);
+    return ctx;
+}
 
 cudaError_t noalloc_workspace(const DeviceInfo& dev, Workspace* out) {
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev.device]) {
+    const CUcontext ctx = current_context();
+    if (!g_noalloc_addr[dev.device] || g_noalloc_ctx[dev.device] != ctx) {
         void* p = nullptr;
         cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return err;
         g_noalloc_addr[dev.device] = p;
+        g_noalloc_ctx[dev.device] = ctx;
     }
     float* base = static_cast<float*>(g_noalloc_addr[dev.device]);
     out->part = base;

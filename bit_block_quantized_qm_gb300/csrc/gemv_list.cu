@@ -657,9 +657,28 @@ cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned
     int max_wait = -1;
     for (int i = 0; i < count; ++i) max_wait = std::max(max_wait, items[i].wait_for);
     if (max_wait >= 0 && !counters) return cudaErrorInvalidValue;
-    int64_t rg_sum = 0;
+    // A launch without waits runs independent problems, whose order does not
+    // matter: group those with the same activations (stably, in order of
+    // first appearance), so that each CTA loads every activation vector once
+    // instead of at every change.
+    int order[kListMaxProblems];
+    int first_use[kListMaxProblems];
     for (int i = 0; i < count; ++i) {
-        ListProblem& q = P.p[i];
+        order[i] = i;
+        first_use[i] = i;
+        for (int j = 0; j < i; ++j) {
+            if (items[j].A == items[i].A && items[j].K == items[i].K) {
+                first_use[i] = first_use[j];
+                break;
+            }
+        }
+    }
+    if (max_wait < 0)
+        std::stable_sort(order, order + count, [&](int a, int b) { return first_use[a] < first_use[b]; });
+    int64_t rg_sum = 0;
+    for (int o = 0; o < count; ++o) {
+        const int i = order[o];
+        ListProblem& q = P.p[o];
         q.A = items[i].A;
         q.W = items[i].W;
         q.C = items[i].C;
@@ -678,7 +697,7 @@ cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned
         const int64_t dims[4] = {kUnitB, q.c, U / q.c, items[i].N};
         const int64_t strides[3] = {kUnitB, int64_t(kUnitB) * q.c, int64_t(kUnitB) * U};
         const int box[4] = {kUnitB, q.c + 1, 1, 16};
-        cudaError_t e = encode_tiled(&P.map[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].W, 4, dims, strides, box);
+        cudaError_t e = encode_tiled(&P.map[o], CU_TENSOR_MAP_DATA_TYPE_UINT8, items[i].W, 4, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
     if (max_wait >= 0) {

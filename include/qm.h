@@ -218,8 +218,10 @@ QM_API int qm_selftest_wait_timeout(void* stream);
  *   Memory: every GPU that loads the library holds the array (about 1 MB)
  *   until the process exits.
  *   Set-up: the first call on each device looks up the array's device
- *   address (cudaGetSymbolAddress) with that device current; make that first
- *   call before any stream capture.
+ *   address (cudaGetSymbolAddress) with that device current, and looks it up
+ *   again when the device's current context has changed (after
+ *   cudaDeviceReset); make that first call, and the first call after a reset,
+ *   before any stream capture.
  *   Sharing: all calls use the same array, which keeps the last call's
  *   contents; a call clears the counters it needs before its kernel runs.
  *   Calls that overlap on the GPU (different streams, or concurrent graph

@@ -374,8 +374,12 @@ def test_m1_matches_rows_of_m8(env):
 
 # ------------------------------------------------------- workload shapes
 
-def _check_case(qm, o, case, full_limit=6e8, rows=4, pairs=512):
-    blob = case.weights()
+def _check_case(qm, o, case, full_limit=6e8, rows=4, pairs=512, blob=None):
+    """The case through qm_matmul_q4_0 against the oracle: every entry when
+    M*N*K <= full_limit, else `rows` random rows x every column plus `pairs`
+    random entries (the oracle's OpenMP build, bit-identical to the plain one,
+    takes the large samples)."""
+    blob = case.weights() if blob is None else blob
     A = case.acts()
     wq = dev(blob)
     C = qm.qm_matmul_q4_0(dev(A), wq, case.N)
@@ -389,16 +393,18 @@ def _check_case(qm, o, case, full_limit=6e8, rows=4, pairs=512):
     r = g.choice(case.M, size=min(rows, case.M), replace=False)
     mi = np.concatenate([np.repeat(r, case.N), g.integers(0, case.M, pairs)])
     ni = np.concatenate([np.tile(np.arange(case.N), r.size), g.integers(0, case.N, pairs)])
-    C_ref, S_ref = o.matmul_q4_0_entries(A, blob, case.N, case.K, mi, ni)
+    C_ref, S_ref = oracle.load_parallel().matmul_q4_0_entries(A, blob, case.N, case.K, mi, ni)
     assert_close(C[mi, ni], C_ref, S_ref, case.name + " (sampled)")
 
 
 @pytest.mark.parametrize("index", [0, 1, 2, 3])
 def test_workload_full_size(env, index):
+    # Workloads 0-2 every entry; workload 3 (M = 1024) on 16 random rows x
+    # every column plus 1024 random entries.
     qm, o = env
     for case in synth.workload(index):
         if case.op == "matmul":
-            _check_case(qm, o, case)
+            _check_case(qm, o, case, rows=16, pairs=1024)
 
 
 def test_decoder_layer_shapes(env):
@@ -407,3 +413,11 @@ def test_decoder_layer_shapes(env):
     cases = [c for c in synth.workload(4, layers=1)]
     for case in cases:
         _check_case(qm, o, case, full_limit=1e8, rows=2, pairs=256)
+
+
+def test_decoder_sweep_every_layer_m512(env):
+    # Every layer of the 32-layer decoder sweep at M = 512 (the prefill GEMM on
+    # tensor cores): 4 random rows x every column of each of the 7 projections.
+    qm, o = env
+    for case in synth.workload(4, layers=32, sweep_m=(512,)):
+        _check_case(qm, o, case, full_limit=0, rows=4, pairs=0)
