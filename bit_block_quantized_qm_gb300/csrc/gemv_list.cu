@@ -55,6 +55,8 @@
 // lanes of a row group; its 16 row sums go to a shared-memory slot, and the
 // last of the tile's warps to finish adds the slots in a fixed warp order and
 // writes C.  No atomics touch any sum, so results do not depend on timing.
+// A warp hands its stage back to the producer as soon as the unit's bytes are
+// in registers, before any of this, so the reduction never holds up a copy.
 //
 // Launch and waits.  Programmatic dependent launch: before griddepcontrol.wait
 // a CTA only initialises barriers and asks L2 for its first stage (a hint that
@@ -82,7 +84,6 @@ constexpr int kStageB = 2 * box_bytes(8);        // 41,472 bytes (c = 8); c = 16
 constexpr int kLStages = 4;
 constexpr int kLFragB = kListMaxK * 4;           // activations as B fragments (M = 1)
 constexpr int kTileSlots = 4;                    // tiles whose partial sums may be in flight
-constexpr int kProbSlots = 4;                    // problems whose CTA arrivals may be in flight
 constexpr int kSlotFloats = kLW * 16;            // one tile: 16 warps x 16 rows
 
 // Shared memory: ring | fragments | partial-sum slots | barriers and counters.
@@ -91,7 +92,7 @@ constexpr int kOffSlots = kOffFrag + kLFragB;
 constexpr int kOffBars = kOffSlots + kTileSlots * kSlotFloats * 4;
 constexpr int kNumBars = 2 * kLStages + 3;       // full, empty, a_full, a_empty, frag_ready
 constexpr int kOffInts = kOffBars + kNumBars * 8;
-constexpr int kNumInts = 2 * kTileSlots + kProbSlots + 1;  // arrivals, done, problem counts, abort
+constexpr int kNumInts = 2 * kTileSlots + kListMaxProblems + 1;  // arrivals, done, tiles per problem, abort
 // 1 KB of zeros, 64 bytes past a 128-byte boundary: a lane that reads zeros
 // and the lane of the same g that reads real fragments (1024-byte aligned)
 // then hit different banks.
@@ -356,8 +357,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
     uint64_t* frag_ready = a_empty + 1;
     int* arr = reinterpret_cast<int*>(smem + kOffInts);  // [kTileSlots] arrivals per tile slot
     volatile int* done = arr + kTileSlots;               // [kTileSlots] last tile reduced per slot
-    int* red = arr + 2 * kTileSlots;                     // [kProbSlots] reduced tiles per problem
-    volatile int* abort_flag = red + kProbSlots;
+    int* red = arr + 2 * kTileSlots;                     // [count] tiles of a problem reduced here
+    volatile int* abort_flag = red + kListMaxProblems;
     const uint8_t* zeros = smem + kOffZero;
 
     const int warp = threadIdx.x >> 5;
@@ -378,7 +379,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
             arr[i] = 0;
             done[i] = i - kTileSlots;
         }
-        for (int i = 0; i < kProbSlots; ++i) red[i] = 0;
+        for (int i = 0; i < kListMaxProblems; ++i) red[i] = 0;
         for (int i = 0; i < 256; ++i) reinterpret_cast<uint32_t*>(smem + kOffZero)[i] = 0u;
         *abort_flag = 0;
         fence_barrier_init();
@@ -502,7 +503,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     const int g = lane >> 2;
     const int t = lane & 3;
     AKey key;
-    int rounds = 0, st = 0, tl = 0, lp = 0;
+    int rounds = 0, st = 0, tl = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int qi = 0; qi < P.count && ok; ++qi) {
@@ -533,7 +534,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
         }
         const int U = q.K >> 8;
         const int total = n * U;
-        const int slot_p = lp % kProbSlots;
         // This warp's slot of every stage of the problem: box warp / c, unit
         // warp % c of it (c is 16 or 8); its rows g and g + 8 are row_b apart.
         const int cu = q.c;
@@ -558,6 +558,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 if (u < 16) acc[0] = acc[1] = 0.f;
                 const uint8_t* ra = ring + st * kStageB + slot_off;
                 unit_mma(ra, ra + 8 * row_b, fbase + u * fstep, g, t, acc);
+                // The stage's bytes are in registers: hand it back to the
+                // producer before adding anything up.
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
                 if (u + 16 >= U) {
                     // This warp's last unit of tile k: its row sums to the slot.
                     float s0v = acc[0], s1v = acc[1];
@@ -614,8 +618,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
                         if (lane == 0) {
                             arr[sl] = 0;
                             done[sl] = tile_l;
-                            if (q.arrive && atomicAdd(&red[slot_p], 1) == n - 1) {
-                                red[slot_p] = 0;
+                            if (q.arrive && atomicAdd(&red[qi], 1) == n - 1) {
                                 __threadfence();
                                 asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.ctr + qi)
                                              : "memory");
@@ -624,15 +627,16 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
+            if (s0 + warp >= total) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
             if (++st == kLStages) {
                 st = 0;
                 ph ^= 1u;
             }
         }
         tl += n;
-        ++lp;
     }
 }
 
