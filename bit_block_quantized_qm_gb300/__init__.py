@@ -114,7 +114,7 @@ def load_library() -> ctypes.CDLL:
             lib.qm_matmul_q4_0.restype = i32
             lib.qm_matmul_q4_0_algo.argtypes = [p, p, p, i64, i64, i64, i32, p]
             lib.qm_matmul_q4_0_algo.restype = i32
-            lib.qm_gemv_plan.argtypes = [i64, i64, i64, i32, i32, i32, p]
+            lib.qm_gemv_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i32, p]
             lib.qm_gemv_plan.restype = i32
             lib.qm_gemm_plan.argtypes = [i64, i64, i64, i32, i32, i32, i32, p]
             lib.qm_gemm_plan.restype = i32
@@ -322,16 +322,19 @@ def qm_gemv_q4_0_list(problems, M: int = 1, counters=None, stream=None):
     _check(qm_gemv_q4_0_list_ptr(raw, M, ctr, _stream_handle(stream)), "qm_gemv_q4_0_list")
 
 
-GEMV_PLAN_FIELDS = ("RG", "U", "S", "rps", "c", "hs", "rbpc", "nu_max", "stages", "grid", "smem", "W")
+GEMV_PLAN_FIELDS = ("RG", "U", "S", "rps", "c", "hs", "rbpc", "nu_max", "stages", "grid", "smem", "W",
+                    "cl")
 
 
 def qm_gemv_plan(M: int, N: int, K: int, packed: bool = False, sm_count: int = 152,
-                 smem_optin: int = 232448):
+                 smem_optin: int = 232448, fit=(76, 38, 19), noalloc: bool = False):
     """The decode GEMV's launch plan (host only, see include/qm.h) as a dict,
-    or None when no plan fits; raises on invalid arguments."""
-    out = (ctypes.c_int64 * 12)()
-    rc = load_library().qm_gemv_plan(M, N, K, 1 if packed else 0, sm_count, smem_optin,
-                                     ctypes.cast(out, ctypes.c_void_p))
+    or None when no plan fits; raises on invalid arguments.  `fit` = resident
+    clusters of 2, 4 and 8 CTAs (the regular path's K split); with `noalloc`
+    the plan of qm_matmul_q4_0_noalloc."""
+    out = (ctypes.c_int64 * 13)()
+    rc = load_library().qm_gemv_plan(M, N, K, 1 if packed else 0, sm_count, smem_optin, fit[0], fit[1],
+                                     fit[2], 1 if noalloc else 0, ctypes.cast(out, ctypes.c_void_p))
     if rc == QM_ERR_UNSUPPORTED:
         return None
     _check(rc, "qm_gemv_plan")

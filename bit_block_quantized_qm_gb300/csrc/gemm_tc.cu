@@ -20,13 +20,14 @@
 // Structure (one 128-row output tile of BN = 128 or 256 columns per work
 // item, K in 64-wide steps; BN = 128 also runs 112-column tiles, where those
 // fill more SMs):
-//   * a pre-pass splits A once into bf16 hi / lo matrices (workspace);
-//   * warp 0 (one thread) streams, with TMA, the hi / lo activation tiles
-//     (128 rows x 64 k, 128-byte swizzle) and the weight's raw Q4_0 bytes of
-//     each k-step (BN rows x the 48-byte, 16-byte aligned span that holds the
-//     step's 36-byte block pair);
-//   * warps 2..17 decode each BN x 64 weight tile into W_hi / W_lo, written
-//     in the same swizzled K-major layout (2 stages), then run the epilogue;
+//   * warp 0 (one thread) streams, with TMA, the f32 activation tile of each
+//     k-step (128 rows x 64 k) and the weight's raw Q4_0 bytes (BN rows x the
+//     48-byte, 16-byte aligned span that holds the step's 36-byte block pair);
+//   * warps 2..17 decode each BN x 64 weight tile into W_hi / W_lo, and turn
+//     the activation tile, in place, into its a_hi / a_lo tiles (every
+//     thread reads its 16 floats, the 16 warps meet at a named barrier, then
+//     each writes its pieces), all in the 128-byte swizzled K-major layout
+//     the MMA reads; then they run the epilogue;
 //   * warp 1 owns the two TMEM accumulators (128 lanes x BN f32 columns
 //     each: a_hi W_hi, then the three small products) and one thread issues
 //     16 tcgen05.mma (4 products x 4 k-steps of 16, each 128 x N x 16) per
@@ -39,20 +40,18 @@
 // shared-memory bandwidth sustains together with the decode's stores.
 // Work items (a 1-D grid, one per CTA): whole tiles fill as many full waves
 // of SMs as they can; the tiles of a last, partial wave become 128-column
-// halves of 256-column tiles, or are split into s_rem K ranges of whole
-// 256-wide units.  The partial tiles of a K split meet through a thread-block
-// cluster (each CTA keeps its partial tile in shared memory and, after a
-// bounded mbarrier handshake, sums a slice of rows of all of them in rank
-// order over distributed shared memory) when the split tiles' clusters fit
-// on the GPU at once; otherwise each CTA writes its partial tile to the
-// workspace and the last to arrive adds them in range order.  Either way the
-// result does not depend on timing.  The arrival counters are zeroed by the
-// A-split kernel that runs before every GEMM.  An entry that comes out
-// infinite or NaN is recomputed element by element from A and the Q4_0
-// stream, so non-finite scales keep the per-element semantics.
-// Both kernels are launched with programmatic stream serialization: they let
-// the next kernel start its prologue early and wait (griddepcontrol.wait)
-// before touching global memory.
+// halves of 256-column tiles, or are split into s_rem = 2, 4 or 8 K ranges of
+// whole 256-wide units when the split tiles' clusters of s_rem CTAs all fit
+// on the GPU at once.  The partial tiles of a K split meet through the
+// thread-block cluster: each CTA keeps its partial tile in shared memory and,
+// after a bounded mbarrier handshake, sums a slice of rows of all of them in
+// rank order over distributed shared memory, so the result does not depend
+// on timing and nothing but C is written to global memory.  An entry that
+// comes out infinite or NaN is recomputed element by element from A and the
+// Q4_0 stream, so non-finite scales keep the per-element semantics.
+// The kernel is launched with programmatic stream serialization: it lets the
+// next kernel start its prologue early and waits (griddepcontrol.wait) before
+// touching global memory.
 // Every wait is bounded; a wait that gives up sets the device error word.
 #include <algorithm>
 
@@ -81,10 +80,10 @@ struct Tile {
     static constexpr int kTileW = BN * BK * 2;  // one bf16 weight tile
     static constexpr int kRawBytes = BN * kRawRow;
     static constexpr int kTmemCols = 2 * BN;    // two f32 accumulators of BN columns
-    // Barriers (full and empty per stage, acc_full, two cluster-reduction
-    // barriers), then the TMEM address and the split-K arrival flag, rounded
-    // up to 16 bytes.
-    static constexpr int kBarBytes = ((2 * (kAStages + kWStages + kRawStages) + 3) * 8 + 8 + 15) / 16 * 16;
+    // Barriers (full and empty per stage, converted per activation stage,
+    // acc_full, two cluster-reduction barriers), then the TMEM address,
+    // rounded up to 16 bytes.
+    static constexpr int kBarBytes = ((2 * (kAStages + kWStages + kRawStages) + kAStages + 3) * 8 + 8 + 15) / 16 * 16;
     static constexpr int kSmemBytes = kAStages * 2 * kTileA + kWStages * 2 * kTileW +
                                       kRawStages * kRawBytes + kBarBytes + 1024;  // + alignment slack
     // Instruction descriptor, kind::f16: D f32, A and B bf16, both K-major,
@@ -224,6 +223,43 @@ __device__ __forceinline__ void decode_half_block(const uint8_t* blk, int p, int
     }
 }
 
+// The activation pieces of four consecutive f32 values x (k = 4f .. 4f + 3 of
+// row r of a 128 x 64 tile): hi = bf16(a), lo = bf16(a - hi) (packed
+// conversions, lo = a - hi by one packed FMA, exact), stored as 8 bytes of row
+// r of the 128-byte swizzled K-major hi and lo tiles.  A non-finite piece
+// makes the entries that use it non-finite, and the epilogue recomputes those
+// element by element.
+__device__ __forceinline__ void split_store4(float4 x, int r, int f, uint8_t* tile_hi, uint8_t* tile_lo) {
+    const float2 v[2] = {make_float2(x.x, x.y), make_float2(x.z, x.w)};
+    uint32_t hw[2], lw[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(v[e].x, v[e].y);
+        hw[e] = *reinterpret_cast<const uint32_t*>(&hb);
+        const float2 rest = __ffma2_rn(make_float2(__uint_as_float(hw[e] << 16), __uint_as_float(hw[e] & 0xFFFF0000u)),
+                                       make_float2(-1.0f, -1.0f), v[e]);
+        const __nv_bfloat162 lb = __floats2bfloat162_rn(rest.x, rest.y);
+        lw[e] = *reinterpret_cast<const uint32_t*>(&lb);
+    }
+    const int off = r * 128 + ((((f >> 1) ^ (r & 7))) << 4) + (f & 1) * 8;
+    *reinterpret_cast<uint2*>(tile_hi + off) = make_uint2(hw[0], hw[1]);
+    *reinterpret_cast<uint2*>(tile_lo + off) = make_uint2(lw[0], lw[1]);
+}
+
+// Named barrier over `threads` threads that also ANDs their `v`.
+__device__ __forceinline__ bool named_barrier_and(int id, int threads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(threads)
+        : "memory");
+    return r != 0;
+}
+
 // Exact C[m][n] for an entry whose tensor-core sum is not finite:
 // sum_k A[m][k] * ((q - 8) * d) element by element.
 __device__ __noinline__ float entry_exact(const float* __restrict__ A, const uint8_t* __restrict__ wq,
@@ -247,13 +283,11 @@ __device__ __noinline__ float entry_exact(const float* __restrict__ A, const uin
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_ahi,
-                 const __grid_constant__ CUtensorMap map_alo,
+    gemm_q4_0_tc(const __grid_constant__ CUtensorMap map_a,
                  const __grid_constant__ CUtensorMap map_w,
                  const __grid_constant__ CUtensorMap map_w2, const float* __restrict__ A,
                  const uint8_t* __restrict__ wq, float* __restrict__ C, int M, int N, int K,
-                 int c_vec, int tw, int nt, int n_full, int s_rem, int hw, int cl, float* __restrict__ partial,
-                 unsigned* __restrict__ ctr) {
+                 int c_vec, int tw, int nt, int n_full, int s_rem, int hw) {
     using T = Tile<BN>;
     constexpr int kAStages = T::kAStages;
     constexpr int kWStages = T::kWStages;
@@ -264,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment for the swizzled tiles, by indexing the shared array
     // itself so the compiler keeps every access below in the shared space.
     uint8_t* base = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t* a_st = base;                                // [kAStages][hi, lo][16 KB]
+    uint8_t* a_st = base;                                // [kAStages][f32 tile | hi, lo][32 KB]
     uint8_t* w_st = a_st + kAStages * 2 * kTileA;        // [kWStages][hi, lo][BN rows][128 B]
     uint8_t* raw = w_st + kWStages * 2 * kTileW;         // [kRawStages][BN rows][48 B]
     uint64_t* bars = reinterpret_cast<uint64_t*>(raw + kRawStages * kRawBytes);
@@ -274,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* w_empty = w_full + kWStages;
     uint64_t* raw_full = w_empty + kWStages;
     uint64_t* raw_empty = raw_full + kRawStages;
-    uint64_t* acc_full = raw_empty + kRawStages;
+    uint64_t* a_conv = raw_empty + kRawStages;  // [kAStages] activation pieces written
+    uint64_t* acc_full = a_conv + kAStages;
     uint64_t* red_bar = acc_full + 1;  // [2]: partial tiles written, partial tiles read
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_bar + 2);
 
@@ -295,12 +330,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n0 = (tile % nt) * tw + (half_item ? ((b - n_full) & 1) * (BN / 2) : 0);
     const int KT = K / BK / S;  // k-steps of this CTA's K range
     const int kt0 = split * KT;
+    const int cl = S > 1;       // a K split adds up through the cluster
 
     grid_launch_dependents();
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAStages; ++s) {
             mbar_init(&a_full[s], 1);
             mbar_init(&a_empty[s], 1);
+            mbar_init(&a_conv[s], kDecodeWarps);
         }
         for (int s = 0; s < kWStages; ++s) {
             mbar_init(&w_full[s], kDecodeWarps);
@@ -311,8 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&raw_empty[s], kDecodeWarps);
         }
         mbar_init(acc_full, 1);
-        mbar_init(&red_bar[0], cl ? s_rem : 1);  // one arrival per CTA of the cluster
-        mbar_init(&red_bar[1], cl ? s_rem : 1);
+        mbar_init(&red_bar[0], S);  // one arrival per CTA of the cluster
+        mbar_init(&red_bar[1], S);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -330,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // can arrive on them remotely.
     if (cl) cluster_sync_all();
     const uint32_t tmem = *tmem_slot;
-    grid_dependency_wait();  // A's pieces come from the split kernel before this one
+    grid_dependency_wait();  // A and C may belong to the kernel before this one
 
     if (warp == 0) {
         if (lane == 0) {
@@ -338,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // k-step.  The step's block pair is bytes 36 j .. 36 j + 35 of each
             // row (j = k-step); the 48-byte box starts at the 16-byte boundary
             // below it, which TMA requires, and still covers the pair.
-            prefetch_tensormap(&map_ahi);
-            prefetch_tensormap(&map_alo);
+            prefetch_tensormap(&map_a);
             const CUtensorMap* mw = half_item ? &map_w2 : &map_w;
             prefetch_tensormap(mw);
             for (int kt = 0; kt < KT; ++kt) {
@@ -354,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (kt >= kAStages &&
                     !mbar_wait_bounded(&a_empty[as], ((kt / kAStages) - 1) & 1, &g_gemm_error))
                     break;
+                // The f32 tile (128 rows x 256 B) fills the stage's hi and lo space.
                 mbar_arrive_expect_tx(&a_full[as], 2 * kTileA);
-                tma_load_2d(a_st + (2 * as) * kTileA, &map_ahi, (kt0 + kt) * BK, m0, &a_full[as]);
-                tma_load_2d(a_st + (2 * as + 1) * kTileA, &map_alo, (kt0 + kt) * BK, m0, &a_full[as]);
+                tma_load_2d(a_st + (2 * as) * kTileA, &map_a, (kt0 + kt) * BK, m0, &a_full[as]);
             }
         }
     } else if (warp == 1) {
@@ -370,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kt = 0; kt < KT && ok; ++kt) {
                 const int as = kt % kAStages;
                 const int ws = kt % kWStages;
-                ok = mbar_wait_bounded(&a_full[as], (kt / kAStages) & 1, &g_gemm_error) &&
+                ok = mbar_wait_bounded(&a_conv[as], (kt / kAStages) & 1, &g_gemm_error) &&
                      mbar_wait_bounded(&w_full[ws], (kt / kWStages) & 1, &g_gemm_error);
                 if (!ok) break;
                 tc_fence_after();
@@ -405,28 +441,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int dt = threadIdx.x - 64;
         const int n = dt / tpr;
         const int half = (tpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
-        bool ok = true;
-        for (int kt = 0; kt < KT && ok; ++kt) {
+        for (int kt = 0; kt < KT; ++kt) {
             const int rs = kt % kRawStages;
             const int ws = kt % kWStages;
-            ok = mbar_wait_bounded(&raw_full[rs], (kt / kRawStages) & 1, &g_gemm_error);
+            const int as = kt % kAStages;
+            bool ok = mbar_wait_bounded(&raw_full[rs], (kt / kRawStages) & 1, &g_gemm_error);
             if (ok && kt >= kWStages)
                 ok = mbar_wait_bounded(&w_empty[ws], ((kt / kWStages) - 1) & 1, &g_gemm_error);
-            if (!ok) break;
-            const uint8_t* blk =
-                raw + rs * kRawBytes + n * kRawRow + ((36 * (kt0 + kt)) & 15) + half * kBlockBytes;
-            uint8_t* thi = w_st + (2 * ws) * kTileW;
-            if (tpr == 2) {
-                decode_half_block(blk, 0, n, half, thi, thi + kTileW);
-                decode_half_block(blk, 1, n, half, thi, thi + kTileW);
-            } else if (n < wn) {  // rows past a 112-column tile are not decoded
-                decode_half_block(blk, dt & 1, n, half, thi, thi + kTileW);
+            if (ok) ok = mbar_wait_bounded(&a_full[as], (kt / kAStages) & 1, &g_gemm_error);
+            uint8_t* ast = a_st + (2 * as) * kTileA;
+            float4 x[4];
+            if (ok) {
+                const uint8_t* blk =
+                    raw + rs * kRawBytes + n * kRawRow + ((36 * (kt0 + kt)) & 15) + half * kBlockBytes;
+                uint8_t* thi = w_st + (2 * ws) * kTileW;
+                if (tpr == 2) {
+                    decode_half_block(blk, 0, n, half, thi, thi + kTileW);
+                    decode_half_block(blk, 1, n, half, thi, thi + kTileW);
+                } else if (n < wn) {  // rows past a 112-column tile are not decoded
+                    decode_half_block(blk, dt & 1, n, half, thi, thi + kTileW);
+                }
+                // This thread's 16 floats of the f32 activation tile: float4
+                // j * 512 + dt, i.e. row 32 j + dt / 16, k = 4 (dt % 16) .. + 3
+                // (each quarter warp reads 128 contiguous bytes).
+#pragma unroll
+                for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(ast + (j * 512 + dt) * 16);
             }
+            // Every thread has read its floats before any piece overwrites
+            // them; a failed wait anywhere stops all decode warps together.
+            if (!named_barrier_and(2, kDecodeWarps * 32, ok)) break;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) split_store4(x[j], 32 * j + (dt >> 4), dt & 15, ast, ast + kTileA);
             fence_proxy_async_shared();  // make the tiles visible to the tensor cores
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&w_full[ws]);
                 mbar_arrive(&raw_empty[rs]);
+                mbar_arrive(&a_conv[as]);
             }
         }
         // Epilogue: TMEM lane quarter q = warp % 4; warp (q, cq) owns rows
@@ -447,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* stg = reinterpret_cast<float*>(a_st) + (warp - 2) * (32 * 36);
         const int cw = wn / 4;              // columns of this warp (28, 32, 64)
         const int ncb = (cw + 31) / 32;     // 32-column blocks of this warp
-        if (S > 1 && cl) {
+        if (cl) {
             // Split K through the cluster (the S CTAs of this tile, ranks in
             // range order): each CTA leaves its partial tile in its own shared
             // memory, [128 rows][wn + 4] f32, then adds rows r 128/S ..
@@ -539,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             __syncwarp();
             const int nn = n0 + col + lane;  // this lane's column in the row-wise passes
-            if (S == 1) {
+            {
                 if (!acc_ok) continue;
                 // Entries that came out non-finite: recompute element by element.
 #pragma unroll
@@ -565,57 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             C[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
                     }
                 }
-            } else {
-                // Split K: the partial block to the workspace [S][M][N].
-                float* pw = partial + static_cast<int64_t>(split) * M * N;
-                for (int row = 0; row < 32; ++row) {
-                    if (mrow + row < M && nn < N && lane < valid)
-                        pw[static_cast<int64_t>(mrow + row) * N + nn] = stg[row * 36 + lane];
-                }
             }
         }
-        if (S > 1) {
-            // Every decode warp reaches both barriers, whatever its waits returned.
-            __threadfence();
-            named_barrier_sync(1, kDecodeWarps * 32);
-            uint32_t* last = tmem_slot + 1;  // CTA-local broadcast of the arrival
-            if (threadIdx.x == 64) {
-                const unsigned old = atomicAdd(&ctr[tile], 1u);
-                *last = (old == static_cast<unsigned>(S - 1)) ? 1u : 0u;
-            }
-            named_barrier_sync(1, kDecodeWarps * 32);
-            if (*last != 0) {
-                // The last of the tile's S CTAs: add the partials in range
-                // order, 8 rows at a time so that 8 * S loads are in flight
-                // together (one row at a time would serialise 32 L2 round trips).
-                __threadfence();
-                for (int jb = 0; jb < ncb; ++jb) {
-                    const int nn = (lane < min(32, cw - 32 * jb)) ? n0 + cw * cq + 32 * jb + lane : N;
-                    for (int r0 = 0; r0 < 32; r0 += 8) {
-                        float x[8];
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr) x[rr] = 0.f;
-                        for (int q2 = 0; q2 < S; ++q2) {
-                            const float* pq = partial + static_cast<int64_t>(q2) * M * N;
-#pragma unroll
-                            for (int rr = 0; rr < 8; ++rr) {
-                                const int m = mrow + r0 + rr;
-                                if (m < M && nn < N) x[rr] += __ldcg(pq + static_cast<int64_t>(m) * N + nn);
-                            }
-                        }
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr) {
-                            const int m = mrow + r0 + rr;
-                            if (m >= M || nn >= N) continue;
-                            float v = x[rr];
-                            if (!isfinite(v)) v = entry_exact(A, wq, K, m, nn);
-                            C[static_cast<int64_t>(m) * N + nn] = v;
-                        }
-                    }
-                }
-            }
-        }
-        }  // global split-K path
+        }  // whole tiles
     }
 
     tc_fence_before();
@@ -625,39 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(T::kTmemCols)
                      : "memory");
-    }
-}
-
-// A f32 -> bf16 hi = bf16(a), lo = bf16(a - hi).
-// Also zeroes the split-K arrival counters of the GEMM that follows.
-__global__ void __launch_bounds__(256)
-    split_bf16(const float4* __restrict__ a, uint2* __restrict__ hi, uint2* __restrict__ lo,
-               int64_t n4, unsigned* __restrict__ ctr, int n_ctr) {
-    grid_launch_dependents();
-    grid_dependency_wait();  // the workspace may still be in use by an earlier GEMM
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0u;
-    }
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float4 v = __ldg(a + i);
-        const float2 x[2] = {make_float2(v.x, v.y), make_float2(v.z, v.w)};
-        uint32_t hw[2], lw[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            // Packed conversions (two values per instruction); lo = x - hi by
-            // one packed FMA, exact.  A non-finite piece makes the entries
-            // that use it non-finite, and the GEMM recomputes those exactly.
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(x[e].x, x[e].y);
-            hw[e] = *reinterpret_cast<const uint32_t*>(&hb);
-            const float2 r = __ffma2_rn(make_float2(__uint_as_float(hw[e] << 16),
-                                                    __uint_as_float(hw[e] & 0xFFFF0000u)),
-                                        make_float2(-1.0f, -1.0f), x[e]);
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(r.x, r.y);
-            lw[e] = *reinterpret_cast<const uint32_t*>(&lb);
-        }
-        hi[i] = make_uint2(hw[0], hw[1]);
-        lo[i] = make_uint2(lw[0], lw[1]);
     }
 }
 
@@ -690,51 +660,64 @@ int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
 // can; the tiles of the last, partial wave (all tiles when there are fewer
 // than SMs) are split so that the last wave is not left mostly idle:
 // 256-column tiles after a full wave into two 128-column halves when those fit
-// the SMs (no partial sums to add), otherwise into s_rem K ranges of whole
-// 256-wide units, as many as fit the SMs.
+// the SMs (no partial sums to add), otherwise into s_rem = 2, 4 or 8 K ranges
+// of whole 256-wide units, the most that fit the SMs, where the split tiles'
+// clusters of s_rem CTAs can all be resident at once (fit[0..2] clusters of
+// 2, 4 and 8) and the whole tiles before them come in whole clusters (a
+// split adds up through its cluster); else the last wave stays whole.
 struct GemmItems {
     int64_t nt, tiles, rem, n_full, items;
     int s_rem, hw;
 };
 
-GemmItems plan_gemm_items(int bn, int64_t M, int64_t N, int64_t K, int64_t P) {
+GemmItems plan_gemm_items(int bn, int64_t M, int64_t N, int64_t K, int64_t P, const int fit[3]) {
     GemmItems g;
     g.nt = (N + bn - 1) / bn;
     g.tiles = g.nt * ((M + BM - 1) / BM);
     g.rem = g.tiles % P;
     g.hw = (bn == 256 && g.tiles >= P && g.rem > 0 && 2 * g.rem <= P) ? 1 : 0;
     g.s_rem = 1;
-    for (int c = 2; c <= 16 && !g.hw; ++c) {
-        if ((K / 256) % c == 0 && g.rem * c <= P) g.s_rem = c;
+    for (int i = 0; i < 3 && !g.hw && g.rem > 0; ++i) {
+        const int c = 2 << i;
+        if ((K / 256) % c == 0 && g.rem * c <= P && (g.tiles - g.rem) % c == 0 && fit[i] >= g.rem)
+            g.s_rem = c;
     }
     g.n_full = (g.s_rem > 1 || g.hw) ? g.tiles - g.rem : g.tiles;
     g.items = g.n_full + (g.tiles - g.n_full) * (g.hw ? 2 : g.s_rem);
     return g;
 }
 
-// A tile split over K is added up through a cluster of its s_rem CTAs
-// (distributed shared memory) when s_rem is 2, 4 or 8, whole tiles come in
-// whole clusters, and all of the split tiles' clusters fit on the GPU at once
-// (`fit` resident clusters of s_rem CTAs); otherwise through the workspace by
-// the last CTA to arrive.
-bool cluster_split(const GemmItems& g, int fit) {
-    return (g.s_rem == 2 || g.s_rem == 4 || g.s_rem == 8) && g.n_full % g.s_rem == 0 && fit >= g.rem;
-}
-
 // 112-column tiles (with the 128-column kernel) where 128-column tiles leave
 // SMs idle, need no K split, and 112-column ones fill more SMs, still without
 // a split: 512 x 4096 makes 148 tiles of 112 against 128 tiles of 128 on 152
 // SMs, each with 12.5% less work.
-bool narrow_tiles(int64_t M, int64_t N, int64_t K, int64_t P) {
-    const GemmItems g128 = plan_gemm_items(128, M, N, K, P);
-    const GemmItems g112 = plan_gemm_items(112, M, N, K, P);
+bool narrow_tiles(int64_t M, int64_t N, int64_t K, int64_t P, const int fit[3]) {
+    const GemmItems g128 = plan_gemm_items(128, M, N, K, P, fit);
+    const GemmItems g112 = plan_gemm_items(112, M, N, K, P, fit);
     return g128.tiles < P && g128.s_rem == 1 && g112.s_rem == 1 && g112.tiles <= P &&
            g112.tiles > g128.tiles;
 }
 
+// Resident clusters of 2, 4 and 8 CTAs of the BN kernel, queried once per
+// device.
 template <int BN>
-cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
-                      cudaStream_t stream, const DeviceInfo& dev, int tw) {
+cudaError_t gemm_cluster_fits(const DeviceInfo& dev, int fit[3]) {
+    static int cached[64][3] = {};  // 0: not queried; else 1 + the count
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    for (int i = 0; i < 3; ++i) {
+        int f = __atomic_load_n(&cached[dev.device][i], __ATOMIC_ACQUIRE);
+        if (f == 0) {
+            f = 1 + max_active_clusters(gemm_q4_0_tc<BN>, dim3(kThreads), Tile<BN>::kSmemBytes, 2u << i);
+            __atomic_store_n(&cached[dev.device][i], f, __ATOMIC_RELEASE);
+        }
+        fit[i] = f - 1;
+    }
+    return cudaSuccess;
+}
+
+// Shared-memory attribute of the BN kernel, set once per device.
+template <int BN>
+cudaError_t ensure_gemm_smem_attr(const DeviceInfo& dev) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
@@ -743,53 +726,22 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
         if (e != cudaSuccess) return e;
         __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
     }
-    const GemmItems g = plan_gemm_items(tw, M, N, K, dev.sm_count);
-    const int64_t nt = g.nt, tiles = g.tiles, n_full = g.n_full, items = g.items;
-    const int s_rem = g.s_rem, hw = g.hw;
-    int cl = 0;
-    if ((s_rem == 2 || s_rem == 4 || s_rem == 8) && n_full % s_rem == 0) {
-        // Resident clusters per device and size, queried once.
-        static int fit[64][4] = {};  // 0: not queried; else 1 + the count
-        const int si = s_rem == 2 ? 1 : s_rem == 4 ? 2 : 3;
-        int f = __atomic_load_n(&fit[dev.device][si], __ATOMIC_ACQUIRE);
-        if (f == 0) {
-            f = 1 + max_active_clusters(gemm_q4_0_tc<BN>, dim3(kThreads), Tile<BN>::kSmemBytes,
-                                        static_cast<unsigned>(s_rem));
-            __atomic_store_n(&fit[dev.device][si], f, __ATOMIC_RELEASE);
-        }
-        cl = cluster_split(g, f - 1) ? 1 : 0;
-    }
-    // Workspace: bf16 hi / lo copies of A, then (tiles split through the
-    // workspace) the partial tiles [s_rem][M][N] and one arrival counter per
-    // tile.
-    const bool ws_split = s_rem > 1 && !cl;
-    const size_t piece_bytes = static_cast<size_t>(M) * K * 2;
-    const size_t part_bytes = ws_split ? static_cast<size_t>(s_rem) * M * N * 4 : 0;
-    const size_t ctr_bytes = ws_split ? static_cast<size_t>(tiles) * 4 : 0;
-    void* ws = nullptr;
-    cudaError_t err = prefill_workspace(dev, stream, 2 * piece_bytes + part_bytes + ctr_bytes, &ws);
-    if (err != cudaSuccess) return err;
-    auto* a_hi = static_cast<uint8_t*>(ws);
-    auto* a_lo = a_hi + piece_bytes;
-    float* part = reinterpret_cast<float*>(a_lo + piece_bytes);
-    unsigned* ctr = reinterpret_cast<unsigned*>(reinterpret_cast<uint8_t*>(part) + part_bytes);
-    const int64_t n4 = M * K / 4;
-    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, static_cast<int64_t>(dev.sm_count) * 8);
-    err = launch_pdl(split_bf16, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
-                     reinterpret_cast<const float4*>(A), reinterpret_cast<uint2*>(a_hi),
-                     reinterpret_cast<uint2*>(a_lo), n4, ctr, static_cast<int>(ws_split ? tiles : 0));
-    if (err != cudaSuccess) return err;
-    note_launch();
+    return cudaSuccess;
+}
 
-    CUtensorMap map_ahi, map_alo, map_w, map_w2;
+template <int BN>
+cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t stream, const DeviceInfo& dev, int tw, const int fit[3]) {
+    const GemmItems g = plan_gemm_items(tw, M, N, K, dev.sm_count, fit);
+    const int64_t nt = g.nt, n_full = g.n_full, items = g.items;
+    const int s_rem = g.s_rem, hw = g.hw;
+
+    CUtensorMap map_a, map_w, map_w2;
+    // Activations as f32 [M][K]; boxes of 128 rows x 64 k (256-byte rows).
     const int64_t adims[2] = {K, M};
-    const int64_t astrides[1] = {K * 2};
+    const int64_t astrides[1] = {K * 4};
     const int abox[2] = {BK, BM};
-    err = encode_tiled(&map_ahi, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a_hi, 2, adims, astrides, abox,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-    if (err != cudaSuccess) return err;
-    err = encode_tiled(&map_alo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a_lo, 2, adims, astrides, abox,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    cudaError_t err = encode_tiled(&map_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
     if (err != cudaSuccess) return err;
     // Weights as bytes [N rows][K/32 * 18 B] (a row is a multiple of 144 B,
     // so of 16 B); boxes of BN rows x 48 B, bytes past a row's end read as 0.
@@ -804,17 +756,17 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
     if (err != cudaSuccess) return err;
 
     const int c_vec = ((reinterpret_cast<uintptr_t>(C) & 15u) == 0 && (N % 4) == 0) ? 1 : 0;
-    if (cl) {
+    if (s_rem > 1) {
         err = launch_pdl_cluster(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
-                                 Tile<BN>::kSmemBytes, stream, static_cast<unsigned>(s_rem), map_ahi,
-                                 map_alo, map_w, map_w2, A, wq, C, static_cast<int>(M),
-                                 static_cast<int>(N), static_cast<int>(K), c_vec, tw, static_cast<int>(nt),
-                                 static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
+                                 Tile<BN>::kSmemBytes, stream, static_cast<unsigned>(s_rem), map_a, map_w,
+                                 map_w2, A, wq, C, static_cast<int>(M), static_cast<int>(N),
+                                 static_cast<int>(K), c_vec, tw, static_cast<int>(nt),
+                                 static_cast<int>(n_full), s_rem, hw);
     } else {
         err = launch_pdl(gemm_q4_0_tc<BN>, dim3(static_cast<unsigned>(items)), dim3(kThreads),
-                         Tile<BN>::kSmemBytes, stream, map_ahi, map_alo, map_w, map_w2, A, wq, C,
-                         static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), c_vec, tw,
-                         static_cast<int>(nt), static_cast<int>(n_full), s_rem, hw, cl, part, ctr);
+                         Tile<BN>::kSmemBytes, stream, map_a, map_w, map_w2, A, wq, C, static_cast<int>(M),
+                         static_cast<int>(N), static_cast<int>(K), c_vec, tw, static_cast<int>(nt),
+                         static_cast<int>(n_full), s_rem, hw);
     }
     if (err != cudaSuccess) return err;
     note_launch();
@@ -825,18 +777,26 @@ cudaError_t launch_bn(const float* A, const uint8_t* wq, float* C, int64_t M, in
 
 cudaError_t launch_gemm_q4_0_tc(const float* A, const uint8_t* wq, float* C, int64_t M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev) {
-    if (choose_bn(M, N, K, dev) == 256) return launch_bn<256>(A, wq, C, M, N, K, stream, dev, 256);
-    return launch_bn<128>(A, wq, C, M, N, K, stream, dev,
-                          narrow_tiles(M, N, K, dev.sm_count) ? 112 : 128);
+    int fit[3] = {0, 0, 0};
+    if (choose_bn(M, N, K, dev) == 256) {
+        cudaError_t err = ensure_gemm_smem_attr<256>(dev);
+        if (err == cudaSuccess) err = gemm_cluster_fits<256>(dev, fit);
+        if (err != cudaSuccess) return err;
+        return launch_bn<256>(A, wq, C, M, N, K, stream, dev, 256, fit);
+    }
+    cudaError_t err = ensure_gemm_smem_attr<128>(dev);
+    if (err == cudaSuccess) err = gemm_cluster_fits<128>(dev, fit);
+    if (err != cudaSuccess) return err;
+    return launch_bn<128>(A, wq, C, M, N, K, stream, dev, narrow_tiles(M, N, K, dev.sm_count, fit) ? 112 : 128,
+                          fit);
 }
 
 void gemm_tc_plan_query(int64_t M, int64_t N, int64_t K, int sm_count, const int fit[3], int64_t out[8]) {
     const DeviceInfo dev{0, sm_count, 0};
     int bn = choose_bn(M, N, K, dev);
-    if (bn == 128 && narrow_tiles(M, N, K, sm_count)) bn = 112;
-    const GemmItems g = plan_gemm_items(bn, M, N, K, sm_count);
-    const int f = g.s_rem == 2 ? fit[0] : g.s_rem == 4 ? fit[1] : g.s_rem == 8 ? fit[2] : 0;
-    const int64_t v[8] = {bn, g.nt, g.tiles, g.n_full, g.s_rem, g.hw, g.items, cluster_split(g, f) ? 1 : 0};
+    if (bn == 128 && narrow_tiles(M, N, K, sm_count, fit)) bn = 112;
+    const GemmItems g = plan_gemm_items(bn, M, N, K, sm_count, fit);
+    const int64_t v[8] = {bn, g.nt, g.tiles, g.n_full, g.s_rem, g.hw, g.items, g.s_rem > 1 ? 1 : 0};
     for (int i = 0; i < 8; ++i) out[i] = v[i];
 }
 

@@ -25,9 +25,11 @@
 //     subtraction, all exact; 32 products are summed per block and scaled
 //     once by d (element by element when d is not finite).
 //   * Partial sums of a row group meet in shared memory (fixed warp order).
-//     When K is split (S > 1) each CTA writes its row groups' partials to a
-//     workspace and the last of the S CTAs to arrive at a row group adds them
-//     in split order and writes C, so results do not depend on timing.
+//     When K is split (S > 1: only with scratch memory, which the regular
+//     entry point does not give this kernel) each CTA writes its row groups'
+//     partials to the scratch and the last of the S CTAs to arrive at a row
+//     group adds them in split order and writes C, so results do not depend
+//     on timing.
 // Generic kernel (any K % 32 == 0, 2-byte aligned wq, 4-byte aligned A): one
 // warp per row, lanes striding over blocks, shuffle reduction.
 #include <algorithm>
@@ -589,14 +591,14 @@ template <int M>
 cudaError_t launch_m(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
                      cudaStream_t stream, const DeviceInfo& dev, GemvKind kind) {
     if (persistent_ok(A, wq, N, K)) {
-        Workspace ws;
-        cudaError_t err = stream_workspace(dev, stream, &ws);
-        if (err != cudaSuccess) return err;
+        // No scratch: the FP32 FMA kernel then takes whole K ranges, and the
+        // staged GEMV adds a split K up through thread-block clusters.
+        const Workspace none;
         bool launched = false;
-        err = kind == GemvKind::kSimt
-                  ? launch_persistent<M>(A, wq, C, N, K, stream, dev, ws, false, &launched)
-                  : launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws,
-                                        kind == GemvKind::kPacked, false, &launched);
+        cudaError_t err = kind == GemvKind::kSimt
+                              ? launch_persistent<M>(A, wq, C, N, K, stream, dev, none, false, &launched)
+                              : launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, nullptr,
+                                                    kind == GemvKind::kPacked, false, &launched);
         if (err != cudaSuccess || launched) return err;
     }
     return launch_generic<M>(A, wq, C, N, K, stream, dev);
@@ -636,12 +638,12 @@ cudaError_t gemv_read_device_error(unsigned int* bits, bool clear) {
 // cudaMalloc: code that runs where the CUDA allocator is off limits (inside a
 // custom allocator or memory-pool callback, under a process-wide memory cap,
 // or in a runtime that owns all device memory and forbids stray allocations).
-// For them the split-K GEMV takes its scratch from this fixed array instead of
-// a per-stream workspace.  Every GPU that loads the library holds the array
+// For them the split-K GEMV takes its scratch from this fixed array.  (The
+// regular entry point allocates nothing either: it adds split K ranges up
+// through thread-block clusters.  This entry point keeps its own split, which
+// needs no cluster launch.)  Every GPU that loads the library holds the array
 // until the process exits; all calls share it.
-constexpr size_t kStaticPartFloats = size_t(256) * 1024;  // 1 MB of split partial sums
-constexpr int kStaticCounters = 4096;                      // row groups with a split K
-static __device__ __align__(256) float g_noalloc_scratch[kStaticPartFloats + kStaticCounters];
+static __device__ __align__(256) float g_noalloc_scratch[kNoallocPartFloats + kNoallocCounters];
 
 namespace {
 
@@ -683,9 +685,9 @@ cudaError_t noalloc_workspace(const DeviceInfo& dev, Workspace* out) {
     }
     float* base = static_cast<float*>(g_noalloc_addr[dev.device]);
     out->part = base;
-    out->part_floats = kStaticPartFloats;
-    out->ctr = reinterpret_cast<unsigned*>(base + kStaticPartFloats);
-    out->ctr_count = kStaticCounters;
+    out->part_floats = kNoallocPartFloats;
+    out->ctr = reinterpret_cast<unsigned*>(base + kNoallocPartFloats);
+    out->ctr_count = kNoallocCounters;
     return cudaSuccess;
 }
 
@@ -699,7 +701,7 @@ cudaError_t launch_m_noalloc(const float* A, const uint8_t* wq, float* C, int64_
         // The arrival counters must start at zero; the array keeps whatever
         // the previous call (or an abandoned one) left, so clear them first.
         bool launched = false;
-        err = launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, ws,
+        err = launch_gemv_q4_0_tc(A, wq, C, M, N, K, stream, dev, &ws,
                                   gemv_auto_kind(M, N, K) == GemvKind::kPacked, true, &launched);
         if (err != cudaSuccess || launched) return err;
     }

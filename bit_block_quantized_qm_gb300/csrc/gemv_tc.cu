@@ -46,9 +46,14 @@
 // return stale data); every read of A or the weights into the SM, and every
 // write, comes after griddepcontrol.wait.
 //
-// Split K.  With S > 1 ranges a row group's partial sums go to a workspace;
-// the last of the S CTAs to arrive adds them in range order and writes C, so
-// results do not depend on timing.  Counters are left at zero.
+// Split K.  With S > 1 ranges (S = 2, 4 or 8) the S CTAs of a row-block range
+// form a thread-block cluster: each keeps its row groups' partial sums in its
+// own shared memory and, after a bounded mbarrier handshake, adds a share of
+// the row groups over all S CTAs in range order through distributed shared
+// memory and writes C, so results do not depend on timing and nothing is
+// written outside C.  The allocation-free entry point (qm_matmul_q4_0_noalloc)
+// instead meets the partial sums in its fixed scratch array, where the last of
+// the S CTAs to arrive adds them in range order; it leaves the counters at zero.
 #include <algorithm>
 #include <mutex>
 
@@ -88,8 +93,9 @@ struct TcPlan {
     int rbpc;       // row blocks per CTA
     int nu_max;     // units in the largest K range
     int stages;     // ring depth
-    float* part;    // [RG][S][M][16] split partial sums (S > 1)
-    unsigned* ctr;  // [RG] arrival counters (S > 1), zero between launches
+    int cl;         // 1: the S K ranges add up through a cluster (no scratch)
+    float* part;    // [RG][S][M][16] split partial sums (S > 1, cl = 0)
+    unsigned* ctr;  // [RG] arrival counters (S > 1, cl = 0), zero between launches
 };
 
 __device__ __forceinline__ uint32_t lds_u32(const uint8_t* p) {
@@ -436,15 +442,20 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
     extern __shared__ __align__(128) uint8_t smem[];
     // ring [stages][c boxes][kRows rps rows][144 B] | activations [nu_max][M KB]
     // (B fragments for the MMA consumer, f32 for the packed one) | partial-sum
-    // slots [2][W][kRows][8] f32 | full[stages] | empty[stages] | a_bar
+    // slots [2][W][kRows][8] f32 | the CTA's split partial sums [rbpc][rps]
+    // [M][kRows] f32 (cluster split only) | full[stages] | empty[stages] |
+    // a_bar | red_bar[2] (cluster split: partial sums written, partial sums
+    // read)
     const int box_bytes = p.rps * kRows * kUnitBytes;
     const int stage_bytes = p.c * box_bytes;
     uint8_t* ring = smem;
     uint8_t* frag = smem + p.stages * stage_bytes;
     float* slots = reinterpret_cast<float*>(frag + p.nu_max * M * 1024);
-    uint64_t* full = reinterpret_cast<uint64_t*>(slots + 2 * W * kSlot);
+    float* cpart = slots + 2 * W * kSlot;
+    uint64_t* full = reinterpret_cast<uint64_t*>(cpart + (p.cl ? p.rbpc * p.rps * M * kRows : 0));
     uint64_t* empty = full + p.stages;
     uint64_t* a_bar = empty + p.stages;
+    uint64_t* red_bar = a_bar + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -464,9 +475,14 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
             mbar_init(&empty[s], W);  // every consumer warp, once per stage
         }
         mbar_init(a_bar, 1);
+        mbar_init(&red_bar[0], p.S);  // one arrival per CTA of the cluster
+        mbar_init(&red_bar[1], p.S);
         fence_barrier_init();
     }
     __syncthreads();
+    // Cluster launches: every CTA's barriers are initialised before any CTA
+    // can arrive on them remotely.
+    if (p.cl) cluster_sync_all();
 
     if (warp == W) {
         if (lane == 0 && nst > 0) {
@@ -628,12 +644,51 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
                 for (int m = 0; m < M; ++m) C[static_cast<int64_t>(m) * p.N + row] = tot[m];
             }
         } else if (lane < kRows) {
-            float* part = p.part + (static_cast<int64_t>(rg) * p.S + split) * (M * kRows);
+            float* part = p.cl ? cpart + (rbi * p.rps + rgl) * (M * kRows)
+                               : p.part + (static_cast<int64_t>(rg) * p.S + split) * (M * kRows);
 #pragma unroll
             for (int m = 0; m < M; ++m) part[m * kRows + lane] = tot[m];
         }
     }
-    if (p.S == 1 || ul != 0 || h != 0) return;
+    if (p.S == 1) return;
+    if (p.cl) {
+        // Split K through the cluster (ranks in range order).  Every consumer
+        // warp comes here, whatever its waits returned, so the arrivals come
+        // on every path.  Row group i of the CTA's row blocks (i = rbi * rps +
+        // rgl) is added up by rank i % S, one warp per row group, over the S
+        // CTAs' partial sums in rank order.
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        named_barrier_sync(1, W * 32);
+        if (threadIdx.x == 0) {
+            for (int r = 0; r < p.S; ++r)
+                mbar_arrive_cluster(mapa_shared(smem_addr(&red_bar[0]), static_cast<uint32_t>(r)));
+        }
+        const uint32_t rank = cluster_ctarank();
+        if (mbar_wait_cluster_bounded(&red_bar[0], 0, &g_gemv_tc_error)) {
+            const uint32_t cbase = smem_addr(cpart);
+            for (int i = static_cast<int>(rank) + p.S * warp; i < nrb * p.rps; i += p.S * W) {
+                const int rg = rb0 * p.rps + i;
+                const int row = rg * kRows + lane;
+                if (rg >= p.RG || lane >= kRows || row >= p.N) continue;
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    const uint32_t off = static_cast<uint32_t>(((i * M + m) * kRows + lane) * 4);
+                    float v = 0.f;
+                    for (int r = 0; r < p.S; ++r) v += ld_dsmem_f32(mapa_shared(cbase + off, static_cast<uint32_t>(r)));
+                    C[static_cast<int64_t>(m) * p.N + row] = v;
+                }
+            }
+        }
+        // No CTA leaves while another may still read its partial sums.
+        named_barrier_sync(1, W * 32);
+        if (threadIdx.x == 0) {
+            for (int r = 0; r < p.S; ++r)
+                mbar_arrive_cluster(mapa_shared(smem_addr(&red_bar[1]), static_cast<uint32_t>(r)));
+        }
+        mbar_wait_cluster_bounded(&red_bar[1], 0, &g_gemv_tc_error);
+        return;
+    }
+    if (ul != 0 || h != 0) return;
 
     // Split K: one fence for all of this warp's partial sums, then its
     // arrivals; the last of the S arrivals at a row group adds the partials
@@ -665,12 +720,17 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
     }
 }
 
-// Shared memory of one CTA: W consumer warps, stages of `tiles` tiles.
-int64_t tc_smem_bytes(int M, bool packed, int W, int tiles, int stages, int nu_max) {
+// Shared memory of one CTA: W consumer warps, stages of `tiles` tiles,
+// cpart floats of split partial sums (cluster split).
+int64_t tc_smem_bytes(int M, bool packed, int W, int tiles, int stages, int nu_max, int64_t cpart) {
     return static_cast<int64_t>(stages) * tiles * group_rows(packed) * kUnitBytes +
-           static_cast<int64_t>(nu_max) * M * 1024 + 2LL * W * slot_floats(packed) * 4 +
-           (2LL * stages + 1) * 8;
+           static_cast<int64_t>(nu_max) * M * 1024 + 2LL * W * slot_floats(packed) * 4 + cpart * 4 +
+           (2LL * stages + 3) * 8;
 }
+
+// Largest cluster split's partial sums in one CTA (floats): keeps the ring
+// deep where a split is worth taking.
+constexpr int64_t kMaxClusterPartFloats = 8192;
 
 // Relative rate of one SM with W consumer warps (more warps hide more of the
 // shared-memory, barrier and arithmetic latency; past 16 measured no gain).
@@ -679,7 +739,10 @@ double warp_efficiency(int W) {
 }
 
 // Best stage shape with hs warps a tile (rps row groups x c units, W = rps c
-// hs consumer warps) and S (K ranges) for one CTA per SM.  The cost is the
+// hs consumer warps) and S (K ranges) for one CTA per SM.  The K ranges add
+// up through a cluster when `fit` is given (S = 2, 4 or 8; fit[0..2] clusters
+// of 2, 4 and 8 CTAs can be resident at once, and the split's clusters must
+// all be), otherwise through the scratch `ws`.  The cost is the
 // largest per-CTA tile count (idle tile slots included) over the warp
 // efficiency, with charges for split-K partial sums (their bytes against the
 // weight bytes, plus a little per split), for short K ranges (a CTA that reads
@@ -687,7 +750,7 @@ double warp_efficiency(int W) {
 // shallow ring, and for cross-warp reductions at more than one row block per
 // CTA.  Returns the cost (infinite when nothing fits).
 double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const DeviceInfo& dev,
-                  const Workspace& ws, TcPlan* out, int* grid, int* smem) {
+                  const Workspace* ws, const int* fit, TcPlan* out, int* grid, int* smem) {
     const int kRows = group_rows(packed);
     const int U = static_cast<int>(K / kUnitElems);
     const int64_t RG = (N + kRows - 1) / kRows;
@@ -702,15 +765,23 @@ double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const Device
             if (rps * kRows > 256) continue;  // TMA box height
             const int64_t RB = (RG + rps - 1) / rps;
             for (int S = 1; S <= kMaxSplits && S <= U; ++S) {
-                if (S > 1 && (RG * S * M * kRows > static_cast<int64_t>(ws.part_floats) ||
-                              RG > static_cast<int64_t>(ws.ctr_count)))
+                const bool cl = S > 1 && fit != nullptr;
+                int64_t Gs = std::max(1, P / S);
+                if (cl) {
+                    if (S != 2 && S != 4 && S != 8) continue;
+                    Gs = std::min<int64_t>(Gs, fit[S == 2 ? 0 : S == 4 ? 1 : 2]);
+                    if (Gs < 1) continue;
+                } else if (S > 1 && (!ws || RG * S * M * kRows > static_cast<int64_t>(ws->part_floats) ||
+                                     RG > static_cast<int64_t>(ws->ctr_count))) {
                     continue;
+                }
                 const int nu_max = (U + S - 1) / S;
-                const int64_t Gs = std::max(1, P / S);
                 const int64_t rbpc = (RB + Gs - 1) / Gs;
                 const int64_t g_used = (RB + rbpc - 1) / rbpc;
                 const int64_t spr = (nu_max + c - 1) / c;
-                const int64_t fixed = tc_smem_bytes(M, packed, W, tiles, 0, nu_max);
+                const int64_t cpart = cl ? rbpc * rps * M * kRows : 0;
+                if (cpart > kMaxClusterPartFloats) continue;
+                const int64_t fixed = tc_smem_bytes(M, packed, W, tiles, 0, nu_max, cpart);
                 int stages = static_cast<int>(
                     (dev.max_smem_optin - fixed) /
                     (static_cast<int64_t>(tiles) * kRows * kUnitBytes + 16));
@@ -740,10 +811,11 @@ double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const Device
                     q.rbpc = static_cast<int>(rbpc);
                     q.nu_max = nu_max;
                     q.stages = stages;
-                    q.part = ws.part;
-                    q.ctr = ws.ctr;
+                    q.cl = cl ? 1 : 0;
+                    q.part = (S > 1 && !cl) ? ws->part : nullptr;
+                    q.ctr = (S > 1 && !cl) ? ws->ctr : nullptr;
                     *grid = static_cast<int>(g_used * S);
-                    *smem = static_cast<int>(tc_smem_bytes(M, packed, W, tiles, stages, nu_max));
+                    *smem = static_cast<int>(tc_smem_bytes(M, packed, W, tiles, stages, nu_max, cpart));
                 }
             }
         }
@@ -754,9 +826,9 @@ double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const Device
 // The launch plan: whole-unit tiles for the MMA consumer, half-unit warps
 // for the packed one (measured on GB300: half units lose with the MMA
 // consumer, and give the packed one twice the warps on the same stages).
-bool plan_tc(int M, bool packed, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace& ws,
-             TcPlan* out, int* grid, int* smem) {
-    return plan_tc_hs(M, packed, packed ? 2 : 1, N, K, dev, ws, out, grid, smem) < 1e300;
+bool plan_tc(int M, bool packed, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace* ws,
+             const int* fit, TcPlan* out, int* grid, int* smem) {
+    return plan_tc_hs(M, packed, packed ? 2 : 1, N, K, dev, ws, fit, out, grid, smem) < 1e300;
 }
 
 template <int M, bool kPk>
@@ -772,18 +844,42 @@ cudaError_t ensure_tc_smem_attr(const DeviceInfo& dev, int bytes) {
     return cudaSuccess;
 }
 
+// Resident clusters of 2, 4 and 8 CTAs of one kernel (one CTA per SM: the
+// count depends on how the SMs group, not on the launch's shared memory),
+// queried once per device.
+template <int M, bool kPk>
+cudaError_t cluster_fits(const DeviceInfo& dev, int fit[3]) {
+    static int cached[64][3] = {};  // 0: not queried; else 1 + the count
+    if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+    for (int i = 0; i < 3; ++i) {
+        int f = __atomic_load_n(&cached[dev.device][i], __ATOMIC_ACQUIRE);
+        if (f == 0) {
+            f = 1 + max_active_clusters(gemv_q4_0_tc<M, kPk>, dim3(max_threads(kPk)),
+                                        static_cast<size_t>(dev.max_smem_optin), 2u << i);
+            __atomic_store_n(&cached[dev.device][i], f, __ATOMIC_RELEASE);
+        }
+        fit[i] = f - 1;
+    }
+    return cudaSuccess;
+}
+
 template <int M, bool kPk>
 cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
-                      cudaStream_t stream, const DeviceInfo& dev, const Workspace& ws,
+                      cudaStream_t stream, const DeviceInfo& dev, const Workspace* ws,
                       bool clear_counters, bool* launched) {
     *launched = false;
+    cudaError_t err = ensure_tc_smem_attr<M, kPk>(dev, dev.max_smem_optin);
+    if (err != cudaSuccess) return err;
+    int fit[3] = {0, 0, 0};
+    if (!ws) {
+        err = cluster_fits<M, kPk>(dev, fit);
+        if (err != cudaSuccess) return err;
+    }
     TcPlan p;
     int grid = 0, smem = 0;
-    if (!plan_tc(M, kPk, N, K, dev, ws, &p, &grid, &smem)) return cudaSuccess;
+    if (!plan_tc(M, kPk, N, K, dev, ws, ws ? nullptr : fit, &p, &grid, &smem)) return cudaSuccess;
     p.wq = wq;
-    cudaError_t err = ensure_tc_smem_attr<M, kPk>(dev, smem);
-    if (err != cudaSuccess) return err;
-    if (clear_counters && p.S > 1) {
+    if (clear_counters && p.S > 1 && !p.cl) {
         err = cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(p.RG) * sizeof(unsigned), stream);
         if (err != cudaSuccess) return err;
     }
@@ -800,8 +896,13 @@ cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, in
     const int abox[2] = {kUnitElems, M};
     err = encode_tiled(&amap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, 2, adims, astrides, abox);
     if (err != cudaSuccess) return err;
-    err = launch_pdl(gemv_q4_0_tc<M, kPk>, dim3(grid), dim3((p.rps * p.c * p.hs + 1) * 32), smem,
-                     stream, wmap, amap, A, C, p);
+    const dim3 block((p.rps * p.c * p.hs + 1) * 32);
+    if (p.cl) {
+        err = launch_pdl_cluster(gemv_q4_0_tc<M, kPk>, dim3(grid), block, smem, stream,
+                                 static_cast<unsigned>(p.S), wmap, amap, A, C, p);
+    } else {
+        err = launch_pdl(gemv_q4_0_tc<M, kPk>, dim3(grid), block, smem, stream, wmap, amap, A, C, p);
+    }
     if (err != cudaSuccess) return err;
     note_launch();
     *launched = true;
@@ -812,7 +913,7 @@ cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, in
 
 cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                                const Workspace& ws, bool packed, bool clear_counters,
+                                const Workspace* ws, bool packed, bool clear_counters,
                                 bool* launched) {
     if (packed) {
         switch (M) {
@@ -835,7 +936,7 @@ cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
 }
 
 bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, int smem_optin,
-                        int64_t part_floats, int64_t ctr_count, int64_t out[12]) {
+                        const int* fit, int64_t part_floats, int64_t ctr_count, int64_t out[13]) {
     DeviceInfo dev;
     dev.device = 0;
     dev.sm_count = sm_count;
@@ -845,10 +946,10 @@ bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, 
     ws.ctr_count = static_cast<int>(std::min<int64_t>(ctr_count, 0x7FFFFFFF));
     TcPlan p;
     int grid = 0, smem = 0;
-    if (!plan_tc(M, packed, N, K, dev, ws, &p, &grid, &smem)) return false;
-    const int64_t v[12] = {p.RG, p.U, p.S, p.rps, p.c, p.hs, p.rbpc, p.nu_max, p.stages, grid, smem,
-                           static_cast<int64_t>(p.rps) * p.c * p.hs};
-    for (int i = 0; i < 12; ++i) out[i] = v[i];
+    if (!plan_tc(M, packed, N, K, dev, fit ? nullptr : &ws, fit, &p, &grid, &smem)) return false;
+    const int64_t v[13] = {p.RG, p.U, p.S, p.rps, p.c, p.hs, p.rbpc, p.nu_max, p.stages, grid, smem,
+                           static_cast<int64_t>(p.rps) * p.c * p.hs, p.cl};
+    for (int i = 0; i < 13; ++i) out[i] = v[i];
     return true;
 }
 

@@ -1,6 +1,9 @@
 // The C ABI of libqm (declared in include/qm.h): argument checks, algorithm
-// choice and launches on the caller's stream.  No allocation, no
-// synchronization (except qm_device_status), no host fallback.
+// choice and launches on the caller's stream.  No call allocates device or
+// host-pinned memory and none synchronizes with the device, except
+// qm_device_status, which waits for the stream it is given; there is no host
+// fallback.  What a call keeps between calls is host-side only: the device
+// properties and the kernels' shared-memory attributes, set once per device.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -21,100 +24,11 @@ DeviceInfo g_dev[kMaxDevices];
 int g_dev_ready[kMaxDevices] = {0};
 std::mutex g_dev_mutex;
 
-// Split-K workspaces, one per (device, stream).
-constexpr size_t kWorkspacePartFloats = size_t(2) << 20;  // 8 MB of partial sums
-constexpr int kWorkspaceCounters = 1 << 16;
-struct WorkspaceEntry {
-    int device;
-    cudaStream_t stream;
-    Workspace ws;
-};
-std::vector<WorkspaceEntry> g_workspaces;
-std::mutex g_ws_mutex;
-
-struct PrefillEntry {
-    int device;
-    cudaStream_t stream;
-    void* ptr;
-    size_t bytes;
-};
-std::vector<PrefillEntry> g_prefill;
-
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 uint64_t g_launches = 0;
 std::once_flag g_encode_once;
 
 }  // namespace
-
-cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* out) {
-    std::lock_guard<std::mutex> lock(g_ws_mutex);
-    for (const WorkspaceEntry& e : g_workspaces) {
-        if (e.device == dev.device && e.stream == stream) {
-            *out = e.ws;
-            return cudaSuccess;
-        }
-    }
-    Workspace ws;
-    const size_t bytes = kWorkspacePartFloats * sizeof(float) + kWorkspaceCounters * sizeof(unsigned);
-    void* p = nullptr;
-    cudaError_t err = cudaMalloc(&p, bytes);
-    if (err != cudaSuccess) return err;
-    ws.part = static_cast<float*>(p);
-    ws.ctr = reinterpret_cast<unsigned*>(ws.part + kWorkspacePartFloats);
-    ws.part_floats = kWorkspacePartFloats;
-    ws.ctr_count = kWorkspaceCounters;
-    err = cudaMemsetAsync(ws.ctr, 0, kWorkspaceCounters * sizeof(unsigned), stream);
-    if (err != cudaSuccess) {
-        cudaFree(p);
-        return err;
-    }
-    g_workspaces.push_back({dev.device, stream, ws});
-    *out = ws;
-    return cudaSuccess;
-}
-
-cudaError_t prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out) {
-    std::lock_guard<std::mutex> lock(g_ws_mutex);
-    PrefillEntry* e = nullptr;
-    for (PrefillEntry& x : g_prefill) {
-        if (x.device == dev.device && x.stream == stream) e = &x;
-    }
-    if (e && e->bytes >= bytes) {
-        *out = e->ptr;
-        return cudaSuccess;
-    }
-    if (e) {
-        // Earlier work on this stream may still read the old buffer.
-        cudaError_t err = cudaStreamSynchronize(stream);
-        if (err != cudaSuccess) return err;
-        cudaFree(e->ptr);
-        e->ptr = nullptr;
-        e->bytes = 0;
-    }
-    void* p = nullptr;
-    cudaError_t err = cudaMalloc(&p, bytes);
-    if (err != cudaSuccess) return err;
-    if (e) {
-        e->ptr = p;
-        e->bytes = bytes;
-    } else {
-        g_prefill.push_back({dev.device, stream, p, bytes});
-    }
-    *out = p;
-    return cudaSuccess;
-}
-
-// Zero the arrival counters of every workspace of `device` (after a kernel
-// gave up a wait and may have left one behind).
-cudaError_t reset_workspaces(int device) {
-    std::lock_guard<std::mutex> lock(g_ws_mutex);
-    for (const WorkspaceEntry& e : g_workspaces) {
-        if (e.device != device) continue;
-        cudaError_t err = cudaMemset(e.ws.ctr, 0, e.ws.ctr_count * sizeof(unsigned));
-        if (err != cudaSuccess) return err;
-    }
-    return cudaDeviceSynchronize();
-}
 
 void note_launch() { __atomic_fetch_add(&g_launches, 1, __ATOMIC_RELAXED); }
 
@@ -506,14 +420,16 @@ int qm_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, int fit2, int fi
     return QM_OK;
 }
 
-int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin,
-                 int64_t* out) {
+int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin, int fit2,
+                 int fit4, int fit8, int noalloc, int64_t* out) {
     if (!out) return QM_ERR_NULL;
     if (M < 1 || M > (packed ? 2 : 8) || N < 1 || N > 0x7FFFFFFF || K < 256 || (K % 256) != 0 ||
-        K > (int64_t(1) << 30) || sm_count < 1 || smem_optin < 1)
+        K > (int64_t(1) << 30) || sm_count < 1 || smem_optin < 1 || fit2 < 0 || fit4 < 0 || fit8 < 0)
         return QM_ERR_SHAPE;
+    const int fit[3] = {fit2, fit4, fit8};
     return qm::gemv_tc_plan_query(static_cast<int>(M), packed != 0, N, K, sm_count, smem_optin,
-                                  static_cast<int64_t>(qm::kWorkspacePartFloats), qm::kWorkspaceCounters, out)
+                                  noalloc ? nullptr : fit, static_cast<int64_t>(qm::kNoallocPartFloats),
+                                  qm::kNoallocCounters, out)
                ? QM_OK
                : QM_ERR_UNSUPPORTED;
 }
@@ -531,11 +447,6 @@ int qm_device_status(void* stream, int clear) {
     if (qm::gemm_tc_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (qm::gemv_tc_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     if (qm::gemv_list_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
-    if (bits && clear) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || qm::reset_workspaces(dev) != cudaSuccess)
-            return QM_ERR_CUDA;
-    }
     return bits ? QM_ERR_TIMEOUT : QM_OK;
 }
 

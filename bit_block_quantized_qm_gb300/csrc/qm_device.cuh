@@ -201,6 +201,12 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t caddr) {
     return v;
 }
 
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+    return v;
+}
+
 // Arrive on the mbarrier at shared::cluster address `caddr` (possibly another
 // CTA's), releasing this thread's earlier shared-memory writes to the cluster.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {

@@ -13,18 +13,19 @@ struct DeviceInfo {
     int max_smem_optin = 0;  // bytes of dynamic shared memory a CTA may opt into
 };
 
-// Scratch memory of the split-K GEMV: partial sums and per-row-group arrival
-// counters.  One workspace per (device, stream), allocated on first use and
-// kept until exit; kernels leave the counters at zero.
+// Scratch memory of a split-K GEMV that meets its partial sums in global
+// memory: partial sums and per-row-group arrival counters.  Only the
+// allocation-free entry point has one (a fixed array inside the library, of
+// kNoallocPartFloats floats and kNoallocCounters counters); the regular path
+// adds its K ranges up through thread-block clusters and needs none.
 struct Workspace {
     float* part = nullptr;
     unsigned* ctr = nullptr;
     size_t part_floats = 0;
     int ctr_count = 0;
 };
-
-// The workspace of `stream` on device dev.device (the current device).
-cudaError_t stream_workspace(const DeviceInfo& dev, cudaStream_t stream, Workspace* out);
+constexpr size_t kNoallocPartFloats = size_t(256) * 1024;  // 1 MB of split partial sums
+constexpr int kNoallocCounters = 4096;                      // row groups with a split K
 
 // Cached properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo* out);
@@ -66,23 +67,25 @@ inline GemvKind gemv_auto_kind(int64_t M, int64_t N, int64_t /*K*/) {
 cudaError_t launch_gemv_q4_0(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                              int64_t K, cudaStream_t stream, const DeviceInfo& dev, GemvKind kind);
 
-// The staged GEMV for K % 256 == 0 and 16-byte aligned A and wq, with split-K
-// scratch `ws` (counters zeroed on the stream first when clear_counters): on
-// tensor cores (mma.sync on bf16 pieces) for M = 1..8, or with packed FP32
-// FMAs (fma.rn.f32x2, one row per lane) for M = 1..2 when `packed`.  Sets
-// *launched = false and enqueues nothing when no launch plan fits.
+// The staged GEMV for K % 256 == 0 and 16-byte aligned A and wq: on tensor
+// cores (mma.sync on bf16 pieces) for M = 1..8, or with packed FP32 FMAs
+// (fma.rn.f32x2, one row per lane) for M = 1..2 when `packed`.  With ws null
+// a split K adds up through thread-block clusters; otherwise through the
+// scratch *ws (its counters zeroed on the stream first when clear_counters).
+// Sets *launched = false and enqueues nothing when no launch plan fits.
 cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
                                 int64_t K, cudaStream_t stream, const DeviceInfo& dev,
-                                const Workspace& ws, bool packed, bool clear_counters,
+                                const Workspace* ws, bool packed, bool clear_counters,
                                 bool* launched);
 cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 
 // The staged GEMV's launch plan for a device with sm_count SMs and smem_optin
-// bytes of opt-in shared memory and a split-K workspace of the given size,
-// without touching a device: {RG, U, S, rps, c, hs, rbpc, nu_max, stages,
-// grid, smem, W}.  False when no plan fits.
+// bytes of opt-in shared memory, without touching a device: with fit (the
+// resident clusters of 2, 4 and 8 CTAs) the regular path's, else that of a
+// split-K scratch of the given size: {RG, U, S, rps, c, hs, rbpc, nu_max,
+// stages, grid, smem, W, cluster split}.  False when no plan fits.
 bool gemv_tc_plan_query(int M, bool packed, int64_t N, int64_t K, int sm_count, int smem_optin,
-                        int64_t part_floats, int64_t ctr_count, int64_t out[12]);
+                        const int* fit, int64_t part_floats, int64_t ctr_count, int64_t out[13]);
 
 // The prefill GEMM's work items for a device with sm_count SMs on which fit[i]
 // clusters of 2, 4, 8 CTAs can be resident at once: {BN, n-tiles, tiles,
@@ -116,10 +119,6 @@ cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned
                                   cudaStream_t stream, const DeviceInfo& dev);
 cudaError_t gemv_list_read_device_error(unsigned int* bits, bool clear);
 
-// Growable scratch of the prefill GEMM (bf16 pieces of A), one per (device,
-// stream).  Growing it synchronizes the stream first (the old buffer may
-// still be in use by earlier work on it).
-cudaError_t prefill_workspace(const DeviceInfo& dev, cudaStream_t stream, size_t bytes, void** out);
 
 // Prefill GEMM on tcgen05 tensor cores: K % 256 == 0, 16-byte aligned A and wq.
 bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, int64_t K);

@@ -27,24 +27,20 @@
  *     stream) on the current device, and results are visible once that
  *     stream has been synchronized; no entry point but qm_device_status
  *     synchronizes.  Calls are thread-safe.
- *   - Memory: the prefill GEMM on tensor cores keeps bf16 copies of A (4 bytes
- *     per element of A) in a per-(device, stream) buffer that grows with
- *     cudaMalloc as needed (growing synchronizes that stream once).  When it
- *     splits K (too few output tiles to fill the SMs), the S CTAs of a tile
- *     add their partial sums inside a thread-block cluster when S is 2, 4 or
- *     8 and the clusters fit on the GPU at once; otherwise the same buffer
- *     also holds S x M x N floats of partial sums and one counter per tile.
+ *   - Memory: no entry point allocates device memory, and none writes
+ *     anything but its outputs (and, for qm_matmul_q4_0_noalloc, its fixed
+ *     scratch array).  The prefill GEMM splits A into bf16 pieces inside the
+ *     kernel.  Where a GEMM or GEMV splits K over S CTAs (too few output tiles
+ *     or rows to fill the SMs), S is 2, 4 or 8 and the S CTAs form a
+ *     thread-block cluster that adds the partial sums in its shared memory;
+ *     where those clusters would not all be resident at once, K is not split.
+ *     The first call on a device sets kernel attributes and queries the
+ *     device (host-side state only); after it, calls on any stream, including
+ *     one being captured into a CUDA graph, enqueue kernels and nothing else.
  *   - Launch: the fast kernels are launched with programmatic dependent
  *     launch, so one may start its prologue while the previous kernel on the
  *     stream finishes; it reads and writes memory only after that kernel has
  *     completed, so stream order is kept exactly as for ordinary launches.
- *   - Memory: the GEMV (M <= 8) splits K over several CTAs when the matrix
- *     has few rows; their partial sums go through a workspace of about 8 MB
- *     that the library allocates with cudaMalloc on the first such call on
- *     each (device, stream) and keeps until exit.  Make that first call
- *     before capturing the stream into a CUDA graph.  Calls on one stream
- *     share its workspace in stream order; calls on different streams use
- *     different workspaces.  qm_matmul_q4_0_noalloc allocates nothing.
  *   - Operands are contiguous; no strides, offsets or broadcasts.
  *   - Arguments are checked on the host before anything is enqueued; a
  *     failed check returns a negative status and leaves memory untouched.
@@ -206,10 +202,10 @@ QM_API int qm_selftest_wait_timeout(void* stream);
  * kernel-contract pages: it exists for code that must not allocate device
  * memory at call time, such as a custom allocator or memory-pool callback,
  * a process running under a hard device-memory cap, or a runtime that owns
- * all device memory.  qm_matmul_q4_0 gives each stream a small workspace
- * (cudaMalloc on first use) for the partial sums of a split K; this entry
- * point takes that scratch from a fixed array compiled into the library
- * instead, and allocates nothing, ever.
+ * all device memory.  It meets the partial sums of a split K in a fixed array
+ * compiled into the library (qm_matmul_q4_0 adds them up inside thread-block
+ * clusters instead, and allocates nothing either), and allocates nothing,
+ * ever.
  *   Arguments, layouts, alignment and aliasing rules: as qm_matmul_q4_0.
  *   Limit: M <= 8 (the GEMV regime); M > 8 returns QM_ERR_TOO_LARGE.  The
  *   array holds 1 MB of partial sums and 4096 row-group counters; when a
@@ -293,19 +289,25 @@ QM_API int qm_gemm_plan(int64_t M, int64_t N, int64_t K, int sm_count, int fit2,
 /*
  * qm_gemv_plan — the launch plan the decode GEMV (QM_ALGO_GEMV, packed = 0;
  * QM_ALGO_GEMV_PK, packed = 1) takes for (M, N, K) on a device with sm_count
- * SMs and smem_optin bytes of opt-in shared memory per CTA, with the
- * per-stream split-K workspace.  Host only: touches no device and enqueues
- * nothing; meant for tests and tuning.
- *   out: 12 int64 values {RG row groups, U units of 256 k, S K ranges, rps row
+ * SMs and smem_optin bytes of opt-in shared memory per CTA.  With noalloc = 0
+ * the plan of qm_matmul_q4_0, which adds a split K up through thread-block
+ * clusters of 2, 4 or 8 CTAs, fit2, fit4 and fit8 of which can be resident
+ * at once on that device; with noalloc = 1 the plan of
+ * qm_matmul_q4_0_noalloc, whose split K meets in its fixed scratch array
+ * (the fit counts are then ignored).  Host only: touches no device and
+ * enqueues nothing; meant for tests and tuning.
+ *   out: 13 int64 values {RG row groups, U units of 256 k, S K ranges, rps row
  *        groups per row block, c units per stage, hs warps per tile, rbpc row
  *        blocks per CTA, nu_max units in the largest K range, stages, grid
- *        CTAs, dynamic shared memory bytes, W consumer warps}.
- *   M 1..8 (1..2 when packed), N >= 1, K a positive multiple of 256.
+ *        CTAs, dynamic shared memory bytes, W consumer warps, 1 if the K
+ *        ranges add up through a cluster}.
+ *   M 1..8 (1..2 when packed), N >= 1, K a positive multiple of 256, fit
+ *   counts >= 0.
  * Returns QM_OK, QM_ERR_NULL, QM_ERR_SHAPE, or QM_ERR_UNSUPPORTED when no
  * plan fits (the library then runs the generic GEMV).
  */
 QM_API int qm_gemv_plan(int64_t M, int64_t N, int64_t K, int packed, int sm_count, int smem_optin,
-                        int64_t* out);
+                        int fit2, int fit4, int fit8, int noalloc, int64_t* out);
 
 /*
  * qm_launch_count — the number of kernels this library has enqueued in this

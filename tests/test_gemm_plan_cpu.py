@@ -2,8 +2,9 @@
 
 For a GEMM of M x N x K the library picks a tile width (128 or 256 columns),
 fills whole waves of CTAs with whole tiles and splits the tiles of the last,
-partial wave: into two 128-column halves, or into s_rem K ranges whose sums
-meet through a thread-block cluster or through the workspace.  This test
+partial wave: into two 128-column halves, or into s_rem = 2, 4 or 8 K ranges
+whose sums meet through a thread-block cluster, when the split tiles' clusters
+can all be resident at once (else the last wave stays whole).  This test
 replays the kernel's decoding of its 1-D grid for the returned plans and checks
 that every (tile, k-step, column half) is computed exactly once, that K ranges
 are whole 256-wide units, that a cluster never straddles whole and split
@@ -62,8 +63,10 @@ def test_work_items_cover_every_tile_once(lib, shape, sm_count):
     if plan["s_rem"] > 1 or plan["hw"]:
         assert plan["tiles"] - plan["n_full"] == plan["tiles"] % sm_count
         assert plan["items"] - plan["n_full"] <= sm_count, "the split last wave fits the SMs"
+    assert plan["cl"] == (plan["s_rem"] > 1)
     if plan["cl"]:
         assert plan["s_rem"] in (2, 4, 8) and plan["n_full"] % plan["s_rem"] == 0
+        assert plan["tiles"] - plan["n_full"] <= {2: 76, 4: 38, 8: 19}[plan["s_rem"]]
     count = replay(plan, M, N, K)
     assert count.min() == 1 and count.max() == 1
 
@@ -78,9 +81,14 @@ def test_narrow_tiles_fill_more_sms(lib):
 
 
 def test_cluster_split_needs_resident_clusters(lib):
-    # 32 tiles split 4 ways: clusters only when 32 clusters of 4 fit at once.
-    assert qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 38, 19))["cl"] == 1
-    assert qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 31, 19))["cl"] == 0
+    # 32 tiles split 4 ways only when 32 clusters of 4 fit at once; else 2
+    # ways when 32 clusters of 2 do; else not at all.
+    plan = qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 38, 19))
+    assert plan["s_rem"] == 4 and plan["cl"] == 1
+    plan = qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(76, 31, 19))
+    assert plan["s_rem"] == 2 and plan["cl"] == 1
+    plan = qm.qm_gemm_plan(512, 1024, 4096, 152, fit=(31, 15, 7))
+    assert plan["s_rem"] == 1 and plan["cl"] == 0 and plan["items"] == plan["tiles"]
 
 
 def test_plan_rejects_unsupported_shapes(lib):
@@ -112,6 +120,7 @@ def test_work_items_random_shapes(lib, sm_count):
         assert (K // 256) % plan["s_rem"] == 0, (M, N, K)
         if plan["s_rem"] > 1 or plan["hw"]:
             assert plan["items"] - plan["n_full"] <= sm_count, (M, N, K)
+        assert plan["cl"] == (plan["s_rem"] > 1)
         if plan["cl"]:
             assert plan["s_rem"] in (2, 4, 8) and plan["n_full"] % plan["s_rem"] == 0
         count = replay(plan, M, N, K)

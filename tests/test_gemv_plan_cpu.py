@@ -3,9 +3,12 @@
 The planner chooses the stage shape (rps row groups x c units, hs warps per
 tile), the K split S and the ring depth for one CTA per SM.  Whatever it
 chooses, the kernel must visit every (row group, unit) of the matrix exactly
-once, each half of a unit once, stay inside the opt-in shared memory, keep TMA
-boxes at most 256 rows high, and fit its split-K partial sums in the
-per-stream workspace.  This test replays the kernel's work assignment for the
+once, each half of a unit once, stay inside the opt-in shared memory and keep
+TMA boxes at most 256 rows high.  A split K adds up through thread-block
+clusters on the regular path: S is then 2, 4 or 8, a cluster is S consecutive
+CTAs of one row-block range, and all of the launch's clusters are resident at
+once; on the allocation-free path the split partial sums fit its fixed
+scratch array.  This test replays the kernel's work assignment for the
 returned plans in numpy and checks all of that, for a GB300 (152 SMs, 227 KB)
 and for smaller devices.
 """
@@ -15,7 +18,21 @@ import pytest
 import bit_block_quantized_qm_gb300 as qm
 
 UNIT = 256
-PART_FLOATS = 2 << 20
+NOALLOC_PART_FLOATS, NOALLOC_COUNTERS = 262144, 4096
+FIT = {152: (76, 36, 18), 132: (66, 32, 16), 48: (24, 12, 6)}  # resident clusters of 2, 4, 8
+
+
+def check_split(plan, M, rows, sm_count, noalloc):
+    S = plan["S"]
+    if S == 1:
+        assert plan["cl"] == 0
+        return
+    if noalloc:
+        assert plan["cl"] == 0
+        assert plan["RG"] * S * M * rows <= NOALLOC_PART_FLOATS and plan["RG"] <= NOALLOC_COUNTERS
+    else:
+        assert plan["cl"] == 1 and S in (2, 4, 8)
+        assert plan["grid"] // S <= FIT[sm_count][{2: 0, 4: 1, 8: 2}[S]], "every cluster resident"
 
 
 @pytest.fixture(scope="module")
@@ -60,15 +77,16 @@ SHAPES = [(1, 4096, 4096), (1, 14336, 4096), (1, 4096, 14336), (1, 1024, 4096), 
 DEVICES = [(152, 232448), (132, 232448), (48, 101376)]
 
 
+@pytest.mark.parametrize("noalloc", [False, True], ids=["regular", "noalloc"])
 @pytest.mark.parametrize("dev", DEVICES, ids=lambda d: f"{d[0]}sm")
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("packed", [False, True], ids=["mma", "packed"])
-def test_plan_invariants(lib, shape, packed, dev):
+def test_plan_invariants(lib, shape, packed, dev, noalloc):
     M, N, K = shape
     if packed and M > 2:
         pytest.skip("the packed consumer serves M = 1..2")
     sm_count, smem_optin = dev
-    plan = qm.qm_gemv_plan(M, N, K, packed, sm_count, smem_optin)
+    plan = qm.qm_gemv_plan(M, N, K, packed, sm_count, smem_optin, FIT[sm_count], noalloc)
     if plan is None:
         return  # no plan fits: the library runs the generic GEMV instead
     rows = 32 if packed else 16
@@ -81,8 +99,7 @@ def test_plan_invariants(lib, shape, packed, dev):
     assert plan["stages"] >= 2
     assert plan["grid"] % plan["S"] == 0 and plan["grid"] <= sm_count
     assert plan["nu_max"] == -(-plan["U"] // plan["S"])
-    if plan["S"] > 1:
-        assert plan["RG"] * plan["S"] * M * rows <= PART_FLOATS
+    check_split(plan, M, rows, sm_count, noalloc)
     count = covered(plan, packed)
     assert count.min() == 1 and count.max() == 1, "every (row group, unit, half) exactly once"
 
@@ -108,8 +125,8 @@ def test_plan_invariants_random_shapes(lib, dev):
         M = int(g.integers(1, 9))
         N = int(g.choice([int(g.integers(1, 700)), int(g.integers(700, 60000))]))
         K = 256 * int(g.integers(1, 129))
-        for packed in ((False, True) if M <= 2 else (False,)):
-            plan = qm.qm_gemv_plan(M, N, K, packed, sm_count, smem_optin)
+        for packed, noalloc in ((False, False), (True, False), (False, True)) if M <= 2 else ((False, False), (False, True)):
+            plan = qm.qm_gemv_plan(M, N, K, packed, sm_count, smem_optin, FIT[sm_count], noalloc)
             if plan is None:
                 continue
             rows = 32 if packed else 16
@@ -117,7 +134,15 @@ def test_plan_invariants_random_shapes(lib, dev):
             assert plan["W"] == plan["rps"] * plan["c"] * plan["hs"]
             assert plan["rps"] * rows <= 256 and plan["smem"] <= smem_optin
             assert plan["grid"] % plan["S"] == 0 and plan["grid"] <= sm_count
-            if plan["S"] > 1:
-                assert plan["RG"] * plan["S"] * M * rows <= PART_FLOATS
+            check_split(plan, M, rows, sm_count, noalloc)
             count = covered(plan, packed)
             assert count.min() == 1 and count.max() == 1, (M, N, K, packed, plan)
+
+
+def test_cluster_split_follows_resident_clusters(lib):
+    # 1 x 1024 x 4096 has 64 row groups for 152 SMs: it splits K, through
+    # clusters that fit; with no cluster resident it cannot split at all.
+    plan = qm.qm_gemv_plan(1, 1024, 4096, fit=(76, 36, 18))
+    assert plan["S"] > 1 and plan["cl"] == 1
+    plan = qm.qm_gemv_plan(1, 1024, 4096, fit=(0, 0, 0))
+    assert plan["S"] == 1 and plan["cl"] == 0

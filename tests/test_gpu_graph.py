@@ -1,9 +1,9 @@
 """Back-to-back launches of different kernels on one stream, captured into a
 CUDA graph and replayed: the fast kernels start early under programmatic
-dependent launch and consecutive split-K launches share the stream's
-workspace, so this checks that every result still matches the oracle after
-several replays (no kernel reads an input or a workspace slot before the
-kernel that writes it has finished)."""
+dependent launch, one GEMV reads the output of another, and the split-K
+launches add their K ranges up inside thread-block clusters, so this checks
+that every result still matches the oracle after several replays (no kernel
+reads an input before the kernel that writes it has finished)."""
 import numpy as np
 import pytest
 
@@ -60,7 +60,7 @@ def test_mixed_sequence_in_a_cuda_graph(env):
 
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
-        run(stream)  # first use: workspaces are allocated outside the capture
+        run(stream)  # first use of each kernel (module load, attributes) outside the capture
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):

@@ -165,8 +165,8 @@ def test_matmul_tail_shapes(env, shape):
 
 
 # GEMV TMA path: K % 256 == 0, aligned; N ragged against 32-row groups; K
-# split into 1..16 ranges (combined through the workspace); more row groups
-# than fit one wave of CTAs.
+# split into 2, 4 or 8 ranges (added up inside a thread-block cluster) or not
+# at all; more row groups than fit one wave of CTAs.
 GEMV_FAST = [(M, N, K) for M in (1, 2, 4, 7, 8)
              for (N, K) in ((1, 256), (31, 512), (33, 768), (100, 2048), (1000, 256),
                             (64, 14336), (4096, 512), (1024, 4096), (300, 3840))] + \

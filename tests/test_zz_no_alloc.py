@@ -2,14 +2,15 @@
 
 Some callers cannot call cudaMalloc at call time (a custom allocator or
 memory-pool callback, a process under a hard device-memory cap, a runtime that
-owns all device memory).  qm_matmul_q4_0 gives each stream a workspace on
-first use; qm_matmul_q4_0_noalloc uses a fixed array inside the library
-instead.  This test calls it through the C ABI twice in a row on shapes whose
-K is split (checked against the launch plan, so the fixed scratch really holds
-partial sums and counters, and its second use starts from whatever the first
-left), checks each result against qm_matmul_q4_0 and against the oracle within
-the parity tolerance, and checks that a first call on a fresh stream leaves
-the device's free memory unchanged.  It lives in its own file, collected last.
+owns all device memory).  qm_matmul_q4_0_noalloc meets the partial sums of a
+split K in a fixed array inside the library (qm_matmul_q4_0 adds them up
+inside thread-block clusters).  This test calls it through the C ABI twice in
+a row on shapes whose K is split (checked against its launch plan, so the
+fixed scratch really holds partial sums and counters, and its second use
+starts from whatever the first left), checks each result against
+qm_matmul_q4_0 and against the oracle within the parity tolerance, and checks
+that a first call on a fresh stream leaves the device's free memory
+unchanged.  It lives in its own file, collected last.
 """
 import numpy as np
 import pytest
@@ -52,7 +53,7 @@ def test_noalloc_matches_regular_entry_point_twice(env, shape):
     # so the allocation-free call takes the same split through the array.
     props = torch.cuda.get_device_properties(0)
     if K % 256 == 0:
-        plan = qm.qm_gemv_plan(M, N, K, packed=False, sm_count=props.multi_processor_count)
+        plan = qm.qm_gemv_plan(M, N, K, packed=False, sm_count=props.multi_processor_count, noalloc=True)
         assert plan is not None and plan["S"] > 1, f"no K split for {shape}: {plan}"
         assert plan["RG"] * plan["S"] * M * 16 <= ARRAY_FLOATS and plan["RG"] <= ARRAY_COUNTERS
     blob = synth.q4_0_weights(N, K, 70 + M)
