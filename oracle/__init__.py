@@ -95,6 +95,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_dequant_q8_0.argtypes = [p, i64, p]
     lib.oracle_dequant_q8_0.restype = None
     lib.oracle_quantize_q8_0.argtypes = [p, i64, p]
+    lib.oracle_matmul_q4_0_q8act.argtypes = [p, p, i64, i64, i64, p, p]
+    lib.oracle_matmul_q4_0_q8act.restype = ctypes.c_int
+    lib.oracle_matmul_q4_0_q8act_entries.argtypes = [p, p, i64, i64, i64, p, p, i64, p, p]
+    lib.oracle_matmul_q4_0_q8act_entries.restype = ctypes.c_int
     lib.oracle_quantize_q8_0.restype = None
     return lib
 
@@ -186,6 +190,32 @@ class Oracle:
             raise ValueError("oracle rejected the sizes or indices")
         return C, S
 
+
+    def matmul_q4_0_q8act(self, A: np.ndarray, blob: np.ndarray, N: int, K: int):
+        """C and S of A' x dequant(W)^T, A' = dequant_q8_0(quantize_q8_0(A))."""
+        A, blob = self._check(A, blob, N, K)
+        M = A.shape[0]
+        C = np.empty((M, N), dtype=np.float64)
+        S = np.empty((M, N), dtype=np.float64)
+        rc = self.lib.oracle_matmul_q4_0_q8act(_ptr(A), _ptr(blob), M, N, K, _ptr(C), _ptr(S))
+        if rc != 0:
+            raise ValueError("oracle rejected the sizes")
+        return C, S
+
+    def matmul_q4_0_q8act_entries(self, A, blob, N, K, m_idx, n_idx):
+        A, blob = self._check(A, blob, N, K)
+        M = A.shape[0]
+        mi = np.ascontiguousarray(m_idx, dtype=np.int64).ravel()
+        ni = np.ascontiguousarray(n_idx, dtype=np.int64).ravel()
+        if mi.size != ni.size:
+            raise ValueError("index arrays differ in length")
+        C = np.empty(mi.size, dtype=np.float64)
+        S = np.empty(mi.size, dtype=np.float64)
+        rc = self.lib.oracle_matmul_q4_0_q8act_entries(_ptr(A), _ptr(blob), M, N, K, _ptr(mi),
+                                                       _ptr(ni), mi.size, _ptr(C), _ptr(S))
+        if rc != 0:
+            raise ValueError("oracle rejected the sizes or indices")
+        return C, S
 
     def float_to_f16(self, x) -> np.ndarray:
         x = np.ascontiguousarray(np.asarray(x, dtype=np.float32).ravel())

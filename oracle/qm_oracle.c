@@ -10,6 +10,7 @@
 
 #include <math.h>
 #include <stddef.h>
+#include <stdlib.h>
 
 /* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
  *   exponent 0      -> subnormal, value = fraction * 2^-24
@@ -213,5 +214,73 @@ int oracle_matmul_q4_0_entries(const float* A, const uint8_t* wq, int64_t M,
     for (int64_t i = 0; i < count; ++i) {
         entry(A, wq, K, m_idx[i], n_idx[i], &C[i], S ? &S[i] : NULL);
     }
+    return 0;
+}
+
+/* The product with the activations quantized first (the GEMV fused with a
+ * preceding activation quantization, as the efficiency backlog page
+ * "vulkan: shader and sequencing efficiency backlog" lists it): each row of A
+ * goes through quantize_q8_0 and back through dequant_q8_0, and the result
+ * A' enters the same fp64 product as oracle_matmul_q4_0, S being the absolute
+ * sum with A'.  Nothing else: the three steps are the functions above. */
+static int dequantized_row(const float* A, int64_t K, int64_t m, uint8_t* q8, float* row)
+{
+    oracle_quantize_q8_0(A + m * K, K / ORACLE_Q4_0_BLOCK_ELEMS, q8);
+    oracle_dequant_q8_0(q8, K / ORACLE_Q4_0_BLOCK_ELEMS, row);
+    return 0;
+}
+
+int oracle_matmul_q4_0_q8act(const float* A, const uint8_t* wq, int64_t M, int64_t N,
+                             int64_t K, double* C, double* S)
+{
+    if (!sizes_ok(M, N, K)) return -1;
+    int64_t nb = K / ORACLE_Q4_0_BLOCK_ELEMS;
+    uint8_t* q8 = (uint8_t*)malloc((size_t)(nb > 0 ? nb : 1) * ORACLE_Q8_0_BLOCK_BYTES);
+    float* rows = (float*)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(float));
+    if (!q8 || !rows) {
+        free(q8);
+        free(rows);
+        return -2;
+    }
+    for (int64_t m = 0; m < M; ++m) dequantized_row(A, K, m, q8, rows + m * K);
+#ifdef _OPENMP
+#pragma omp parallel for collapse(2) schedule(static)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            entry(rows, wq, K, m, n, &C[m * N + n], S ? &S[m * N + n] : NULL);
+        }
+    }
+    free(q8);
+    free(rows);
+    return 0;
+}
+
+int oracle_matmul_q4_0_q8act_entries(const float* A, const uint8_t* wq, int64_t M,
+                                     int64_t N, int64_t K, const int64_t* m_idx,
+                                     const int64_t* n_idx, int64_t count, double* C,
+                                     double* S)
+{
+    if (!sizes_ok(M, N, K) || count < 0) return -1;
+    for (int64_t i = 0; i < count; ++i) {
+        if (m_idx[i] < 0 || m_idx[i] >= M || n_idx[i] < 0 || n_idx[i] >= N) return -1;
+    }
+    int64_t nb = K / ORACLE_Q4_0_BLOCK_ELEMS;
+    uint8_t* q8 = (uint8_t*)malloc((size_t)(nb > 0 ? nb : 1) * ORACLE_Q8_0_BLOCK_BYTES);
+    float* rows = (float*)malloc((size_t)(M * K > 0 ? M * K : 1) * sizeof(float));
+    if (!q8 || !rows) {
+        free(q8);
+        free(rows);
+        return -2;
+    }
+    for (int64_t m = 0; m < M; ++m) dequantized_row(A, K, m, q8, rows + m * K);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < count; ++i) {
+        entry(rows, wq, K, m_idx[i], n_idx[i], &C[i], S ? &S[i] : NULL);
+    }
+    free(q8);
+    free(rows);
     return 0;
 }

@@ -18,7 +18,10 @@
  *   - section "dequant_q8_0": a 34-byte block holds an f16 scale d followed by
  *     32 signed 8-bit quants; each element is qs * d;
  *   - section "quantize_q8_0": per 32-element block, d = max|x| / 127, the
- *     block stores f16(d) and qs = round(x / d).
+ *     block stores f16(d) and qs = round(x / d);
+ *   - the GEMV fused with a preceding activation quantization ("act-quant
+ *     fusion" in "vulkan: shader and sequencing efficiency backlog"): the
+ *     product above with A replaced by dequant_q8_0(quantize_q8_0(A)).
  * Element j (0..15) of a Q4_0 block sits in the low nibble of quant byte j and
  * element j+16 in its high nibble; d is little-endian IEEE binary16 in the
  * block's first two bytes.  Sums are taken in fp64 in ascending k.
@@ -81,6 +84,19 @@ int oracle_matmul_q4_0_entries(const float* A, const uint8_t* wq, int64_t M,
                                int64_t N, int64_t K, const int64_t* m_idx,
                                const int64_t* n_idx, int64_t count, double* C,
                                double* S);
+
+/* C = A' x dequant(W)^T with A' = dequant_q8_0(quantize_q8_0(A)) row by row:
+ * the product of the GEMV fused with a preceding activation quantization.  S
+ * is the absolute sum with A'.  Returns 0, -1 on a bad size, -2 if scratch
+ * memory could not be had. */
+int oracle_matmul_q4_0_q8act(const float* A, const uint8_t* wq, int64_t M, int64_t N,
+                             int64_t K, double* C, double* S);
+
+/* The same at the (m_idx[i], n_idx[i]) entries only. */
+int oracle_matmul_q4_0_q8act_entries(const float* A, const uint8_t* wq, int64_t M,
+                                     int64_t N, int64_t K, const int64_t* m_idx,
+                                     const int64_t* n_idx, int64_t count, double* C,
+                                     double* S);
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,14 @@ oracle disagrees with a fact that the kernel-contract page ("fuel-vulkan-kernels
   blocks and hand-worked quantizations (``tests/golden/``), numpy's own
   float -> binary16 narrowing, an int8 x binary16 dequant written with numpy
   views, the round-trip bound |qs d - x| <= d / 2, sign symmetry and
-  invariance of the quants under power-of-two scaling.
+  invariance of the quants under power-of-two scaling;
+* for the product with the activations quantized first (the act-quant fusion
+  of "vulkan: shader and sequencing efficiency backlog"): a hand-computed
+  product (``tests/golden/``), identity with the plain product on
+  activations that Q8_0 holds exactly, the block-factored integer form
+  sum_b d_w d_a sum_j (q - 8) qs computed with numpy integers from the quant
+  bytes, and the bound |C' - C| <= sum_k |a_k - a'_k| |W_k| against the plain
+  product.
 
 The same functions run against copies of the oracle with a planted mistake
 (``test_oracle_mutants.py``); every such copy must fail at least one pin.
@@ -60,9 +67,9 @@ def load_golden_blocks():
     return blocks, values
 
 
-def load_golden_matmul():
+def load_golden_matmul(name="q4_0_hand_matmul.txt"):
     rec = {"wrow": [], "arow": []}
-    with open(os.path.join(GOLDEN, "q4_0_hand_matmul.txt")) as f:
+    with open(os.path.join(GOLDEN, name)) as f:
         for line in f:
             parts = line.split()
             if not parts or parts[0].startswith("#"):
@@ -355,9 +362,74 @@ def pin_q8_0_symmetry_and_scaling(o):
             f"scale does not scale by 2^{k}"
 
 
+# ------------------------------------------ product with quantized activations
+
+def pin_q8act_golden(o):
+    M, N, K, A, blob, C_want, S_want = load_golden_matmul("q8act_hand_matmul.txt")
+    C, S = o.matmul_q4_0_q8act(A, blob, N, K)
+    assert np.array_equal(C, C_want), f"hand-computed product differs: {C}"
+    assert np.array_equal(S, S_want), f"hand-computed absolute sums differ: {S}"
+
+
+def pin_q8act_identity_on_representable(o):
+    """Blocks of integers in [-127, 127] times 2^e with a +-127 in each: the
+    scale is exactly 2^e and the quants are the integers, so A' = A and the
+    product equals the plain one bit for bit."""
+    g = synth.rng(21, (0,))
+    M, N, K = 3, 40, 256
+    ints = g.integers(-127, 128, (M, K // 32, 32))
+    ints[:, :, 0] = np.where(g.integers(0, 2, (M, K // 32)) == 1, 127, -127)
+    e = g.integers(-10, 6, (M, K // 32, 1))
+    A = (ints * np.exp2(e)).astype(np.float32).reshape(M, K)
+    blob = synth.q4_0_weights(N, K, 22)
+    C1, S1 = o.matmul_q4_0_q8act(A, blob, N, K)
+    C0, S0 = o.matmul_q4_0(A, blob, N, K)
+    assert np.array_equal(C1, C0) and np.array_equal(S1, S0), "A' differs from an exactly representable A"
+
+
+def pin_q8act_integer_form(o):
+    """sum_b d_w(b) d_a(b) sum_j (q_j - 8) qs_j from the quant bytes with
+    numpy integers equals the product to fp64 rounding."""
+    g = synth.rng(23, (0,))
+    M, N, K = 4, 24, 512
+    A = (g.standard_normal((M, K)) * np.exp(g.uniform(-3, 3, (M, 1)))).astype(np.float32)
+    blob = synth.q4_0_weights(N, K, 24)
+    C, S = o.matmul_q4_0_q8act(A, blob, N, K)
+    nb = K // 32
+    q8 = o.quantize_q8_0(A.ravel()).reshape(M, nb, 34)
+    da = q8[:, :, 0:2].copy().view(np.float16).reshape(M, nb).astype(np.float64)
+    qs = q8[:, :, 2:].view(np.int8).astype(np.int64)                       # [M, nb, 32]
+    w = blob.reshape(N, nb, 18)
+    dw = w[:, :, 0:2].copy().view(np.float16).reshape(N, nb).astype(np.float64)
+    qb = w[:, :, 2:].astype(np.int64)
+    qw = np.concatenate([qb & 0xF, qb >> 4], axis=2) - 8                     # [N, nb, 32]
+    isum = np.einsum("mbj,nbj->mnb", qs, qw)                                  # exact integers
+    want = np.einsum("mnb,mb,nb->mn", isum.astype(np.float64), da, dw)
+    assert np.all(np.abs(C - want) <= 1e-12 * S + 1e-300), "block-factored integer form differs"
+
+
+def pin_q8act_bound_against_plain(o):
+    """|C' - C| <= sum_k |a_k - a'_k| |W_k|, with |a - a'| at most half a
+    quantization step plus the binary16 narrowing of the scale."""
+    g = synth.rng(25, (0,))
+    M, N, K = 2, 32, 1024
+    A = g.standard_normal((M, K)).astype(np.float32)
+    blob = synth.q4_0_weights(N, K, 26)
+    C1, _ = o.matmul_q4_0_q8act(A, blob, N, K)
+    C0, _ = o.matmul_q4_0(A, blob, N, K)
+    W = o.dequant_q4_0(blob).reshape(N, K).astype(np.float64)
+    amax = np.abs(A.astype(np.float64)).reshape(M, K // 32, 32).max(axis=2)
+    step = np.repeat(amax / 127.0, 32, axis=1)                                # d per element
+    da = step * (0.5 + 127 * 2.0**-11) * (1 + 1e-6)
+    bound = da @ np.abs(W).T
+    assert np.all(np.abs(C1 - C0) <= bound), "quantized product strays past the quantization bound"
+
+
 ALL_PINS = (pin_f16_exhaustive, pin_golden_blocks, pin_all8_and_zero_scale,
             pin_extreme_nibbles, pin_golden_matmul, pin_one_hot,
             pin_ones_closed_form, pin_dense_equivalence, pin_rows_independent,
             pin_block_permutation, pin_entries_match_full,
             pin_f16_narrowing_vs_numpy, pin_q8_0_golden_blocks, pin_q8_0_dequant_numpy,
-            pin_q8_0_golden_quantize, pin_q8_0_roundtrip_bound, pin_q8_0_symmetry_and_scaling)
+            pin_q8_0_golden_quantize, pin_q8_0_roundtrip_bound, pin_q8_0_symmetry_and_scaling,
+            pin_q8act_golden, pin_q8act_identity_on_representable, pin_q8act_integer_form,
+            pin_q8act_bound_against_plain)

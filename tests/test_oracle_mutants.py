@@ -58,6 +58,11 @@ MUTANTS = {
     "q8_scale_big_endian": ("block[0] = (uint8_t)(bits & 0xFF);\n        block[1] = (uint8_t)(bits >> 8);",
                             "block[1] = (uint8_t)(bits & 0xFF);\n        block[0] = (uint8_t)(bits >> 8);"),
     "q8_max_without_abs": ("float a = fabsf(xb[j]);", "float a = xb[j];"),
+    # the product with quantized activations
+    "q8act_skips_quantization": ("oracle_dequant_q8_0(q8, K / ORACLE_Q4_0_BLOCK_ELEMS, row);",
+                                 "for (int64_t k = 0; k < K; ++k) row[k] = A[m * K + k];"),
+    "q8act_every_row_from_row_0": ("for (int64_t m = 0; m < M; ++m) dequantized_row(A, K, m, q8, rows + m * K);\n#ifdef _OPENMP\n#pragma omp parallel for collapse(2)",
+                                   "for (int64_t m = 0; m < M; ++m) dequantized_row(A, K, 0, q8, rows + m * K);\n#ifdef _OPENMP\n#pragma omp parallel for collapse(2)"),
     "q8_quants_offset_128": ("block[2 + j] = (uint8_t)(int8_t)q;", "block[2 + j] = (uint8_t)(q + 128);"),
     "q8_no_zero_scale_guard": ("if (d != 0.0f) {", "if (1) {"),
     "q8_no_clamp": ("if (r > 127.0) r = 127.0;", ""),
