@@ -643,6 +643,23 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
     gemv["cfg0_gemv_m1_k4096_n4096"] = gemv_row(
         "GEMV M=1, K=N=4096, 16 replicas back to back in a CUDA graph", "gemv_q4_0_tc",
         c0.weight_bytes, ms0)
+
+    # The same GEMVs with the activations quantized to Q8_0 first (the
+    # act-quant fused GEMV, qm_matmul_q4_0_q8act): a different product, timed
+    # on the same weights.
+    def q8act(A, W, C, M, N, K, what):
+        rc = qm.qm_matmul_q4_0_q8act_ptr(A.data_ptr(), W.data_ptr(), C.data_ptr(), M, N, K, sh())
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"{what}: {qm.qm_status_string(rc)}")
+
+    def m1_q8_fn():
+        for w in w0:
+            q8act(a0, w, o0, 1, c0.N, c0.K, "cfg0 q8act")
+    ms0q = graph_ms(torch, m1_q8_fn) / len(w0)
+    gemv["cfg0_q8act_m1_k4096_n4096"] = gemv_row(
+        "GEMV M=1, K=N=4096 with the activations quantized to Q8_0 in the kernel "
+        "(qm_matmul_q4_0_q8act), 16 replicas back to back in a CUDA graph", "gemv_q4_0_tc<q8>",
+        c0.weight_bytes, ms0q)
     del w0
 
     # cfg1 dequant.
@@ -695,6 +712,20 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
             for i, c in enumerate(cases):
                 mm(A[c.K], weights[i], outs[i % 7], M, c.N, c.K, f"sweep {c.name} M={M}")
         return fn
+
+    # The sweep through the act-quant fused GEMV (qm_matmul_q4_0_q8act).
+    for M in (1, 8):
+        A = acts(M)
+        outs = [torch.empty((M, N), dtype=torch.float32, device=dev) for (N, K) in layer_shapes]
+
+        def q8_sweep(M=M, A=A, outs=outs):
+            for i, c in enumerate(cases):
+                q8act(A[c.K], weights[i], outs[i % 7], M, c.N, c.K, f"q8act sweep {c.name} M={M}")
+        ms = graph_ms(torch, q8_sweep)
+        gemv[f"cfg4_sweep_m{M}_q8act"] = gemv_row(
+            f"32-layer decoder sweep at M={M} with the activations quantized to Q8_0 in the kernel "
+            f"(qm_matmul_q4_0_q8act): CUDA graph of {len(cases)} launches", "gemv_q4_0_tc<q8>",
+            wbytes, ms, len(cases))
 
     for M in (1, 8):
         A = acts(M)

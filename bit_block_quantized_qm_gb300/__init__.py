@@ -35,6 +35,7 @@ __all__ = [
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr", "qm_selftest_wait_timeout",
+    "qm_matmul_q4_0_q8act", "qm_matmul_q4_0_q8act_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
     "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
     "EXPORTED_SYMBOLS", "QmGemvProblem", "qm_gemv_q4_0_list_ptr", "qm_gemv_q4_0_list",
@@ -66,7 +67,7 @@ Q8_0_BLOCK_BYTES = 34
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
                     "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan", "qm_gemm_plan",
                     "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0",
-                    "qm_selftest_wait_timeout", "qm_gemv_q4_0_list")
+                    "qm_selftest_wait_timeout", "qm_gemv_q4_0_list", "qm_matmul_q4_0_q8act")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
@@ -124,6 +125,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_device_status.restype = i32
             lib.qm_matmul_q4_0_noalloc.argtypes = [p, p, p, i64, i64, i64, p]
             lib.qm_matmul_q4_0_noalloc.restype = i32
+            lib.qm_matmul_q4_0_q8act.argtypes = [p, p, p, i64, i64, i64, p]
+            lib.qm_matmul_q4_0_q8act.restype = i32
             lib.qm_dequant_q8_0.argtypes = [p, i64, p, p]
             lib.qm_dequant_q8_0.restype = i32
             lib.qm_quantize_q8_0.argtypes = [p, i64, p, p]
@@ -184,6 +187,13 @@ def qm_matmul_q4_0_noalloc_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
                                stream: int = 0) -> int:
     """The allocation-free GEMV (M <= 8); see include/qm.h."""
     return load_library().qm_matmul_q4_0_noalloc(A, wq, C, M, N, K, stream)
+
+
+def qm_matmul_q4_0_q8act_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
+                             stream: int = 0) -> int:
+    """The product with the activations quantized to Q8_0 first (M <= 8);
+    see include/qm.h."""
+    return load_library().qm_matmul_q4_0_q8act(A, wq, C, M, N, K, stream)
 
 
 def qm_gemv_q4_0_list_ptr(problems, M: int, counters: int = 0, stream: int = 0) -> int:
@@ -295,6 +305,26 @@ def qm_matmul_q4_0_algo(A, wq, N: int, algo: int, out=None, stream=None):
 def qm_matmul_q4_0(A, wq, N: int, out=None, stream=None):
     """C[M, N] = A[M, K] x dequant(W)^T; GEMV kernels for M <= 8, GEMM above."""
     return qm_matmul_q4_0_algo(A, wq, N, QM_ALGO_AUTO, out=out, stream=stream)
+
+
+def qm_matmul_q4_0_q8act(A, wq, N: int, out=None, stream=None):
+    """C[M, N] = dequant_q8_0(quantize_q8_0(A)) x dequant(W)^T for M <= 8."""
+    import torch
+    _require(A, torch.float32, "A")
+    _require(wq, torch.uint8, "wq")
+    if A.dim() != 2:
+        raise ValueError("A must be 2-D [M, K]")
+    M, K = A.shape
+    if K % BLOCK_ELEMS or wq.numel() != N * (K // BLOCK_ELEMS) * BLOCK_BYTES:
+        raise ValueError("wq size does not match N x K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _require(out, torch.float32, "out")
+    if out.numel() != M * N:
+        raise ValueError("out has the wrong number of elements")
+    _check(qm_matmul_q4_0_q8act_ptr(A.data_ptr(), wq.data_ptr(), out.data_ptr(), M, N, K,
+                                    _stream_handle(stream)), "qm_matmul_q4_0_q8act")
+    return out
 
 
 def qm_gemv_q4_0_list(problems, M: int = 1, counters=None, stream=None):

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libqm.so")
-SOURCES = ("qm_api.cu", "dequant.cu", "q8_0.cu", "gemv.cu", "gemv_tc.cu", "gemv_list.cu", "gemm.cu",
+SOURCES = ("qm_api.cu", "dequant.cu", "q8_0.cu", "gemv.cu", "gemv_tc.cu", "gemv_list.cu", "gemv_q8act.cu", "gemm.cu",
            "gemm_tc.cu")
 HEADERS = ("qm_device.cuh", "qm_internal.h")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -72,9 +72,15 @@ constexpr int kUnitElems = 256;
 // packed FP32 consumer.
 __host__ __device__ constexpr int group_rows(bool packed) { return packed ? 32 : 16; }
 // Consumer warps at most (the MMA consumer needs more registers per thread).
-__host__ __device__ constexpr int max_warps(bool packed) { return packed ? 24 : 16; }
+// (The integer consumer keeps more values per lane as M grows: fewer warps,
+// so that the CTA's warps, counted in fours, leave it more registers.)
+__host__ __device__ constexpr int max_warps(bool packed, int M = 1, bool q8 = false) {
+    return !packed ? 16 : !q8 ? 24 : M == 1 ? 24 : M == 2 ? 22 : 14;
+}
 // Threads of a CTA at most: the consumers and the producer warp.
-__host__ __device__ constexpr int max_threads(bool packed) { return (max_warps(packed) + 1) * 32; }
+__host__ __device__ constexpr int max_threads(bool packed, int M = 1, bool q8 = false) {
+    return (max_warps(packed, M, q8) + 1) * 32;
+}
 constexpr int kMaxStages = 12;
 constexpr int kMaxSplits = 16;
 // One warp's partial sums at the end of a row block: group rows x 8 columns.
@@ -432,8 +438,175 @@ __device__ __forceinline__ void half_dot_pk(const uint8_t* row, int h, const flo
     }
 }
 
-template <int M, bool kPk>
-__global__ void __launch_bounds__(max_threads(kPk), 1)
+// ---------------------------------------------------------------------------
+// Integer consumer with the activations quantized to Q8_0 first (the GEMV
+// fused with a preceding activation quantization: "act-quant fusion" in
+// "vulkan: shader and sequencing efficiency backlog"; quantization as in
+// section "quantize_q8_0" of "fuel-vulkan-kernels — quantized (GGML) kernel
+// contracts").  The product is A' x dequant(W)^T with A' = dequant_q8_0(
+// quantize_q8_0(A)), and per block of 32 it factors exactly:
+//     sum_j A'_j W_j = (d_a d_w) * (sum_j q_j qs_j - 8 sum_j qs_j),
+// q the weight nibbles 0..15, qs the activation quants, d_a and d_w the two
+// binary16 scales.  The integer sums are exact (dp4a on the nibbles as
+// unsigned bytes against the signed quants; 8 sum qs, the block's "row sum",
+// is computed once per activation block for all N rows), d_a d_w is exact in
+// f32 (two 11-bit significands), and |sum| <= 32 * 8 * 127 is exact too, so a
+// block adds to its row's sum with one rounding.  A row whose total comes out
+// infinite or NaN (a non-finite scale) is recomputed element by element from
+// A' and W, as the definition does it.
+
+// Quantize one unit of staged activations, f32 [M][256] as the TMA box lands,
+// in place into [M][256] signed quants, then [M][8] f32 scales (the narrowed
+// binary16 d, as f32), then [M][8] int32 values 8 * sum qs.  Lane l takes
+// elements 8 (l % 4) .. + 7 of block l / 4 of every row; a block's max and
+// quant sum meet over its four lanes by shuffles.  All rows are read before
+// anything is written (the outputs overlap the inputs).
+template <int M>
+__device__ __forceinline__ void quantize_unit_q8(uint8_t* unit, int lane) {
+    const int bl = lane >> 2;
+    const int part = lane & 3;
+    uint32_t qw[M][2];
+    float dv[M];
+    int bs[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const float4* src = reinterpret_cast<const float4*>(unit + (m * kUnitElems + bl * 32 + 8 * part) * 4);
+        const float4 x0 = src[0], x1 = src[1];
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const float d = __fdiv_rn(amax, 127.f);
+        const float r = __frcp_rn(d);
+        uint32_t qb[8];
+        int sum = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            qb[e] = q8_quant_byte(x[e], d, r);
+            sum += static_cast<int>(static_cast<int8_t>(qb[e]));
+        }
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        qw[m][0] = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+        qw[m][1] = qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24);
+        dv[m] = f16_bits_to_float(f16_bits_rn(d));
+        bs[m] = 8 * sum;
+    }
+    __syncwarp();
+    float* dq = reinterpret_cast<float*>(unit + M * kUnitElems);
+    int* sq = reinterpret_cast<int*>(unit + M * kUnitElems + M * 32);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        *reinterpret_cast<uint2*>(unit + m * kUnitElems + bl * 32 + 8 * part) = make_uint2(qw[m][0], qw[m][1]);
+        if (part == 0) {
+            dq[m * 8 + bl] = dv[m];
+            sq[m * 8 + bl] = bs[m];
+        }
+    }
+}
+
+// One block (index bi of 8 in the unit): quant words q (elements j and
+// j + 16 in byte j of the 16), the weight scale dw, the unit's quantized
+// activations au.
+template <int M>
+__device__ __forceinline__ void block_dot_q8(const uint8_t* au, int bi, const uint32_t q[4], float dw,
+                                             float (&acc)[4 * M]) {
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        lo[w] = q[w] & 0x0F0F0F0Fu;         // elements 4w .. 4w+3
+        hi[w] = (q[w] >> 4) & 0x0F0F0F0Fu;  // elements 16+4w .. 16+4w+3
+    }
+    const float* dq = reinterpret_cast<const float*>(au + M * kUnitElems);
+    const int* sq = reinterpret_cast<const int*>(au + M * kUnitElems + M * 32);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const int4* qa = reinterpret_cast<const int4*>(au + m * kUnitElems + bi * 32);
+        const int4 a0 = qa[0], a1 = qa[1];
+        int s = __dp4a(static_cast<int>(lo[0]), a0.x, 0);
+        s = __dp4a(static_cast<int>(lo[1]), a0.y, s);
+        s = __dp4a(static_cast<int>(lo[2]), a0.z, s);
+        s = __dp4a(static_cast<int>(lo[3]), a0.w, s);
+        s = __dp4a(static_cast<int>(hi[0]), a1.x, s);
+        s = __dp4a(static_cast<int>(hi[1]), a1.y, s);
+        s = __dp4a(static_cast<int>(hi[2]), a1.z, s);
+        s = __dp4a(static_cast<int>(hi[3]), a1.w, s);
+        // Independent sums per row: four for M <= 2, two above (registers).
+        float& a = acc[4 * m + (M <= 2 ? (bi & 3) : (bi & 1))];
+        a = fmaf(dw * dq[m * 8 + bi], static_cast<float>(s - sq[m * 8 + bi]), a);
+    }
+}
+
+// Half h of a unit (blocks 4h .. 4h + 3) of this lane's row, 72 bytes
+// realigned as for the packed consumer, against the unit's quantized
+// activations au.
+template <int M>
+__device__ __forceinline__ void half_dot_q8(const uint8_t* row, int h, const uint8_t* au, float (&acc)[4 * M]) {
+    uint32_t w[18];
+    if (h == 0) {  // bytes 0 .. 71: 16-byte loads first
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+            w[4 * i + 0] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 64);
+        w[16] = v.x;
+        w[17] = v.y;
+    } else {  // bytes 72 .. 143: 16-byte loads from byte 80
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 72);
+        w[0] = v.x;
+        w[1] = v.y;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = reinterpret_cast<const uint4*>(row + 80)[i];
+            w[2 + 4 * i + 0] = u.x;
+            w[2 + 4 * i + 1] = u.y;
+            w[2 + 4 * i + 2] = u.z;
+            w[2 + 4 * i + 3] = u.w;
+        }
+    }
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        const uint32_t* Wp = w + 9 * pp;
+        const uint32_t qa[4] = {__byte_perm(Wp[0], Wp[1], 0x5432u), __byte_perm(Wp[1], Wp[2], 0x5432u),
+                                __byte_perm(Wp[2], Wp[3], 0x5432u), __byte_perm(Wp[3], Wp[4], 0x5432u)};
+        block_dot_q8<M>(au, 4 * h + 2 * pp, qa, f16_bits_to_float(Wp[0] & 0xFFFFu), acc);
+        const uint32_t qb[4] = {Wp[5], Wp[6], Wp[7], Wp[8]};
+        block_dot_q8<M>(au, 4 * h + 2 * pp + 1, qb, f16_bits_to_float(Wp[4] >> 16), acc);
+    }
+}
+
+// Exact row sum over nblocks blocks from the quantized activations of the
+// CTA's units (frag: unit j at frag + j M KB), element by element: A'_k =
+// qs_k d_a exactly in f32, then the product with (q - 8) d_w, as the
+// definition does it (a non-finite scale times a zero weight gives NaN).
+template <int M>
+__device__ __noinline__ float row_range_exact_q8(const uint8_t* row_blocks, int nblocks, const uint8_t* frag,
+                                                 int m) {
+    float s = 0.f;
+    for (int b = 0; b < nblocks; ++b) {
+        const uint8_t* au = frag + (b >> 3) * (M * 1024);
+        const int bi = b & 7;
+        const float da = reinterpret_cast<const float*>(au + M * kUnitElems)[m * 8 + bi];
+        const int8_t* qs = reinterpret_cast<const int8_t*>(au + m * kUnitElems + bi * 32);
+        const uint8_t* blk = row_blocks + kBlockBytes * b;
+        const float d = f16_bits_to_float(static_cast<uint32_t>(blk[0]) | (static_cast<uint32_t>(blk[1]) << 8));
+        for (int j = 0; j < kBlockElems; ++j) {
+            const uint32_t byte = blk[2 + (j & 15)];
+            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+            s = fmaf(static_cast<float>(qs[j]) * da, magic_minus8(nib | kMagicBits) * d, s);
+        }
+    }
+    return s;
+}
+
+template <int M, bool kPk, bool kQ8 = false>
+__global__ void __launch_bounds__(max_threads(kPk, M, kQ8), 1)
     gemv_q4_0_tc(const __grid_constant__ CUtensorMap wmap, const __grid_constant__ CUtensorMap amap,
                  const float* __restrict__ A, float* __restrict__ C, const TcPlan p) {
     constexpr int kRows = group_rows(kPk);
@@ -541,6 +714,10 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
         if (ok) {
             for (int j = warp; j < nu; j += W) build_fragments<M>(frag + j * M * 1024, lane);
         }
+    } else if constexpr (kQ8) {
+        if (ok) {
+            for (int j = warp; j < nu; j += W) quantize_unit_q8<M>(frag + j * M * 1024, lane);
+        }
     }
     named_barrier_sync(1, W * 32);
 
@@ -572,7 +749,10 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
                 const uint8_t* r0 = tile0 + st * stage_bytes;
                 const float* aj = reinterpret_cast<const float*>(frag + j * M * 1024);
                 const uint2* Fj = F + j * (M * 128);
-                if constexpr (kPk) {
+                if constexpr (kQ8) {
+                    // (The planner gives the lane-per-row consumers half units: hs = 2.)
+                    half_dot_q8<M>(r0, h, frag + j * M * 1024, acc);
+                } else if constexpr (kPk) {
                     if (p.hs == 1) unit_dot_pk<M>(r0, aj, acc);
                     else half_dot_pk<M>(r0, h, aj, acc);
                 } else {
@@ -633,9 +813,13 @@ __global__ void __launch_bounds__(max_threads(kPk), 1)
                 p.wq + (static_cast<int64_t>(row) * p.U + u0) * kUnitBytes;
 #pragma unroll
             for (int m = 0; m < M; ++m) {
-                if (!isfinite(tot[m]))
-                    tot[m] = row_range_exact(row_blocks, nu * 8,
-                                             A + m * p.K + static_cast<int64_t>(u0) * kUnitElems);
+                if (!isfinite(tot[m])) {
+                    if constexpr (kQ8)
+                        tot[m] = row_range_exact_q8<M>(row_blocks, nu * 8, frag, m);
+                    else
+                        tot[m] = row_range_exact(row_blocks, nu * 8,
+                                                 A + m * p.K + static_cast<int64_t>(u0) * kUnitElems);
+                }
             }
         }
         if (p.S == 1) {
@@ -749,14 +933,14 @@ double warp_efficiency(int W) {
 // few bytes of each row leaves DRAM pages to be reopened by others), for a
 // shallow ring, and for cross-warp reductions at more than one row block per
 // CTA.  Returns the cost (infinite when nothing fits).
-double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const DeviceInfo& dev,
+double plan_tc_hs(int M, bool packed, bool q8, int hs, int64_t N, int64_t K, const DeviceInfo& dev,
                   const Workspace* ws, const int* fit, TcPlan* out, int* grid, int* smem) {
     const int kRows = group_rows(packed);
     const int U = static_cast<int>(K / kUnitElems);
     const int64_t RG = (N + kRows - 1) / kRows;
     const int P = dev.sm_count;
     double best = 1e300;
-    for (int W = std::min(max_warps(packed), 16 * hs); W >= 8; --W) {
+    for (int W = std::min(max_warps(packed, M, q8), 16 * hs); W >= 8; --W) {
         if (W % hs != 0) continue;
         const int tiles = W / hs;
         for (int c = 1; c <= tiles; ++c) {
@@ -827,17 +1011,17 @@ double plan_tc_hs(int M, bool packed, int hs, int64_t N, int64_t K, const Device
 // for the packed one (measured on GB300: half units lose with the MMA
 // consumer, and give the packed one twice the warps on the same stages).
 bool plan_tc(int M, bool packed, int64_t N, int64_t K, const DeviceInfo& dev, const Workspace* ws,
-             const int* fit, TcPlan* out, int* grid, int* smem) {
-    return plan_tc_hs(M, packed, packed ? 2 : 1, N, K, dev, ws, fit, out, grid, smem) < 1e300;
+             const int* fit, TcPlan* out, int* grid, int* smem, bool q8 = false) {
+    return plan_tc_hs(M, packed, q8, packed ? 2 : 1, N, K, dev, ws, fit, out, grid, smem) < 1e300;
 }
 
-template <int M, bool kPk>
+template <int M, bool kPk, bool kQ8 = false>
 cudaError_t ensure_tc_smem_attr(const DeviceInfo& dev, int bytes) {
     static int configured[64] = {0};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (bytes > dev.max_smem_optin) return cudaErrorInvalidValue;
     if (__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) return cudaSuccess;
-    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_tc<M, kPk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(gemv_q4_0_tc<M, kPk, kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            dev.max_smem_optin);
     if (err != cudaSuccess) return err;
     __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
@@ -847,14 +1031,14 @@ cudaError_t ensure_tc_smem_attr(const DeviceInfo& dev, int bytes) {
 // Resident clusters of 2, 4 and 8 CTAs of one kernel (one CTA per SM: the
 // count depends on how the SMs group, not on the launch's shared memory),
 // queried once per device.
-template <int M, bool kPk>
+template <int M, bool kPk, bool kQ8 = false>
 cudaError_t cluster_fits(const DeviceInfo& dev, int fit[3]) {
     static int cached[64][3] = {};  // 0: not queried; else 1 + the count
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     for (int i = 0; i < 3; ++i) {
         int f = __atomic_load_n(&cached[dev.device][i], __ATOMIC_ACQUIRE);
         if (f == 0) {
-            f = 1 + max_active_clusters(gemv_q4_0_tc<M, kPk>, dim3(max_threads(kPk)),
+            f = 1 + max_active_clusters(gemv_q4_0_tc<M, kPk, kQ8>, dim3(max_threads(kPk, M, kQ8)),
                                         static_cast<size_t>(dev.max_smem_optin), 2u << i);
             __atomic_store_n(&cached[dev.device][i], f, __ATOMIC_RELEASE);
         }
@@ -863,21 +1047,21 @@ cudaError_t cluster_fits(const DeviceInfo& dev, int fit[3]) {
     return cudaSuccess;
 }
 
-template <int M, bool kPk>
+template <int M, bool kPk, bool kQ8 = false>
 cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, int64_t K,
                       cudaStream_t stream, const DeviceInfo& dev, const Workspace* ws,
                       bool clear_counters, bool* launched) {
     *launched = false;
-    cudaError_t err = ensure_tc_smem_attr<M, kPk>(dev, dev.max_smem_optin);
+    cudaError_t err = ensure_tc_smem_attr<M, kPk, kQ8>(dev, dev.max_smem_optin);
     if (err != cudaSuccess) return err;
     int fit[3] = {0, 0, 0};
     if (!ws) {
-        err = cluster_fits<M, kPk>(dev, fit);
+        err = cluster_fits<M, kPk, kQ8>(dev, fit);
         if (err != cudaSuccess) return err;
     }
     TcPlan p;
     int grid = 0, smem = 0;
-    if (!plan_tc(M, kPk, N, K, dev, ws, ws ? nullptr : fit, &p, &grid, &smem)) return cudaSuccess;
+    if (!plan_tc(M, kPk, N, K, dev, ws, ws ? nullptr : fit, &p, &grid, &smem, kQ8)) return cudaSuccess;
     p.wq = wq;
     if (clear_counters && p.S > 1 && !p.cl) {
         err = cudaMemsetAsync(p.ctr, 0, static_cast<size_t>(p.RG) * sizeof(unsigned), stream);
@@ -898,10 +1082,10 @@ cudaError_t launch_tc(const float* A, const uint8_t* wq, float* C, int64_t N, in
     if (err != cudaSuccess) return err;
     const dim3 block((p.rps * p.c * p.hs + 1) * 32);
     if (p.cl) {
-        err = launch_pdl_cluster(gemv_q4_0_tc<M, kPk>, dim3(grid), block, smem, stream,
+        err = launch_pdl_cluster(gemv_q4_0_tc<M, kPk, kQ8>, dim3(grid), block, smem, stream,
                                  static_cast<unsigned>(p.S), wmap, amap, A, C, p);
     } else {
-        err = launch_pdl(gemv_q4_0_tc<M, kPk>, dim3(grid), block, smem, stream, wmap, amap, A, C, p);
+        err = launch_pdl(gemv_q4_0_tc<M, kPk, kQ8>, dim3(grid), block, smem, stream, wmap, amap, A, C, p);
     }
     if (err != cudaSuccess) return err;
     note_launch();
@@ -931,6 +1115,21 @@ cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
         case 6: return launch_tc<6, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
         case 7: return launch_tc<7, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
         case 8: return launch_tc<8, false>(A, wq, C, N, K, stream, dev, ws, clear_counters, launched);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemv_q4_0_q8act_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                      int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool* launched) {
+    switch (M) {
+        case 1: return launch_tc<1, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 2: return launch_tc<2, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 3: return launch_tc<3, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 4: return launch_tc<4, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 5: return launch_tc<5, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 6: return launch_tc<6, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 7: return launch_tc<7, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
+        case 8: return launch_tc<8, true, true>(A, wq, C, N, K, stream, dev, nullptr, false, launched);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -117,40 +117,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// d narrowed to binary16 (round to nearest even), as its 16 bits in the low
-// half of a word: the packed conversion of (0, d), kept in 32-bit registers.
-__device__ __forceinline__ uint32_t f16_bits_rn(float d) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(d));
-    return r & 0xFFFFu;
-}
-
-// The quant of x for the block scale d (see the readings above).
-__device__ __forceinline__ int q8_quant(float x, float d) {
-    if (d == 0.f) return 0;
-    const float t = __fdiv_rn(x, d);
-    if (isnan(t)) return 0;
-    return static_cast<int>(fminf(fmaxf(roundf(t), -127.f), 127.f));
-}
-
-// The quant byte of x, as q8_quant gives it, without a division in the
-// common case.  With r = 1/d correctly rounded and t' = x * r rounded,
-// t' = (x/d)(1 + e1)(1 + e2) and fl(x/d) = (x/d)(1 + e3), |e_i| <= 2^-24, so
-// |t' - fl(x/d)| <= 127.5 * (3 * 2^-24 + 2^-48) < 2.3e-5 when |t'| < 127.4.
-// Rounding t' to the nearest integer (adding 1.5 * 2^23 leaves it in the low
-// mantissa bits, two's complement for negatives) then gives the same integer
-// as rounding fl(x/d), half away from zero, unless t' is within 1e-4 of a
-// half-integer; those, and every t' out of range or not finite (d = 0, a
-// subnormal d whose reciprocal overflows, NaN or infinite x), take q8_quant.
-constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
-__device__ __forceinline__ uint32_t q8_quant_byte(float x, float d, float r) {
-    const float t = __fmul_rn(x, r);
-    const float m = __fadd_rn(t, kRoundMagic);
-    const float ri = __fsub_rn(m, kRoundMagic);  // t rounded to an integer, exactly
-    if (fabsf(t) < 127.4f && fabsf(__fsub_rn(t, ri)) < 0.4999f) return __float_as_uint(m) & 0xFFu;
-    return static_cast<uint32_t>(q8_quant(x, d)) & 0xFFu;
-}
-
 __device__ __forceinline__ uint32_t pack_q4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     return a | (b << 8) | (c << 16) | (d << 24);
 }

@@ -316,6 +316,27 @@ int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int64_t M, 
                                                   static_cast<int>(M), N, K, s, dev));
 }
 
+// The product with the activations quantized to Q8_0 first: the checks of
+// qm_matmul_q4_0, M <= 8.
+int qm_matmul_q4_0_q8act(const float* A, const void* wq, float* C, int64_t M, int64_t N, int64_t K,
+                         void* stream) {
+    int64_t a_bytes = 0, w_bytes = 0, c_bytes = 0;
+    int rc = check_matmul(A, wq, C, M, N, K, &a_bytes, &w_bytes, &c_bytes);
+    if (rc != QM_OK) return rc;
+    if (M > 8) return QM_ERR_TOO_LARGE;
+    if (M == 0 || N == 0) return QM_OK;
+    qm::DeviceInfo dev;
+    if (qm::current_device_info(&dev) != cudaSuccess) return QM_ERR_CUDA;
+    rc = check_pointer(C, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(A, dev.device);
+    if (rc == QM_OK && K > 0) rc = check_pointer(wq, dev.device);
+    if (rc != QM_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(C, 0, static_cast<size_t>(c_bytes), s));
+    return from_cuda(qm::launch_matmul_q4_0_q8act(A, static_cast<const uint8_t*>(wq), C, static_cast<int>(M), N,
+                                                  K, s, dev));
+}
+
 // The list GEMV: checks every problem as qm_matmul_q4_0 does, then the
 // ordering rules between problems, then runs maximal runs of problems the
 // persistent kernel takes (M = 1, K % 2048 == 0, K <= 14336, 16-byte aligned

@@ -232,6 +232,47 @@ __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_
     return false;
 }
 
+// ---- Q8_0 quantization (section "quantize_q8_0": d = max|x| / 127, the
+// block keeps d narrowed to binary16 and qs = round(x / d)), with the readings
+// the library takes where the section is silent: f32 arithmetic with
+// correctly rounded divisions, NaN elements do not raise the max, the
+// narrowing rounds to nearest even, round() takes halfway cases away from
+// zero, qs is clamped to [-127, 127], qs = 0 where d = 0 or x / d is NaN.
+
+// d narrowed to binary16 (round to nearest even), as its 16 bits in the low
+// half of a word: the packed conversion of (0, d), kept in 32-bit registers.
+__device__ __forceinline__ uint32_t f16_bits_rn(float d) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(0.f), "f"(d));
+    return r & 0xFFFFu;
+}
+
+// The quant of x for the block scale d (see the readings above).
+__device__ __forceinline__ int q8_quant(float x, float d) {
+    if (d == 0.f) return 0;
+    const float t = __fdiv_rn(x, d);
+    if (isnan(t)) return 0;
+    return static_cast<int>(fminf(fmaxf(roundf(t), -127.f), 127.f));
+}
+
+// The quant byte of x, as q8_quant gives it, without a division in the
+// common case.  With r = 1/d correctly rounded and t' = x * r rounded,
+// t' = (x/d)(1 + e1)(1 + e2) and fl(x/d) = (x/d)(1 + e3), |e_i| <= 2^-24, so
+// |t' - fl(x/d)| <= 127.5 * (3 * 2^-24 + 2^-48) < 2.3e-5 when |t'| < 127.4.
+// Rounding t' to the nearest integer (adding 1.5 * 2^23 leaves it in the low
+// mantissa bits, two's complement for negatives) then gives the same integer
+// as rounding fl(x/d), half away from zero, unless t' is within 1e-4 of a
+// half-integer; those, and every t' out of range or not finite (d = 0, a
+// subnormal d whose reciprocal overflows, NaN or infinite x), take q8_quant.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+__device__ __forceinline__ uint32_t q8_quant_byte(float x, float d, float r) {
+    const float t = __fmul_rn(x, r);
+    const float m = __fadd_rn(t, kRoundMagic);
+    const float ri = __fsub_rn(m, kRoundMagic);  // t rounded to an integer, exactly
+    if (fabsf(t) < 127.4f && fabsf(__fsub_rn(t, ri)) < 0.4999f) return __float_as_uint(m) & 0xFFu;
+    return static_cast<uint32_t>(q8_quant(x, d)) & 0xFFu;
+}
+
 // 16-byte streaming store (output written once, not re-read by this kernel).
 __device__ __forceinline__ void st_global_cs_v4(float* p, float a, float b, float c, float d) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),

@@ -79,6 +79,18 @@ cudaError_t launch_gemv_q4_0_tc(const float* A, const uint8_t* wq, float* C, int
                                 bool* launched);
 cudaError_t gemv_tc_read_device_error(unsigned int* bits, bool clear);
 
+// The staged GEMV's integer consumer for the product with the activations
+// quantized to Q8_0 first (K % 256 == 0, 16-byte aligned A and wq, M = 1..8);
+// a split K adds up through thread-block clusters.  Sets *launched = false and
+// enqueues nothing when no launch plan fits.
+cudaError_t launch_gemv_q4_0_q8act_tc(const float* A, const uint8_t* wq, float* C, int M, int64_t N,
+                                      int64_t K, cudaStream_t stream, const DeviceInfo& dev, bool* launched);
+
+// C = dequant_q8_0(quantize_q8_0(A)) x dequant(W)^T for M = 1..8, K % 32 == 0
+// (gemv_q8act.cu): the staged kernel where it applies, else a generic one.
+cudaError_t launch_matmul_q4_0_q8act(const float* A, const uint8_t* wq, float* C, int M, int64_t N, int64_t K,
+                                     cudaStream_t stream, const DeviceInfo& dev);
+
 // The staged GEMV's launch plan for a device with sm_count SMs and smem_optin
 // bytes of opt-in shared memory, without touching a device: with fit (the
 // resident clusters of 2, 4 and 8 CTAs) the regular path's, else that of a

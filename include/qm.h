@@ -228,6 +228,27 @@ QM_API int qm_matmul_q4_0_noalloc(const float* A, const void* wq, float* C, int6
                                   int64_t N, int64_t K, void* stream);
 
 /*
+ * qm_matmul_q4_0_q8act — the decode-regime product with the activations
+ * quantized to Q8_0 first: C = A' x dequant(W)^T, A' = dequant_q8_0(
+ * quantize_q8_0(A)) row by row (the GEMV fused with a preceding activation
+ * quantization, the "act-quant fusion" item of "vulkan: shader and sequencing
+ * efficiency backlog"; quantize_q8_0 with the readings of qm_quantize_q8_0).
+ * A is read as f32 and quantized on chip; nothing but C is written.  Each
+ * block of 32 then factors exactly into integers (d_a d_w (sum q qs - 8 sum
+ * qs)), so the product runs on integer dot products, with one f32 rounding per
+ * block; results agree with the exact product of A' and W to |error| <= 1e-5 *
+ * sum_k |A'[m][k] * W[n][k]| + 1e-7, and infinities and NaN (a scale past
+ * binary16's range) by class.  It is NOT the product with A: quantization
+ * moves each activation by up to about half its block's step, max|x| / 254.
+ *   A, wq, C, M, N, K, stream, alignment and aliasing: as qm_matmul_q4_0.
+ *   M = 1..8 (M > 8 returns QM_ERR_TOO_LARGE); K % 256 == 0 with 16-byte
+ *   aligned A and wq takes the staged kernel, other shapes a generic one.
+ * Returns QM_OK or a negative status.
+ */
+QM_API int qm_matmul_q4_0_q8act(const float* A, const void* wq, float* C, int64_t M, int64_t N,
+                                int64_t K, void* stream);
+
+/*
  * qm_gemv_q4_0_list — a list of decode-regime products C_p = A_p x
  * dequant(W_p)^T (sections "qmatvec_q4_0" and "matmul_q4_0_tiled"; the
  * GEMV's cost is streaming the weight blocks once), all with the same M, in
