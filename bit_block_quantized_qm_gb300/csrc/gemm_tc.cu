@@ -448,10 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait_bounded(&raw_full[rs], (kt / kRawStages) & 1, &g_gemm_error);
             if (ok && kt >= kWStages)
                 ok = mbar_wait_bounded(&w_empty[ws], ((kt / kWStages) - 1) & 1, &g_gemm_error);
-            if (ok) ok = mbar_wait_bounded(&a_full[as], (kt / kAStages) & 1, &g_gemm_error);
-            uint8_t* ast = a_st + (2 * as) * kTileA;
-            float4 x[4];
             if (ok) {
+                // The weight tile first: the activation tile's copy, issued
+                // when its stage came free, lands meanwhile.
                 const uint8_t* blk =
                     raw + rs * kRawBytes + n * kRawRow + ((36 * (kt0 + kt)) & 15) + half * kBlockBytes;
                 uint8_t* thi = w_st + (2 * ws) * kTileW;
@@ -461,6 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else if (n < wn) {  // rows past a 112-column tile are not decoded
                     decode_half_block(blk, dt & 1, n, half, thi, thi + kTileW);
                 }
+            }
+            if (ok) ok = mbar_wait_bounded(&a_full[as], (kt / kAStages) & 1, &g_gemm_error);
+            uint8_t* ast = a_st + (2 * as) * kTileA;
+            float4 x[4];
+            if (ok) {
                 // This thread's 16 floats of the f32 activation tile: float4
                 // j * 512 + dt, i.e. row 32 j + dt / 16, k = 4 (dt % 16) .. + 3
                 // (each quarter warp reads 128 contiguous bytes).
@@ -643,17 +647,16 @@ bool gemm_tc_supported(const float* A, const uint8_t* wq, int64_t M, int64_t N, 
 
 namespace {
 
-// Tile width: 256 columns where the output has enough of them to fill the
-// GPU without splitting K, or K is long, and M is at least 256; 128 columns
-// otherwise.  Measured on GB300 (CUDA-graph replay): 256 columns run 512 x
-// 14336 x 4096 in 164 against 178 us, 512 x 4096 x 14336 in 166 against
-// 202 us and 1024 x 14336 x 4096 in 257 against 348 us; 128 columns run
-// 512 x 4096 x 4096 in 62 against 66 us, 256 x 4096 x 4096 in 43 against
-// 55 us and 32 x 4096 x 4096 in 33 against 62 us (wide tiles decode twice
-// the weight rows for the same few activation rows).
-int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& dev) {
-    const int64_t tiles256 = ((N + 255) / 256) * ((M + BM - 1) / BM);
-    return (M >= 256 && (4 * tiles256 >= 3 * dev.sm_count || K >= 8192)) ? 256 : 128;
+// Tile width: 256 columns when M is at least 256 and N at least 2048 (or K is
+// long), 128 columns otherwise.  With the activation split inside the kernel a
+// 256-column tile splits each activation tile for twice the columns, and
+// that decides most shapes (CUDA-graph replay on GB300): 256 x 4096 x 4096
+// runs in 36.7 against 49.2 us, 512 x 4096 x 4096 in 61.7 (K split in two
+// through clusters) against 83.1 us with 112-column tiles; 512 x 1024 x 4096
+// stays faster with 128 columns (29.5 against 37.3 us), and so does M = 32
+// (29.0 against 29.3, 36.8 us with N-wide tiles at any M).
+int choose_bn(int64_t M, int64_t N, int64_t K, const DeviceInfo& /*dev*/) {
+    return (M >= 256 && (N >= 2048 || K >= 8192)) ? 256 : 128;
 }
 
 // Work items for one CTA per SM.  Whole tiles fill as many full waves as they

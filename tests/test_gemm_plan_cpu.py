@@ -71,11 +71,14 @@ def test_work_items_cover_every_tile_once(lib, shape, sm_count):
     assert count.min() == 1 and count.max() == 1
 
 
-def test_narrow_tiles_fill_more_sms(lib):
-    # 512 x 4096: 128 tiles of 128 columns, 148 of 112, both without a K split.
+def test_tile_widths(lib):
+    # 130 x 8000: 126 tiles of 128 columns, 144 of 112, both without a K split.
+    plan = qm.qm_gemm_plan(130, 8000, 512, 152)
+    assert plan["BN"] == 112 and plan["tiles"] == 144 and plan["items"] == 144
+    # M >= 256 with N >= 2048 takes 256-column tiles (512 x 4096: 64 tiles,
+    # K split in two through clusters); 512 x 1024 splits K with 128 columns.
     plan = qm.qm_gemm_plan(512, 4096, 4096, 152)
-    assert plan["BN"] == 112 and plan["tiles"] == 148 and plan["items"] == 148
-    # 1024 x 14336 takes 256-column tiles; 512 x 1024 splits K with 128 columns.
+    assert plan["BN"] == 256 and plan["s_rem"] == 2 and plan["items"] == 128
     assert qm.qm_gemm_plan(1024, 14336, 4096, 152)["BN"] == 256
     assert qm.qm_gemm_plan(512, 1024, 4096, 152)["BN"] == 128
 
