@@ -874,15 +874,18 @@ def q8_0_leg(qm, dev, peaks) -> dict:
 
 def profile_case(args) -> None:
     """Run one operation a few times on cuda:0 and exit, for profiler captures
-    (``--profile-case gemm --M .. --N .. --K .. [--algo QM_ALGO_*]``, any M,
-    or ``--profile-case q8_0``).
+    (``--profile-case gemm --M .. --N .. --K .. [--algo QM_ALGO_*]``, any M;
+    ``--profile-case q8act --M .. --N .. --K ..``, M <= 8; ``--profile-case
+    list --layers L``: the M = 1 decoder projections of L layers (the
+    decoder sweep's shapes and weights) as one independent list through
+    qm_gemv_q4_0_list; or ``--profile-case q8_0``).
     Prints a one-line note, not a bench line."""
     import torch
     import bit_block_quantized_qm_gb300 as qm
     qm.load_library()
     dev = torch.device("cuda", 0)
     sh = int(torch.cuda.current_stream().cuda_stream)
-    if args.profile_case == "gemm":
+    if args.profile_case in ("gemm", "q8act"):
         M, N, K = args.M, args.N, args.K
         blob = synth.q4_0_weights(N, K, 1)
         A = synth.activations(M, K, 2)
@@ -890,8 +893,22 @@ def profile_case(args) -> None:
         a = torch.from_numpy(A).to(dev)
         c = torch.empty((M, N), dtype=torch.float32, device=dev)
         for _ in range(args.calls):
-            rc = qm.qm_matmul_q4_0_algo_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K,
-                                            args.algo, sh)
+            if args.profile_case == "gemm":
+                rc = qm.qm_matmul_q4_0_algo_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K,
+                                                args.algo, sh)
+            else:
+                rc = qm.qm_matmul_q4_0_q8act_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, sh)
+            if rc != qm.QM_OK:
+                raise RuntimeError(qm.qm_status_string(rc))
+    elif args.profile_case == "list":
+        cases = synth.workload(4, layers=args.layers, sweep_m=(1,))
+        ws = [torch.from_numpy(c.weights()).to(dev) for c in cases]
+        acts = {K: torch.from_numpy(synth.activations(1, K, 5, key=(2, 1, K))).to(dev) for K in (4096, 14336)}
+        outs = [torch.empty((1, c.N), dtype=torch.float32, device=dev) for c in cases]
+        problems = [(acts[c.K].data_ptr(), w.data_ptr(), o.data_ptr(), c.N, c.K, -1)
+                    for c, w, o in zip(cases, ws, outs)]
+        for _ in range(args.calls):
+            rc = qm.qm_gemv_q4_0_list_ptr(problems, 1, 0, sh)
             if rc != qm.QM_OK:
                 raise RuntimeError(qm.qm_status_string(rc))
     else:
@@ -918,12 +935,13 @@ def main(argv=None) -> None:
                    help="skip the CPU oracle timing (for profiler runs)")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the M=1 GEMV, decoder-sweep and prefill reports (profiler runs)")
-    p.add_argument("--profile-case", choices=("gemm", "q8_0"), default=None,
+    p.add_argument("--profile-case", choices=("gemm", "q8act", "list", "q8_0"), default=None,
                    help="run one operation a few times and exit (profiler captures)")
     p.add_argument("--M", type=int, default=512)
     p.add_argument("--N", type=int, default=4096)
     p.add_argument("--K", type=int, default=4096)
     p.add_argument("--calls", type=int, default=3)
+    p.add_argument("--layers", type=int, default=8, help="decoder layers for --profile-case list")
     p.add_argument("--algo", type=int, default=0,
                    help="QM_ALGO_* value for --profile-case gemm (0: automatic choice)")
     args = p.parse_args(argv)
