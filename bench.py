@@ -509,11 +509,13 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
 
     prefill = None
     q8 = None
+    host_cost = None
     if not args.no_sweep:
         legs = configs_leg(qm, dev, peaks, clocks)
         roofline["per_config"].update(legs["gemv"])
         prefill = legs["prefill"]
         q8 = legs["q8_0"]
+        host_cost = legs["host"]
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -528,6 +530,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                 "overlap": "inputs, kernels and outputs on three streams; step i+1's inputs "
                            "and step i-1's outputs move while step i computes"},
         "gpu_launches": launches,
+        "host_us_per_call": host_cost,
         "paths": paths,
         "q8_0": q8,
         "clocks": clocks,
@@ -819,7 +822,56 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
                              f"{fp32_peak:.1f} TFLOP/s at {sm_max} MHz")
     del weights
     torch.cuda.empty_cache()
-    return {"gemv": gemv, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks)}
+    return {"gemv": gemv, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks),
+            "host": host_cost_leg(qm, dev)}
+
+
+def host_cost_leg(qm, dev) -> dict:
+    """Host time per call, eager: 200 calls enqueued back to back (the GPU
+    queue never fills), wall clock around the enqueue loop only.  Includes
+    the ctypes call from Python; ``ctypes_floor`` is a call of qm_version
+    through the same binding."""
+    import torch
+    sh = int(torch.cuda.current_stream().cuda_stream)
+
+    def per_call(fn, n=200):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        t1 = time.perf_counter()
+        torch.cuda.synchronize()
+        return (t1 - t0) / n * 1e6
+
+    lib = qm.load_library()
+    out = {"unit": "us per call", "ctypes_floor": per_call(lambda: lib.qm_version(), 2000)}
+    for name, (M, N, K) in (("gemv_m1_k4096_n4096", (1, 4096, 4096)), ("gemv_m8_k4096_n14336", (8, 14336, 4096)),
+                            ("gemm_m512_k4096_n4096", (512, 4096, 4096))):
+        w = torch.from_numpy(synth.q4_0_weights(N, K, 1)).to(dev)
+        a = torch.from_numpy(synth.activations(M, K, 2)).to(dev)
+        c = torch.empty((M, N), dtype=torch.float32, device=dev)
+
+        def call(a=a, w=w, c=c, M=M, N=N, K=K):
+            rc = qm.qm_matmul_q4_0_ptr(a.data_ptr(), w.data_ptr(), c.data_ptr(), M, N, K, sh)
+            if rc != qm.QM_OK:
+                raise RuntimeError(qm.qm_status_string(rc))
+        out["qm_matmul_q4_0_" + name] = per_call(call, 200 if M < 512 else 50)
+        del w, a, c
+    cases = synth.workload(4, layers=1, sweep_m=(1,))
+    ws = [torch.from_numpy(c.weights()).to(dev) for c in cases]
+    acts = {K: torch.from_numpy(synth.activations(1, K, 5)).to(dev) for K in (4096, 14336)}
+    outs = [torch.empty((1, c.N), dtype=torch.float32, device=dev) for c in cases]
+    problems = [(acts[c.K].data_ptr(), w.data_ptr(), o.data_ptr(), c.N, c.K, -1)
+                for c, w, o in zip(cases, ws, outs)]
+
+    def list_call():
+        rc = qm.qm_gemv_q4_0_list_ptr(problems, 1, 0, sh)
+        if rc != qm.QM_OK:
+            raise RuntimeError(qm.qm_status_string(rc))
+    out["qm_gemv_q4_0_list_one_layer_7_problems"] = per_call(list_call, 100)
+    return out
 
 
 def q8_0_leg(qm, dev, peaks) -> dict:

@@ -3,6 +3,10 @@
 Each CUDA source compiles to an object in parallel; the objects link into
 ``bit_block_quantized_qm_gb300/_build/libqm.so`` with the CUDA runtime linked
 statically, so the library needs only the NVIDIA driver at run time.
+
+``build_test_hooks()`` builds a second copy with the test-only hooks of
+``include/qm_test.h`` compiled in (``-DQM_TEST_HOOKS``), into
+``_build/test/libqm.so``; the product library never carries them.
 """
 from __future__ import annotations
 
@@ -39,11 +43,11 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra, out_dir: str = BUILD) -> str:
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
     deps = [os.path.join(CSRC, src), *(os.path.join(CSRC, h) for h in HEADERS),
-            os.path.join(ROOT, "include", "qm.h")]
-    if _stale(obj, deps) or extra:
+            os.path.join(ROOT, "include", "qm.h"), os.path.join(ROOT, "include", "qm_test.h")]
+    if _stale(obj, deps) or (extra and out_dir == BUILD):
         cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,6 +72,24 @@ def build(extra_flags=(), force: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
     return LIB
+
+
+TEST_BUILD = os.path.join(BUILD, "test")
+TEST_LIB = os.path.join(TEST_BUILD, "libqm.so")
+
+
+def build_test_hooks() -> str:
+    """Compile (if stale) and link the test-hook copy of libqm.so; returns its path."""
+    os.makedirs(TEST_BUILD, exist_ok=True)
+    flags = ["-DQM_TEST_HOOKS"]
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(lambda s: _compile(s, flags, TEST_BUILD), SOURCES))
+    if _stale(TEST_LIB, objs):
+        cmd = [nvcc(), *ARCH, "-shared", "-o", TEST_LIB, *objs, "-cudart", "static"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    return TEST_LIB
 
 
 if __name__ == "__main__":

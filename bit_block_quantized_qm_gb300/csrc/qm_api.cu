@@ -14,6 +14,11 @@
 
 #include "qm.h"
 #include "qm_internal.h"
+#ifdef QM_TEST_HOOKS
+#include <atomic>
+
+#include "qm_test.h"
+#endif
 
 namespace qm {
 
@@ -30,11 +35,29 @@ std::once_flag g_encode_once;
 
 }  // namespace
 
+#ifdef QM_TEST_HOOKS
+namespace {
+std::atomic<int> g_injected_errors{0};
+}  // namespace
+
+bool take_injected_error() {
+    int n = g_injected_errors.load();
+    while (n > 0 && !g_injected_errors.compare_exchange_weak(n, n - 1)) {
+    }
+    return n > 0;
+}
+#endif
+
 void note_launch() { __atomic_fetch_add(&g_launches, 1, __ATOMIC_RELAXED); }
 
 uint64_t launch_count() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
 
 cudaError_t current_device_info(DeviceInfo* out) {
+#ifdef QM_TEST_HOOKS
+    // An injected failure (qm_test_inject_error): the calling entry point
+    // returns QM_ERR_CUDA before anything is enqueued.
+    if (take_injected_error()) return cudaErrorUnknown;
+#endif
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -470,5 +493,13 @@ int qm_device_status(void* stream, int clear) {
     if (qm::gemv_list_read_device_error(&bits, clear != 0) != cudaSuccess) return QM_ERR_CUDA;
     return bits ? QM_ERR_TIMEOUT : QM_OK;
 }
+
+#ifdef QM_TEST_HOOKS
+int qm_test_inject_error(int calls) {
+    if (calls < 0) return QM_ERR_SHAPE;
+    qm::g_injected_errors.store(calls);
+    return QM_OK;
+}
+#endif
 
 }  // extern "C"
