@@ -786,6 +786,21 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
         gemv[f"cfg4_sweep_m1_list_{name}"] = gemv_row(
             f"32-layer decoder sweep at M=1 through qm_gemv_q4_0_list ({name}): CUDA graph of "
             f"{nl} list launches", "gemv_q4_0_list", wbytes, ms, nl)
+
+    # The act-quant product through its list (qm_gemv_q4_0_q8act_list): one
+    # list of all 224 independent GEMVs, and the chained one.
+    def run_q8_lists(lists, with_ctr):
+        s = sh()
+        for lst in lists:
+            rc = qm.qm_gemv_q4_0_list_ptr(lst, 1, ctr.data_ptr() if with_ctr else 0, s, q8act=True)
+            if rc != qm.QM_OK:
+                raise RuntimeError(f"q8act gemv list: {qm.qm_status_string(rc)}")
+    for name, lists, with_ctr, nl in variants[1:]:
+        ms = graph_ms(torch, lambda lists=lists, with_ctr=with_ctr: run_q8_lists(lists, with_ctr))
+        gemv[f"cfg4_sweep_m1_q8act_list_{name}"] = gemv_row(
+            f"32-layer decoder sweep at M=1 with the activations quantized to Q8_0 in the kernel, "
+            f"through qm_gemv_q4_0_q8act_list ({name}): CUDA graph of {nl} list launches",
+            "gemv_q4_0_list<q8>", wbytes, ms, nl)
     del louts
 
     # The same weights with q|k|v and gate|up stacked by rows (one row-major
@@ -930,7 +945,8 @@ def profile_case(args) -> None:
     ``--profile-case q8act --M .. --N .. --K ..``, M <= 8; ``--profile-case
     list --layers L``: the M = 1 decoder projections of L layers (the
     decoder sweep's shapes and weights) as one independent list through
-    qm_gemv_q4_0_list; or ``--profile-case q8_0``).
+    qm_gemv_q4_0_list (``--q8act``: qm_gemv_q4_0_q8act_list); or
+    ``--profile-case q8_0``).
     Prints a one-line note, not a bench line."""
     import torch
     import bit_block_quantized_qm_gb300 as qm
@@ -960,7 +976,7 @@ def profile_case(args) -> None:
         problems = [(acts[c.K].data_ptr(), w.data_ptr(), o.data_ptr(), c.N, c.K, -1)
                     for c, w, o in zip(cases, ws, outs)]
         for _ in range(args.calls):
-            rc = qm.qm_gemv_q4_0_list_ptr(problems, 1, 0, sh)
+            rc = qm.qm_gemv_q4_0_list_ptr(problems, 1, 0, sh, q8act=args.q8act)
             if rc != qm.QM_OK:
                 raise RuntimeError(qm.qm_status_string(rc))
     else:
@@ -994,6 +1010,8 @@ def main(argv=None) -> None:
     p.add_argument("--K", type=int, default=4096)
     p.add_argument("--calls", type=int, default=3)
     p.add_argument("--layers", type=int, default=8, help="decoder layers for --profile-case list")
+    p.add_argument("--q8act", action="store_true",
+                   help="--profile-case list through qm_gemv_q4_0_q8act_list (the act-quant product)")
     p.add_argument("--algo", type=int, default=0,
                    help="QM_ALGO_* value for --profile-case gemm (0: automatic choice)")
     args = p.parse_args(argv)

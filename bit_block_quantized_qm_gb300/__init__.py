@@ -35,7 +35,7 @@ __all__ = [
     "QM_OK", "QM_ERR_NULL", "QM_ERR_SHAPE", "QM_ERR_ALIGN", "QM_ERR_ALIAS", "QM_ERR_CUDA",
     "QM_ERR_TIMEOUT", "QM_ERR_UNSUPPORTED", "QM_ERR_POINTER", "QM_ERR_TOO_LARGE",
     "qm_matmul_q4_0_noalloc_ptr", "qm_selftest_wait_timeout",
-    "qm_matmul_q4_0_q8act", "qm_matmul_q4_0_q8act_ptr",
+    "qm_matmul_q4_0_q8act", "qm_matmul_q4_0_q8act_ptr", "qm_gemv_q4_0_q8act_list_ptr",
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
     "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
     "EXPORTED_SYMBOLS", "QmGemvProblem", "qm_gemv_q4_0_list_ptr", "qm_gemv_q4_0_list",
@@ -67,7 +67,8 @@ Q8_0_BLOCK_BYTES = 34
 EXPORTED_SYMBOLS = ("qm_version", "qm_status_string", "qm_dequant_q4_0", "qm_matmul_q4_0",
                     "qm_matmul_q4_0_algo", "qm_device_status", "qm_launch_count", "qm_gemv_plan", "qm_gemm_plan",
                     "qm_matmul_q4_0_noalloc", "qm_dequant_q8_0", "qm_quantize_q8_0",
-                    "qm_selftest_wait_timeout", "qm_gemv_q4_0_list", "qm_matmul_q4_0_q8act")
+                    "qm_selftest_wait_timeout", "qm_gemv_q4_0_list", "qm_matmul_q4_0_q8act",
+                    "qm_gemv_q4_0_q8act_list")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libqm.so")
@@ -133,6 +134,8 @@ def load_library() -> ctypes.CDLL:
             lib.qm_quantize_q8_0.restype = i32
             lib.qm_gemv_q4_0_list.argtypes = [p, i64, i64, p, p]
             lib.qm_gemv_q4_0_list.restype = i32
+            lib.qm_gemv_q4_0_q8act_list.argtypes = [p, i64, i64, p, p]
+            lib.qm_gemv_q4_0_q8act_list.restype = i32
             lib.qm_launch_count.argtypes = []
             lib.qm_launch_count.restype = ctypes.c_uint64
             _lib = lib
@@ -196,15 +199,22 @@ def qm_matmul_q4_0_q8act_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
     return load_library().qm_matmul_q4_0_q8act(A, wq, C, M, N, K, stream)
 
 
-def qm_gemv_q4_0_list_ptr(problems, M: int, counters: int = 0, stream: int = 0) -> int:
+def qm_gemv_q4_0_list_ptr(problems, M: int, counters: int = 0, stream: int = 0,
+                          q8act: bool = False) -> int:
     """The list GEMV on raw addresses: `problems` is a sequence of (A, wq, C, N,
     K, wait_for) tuples of ints; `counters` the device address of len(problems)
-    uint32 (0 for none).  Returns the C status."""
+    uint32 (0 for none).  With `q8act`, qm_gemv_q4_0_q8act_list (the
+    act-quant product).  Returns the C status."""
     arr = (QmGemvProblem * max(1, len(problems)))()
     for i, (A, wq, C, N, K, wait_for) in enumerate(problems):
         arr[i] = QmGemvProblem(A, wq, C, N, K, wait_for, 0)
-    return load_library().qm_gemv_q4_0_list(ctypes.cast(arr, ctypes.c_void_p), len(problems), M,
-                                            counters or None, stream)
+    fn = load_library().qm_gemv_q4_0_q8act_list if q8act else load_library().qm_gemv_q4_0_list
+    return fn(ctypes.cast(arr, ctypes.c_void_p), len(problems), M, counters or None, stream)
+
+
+def qm_gemv_q4_0_q8act_list_ptr(problems, M: int, counters: int = 0, stream: int = 0) -> int:
+    """qm_gemv_q4_0_q8act_list on raw addresses (see qm_gemv_q4_0_list_ptr)."""
+    return qm_gemv_q4_0_list_ptr(problems, M, counters, stream, q8act=True)
 
 
 # ------------------------------------------------------------ torch tensors

@@ -272,6 +272,96 @@ __device__ __forceinline__ void unit_mma(const uint8_t* ra, const uint8_t* rb, c
     }
 }
 
+// ---- Integer consumer (the list of act-quant GEMVs: activations quantized to
+// Q8_0 on chip; see gemv_tc.cu for the exact block factoring).  Lane l takes
+// row l % 16 of the 16-row unit and half l / 16 of it (4 blocks, 72 bytes:
+// four 16-byte loads and one 8-byte load; rows (c + 1) * 144 bytes apart put
+// the 8 lanes of a quarter warp on distinct bank quads), and adds its blocks'
+// exact integer dots, scaled once per block, into two sums.
+__device__ __forceinline__ void half_unit_q8(const uint8_t* row, int h, const uint8_t* au, float acc[2]) {
+    uint32_t w[18];
+    if (h == 0) {  // bytes 0 .. 71
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 v = reinterpret_cast<const uint4*>(row)[i];
+            w[4 * i + 0] = v.x;
+            w[4 * i + 1] = v.y;
+            w[4 * i + 2] = v.z;
+            w[4 * i + 3] = v.w;
+        }
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 64);
+        w[16] = v.x;
+        w[17] = v.y;
+    } else {  // bytes 72 .. 143
+        const uint2 v = *reinterpret_cast<const uint2*>(row + 72);
+        w[0] = v.x;
+        w[1] = v.y;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint4 u = reinterpret_cast<const uint4*>(row + 80)[i];
+            w[2 + 4 * i + 0] = u.x;
+            w[2 + 4 * i + 1] = u.y;
+            w[2 + 4 * i + 2] = u.z;
+            w[2 + 4 * i + 3] = u.w;
+        }
+    }
+    const float* dq = reinterpret_cast<const float*>(au + 256);
+    const int* sq = reinterpret_cast<const int*>(au + 256 + 32);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t* Wp = w + 9 * (b >> 1);
+        uint32_t q[4];
+        float dw;
+        if ((b & 1) == 0) {  // even block: d in the low half of word 0, quants at bytes 2..17
+            q[0] = __byte_perm(Wp[0], Wp[1], 0x5432u);
+            q[1] = __byte_perm(Wp[1], Wp[2], 0x5432u);
+            q[2] = __byte_perm(Wp[2], Wp[3], 0x5432u);
+            q[3] = __byte_perm(Wp[3], Wp[4], 0x5432u);
+            dw = f16_bits_to_float(Wp[0] & 0xFFFFu);
+        } else {             // odd block: d in the high half of word 4, quants in words 5..8
+            q[0] = Wp[5];
+            q[1] = Wp[6];
+            q[2] = Wp[7];
+            q[3] = Wp[8];
+            dw = f16_bits_to_float(Wp[4] >> 16);
+        }
+        const int bi = 4 * h + b;
+        const int4* qa = reinterpret_cast<const int4*>(au + bi * 32);
+        const int4 a0 = qa[0], a1 = qa[1];
+        int sdot = __dp4a(static_cast<int>(q[0] & 0x0F0F0F0Fu), a0.x, 0);
+        sdot = __dp4a(static_cast<int>(q[1] & 0x0F0F0F0Fu), a0.y, sdot);
+        sdot = __dp4a(static_cast<int>(q[2] & 0x0F0F0F0Fu), a0.z, sdot);
+        sdot = __dp4a(static_cast<int>(q[3] & 0x0F0F0F0Fu), a0.w, sdot);
+        sdot = __dp4a(static_cast<int>((q[0] >> 4) & 0x0F0F0F0Fu), a1.x, sdot);
+        sdot = __dp4a(static_cast<int>((q[1] >> 4) & 0x0F0F0F0Fu), a1.y, sdot);
+        sdot = __dp4a(static_cast<int>((q[2] >> 4) & 0x0F0F0F0Fu), a1.z, sdot);
+        sdot = __dp4a(static_cast<int>((q[3] >> 4) & 0x0F0F0F0Fu), a1.w, sdot);
+        acc[b & 1] = fmaf(dw * dq[bi], static_cast<float>(sdot - sq[bi]), acc[b & 1]);
+    }
+}
+
+// Exact row sum of the act-quant product for a non-finite total: each
+// activation block quantized again from A (read through L2) exactly as on
+// chip, then A'_k = qs_k d_a times (q - 8) d_w element by element.
+__device__ __noinline__ float list_row_exact_q8(const uint8_t* row, int nblocks, const float* a) {
+    float s = 0.f;
+    for (int b = 0; b < nblocks; ++b) {
+        const float* x = a + kBlockElems * b;
+        float amax = 0.f;
+        for (int j = 0; j < kBlockElems; ++j) amax = fmaxf(amax, fabsf(__ldcg(x + j)));
+        const float d = __fdiv_rn(amax, 127.f);
+        const float da = f16_bits_to_float(f16_bits_rn(d));
+        const uint8_t* blk = row + kBlockBytes * b;
+        const float dw = f16_bits_to_float(static_cast<uint32_t>(blk[0]) | (static_cast<uint32_t>(blk[1]) << 8));
+        for (int j = 0; j < kBlockElems; ++j) {
+            const uint32_t byte = blk[2 + (j & 15)];
+            const uint32_t nib = (j < 16) ? (byte & 0xFu) : (byte >> 4);
+            s = fmaf(static_cast<float>(q8_quant(__ldcg(x + j), d)) * da, magic_minus8(nib | kMagicBits) * dw, s);
+        }
+    }
+    return s;
+}
+
 // Exact row sum for a non-finite total (activations read through L2: they may
 // have been written by other CTAs during this launch).
 __device__ __noinline__ float list_row_exact(const uint8_t* row, int nblocks, const float* a) {
@@ -344,6 +434,7 @@ __device__ __forceinline__ bool wait_idle(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+template <bool kQ8>
 __global__ void __launch_bounds__(kLThreads, 1)
     gemv_q4_0_list(const __grid_constant__ ListParams P) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -522,7 +613,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
             ok = wait_stage(a_full, rounds & 1, abort_flag);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
-            for (int u = warp; u < (q.K >> 8); u += kLW) unit_fragments(frag + u * 1024, lane);
+            for (int u = warp; u < (q.K >> 8); u += kLW) {
+                if constexpr (kQ8) quantize_unit_q8<1>(frag + u * 1024, lane);
+                else unit_fragments(frag + u * 1024, lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(frag_ready);
             // Every warp's share of the fragments is written (a bounded wait:
@@ -539,7 +633,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const int cu = q.c;
         const int row_b = (cu + 1) * kUnitB;
         const int slot_off = (cu == 16 ? 0 : (warp >> 3) * box_bytes(8)) + (warp & (cu - 1)) * kUnitB +
-                             g * row_b;
+                             (kQ8 ? (lane & 15) : g) * row_b;
         const uint8_t* fbase = (g >> 1) == t ? frag : zeros;
         const int fstep = (g >> 1) == t ? 1024 : 0;
         // Position warp, then warp + 16, ... of the CTA's unit sequence:
@@ -557,18 +651,26 @@ __global__ void __launch_bounds__(kLThreads, 1)
             if (s0 + warp < total) {
                 if (u < 16) acc[0] = acc[1] = 0.f;
                 const uint8_t* ra = ring + st * kStageB + slot_off;
-                unit_mma(ra, ra + 8 * row_b, fbase + u * fstep, g, t, acc);
+                if constexpr (kQ8) half_unit_q8(ra, lane >> 4, frag + u * 1024, acc);
+                else unit_mma(ra, ra + 8 * row_b, fbase + u * fstep, g, t, acc);
                 // The stage's bytes are in registers: hand it back to the
                 // producer before adding anything up.
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
                 if (u + 16 >= U) {
-                    // This warp's last unit of tile k: its row sums to the slot.
+                    // This warp's last unit of tile k: its row sums to the slot
+                    // (MMA consumer: rows g and g + 8 from the lanes t = 0;
+                    // integer consumer: row l from lanes l < 16).
                     float s0v = acc[0], s1v = acc[1];
-                    s0v += __shfl_xor_sync(0xFFFFFFFFu, s0v, 1);
-                    s1v += __shfl_xor_sync(0xFFFFFFFFu, s1v, 1);
-                    s0v += __shfl_xor_sync(0xFFFFFFFFu, s0v, 2);
-                    s1v += __shfl_xor_sync(0xFFFFFFFFu, s1v, 2);
+                    if constexpr (kQ8) {
+                        s0v += s1v;
+                        s0v += __shfl_xor_sync(0xFFFFFFFFu, s0v, 16);
+                    } else {
+                        s0v += __shfl_xor_sync(0xFFFFFFFFu, s0v, 1);
+                        s1v += __shfl_xor_sync(0xFFFFFFFFu, s1v, 1);
+                        s0v += __shfl_xor_sync(0xFFFFFFFFu, s0v, 2);
+                        s1v += __shfl_xor_sync(0xFFFFFFFFu, s1v, 2);
+                    }
                     const int tile_l = tl + k;
                     const int sl = tile_l % kTileSlots;
                     // The slot's previous tile must have been added up.
@@ -586,7 +688,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     ok = __all_sync(0xFFFFFFFFu, ok);
                     if (!ok) break;
                     float* my = slots + (sl * kLW + warp) * 16;
-                    if (t == 0) {
+                    if constexpr (kQ8) {
+                        if (lane < 16) my[lane] = s0v;
+                    } else if (t == 0) {
                         my[g] = s0v;
                         my[g + 8] = s1v;
                     }
@@ -607,8 +711,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
                         }
                         const int row = 16 * tile + lane;
                         if (lane < 16 && row < q.N) {
-                            if (!isfinite(v))
-                                v = list_row_exact(q.W + static_cast<int64_t>(row) * U * kUnitB, U * 8, q.A);
+                            if (!isfinite(v)) {
+                                const uint8_t* wrow = q.W + static_cast<int64_t>(row) * U * kUnitB;
+                                v = kQ8 ? list_row_exact_q8(wrow, U * 8, q.A) : list_row_exact(wrow, U * 8, q.A);
+                            }
                             q.C[row] = v;
                         }
                         // Only a problem that others wait on needs its stores
@@ -643,16 +749,17 @@ __global__ void __launch_bounds__(kLThreads, 1)
 }  // namespace
 
 cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned* counters,
-                                  cudaStream_t stream, const DeviceInfo& dev) {
+                                  cudaStream_t stream, const DeviceInfo& dev, bool q8) {
     if (count <= 0) return cudaSuccess;
     if (count > kListMaxProblems) return cudaErrorInvalidValue;
-    static int configured[64] = {0};
+    static int configured[2][64] = {};
     if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
     if (kLSmem > dev.max_smem_optin) return cudaErrorInvalidValue;
-    if (!__atomic_load_n(&configured[dev.device], __ATOMIC_ACQUIRE)) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_q4_0_list, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmem);
+    void (*const kernel)(ListParams) = q8 ? gemv_q4_0_list<true> : gemv_q4_0_list<false>;
+    if (!__atomic_load_n(&configured[q8][dev.device], __ATOMIC_ACQUIRE)) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmem);
         if (e != cudaSuccess) return e;
-        __atomic_store_n(&configured[dev.device], 1, __ATOMIC_RELEASE);
+        __atomic_store_n(&configured[q8][dev.device], 1, __ATOMIC_RELEASE);
     }
     ListParams P;
     P.count = count;
@@ -708,7 +815,7 @@ cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned
         cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(max_wait + 1) * sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = launch_pdl(gemv_q4_0_list, dim3(P.grid), dim3(kLThreads), kLSmem, stream, P);
+    cudaError_t e = launch_pdl(kernel, dim3(P.grid), dim3(kLThreads), kLSmem, stream, P);
     if (e != cudaSuccess) return e;
     note_launch();
     return cudaSuccess;

@@ -365,12 +365,19 @@ int qm_matmul_q4_0_q8act(const float* A, const void* wq, float* C, int64_t M, in
 // persistent kernel takes (M = 1, K % 2048 == 0, K <= 14336, 16-byte aligned
 // A and wq) as launches of up to 128 problems; any other problem runs alone
 // through qm_matmul_q4_0's path, in list order on the same stream.
-int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M, uint32_t* counters,
-                      void* stream) {
+}  // extern "C"
+
+namespace {
+
+// qm_gemv_q4_0_list and qm_gemv_q4_0_q8act_list: the same checks and
+// grouping; q8 selects the act-quant product.
+int gemv_list_impl(const qm_gemv_problem* problems, int64_t count, int64_t M, uint32_t* counters,
+                   void* stream, bool q8) {
     if (count < 0 || M < 0) return QM_ERR_SHAPE;
     if (count == 0 || M == 0) return QM_OK;
     if (!problems) return QM_ERR_NULL;
     if (count > (int64_t(1) << 24)) return QM_ERR_SHAPE;
+    if (q8 && M > 8) return QM_ERR_TOO_LARGE;
     if (counters && (reinterpret_cast<uintptr_t>(counters) & 3u) != 0) return QM_ERR_ALIGN;
     std::vector<int64_t> ab(count), wb(count), cb(count);
     for (int64_t i = 0; i < count; ++i) {
@@ -426,7 +433,15 @@ int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M,
             continue;
         }
         if (!list_ok(p)) {
-            const int rc = run_matmul(p.A, p.wq, p.C, M, p.N, p.K, QM_ALGO_AUTO, s, dev);
+            int rc;
+            if (!q8) {
+                rc = run_matmul(p.A, p.wq, p.C, M, p.N, p.K, QM_ALGO_AUTO, s, dev);
+            } else if (p.K == 0) {
+                rc = from_cuda(cudaMemsetAsync(p.C, 0, static_cast<size_t>(M * p.N * 4), s));
+            } else {
+                rc = from_cuda(qm::launch_matmul_q4_0_q8act(p.A, static_cast<const uint8_t*>(p.wq), p.C,
+                                                            static_cast<int>(M), p.N, p.K, s, dev));
+            }
             if (rc != QM_OK) return rc;
             ++i;
             continue;
@@ -444,10 +459,24 @@ int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M,
             ++i;
         }
         const int rc = from_cuda(qm::launch_gemv_q4_0_list(items.data(), static_cast<int>(items.size()),
-                                                           counters ? counters + start : nullptr, s, dev));
+                                                           counters ? counters + start : nullptr, s, dev, q8));
         if (rc != QM_OK) return rc;
     }
     return QM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int64_t M, uint32_t* counters,
+                      void* stream) {
+    return gemv_list_impl(problems, count, M, counters, stream, false);
+}
+
+int qm_gemv_q4_0_q8act_list(const qm_gemv_problem* problems, int64_t count, int64_t M, uint32_t* counters,
+                            void* stream) {
+    return gemv_list_impl(problems, count, M, counters, stream, true);
 }
 
 uint64_t qm_launch_count(void) { return qm::launch_count(); }

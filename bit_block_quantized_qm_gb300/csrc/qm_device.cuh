@@ -273,6 +273,58 @@ __device__ __forceinline__ uint32_t q8_quant_byte(float x, float d, float r) {
     return static_cast<uint32_t>(q8_quant(x, d)) & 0xFFu;
 }
 
+// Quantize one unit of staged activations, f32 [M][256] as the TMA box lands,
+// in place into [M][256] signed quants, then [M][8] f32 scales (the narrowed
+// binary16 d, as f32), then [M][8] int32 values 8 * sum qs.  Lane l takes
+// elements 8 (l % 4) .. + 7 of block l / 4 of every row; a block's max and
+// quant sum meet over its four lanes by shuffles.  All rows are read before
+// anything is written (the outputs overlap the inputs).
+template <int M>
+__device__ __forceinline__ void quantize_unit_q8(uint8_t* unit, int lane) {
+    const int bl = lane >> 2;
+    const int part = lane & 3;
+    uint32_t qw[M][2];
+    float dv[M];
+    int bs[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const float4* src = reinterpret_cast<const float4*>(unit + (m * 256 + bl * 32 + 8 * part) * 4);
+        const float4 x0 = src[0], x1 = src[1];
+        const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(x[e]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const float d = __fdiv_rn(amax, 127.f);
+        const float r = __frcp_rn(d);
+        uint32_t qb[8];
+        int sum = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            qb[e] = q8_quant_byte(x[e], d, r);
+            sum += static_cast<int>(static_cast<int8_t>(qb[e]));
+        }
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);
+        qw[m][0] = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+        qw[m][1] = qb[4] | (qb[5] << 8) | (qb[6] << 16) | (qb[7] << 24);
+        dv[m] = f16_bits_to_float(f16_bits_rn(d));
+        bs[m] = 8 * sum;
+    }
+    __syncwarp();
+    float* dq = reinterpret_cast<float*>(unit + M * 256);
+    int* sq = reinterpret_cast<int*>(unit + M * 256 + M * 32);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        *reinterpret_cast<uint2*>(unit + m * 256 + bl * 32 + 8 * part) = make_uint2(qw[m][0], qw[m][1]);
+        if (part == 0) {
+            dq[m * 8 + bl] = dv[m];
+            sq[m * 8 + bl] = bs[m];
+        }
+    }
+}
+
 // 16-byte streaming store (output written once, not re-read by this kernel).
 __device__ __forceinline__ void st_global_cs_v4(float* p, float a, float b, float c, float d) {
     asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),

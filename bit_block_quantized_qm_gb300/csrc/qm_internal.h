@@ -126,9 +126,11 @@ struct GemvListItem {
 
 // The list GEMV: one persistent launch over `count` (<= kListMaxProblems)
 // problems.  `counters` (count unsigned, device memory) is required when some
-// wait_for >= 0; it is cleared on the stream first.
+// wait_for >= 0; it is cleared on the stream first.  With q8 every problem is
+// the act-quant product (activations quantized to Q8_0 on chip, integer
+// consumer).
 cudaError_t launch_gemv_q4_0_list(const GemvListItem* items, int count, unsigned* counters,
-                                  cudaStream_t stream, const DeviceInfo& dev);
+                                  cudaStream_t stream, const DeviceInfo& dev, bool q8 = false);
 cudaError_t gemv_list_read_device_error(unsigned int* bits, bool clear);
 
 

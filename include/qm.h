@@ -292,6 +292,19 @@ QM_API int qm_gemv_q4_0_list(const qm_gemv_problem* problems, int64_t count, int
                              uint32_t* counters, void* stream);
 
 /*
+ * qm_gemv_q4_0_q8act_list — qm_gemv_q4_0_list for the act-quant product of
+ * qm_matmul_q4_0_q8act: every problem computes C_p = dequant_q8_0(
+ * quantize_q8_0(A_p)) x dequant(W_p)^T, each activation vector quantized on
+ * chip, in one persistent launch where the shapes allow it (M = 1, K % 2048
+ * == 0, K <= 14336, 16-byte aligned A and wq); other problems run through
+ * qm_matmul_q4_0_q8act in list order.  Arguments, ordering (wait_for,
+ * counters), aliasing rules and errors: as qm_gemv_q4_0_list; M > 8 returns
+ * QM_ERR_TOO_LARGE.  Precision: as qm_matmul_q4_0_q8act.
+ */
+QM_API int qm_gemv_q4_0_q8act_list(const qm_gemv_problem* problems, int64_t count, int64_t M,
+                                   uint32_t* counters, void* stream);
+
+/*
  * qm_gemm_plan — the work items the prefill GEMM on tensor cores
  * (QM_ALGO_GEMM_TC) takes for (M, N, K) on a device with sm_count SMs on
  * which fit2, fit4 and fit8 thread-block clusters of 2, 4 and 8 of its CTAs

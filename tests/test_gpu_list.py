@@ -14,7 +14,11 @@ against the oracle, through the C ABI.
 * lists that the persistent kernel does not take (M = 2, K not a multiple of
   2048) run problem by problem and still match the oracle;
 * a row with an infinite scale over all-8 nibbles comes out NaN, as the
-  definition gives it.
+  definition gives it;
+* the act-quant list (qm_gemv_q4_0_q8act_list) against the oracle's
+  composition dequant_q8_0(quantize_q8_0(A)) x dequant(W)^T: mixed shapes,
+  the decoder chain (exact with one-hot weights), a non-finite scale and a
+  shape that runs outside the persistent kernel.
 """
 import numpy as np
 import pytest
@@ -165,3 +169,91 @@ def test_list_nonfinite_scale_row_recomputed(env):
     assert np.array_equal(np.isnan(got), np.isnan(C_ref)) and np.isnan(got[0, 3])
     fin = np.isfinite(C_ref)
     assert oracle.within_tolerance(got[fin], C_ref[fin], S_ref[fin], REL, ABS).all()
+
+
+# --------------------------------------------------- the act-quant list
+# qm_gemv_q4_0_q8act_list: every problem is dequant_q8_0(quantize_q8_0(A)) x
+# dequant(W)^T, checked against the oracle's composition.
+
+def run_q8_list(qm, problems, M, counters=None):
+    s = int(torch.cuda.current_stream().cuda_stream)
+    raw = [(A.data_ptr(), w.data_ptr(), C.data_ptr(), N, K, wf) for (A, w, C, N, K, wf) in problems]
+    rc = qm.qm_gemv_q4_0_q8act_list_ptr(raw, M, counters.data_ptr() if counters is not None else 0, s)
+    assert rc == qm.QM_OK, qm.qm_status_string(rc)
+    torch.cuda.synchronize()
+    assert qm.qm_device_status(clear=True) == qm.QM_OK
+
+
+def test_q8act_list_independent_mixed_shapes(env):
+    qm, o = env
+    host, problems = [], []
+    for i, (N, K) in enumerate(MIXED):
+        blob = synth.q4_0_weights(N, K, 700 + i)
+        A = synth.activations(1, K, 710 + i)
+        host.append((A, blob))
+        problems.append((torch.from_numpy(A).cuda(), torch.from_numpy(blob).cuda(),
+                         torch.full((1, N), float("nan"), device="cuda"), N, K, -1))
+    run_q8_list(qm, problems, 1)
+    first = [p[2].cpu().numpy() for p in problems]
+    for (A, blob), (N, K), C in zip(host, MIXED, first):
+        C_ref, S_ref = o.matmul_q4_0_q8act(A, blob, N, K)
+        ok = oracle.within_tolerance(C, C_ref, S_ref, REL, ABS)
+        assert ok.all(), f"N={N} K={K}: {int((~ok).sum())} entries outside tolerance"
+    for p in problems:
+        p[2].fill_(float("nan"))
+    run_q8_list(qm, problems, 1)
+    for p, C in zip(problems, first):
+        assert np.array_equal(p[2].cpu().numpy().view(np.uint32), C.view(np.uint32)), "not deterministic"
+
+
+@pytest.mark.parametrize("with_counters", [True, False], ids=["counters", "no_counters"])
+def test_q8act_list_dependent_chain_exact(env, with_counters):
+    # One-hot weights with d = 1: every output is one quantized activation,
+    # qs * d_a exactly, on both sides, so the chain is exact.
+    qm, o = env
+    g = synth.rng(720, (0,))
+    x = g.integers(-1000, 1001, (1, 4096)).astype(np.float32)
+    blobs = [one_hot_weights(N, K, 730 + i) for i, (_, N, K, _, _) in enumerate(CHAIN)]
+    ref = []
+    for (name, N, K, src, _), blob in zip(CHAIN, blobs):
+        A = x if src < 0 else ref[src].astype(np.float32).reshape(1, -1)
+        C_ref, _ = o.matmul_q4_0_q8act(A, blob, N, K)
+        ref.append(C_ref)
+    xs = torch.from_numpy(x).cuda()
+    outs = [torch.empty((1, N), device="cuda") for (_, N, _, _, _) in CHAIN]
+    ws = [torch.from_numpy(b).cuda() for b in blobs]
+    problems = []
+    for i, (name, N, K, src, wf) in enumerate(CHAIN):
+        A = xs if src < 0 else outs[src]
+        problems.append((A, ws[i], outs[i], N, K, wf))
+    counters = torch.full((len(CHAIN),), 777, dtype=torch.int32, device="cuda") if with_counters else None
+    for rep in range(2):
+        for c in outs:
+            c.fill_(float("nan"))
+        run_q8_list(qm, problems, 1, counters)
+        for (name, N, K, _, _), C, C_ref in zip(CHAIN, outs, ref):
+            got = C.cpu().numpy().ravel().astype(np.float64)
+            bad = got != C_ref.ravel()
+            assert not bad.any(), f"run {rep} {name}: {int(bad.sum())} entries differ"
+
+
+def test_q8act_list_non_finite_and_fallback(env):
+    qm, o = env
+    # A shape the persistent kernel takes with an infinite weight scale, and
+    # one it does not (K = 96: through qm_matmul_q4_0_q8act).
+    shapes = [(40, 2048), (33, 96)]
+    host, problems = [], []
+    for i, (N, K) in enumerate(shapes):
+        blob = synth.q4_0_weights(N, K, 740 + i).copy()
+        if i == 0:
+            off = (3 * (K // 32) + 1) * 18
+            blob[off:off + 2] = np.frombuffer(np.float16(np.inf).tobytes(), np.uint8)
+        A = synth.activations(1, K, 750 + i)
+        host.append((A, blob))
+        problems.append((torch.from_numpy(A).cuda(), torch.from_numpy(blob).cuda(),
+                         torch.zeros((1, N), device="cuda"), N, K, -1))
+    run_q8_list(qm, problems, 1)
+    for (A, blob), (N, K), p in zip(host, shapes, problems):
+        C_ref, S_ref = o.matmul_q4_0_q8act(A, blob, N, K)
+        assert oracle.within_tolerance(p[2].cpu().numpy(), C_ref, S_ref, REL, ABS).all(), (N, K)
+    assert not np.isfinite(o.matmul_q4_0_q8act(*host[0], *shapes[0])[0]).all()
