@@ -439,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // t / 4, block (t / 2) % 2 and quant bytes 8 (t % 2) .. 8 (t % 2) + 7.
         const int tpr = wn > 128 ? 2 : 4;
         const int dt = threadIdx.x - 64;
+        const int a_rows = min(BM, M - m0);  // activation rows of this tile
         const int n = dt / tpr;
         const int half = (tpr == 2) ? (dt & 1) : ((dt >> 1) & 1);
         for (int kt = 0; kt < KT; ++kt) {
@@ -467,15 +468,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok) {
                 // This thread's 16 floats of the f32 activation tile: float4
                 // j * 512 + dt, i.e. row 32 j + dt / 16, k = 4 (dt % 16) .. + 3
-                // (each quarter warp reads 128 contiguous bytes).
+                // (each quarter warp reads 128 contiguous bytes).  Rows past
+                // M are not split: whatever their pieces hold reaches only
+                // the MMA rows of outputs past M, which are never stored.
 #pragma unroll
-                for (int j = 0; j < 4; ++j) x[j] = *reinterpret_cast<const float4*>(ast + (j * 512 + dt) * 16);
+                for (int j = 0; j < 4; ++j)
+                    if (32 * j < a_rows) x[j] = *reinterpret_cast<const float4*>(ast + (j * 512 + dt) * 16);
             }
             // Every thread has read its floats before any piece overwrites
             // them; a failed wait anywhere stops all decode warps together.
             if (!named_barrier_and(2, kDecodeWarps * 32, ok)) break;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) split_store4(x[j], 32 * j + (dt >> 4), dt & 15, ast, ast + kTileA);
+            for (int j = 0; j < 4; ++j)
+                if (32 * j < a_rows) split_store4(x[j], 32 * j + (dt >> 4), dt & 15, ast, ast + kTileA);
             fence_proxy_async_shared();  // make the tiles visible to the tensor cores
             __syncwarp();
             if (lane == 0) {
