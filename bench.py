@@ -1,31 +1,36 @@
 """Benchmark of the Q4_0 x f32 hot path on GB300 (one JSON line on stdout).
 
-One step = one pass of the decode-batch GEMV workload, the FFN pair at M=8:
-  * GEMV M=8, K=4096,  N=14336 (FFN up projection),
-  * GEMV M=8, K=14336, N=4096  (FFN down projection),
-each through libqm's C ABI (qm_matmul_q4_0) on one stream.  Inputs are
-synthetic (seeded generators in ``synth``).  Every step uses a different
-replica of all operands, and the replicas together exceed the L2 several
-times, so no step finds its inputs in L2.
+One step = one pass of the M = 1 decode GEMVs of the 32-layer decoder sweep
+(hidden 4096, GQA: per layer q, o 4096 -> 4096; k, v 4096 -> 1024; gate, up
+4096 -> 14336; down 14336 -> 4096): 224 GEMVs streaming 3.93 GB of Q4_0
+weights, through libqm's C ABI as one call of qm_gemv_q4_0_list (two
+launches of the persistent list kernel, 128 and 96 independent problems, as
+the library splits a list; within a layer q, k
+and v read one input vector and gate and up another, as in a decoder).
+Inputs are synthetic (seeded generators in ``synth``); the weights are 30
+times the L2, so no step finds them there.
 
 value = Q4_0 weight bytes streamed per step / device time per step (GB/s), the
 GEMV weight-stream rate of the metric, timed with CUDA events over --steps
-steps after --warmup steps.  ``roofline`` is the GEMV launch with the longer
-event-timed duration, against the measured HBM copy rate.  ``e2e`` repeats the
-step with host operands: pinned host -> device copies of every input and
-device -> host copies of every output inside the timed region, the copies of
-neighbouring steps overlapping a step's kernels on separate streams.
+steps after --warmup steps.  ``roofline`` is the step's one launch against
+the measured HBM copy rate.  ``e2e`` repeats the step with host operands: the
+128 activation vectors copied host -> device and all 224 outputs device -> host
+inside the timed region, the copies of neighbouring steps overlapping a
+step's kernel on separate streams.
 
 Every other workload is reported in the same line: ``roofline.per_config``
-holds the GEMV and dequant rows (M=1 at K=N=4096 back to back, the step's two
-GEMVs, the dequant of the 14336 x 4096 weight, the 32-layer decoder sweep at
-M=1 and M=8) as weight GB/s against HBM, and ``prefill`` the GEMM rows (M=32
-and M=256 at 4096 x 4096, M=1024 at both FFN shapes, the decoder sweep at
-M=512) as TFLOP/s against the tensor-core bound.  ``q8_0`` holds the Q8_0
-quantize and dequant.
+holds the GEMV and dequant rows (M=1 at K=N=4096 back to back, config 1's
+M=8 up and down GEMVs, the dequant of the 14336 x 4096 weight, the decoder
+sweep as 224 launches at M=1 and M=8, stacked, through the list GEMV three
+ways, and through the act-quant GEMV and its list) as weight GB/s against HBM,
+and ``prefill`` the GEMM rows (M=32 and M=256 at 4096 x 4096, M=1024 at both
+FFN shapes, the decoder sweep at M=512) as TFLOP/s against the tensor-core
+bound.  ``q8_0`` holds the Q8_0 quantize and dequant, ``host_us_per_call``
+the host time of the C-ABI calls.
 
 ``cpu_baseline`` times the oracle (fp64 C) on this host on a bounded column
-sample of the step: one thread, and all cores through OpenMP.  ``--impl
+sample of the step (the first columns of each of layer 0's seven
+projections): one thread, and all cores through OpenMP.  ``--impl
 reference`` runs that oracle as the reference arm, each step a bounded column
 sample of the same workload, on the same metric.
 """
@@ -49,17 +54,22 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "Q4_0 GEMV weight GB/s (% of HBM peak); prefill TFLOP/s (% of roofline)"
-WORKLOAD = "q4_0_gemv_decode_batch_m8_ffn_up_down"
+WORKLOAD = "q4_0_gemv_decoder_sweep_m1_32_layers"
 FALLBACK_HBM_GBS = 6800.0
-REPLICAS = 4  # 4 x 66 MB of weights (plus activations) > 129 MB of L2
+REPLICAS = 4  # config 1's GEMVs: 4 x 66 MB of weights (plus activations) > 129 MB of L2
+SWEEP_LAYERS = 32
+STEP_REPLICAS = 3  # activation and output buffers of the step (the weights are shared)
 
 
 def bench_config(world: int) -> dict:
     """The workload description both arms print (identical dicts)."""
-    return {"workload": WORKLOAD, "M": 8,
-            "shapes": "K=4096,N=14336 (up); K=14336,N=4096 (down)",
-            "seeds": [1, 2],
-            "l2": f"{REPLICAS} rotating operand replicas (> L2) between steps",
+    return {"workload": WORKLOAD, "M": 1, "layers": SWEEP_LAYERS,
+            "projections": "q, o 4096->4096; k, v 4096->1024; gate, up 4096->14336; down 14336->4096",
+            "inputs": "per layer 4 activation vectors: q, k, v share one, gate and up one, o and down their own",
+            "gemvs_per_step": 7 * SWEEP_LAYERS, "seed": 5,
+            "api": "qm_gemv_q4_0_list: one call per step, 224 independent GEMVs (the library runs them "
+                   "as two persistent launches of at most 128 problems)",
+            "l2": "3.93 GB of weights per step, 30x the L2",
             "parallelism": f"replicas x{world}",
             "value_definition": "Q4_0 weight bytes streamed per step / step time"}
 
@@ -79,7 +89,7 @@ def measured_peaks() -> dict:
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 KERNEL_SOURCES = {"dequant_q4_0": "dequant.cu", "gemv_q4_0_tc": "gemv_tc.cu",
-                  "gemm_q4_0_tc": "gemm_tc.cu"}
+                  "gemm_q4_0_tc": "gemm_tc.cu", "gemv_q4_0_list": "gemv_list.cu"}
 
 
 def source_digest(kernel: str) -> str:
@@ -122,6 +132,41 @@ def job_gbs(bytes_per_rank: int, world: int, ms_step: float) -> float:
     """Whole-job throughput: the bytes every rank streamed in one step over
     the (slowest rank's) step time."""
     return bytes_per_rank * world / (ms_step * 1e-3) / 1e9
+
+
+DECODER_PROJS = tuple(p for (p, _, _) in synth.DECODER_LAYER)
+# The projection (index within a layer) whose input vector each one reads.
+SHARED_INPUT = {"q": 0, "k": 0, "v": 0, "o": 3, "gate": 4, "up": 4, "down": 6}
+
+
+def sweep_cases():
+    """The step's 224 GEMVs (M = 1), layer by layer."""
+    return synth.workload(4, layers=SWEEP_LAYERS, sweep_m=(1,))
+
+
+def sweep_operands(qm, torch, dev, cases, replicas: int):
+    """Device operands of the decoder sweep's GEMVs: the weights (resident,
+    shared by the replicas), and per replica one buffer of the layers'
+    activation vectors (q, k and v read one, gate and up another, o and down
+    their own), one buffer of all outputs and the list of problems over them.
+    Returns (weights, host activations, output floats, replicas)."""
+    weights = [torch.from_numpy(c.weights()).to(dev) for c in cases]
+    src = [7 * (i // 7) + SHARED_INPUT[DECODER_PROJS[i % 7]] for i in range(len(cases))]
+    inputs = sorted(set(src))
+    a_start = dict(zip(inputs, np.cumsum([0] + [cases[j].K for j in inputs])))
+    a_off = [a_start[j] for j in src]
+    c_off = np.cumsum([0] + [c.N for c in cases])
+    a_host = np.concatenate([cases[j].acts().ravel() for j in inputs])
+    reps = []
+    for _ in range(replicas):
+        A = torch.from_numpy(a_host).to(dev)
+        C = torch.empty(int(c_off[-1]), dtype=torch.float32, device=dev)
+        arr = qm.gemv_problem_array([
+            (A.data_ptr() + 4 * int(a_off[i]), weights[i].data_ptr(), C.data_ptr() + 4 * int(c_off[i]),
+             c.N, c.K, -1) for i, c in enumerate(cases)])
+        reps.append({"A": A, "C": C, "problems": arr})
+    torch.cuda.synchronize()
+    return weights, a_host, int(c_off[-1]), reps
 
 
 def step_cases():
@@ -221,12 +266,14 @@ def host_cores() -> int:
 
 
 class OracleSample:
-    """The CPU oracle on a bounded sample of one step: all M rows of the
-    first `cols` output columns of each GEMV (the rows of W they stream), with
-    `cols` sized so that the sample takes about `budget_s` seconds.  The
-    metric is a rate, weight bytes streamed per second, so the sample's own
-    bytes over its own time need no scaling.  With parallel=True the oracle
-    is the OpenMP build of the same source (entries shared over every core)."""
+    """The CPU oracle on a bounded sample of one step: the first `cols` output
+    columns (the rows of W they stream) of each of layer 0's seven
+    projections, with `cols` sized so that the sample takes about `budget_s`
+    seconds.  Every layer has the same shapes and weight distribution, so a
+    column of layer 0 costs what any layer's does.  The metric is a rate,
+    weight bytes streamed per second, so the sample's own bytes over its own
+    time need no scaling.  With parallel=True the oracle is the OpenMP build
+    of the same source (entries shared over every core)."""
 
     def __init__(self, budget_s: float, parallel: bool):
         import oracle
@@ -238,18 +285,17 @@ class OracleSample:
         else:
             self.threads = 1
             self.o = oracle.load()
-        self.up, self.down, _ = step_cases()
-        self.data = {c.name: (c.acts(), c.weights()) for c in (self.up, self.down)}
-        # Calibrate seconds per column (all M rows of one output column).
-        c = self.up
-        A, blob = self.data[c.name]
+        self.cases = synth.workload(4, layers=1, sweep_m=(1,))
+        self.data = {c.name: (c.acts(), c.weights()) for c in self.cases}
+        # Calibrate seconds per column per unit of K.
+        c = self.cases[0]
         n0 = 4 * self.threads
         self._run(c, n0)
         t0 = time.perf_counter()
         self._run(c, n0)
         per_col_k = (time.perf_counter() - t0) / (n0 * c.K)
-        self.cols = {x.name: int(max(1, min(x.N, budget_s * 0.5 / (per_col_k * x.K))))
-                     for x in (self.up, self.down)}
+        share = budget_s / len(self.cases)
+        self.cols = {x.name: int(max(1, min(x.N, share / (per_col_k * x.K)))) for x in self.cases}
 
     def _run(self, c, n):
         A, blob = self.data[c.name]
@@ -259,21 +305,21 @@ class OracleSample:
     def run(self) -> float:
         """One sampled step; its wall time in seconds."""
         t0 = time.perf_counter()
-        for c in (self.up, self.down):
+        for c in self.cases:
             self._run(c, self.cols[c.name])
         return time.perf_counter() - t0
 
     @property
     def weight_bytes(self) -> int:
         """Q4_0 bytes of the sampled columns (each column is one row of W)."""
-        return sum(self.cols[c.name] * (c.K // 32) * 18 for c in (self.up, self.down))
+        return sum(self.cols[c.name] * (c.K // 32) * 18 for c in self.cases)
 
     def describe(self) -> str:
+        per = ", ".join(f"{c.tags[1][1]} {self.cols[c.name]}/{c.N}" for c in self.cases)
         return (f"{'OpenMP, ' + str(self.threads) + ' threads' if self.parallel else 'one thread'}: "
-                f"all {self.up.M} rows x the first {self.cols[self.up.name]} of {self.up.N} columns "
-                f"of the up GEMV and the first {self.cols[self.down.name]} of {self.down.N} columns "
-                f"of the down GEMV per step ({self.weight_bytes} weight bytes); value = sampled "
-                f"weight bytes / sample time")
+                f"the first columns of each of layer 0's seven M=1 projections per step "
+                f"({per}; {self.weight_bytes} weight bytes); value = sampled weight bytes / "
+                f"sample time")
 
 
 def run_reference(args, rank: int, world: int) -> None:
@@ -335,36 +381,25 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     stream = torch.cuda.current_stream()
     sh = int(stream.cuda_stream)
 
-    up, down, _ = step_cases()
-    host = {"up_A": up.acts(), "up_W": up.weights(), "down_A": down.acts(),
-            "down_W": down.weights()}
-    reps = []
-    for r in range(REPLICAS):
-        reps.append({
-            "up_A": torch.from_numpy(host["up_A"]).to(dev),
-            "up_W": torch.from_numpy(host["up_W"]).to(dev),
-            "up_C": torch.empty((up.M, up.N), dtype=torch.float32, device=dev),
-            "down_A": torch.from_numpy(host["down_A"]).to(dev),
-            "down_W": torch.from_numpy(host["down_W"]).to(dev),
-            "down_C": torch.empty((down.M, down.N), dtype=torch.float32, device=dev),
-        })
-    torch.cuda.synchronize()
-
-    def call(rc, what):
-        if rc != qm.QM_OK:
-            raise RuntimeError(f"{what}: {qm.qm_status_string(rc)}")
+    # The step's operands.  The 224 weights are resident (loaded once, as a
+    # model's are) and read only; each step's inputs are the layers'
+    # activation vectors, its result the 224 output vectors, each held in one
+    # contiguous buffer per replica so that a step moves them with one copy
+    # each way.  Within a layer q, k and v read one vector (the attention
+    # input), gate and up another (the FFN input), o and down their own.
+    cases = sweep_cases()
+    weights, a_host, c_total, reps = sweep_operands(qm, torch, dev, cases, STEP_REPLICAS)
+    wbytes = sum(c.weight_bytes for c in cases)
+    alg_bytes = sum(gemv_bytes(c) for c in cases)
 
     def step(rp, ev=None):
         if ev is not None:
             ev[0].record(stream)
-        call(qm.qm_matmul_q4_0_ptr(rp["up_A"].data_ptr(), rp["up_W"].data_ptr(),
-                                   rp["up_C"].data_ptr(), up.M, up.N, up.K, sh), "up")
+        rc = qm.qm_gemv_q4_0_list_ptr(rp["problems"], 1, 0, sh)
+        if rc != qm.QM_OK:
+            raise RuntimeError(f"decoder sweep list: {qm.qm_status_string(rc)}")
         if ev is not None:
             ev[1].record(stream)
-        call(qm.qm_matmul_q4_0_ptr(rp["down_A"].data_ptr(), rp["down_W"].data_ptr(),
-                                   rp["down_C"].data_ptr(), down.M, down.N, down.K, sh), "down")
-        if ev is not None:
-            ev[2].record(stream)
 
     def barrier():
         if dist is not None:
@@ -372,7 +407,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         torch.cuda.synchronize()
 
     for i in range(args.warmup):
-        step(reps[i % REPLICAS])
+        step(reps[i % STEP_REPLICAS])
     torch.cuda.synchronize()
     if qm.qm_device_status(clear=True) != qm.QM_OK:
         raise RuntimeError("device error word set during warm-up")
@@ -386,7 +421,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     t_wall0 = time.time()
     start.record(stream)
     for i in range(args.steps):
-        step(reps[i % REPLICAS])
+        step(reps[i % STEP_REPLICAS])
     end.record(stream)
     barrier()
     t_wall1 = time.time()
@@ -397,7 +432,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         t_soak0 = time.time()
         i = 0
         while time.time() - t_soak0 < 1.5:
-            step(reps[i % REPLICAS])
+            step(reps[i % STEP_REPLICAS])
             i += 1
             if i % 64 == 0:
                 torch.cuda.synchronize()
@@ -410,43 +445,36 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         raise RuntimeError("device error word set during the timed region")
 
     ms_step = max_over_ranks(total_ms / args.steps, dist, dev)
-
-    # Per-kernel split, from a separate pass with events between the kernels
-    # (an event between two kernels also ends their programmatic overlap, so
-    # these times are slightly longer than their share of the timed step).
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for i in range(args.steps):
-        step(reps[i % REPLICAS], evs[i])
-    torch.cuda.synchronize()
-    avg = {"gemv_up": statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs),
-           "gemv_down": statistics.mean(ev[1].elapsed_time(ev[2]) for ev in evs)}
-
-    wbytes = up.weight_bytes + down.weight_bytes
     value = job_gbs(wbytes, world, ms_step)
 
-    # ---------------------------------------------------------------- e2e
-    pinned = {k: torch.from_numpy(v.view(np.uint8).ravel() if v.dtype != np.uint8 else v)
-              .pin_memory() for k, v in host.items()}
-    out_host = {"up_C": torch.empty(up.M * up.N * 4, dtype=torch.uint8).pin_memory(),
-                "down_C": torch.empty(down.M * down.N * 4, dtype=torch.uint8).pin_memory()}
+    # The kernel alone: events on the launching stream around each call of a
+    # second pass (a call is two launches of the list kernel, back to back;
+    # the gap between two steps is the difference from ms_step).
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        step(reps[i % STEP_REPLICAS], evs[i])
+    torch.cuda.synchronize()
+    launch_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
 
-    # Each step copies its inputs in, runs, and copies its outputs back, as a
-    # serving loop would: inputs on one copy stream, the kernels on the main
-    # stream, outputs on a second copy stream, so that step i + 1's inputs and
-    # step i - 1's outputs move (in opposite directions) while step i
+    # ---------------------------------------------------------------- e2e
+    # Each step copies its activations in from pinned host memory, runs, and
+    # copies its outputs back, as a decode loop would: inputs on one copy
+    # stream, the kernel on the main stream, outputs on a second copy stream,
+    # so that step i + 1's inputs and step i - 1's outputs move while step i
     # computes.  A replica's buffers are refilled only after its previous
     # step's outputs have been read back.
+    a_pinned = torch.from_numpy(a_host).pin_memory()
+    c_pinned = torch.empty(c_total, dtype=torch.float32).pin_memory()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    freed = [None] * REPLICAS
+    freed = [None] * STEP_REPLICAS
 
     def e2e_step(i):
-        r = i % REPLICAS
+        r = i % STEP_REPLICAS
         rp = reps[r]
         with torch.cuda.stream(s_in):
             if freed[r] is not None:
                 s_in.wait_event(freed[r])
-            for k in host:
-                rp[k].view(torch.uint8).view(-1).copy_(pinned[k], non_blocking=True)
+            rp["A"].copy_(a_pinned, non_blocking=True)
             ev_in = torch.cuda.Event()
             ev_in.record(s_in)
         stream.wait_event(ev_in)
@@ -455,16 +483,15 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         ev_c.record(stream)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_c)
-            for k in out_host:
-                out_host[k].copy_(rp[k].view(torch.uint8).view(-1), non_blocking=True)
+            c_pinned.copy_(rp["C"], non_blocking=True)
             ev_out = torch.cuda.Event()
             ev_out.record(s_out)
         freed[r] = ev_out
 
-    h2d = sum(v.nbytes for v in host.values())
-    d2h = sum(int(v.numel()) for v in out_host.values())
-    e2e_steps = max(3, min(args.steps, 50))
-    for i in range(2 * REPLICAS):
+    h2d = a_pinned.numel() * 4
+    d2h = c_pinned.numel() * 4
+    e2e_steps = max(3, min(args.steps, 100))
+    for i in range(2 * STEP_REPLICAS):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier()
@@ -477,45 +504,37 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_value = job_gbs(wbytes, world, e2e_ms)
-    del pinned, out_host
+    # Outputs read back against a fresh device result of the same list.
+    torch.cuda.synchronize()
+    e2e_readback_ok = bool(torch.equal(c_pinned, reps[(e2e_steps - 1) % STEP_REPLICAS]["C"].cpu()))
+    del a_pinned, c_pinned
 
     # ------------------------------------------------------------ roofline
     hbm = peaks["hbm_gbs"]
-    paths = {}
-    for key, c in (("gemv_up", up), ("gemv_down", down)):
-        ms = avg[key]
-        paths[key] = {
-            "kernel": "gemv_q4_0_tc (mma.sync bf16 split, f32 accumulation)",
-            "workload": c.name, "ms": ms, "weight_gbs": c.weight_bytes / (ms * 1e-3) / 1e9,
-            "alg_gbs": gemv_bytes(c) / (ms * 1e-3) / 1e9,
-            "hbm_frac": gemv_bytes(c) / (ms * 1e-3) / 1e9 / hbm,
-            "tflops": 2.0 * c.M * c.N * c.K / (ms * 1e-3) / 1e12,
-            "bound_time_ms": gemv_bytes(c) / (hbm * 1e9) * 1e3,
-        }
-    dominant = max(avg, key=avg.get)
-    c = up if dominant == "gemv_up" else down
-    achieved = paths[dominant]["alg_gbs"]
-    roofline = {"bound": "hbm", "kernel": f"gemv_q4_0_tc ({c.name}, the step's longer launch)",
+    achieved = alg_bytes / (launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm",
+                "kernel": "gemv_q4_0_list (persistent list GEMV, mma.sync bf16 split, f32 accumulation)",
                 "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                "traffic": measured_traffic("gemv_q4_0_tc", c.name),
+                "traffic": measured_traffic("gemv_q4_0_list", WORKLOAD),
                 "peak_source": peaks["source"],
-                "algorithmic_bytes_per_launch": gemv_bytes(c),
-                "algorithmic_bytes_definition": "N*K*0.5625 weight + M*K*4 A + M*N*4 C",
-                "launch_ms": paths[dominant]["ms"],
-                "per_config": {"cfg1_" + k: {"workload": v["workload"], "ms": v["ms"],
-                                             "weight_gbs": v["weight_gbs"],
-                                             "frac": v["hbm_frac"], "bound": "hbm"}
-                               for k, v in paths.items()}}
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "algorithmic_bytes_definition": "sum over the 224 GEMVs of N*K*0.5625 weight + K*4 A + N*4 C",
+                "launch_unit": "one qm_gemv_q4_0_list call: two launches of the list kernel (128 and 96 "
+                               "problems); achieved and traffic are per call",
+                "launch_ms": launch_ms,
+                "weight_gbs_per_launch": wbytes / (launch_ms * 1e-3) / 1e9,
+                "per_config": {}}
 
     prefill = None
     q8 = None
     host_cost = None
     if not args.no_sweep:
-        legs = configs_leg(qm, dev, peaks, clocks)
+        legs = configs_leg(qm, dev, peaks, clocks, cases, weights)
         roofline["per_config"].update(legs["gemv"])
         prefill = legs["prefill"]
         q8 = legs["q8_0"]
         host_cost = legs["host"]
+    del weights, reps
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
@@ -523,15 +542,18 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": bench_config(world),
+        "hbm_frac": value / hbm,
         "roofline": roofline,
         "prefill": prefill,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "overlap": "inputs, kernels and outputs on three streams; step i+1's inputs "
+                "readback_matches_device": e2e_readback_ok,
+                "inputs": "the 128 activation vectors (4 per layer) in, the 224 output vectors out; the "
+                          "3.93 GB of weights resident (loaded once before timing)",
+                "overlap": "inputs, kernel and outputs on three streams; step i+1's inputs "
                            "and step i-1's outputs move while step i computes"},
         "gpu_launches": launches,
         "host_us_per_call": host_cost,
-        "paths": paths,
         "q8_0": q8,
         "clocks": clocks,
         "hbm_peak_gbs": hbm, "peak_source": peaks["source"],
@@ -570,7 +592,6 @@ def graph_ms(torch, fn, passes: int = 5) -> float:
 
 
 MMAS_PER_PRODUCT = 4  # the tensor-core GEMM takes all four bf16 piece products
-DECODER_PROJS = tuple(p for (p, _, _) in synth.DECODER_LAYER)
 
 
 def timed_loop(torch, fn, calls: int, warm: int = 3) -> float:
@@ -588,12 +609,15 @@ def timed_loop(torch, fn, calls: int, warm: int = 3) -> float:
     return e0.elapsed_time(e1) / calls
 
 
-def configs_leg(qm, dev, peaks, clocks) -> dict:
-    """Every other workload, each on its own synthetic inputs:
+def configs_leg(qm, dev, peaks, clocks, cases, weights) -> dict:
+    """Every other workload, each on its own synthetic inputs (`cases` and
+    `weights`: the decoder sweep's 224 GEMVs and their resident weights):
 
     GEMV / dequant rows (weight GB/s against HBM):
       cfg0: GEMV M=1, K=N=4096 (9.44 MB), 16 weight replicas back to back in
             a CUDA graph (the replicas exceed L2);
+      cfg1: GEMV M=8 up (K=4096, N=14336) and down (K=14336, N=4096), 4
+            rotating replicas, each launch timed with events around it;
       cfg1_dequant: dequant of the 14336 x 4096 weight, 4 rotating replicas;
       cfg4 M=1 / M=8: the 32-layer decoder sweep (q, k, v, o, gate, up, down;
             hidden 4096, GQA; 3.93 GB of weights, all resident), a CUDA graph
@@ -665,6 +689,28 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
         c0.weight_bytes, ms0q)
     del w0
 
+    # cfg1: the M = 8 decode-batch GEMVs, each launch between two events.
+    for key, c in zip(("cfg1_gemv_up", "cfg1_gemv_down"), step_cases()[:2]):
+        ws = [torch.from_numpy(c.weights()).to(dev) for _ in range(REPLICAS)]
+        A = torch.from_numpy(c.acts()).to(dev)
+        C = torch.empty((c.M, c.N), dtype=torch.float32, device=dev)
+        for i in range(2 * REPLICAS):
+            mm(A, ws[i % REPLICAS], C, c.M, c.N, c.K, c.name)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(40)]
+        for i, ev in enumerate(evs):
+            ev[0].record()
+            mm(A, ws[i % REPLICAS], C, c.M, c.N, c.K, c.name)
+            ev[1].record()
+        torch.cuda.synchronize()
+        ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
+        row = gemv_row(f"{c.name}: M=8 decode batch, {REPLICAS} rotating weight replicas, "
+                       "events around each launch", "gemv_q4_0_tc", c.weight_bytes, ms)
+        row["alg_gbs"] = gemv_bytes(c) / (ms * 1e-3) / 1e9
+        row["algorithmic_bytes_per_launch"] = gemv_bytes(c)
+        row["traffic"] = measured_traffic("gemv_q4_0_tc", c.name)
+        gemv[key] = row
+        del ws, A, C
+
     # cfg1 dequant.
     deq = step_cases()[2]
     nb = deq.weight_bytes // 18
@@ -701,8 +747,6 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
         del ws, A, C
 
     # cfg4: the 32-layer decoder sweep.
-    cases = synth.workload(4, layers=32, sweep_m=(1,))
-    weights = [torch.from_numpy(c.weights()).to(dev) for c in cases]
     wbytes = sum(c.weight_bytes for c in cases)
     layer_shapes = [(c.N, c.K) for c in cases[:7]]
 
@@ -835,7 +879,7 @@ def configs_leg(qm, dev, peaks, clocks) -> dict:
     prefill["bound_note"] = (f"tensor-core bound = measured bf16 dense peak {bf16} TFLOP/s / "
                              f"{MMAS_PER_PRODUCT} bf16 MMAs per useful product; FP32 FMA peak "
                              f"{fp32_peak:.1f} TFLOP/s at {sm_max} MHz")
-    del weights
+    del A, outs, fn
     torch.cuda.empty_cache()
     return {"gemv": gemv, "prefill": prefill, "q8_0": q8_0_leg(qm, dev, peaks),
             "host": host_cost_leg(qm, dev)}
@@ -943,8 +987,8 @@ def profile_case(args) -> None:
     """Run one operation a few times on cuda:0 and exit, for profiler captures
     (``--profile-case gemm --M .. --N .. --K .. [--algo QM_ALGO_*]``, any M;
     ``--profile-case q8act --M .. --N .. --K ..``, M <= 8; ``--profile-case
-    list --layers L``: the M = 1 decoder projections of L layers (the
-    decoder sweep's shapes and weights) as one independent list through
+    list --layers L``: the bench step's list for L layers (the decoder
+    sweep's shapes, weights and activation vectors) through
     qm_gemv_q4_0_list (``--q8act``: qm_gemv_q4_0_q8act_list); or
     ``--profile-case q8_0``).
     Prints a one-line note, not a bench line."""
@@ -970,13 +1014,9 @@ def profile_case(args) -> None:
                 raise RuntimeError(qm.qm_status_string(rc))
     elif args.profile_case == "list":
         cases = synth.workload(4, layers=args.layers, sweep_m=(1,))
-        ws = [torch.from_numpy(c.weights()).to(dev) for c in cases]
-        acts = {K: torch.from_numpy(synth.activations(1, K, 5, key=(2, 1, K))).to(dev) for K in (4096, 14336)}
-        outs = [torch.empty((1, c.N), dtype=torch.float32, device=dev) for c in cases]
-        problems = [(acts[c.K].data_ptr(), w.data_ptr(), o.data_ptr(), c.N, c.K, -1)
-                    for c, w, o in zip(cases, ws, outs)]
+        _, _, _, reps = sweep_operands(qm, torch, dev, cases, 1)
         for _ in range(args.calls):
-            rc = qm.qm_gemv_q4_0_list_ptr(problems, 1, 0, sh, q8act=args.q8act)
+            rc = qm.qm_gemv_q4_0_list_ptr(reps[0]["problems"], 1, 0, sh, q8act=args.q8act)
             if rc != qm.QM_OK:
                 raise RuntimeError(qm.qm_status_string(rc))
     else:

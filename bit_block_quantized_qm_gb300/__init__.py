@@ -39,6 +39,7 @@ __all__ = [
     "QM_ALGO_AUTO", "QM_ALGO_GEMV", "QM_ALGO_GEMM_SIMT", "QM_ALGO_GEMV_SIMT", "QM_ALGO_GEMM_TC",
     "QM_ALGO_GEMV_PK", "qm_gemv_plan", "GEMV_PLAN_FIELDS", "qm_gemm_plan", "GEMM_PLAN_FIELDS",
     "EXPORTED_SYMBOLS", "QmGemvProblem", "qm_gemv_q4_0_list_ptr", "qm_gemv_q4_0_list",
+    "gemv_problem_array",
 ]
 
 QM_OK = 0
@@ -202,14 +203,22 @@ def qm_matmul_q4_0_q8act_ptr(A: int, wq: int, C: int, M: int, N: int, K: int,
 def qm_gemv_q4_0_list_ptr(problems, M: int, counters: int = 0, stream: int = 0,
                           q8act: bool = False) -> int:
     """The list GEMV on raw addresses: `problems` is a sequence of (A, wq, C, N,
-    K, wait_for) tuples of ints; `counters` the device address of len(problems)
+    K, wait_for) tuples of ints, or an array built once by
+    gemv_problem_array; `counters` the device address of len(problems)
     uint32 (0 for none).  With `q8act`, qm_gemv_q4_0_q8act_list (the
     act-quant product).  Returns the C status."""
-    arr = (QmGemvProblem * max(1, len(problems)))()
-    for i, (A, wq, C, N, K, wait_for) in enumerate(problems):
-        arr[i] = QmGemvProblem(A, wq, C, N, K, wait_for, 0)
+    arr = problems if isinstance(problems, ctypes.Array) else gemv_problem_array(problems)
     fn = load_library().qm_gemv_q4_0_q8act_list if q8act else load_library().qm_gemv_q4_0_list
     return fn(ctypes.cast(arr, ctypes.c_void_p), len(problems), M, counters or None, stream)
+
+
+def gemv_problem_array(problems):
+    """The C array of qm_gemv_problem for a sequence of (A, wq, C, N, K,
+    wait_for) tuples, for callers that pass the same list many times."""
+    arr = (QmGemvProblem * len(problems))()
+    for i, (A, wq, C, N, K, wait_for) in enumerate(problems):
+        arr[i] = QmGemvProblem(A, wq, C, N, K, wait_for, 0)
+    return arr
 
 
 def qm_gemv_q4_0_q8act_list_ptr(problems, M: int, counters: int = 0, stream: int = 0) -> int:

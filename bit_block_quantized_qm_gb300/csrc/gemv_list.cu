@@ -75,22 +75,29 @@ __device__ unsigned int g_gemv_list_error = 0;
 
 namespace {
 
+constexpr int kUnitB = 144;                      // bytes of one row's unit (8 blocks)
+// A box of 16 rows x (c + 1) units (c = 16 or 8).
+__host__ __device__ constexpr int box_bytes(int c) { return 16 * (c + 1) * kUnitB; }
+constexpr int kLFragB = kListMaxK * 4;           // activations (f32 as loaded; M = 1)
+
 constexpr int kLW = 16;                          // consumer warps
 constexpr int kLThreads = (kLW + 2) * 32;        // + producer warp + activation-loader warp
-constexpr int kUnitB = 144;                      // bytes of one row's unit (8 blocks)
-// A box of 16 rows x (c + 1) units; a stage holds 16 / c boxes.
-__host__ __device__ constexpr int box_bytes(int c) { return 16 * (c + 1) * kUnitB; }
+// A stage holds 16 units (one per consumer warp) as 16 / c boxes.
 constexpr int kStageB = 2 * box_bytes(8);        // 41,472 bytes (c = 8); c = 16 needs 39,168
 constexpr int kLStages = 4;
-constexpr int kLFragB = kListMaxK * 4;           // activations as B fragments (M = 1)
 constexpr int kTileSlots = 4;                    // tiles whose partial sums may be in flight
 constexpr int kSlotFloats = kLW * 16;            // one tile: 16 warps x 16 rows
 
-// Shared memory: ring | fragments | partial-sum slots | barriers and counters.
+// Shared memory: ring | activations | partial-sum slots | barriers and
+// counters | 1 KB of zeros.  (24 consumer warps, which
+// fit in 72 registers each, on 2 stages of 24 units measured slower: 0.435
+// against 0.50 of HBM over the 32-layer sweep; 3 stages ran 4% slower than 4.)
 constexpr int kOffFrag = kLStages * kStageB;
 constexpr int kOffSlots = kOffFrag + kLFragB;
 constexpr int kOffBars = kOffSlots + kTileSlots * kSlotFloats * 4;
-constexpr int kNumBars = 2 * kLStages + 3;       // full, empty, a_full, a_empty, frag_ready
+// full, empty; a_full, a_empty (activations copied in by the loader); one
+// barrier per pair of consumer warps (w, w + 8).
+constexpr int kNumBars = 2 * kLStages + 2 + 8;
 constexpr int kOffInts = kOffBars + kNumBars * 8;
 constexpr int kNumInts = 2 * kTileSlots + kListMaxProblems + 1;  // arrivals, done, tiles per problem, abort
 // 1 KB of zeros, 64 bytes past a 128-byte boundary: a lane that reads zeros
@@ -99,7 +106,7 @@ constexpr int kNumInts = 2 * kTileSlots + kListMaxProblems + 1;  // arrivals, do
 constexpr int kOffZero = (kOffInts + kNumInts * 4 + 127) / 128 * 128 + 64;
 constexpr int kLSmem = kOffZero + 1024;
 static_assert(kLSmem <= 232448, "shared memory of one CTA");
-static_assert(kOffFrag % 16 == 0 && kOffSlots % 16 == 0 && kOffBars % 8 == 0, "alignment");
+static_assert(kOffFrag % 1024 == 0 && kOffSlots % 16 == 0 && kOffBars % 8 == 0, "alignment");
 
 // Polls of a global completion counter (each followed by a short sleep).
 constexpr uint32_t kMaxCounterPolls = 1u << 21;
@@ -445,7 +452,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     uint64_t* empty = full + kLStages;
     uint64_t* a_full = empty + kLStages;
     uint64_t* a_empty = a_full + 1;
-    uint64_t* frag_ready = a_empty + 1;
+    uint64_t* pair_bar = a_empty + 1;  // [8]
     int* arr = reinterpret_cast<int*>(smem + kOffInts);  // [kTileSlots] arrivals per tile slot
     volatile int* done = arr + kTileSlots;               // [kTileSlots] last tile reduced per slot
     int* red = arr + 2 * kTileSlots;                     // [count] tiles of a problem reduced here
@@ -465,7 +472,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         }
         mbar_init(a_full, 1);
         mbar_init(a_empty, kLW);
-        mbar_init(frag_ready, kLW);
+        for (int i = 0; i < 8; ++i) mbar_init(&pair_bar[i], 2);
         for (int i = 0; i < kTileSlots; ++i) {
             arr[i] = 0;
             done[i] = i - kTileSlots;
@@ -498,17 +505,18 @@ __global__ void __launch_bounds__(kLThreads, 1)
             const int total = n * U;
             const int cu = q.c;
             const CUtensorMap* map = &P.map[qi];
+            if (qi + 1 < P.count) prefetch_tensormap(&P.map[qi + 1]);
             if (!warmed) {
                 // Ask L2 for the first stage before waiting on earlier kernels.
                 warmed = true;
-                for (int i = 0; i < min(16, total); i += cu)
+                for (int i = 0; i < min(kLW, total); i += cu)
                     tma_prefetch_l2_4d(map, 0, 0, (i % U) / cu, 16 * (first + (i / U) * G));
                 grid_dependency_wait();
             }
-            for (int s0 = 0; s0 < total; s0 += 16) {
+            for (int s0 = 0; s0 < total; s0 += kLW) {
                 if (issued >= kLStages && !wait_idle(&empty[st], ph ^ 1u, abort_flag)) break;
                 if (aborted(abort_flag)) break;
-                const int boxes = (min(16, total - s0) + cu - 1) / cu;
+                const int boxes = (min(kLW, total - s0) + cu - 1) / cu;
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(boxes * box_bytes(cu)));
                 uint8_t* stage = ring + st * kStageB;
                 for (int j = 0; j < boxes; ++j) {
@@ -539,10 +547,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
     if (warp == kLW + 1) {
         // -------------------------------------------- activation loader
+        // New activations of a problem that waits for nothing (wait_for <
+        // 0) are read by the consumers straight from global memory; the
+        // loader copies in only those that wait for earlier problems, once
+        // every consumer is done with the buffer and the problems waited for
+        // are finished on every CTA.
         grid_dependency_wait();
         if (lane != 0) return;
         AKey key;
-        int rounds = 0, verified = -1;
+        int rounds = 0, direct = 0, handbacks = 0, verified = -1;
         for (int qi = 0; qi < P.count && !aborted(abort_flag); ++qi) {
             const ListProblem& q = P.p[qi];
             int first;
@@ -554,7 +567,16 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 continue;
             }
             if (!key.advance(q)) continue;
-            if (rounds > 0 && !wait_idle(a_empty, (rounds - 1) & 1, abort_flag)) break;
+            if (q.wait_for < 0) {
+                ++rounds;
+                continue;
+            }
+            // The consumers hand the buffer back before every copy after the
+            // first round.
+            if (rounds > 0) {
+                if (!wait_idle(a_empty, handbacks & 1, abort_flag)) break;
+                ++handbacks;
+            }
             // Activations that are earlier problems' outputs: wait until every
             // CTA has finished every problem up to q.wait_for.
             bool ok = true;
@@ -583,9 +605,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
             mbar_arrive_expect_tx(a_full, bytes);
             for (uint32_t o = 0; o < bytes; o += 16384u)
                 bulk_load_1d(frag + o, reinterpret_cast<const uint8_t*>(q.A) + o, min(16384u, bytes - o), a_full);
+            ++direct;
             ++rounds;
         }
-        if (rounds > 0) mbar_wait_bounded(a_full, (rounds - 1) & 1, &g_gemv_list_error);
+        // Let the copy still in flight land (bounded).
+        if (direct > 0) mbar_wait_bounded(a_full, (direct - 1) & 1, &g_gemv_list_error);
         return;
     }
 
@@ -594,35 +618,82 @@ __global__ void __launch_bounds__(kLThreads, 1)
     const int g = lane >> 2;
     const int t = lane & 3;
     AKey key;
-    int rounds = 0, st = 0, tl = 0;
+    int rounds = 0, direct = 0, pair_ph = 0, st = 0, tl = 0;
+    bool prev_own = true;  // the fragments in place are read only by the warps that wrote them
     uint32_t ph = 0;
     bool ok = true;
+    // A warp pair (w, w + 8) meets at its barrier; bounded, so that a warp
+    // that gave up never leaves its partner blocked.
+    auto pair_meet = [&]() {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pair_bar[warp & 7]);
+        const bool r = wait_stage(&pair_bar[warp & 7], pair_ph & 1, abort_flag);
+        ++pair_ph;
+        return __all_sync(0xFFFFFFFFu, r);
+    };
     for (int qi = 0; qi < P.count && ok; ++qi) {
         const ListProblem& q = P.p[qi];
         int first;
         const int n = cta_tiles(q, c, G, &first);
         if (n == 0) continue;
         if (key.advance(q)) {
-            if (rounds > 0) {
-                // Done with the previous activations: order this warp's
-                // accesses to them before the loader's next bulk copy.
-                fence_proxy_async_shared();
+            // New activations.  Warp w takes unit u of every tile exactly
+            // when u = w (mod 8) (a stage is 16 consecutive units of the
+            // CTA's sequence and K / 256 is a multiple of 8), so the
+            // fragments of unit u are read by warps u % 8 and u % 8 + 8
+            // alone: warp w writes units w, w + 16, w + 32, ..., and only its
+            // partner ever has to wait for them.  When K / 256 is a multiple
+            // of 16 a warp reads exactly the units it writes ("own").
+            const int U = q.K >> 8;
+            const bool own = (U % kLW) == 0;
+            if (q.wait_for < 0) {
+                // Straight from global memory (nothing in this launch writes
+                // these activations).  The partner must be done with the
+                // units about to be rewritten, unless the warp read them alone.
+                if (rounds > 0 && !prev_own) ok = pair_meet();
+                if (!ok) break;
+                if (warp == 0 && lane == 0 && qi + 1 < P.count && P.p[qi + 1].A != q.A &&
+                    P.p[qi + 1].wait_for < 0) {
+                    // The next problem's activations, on their way to L2.
+                    const uint32_t nb = static_cast<uint32_t>(P.p[qi + 1].K) * 4u;
+                    for (uint32_t o = 0; o < nb; o += 16384u)
+                        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(P.p[qi + 1].A) + o, min(16384u, nb - o));
+                }
+                // All of this warp's units in flight at once, then converted.
+                const uint8_t* a_g = reinterpret_cast<const uint8_t*>(q.A);
+                for (int u = warp; u < U; u += kLW) {
+                    cp_async16(frag + u * 1024 + lane * 16, a_g + u * 1024 + lane * 16);
+                    cp_async16(frag + u * 1024 + 512 + lane * 16, a_g + u * 1024 + 512 + lane * 16);
+                }
+                cp_async_wait_all();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(a_empty);
-            }
-            ok = wait_stage(a_full, rounds & 1, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) break;
-            for (int u = warp; u < (q.K >> 8); u += kLW) {
-                if constexpr (kQ8) quantize_unit_q8<1>(frag + u * 1024, lane);
-                else unit_fragments(frag + u * 1024, lane);
+                for (int u = warp; u < U; u += kLW) {
+                    if constexpr (kQ8) quantize_unit_q8<1>(frag + u * 1024, lane);
+                    else unit_fragments(frag + u * 1024, lane);
+                }
+            } else {
+                // Copied in by the loader once every consumer is done with
+                // the buffer, then converted in place.
+                if (rounds > 0) {
+                    // Order this warp's accesses to the buffer before the
+                    // loader's next bulk copy.
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(a_empty);
+                }
+                ok = wait_stage(a_full, direct & 1, abort_flag);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
+                for (int u = warp; u < U; u += kLW) {
+                    if constexpr (kQ8) quantize_unit_q8<1>(frag + u * 1024, lane);
+                    else unit_fragments(frag + u * 1024, lane);
+                }
+                ++direct;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(frag_ready);
-            // Every warp's share of the fragments is written (a bounded wait:
-            // a warp that gave up never leaves the others blocked).
-            ok = wait_stage(frag_ready, rounds & 1, abort_flag);
-            ok = __all_sync(0xFFFFFFFFu, ok);
+            // The partner's units are this warp's too unless it is "own".
+            if (!own) ok = pair_meet();
+            prev_own = own;
             ++rounds;
             if (!ok) break;
         }
@@ -640,7 +711,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         // tile k, unit u, advanced without dividing.
         int k = warp / U, u = warp - (warp / U) * U;
         float acc[2] = {0.f, 0.f};
-        for (int s0 = 0; s0 < total; s0 += 16, u += 16) {
+        for (int s0 = 0; s0 < total; s0 += kLW, u += kLW) {
             while (u >= U) {
                 u -= U;
                 ++k;
@@ -649,7 +720,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             if (s0 + warp < total) {
-                if (u < 16) acc[0] = acc[1] = 0.f;
+                if (u < kLW) acc[0] = acc[1] = 0.f;
                 const uint8_t* ra = ring + st * kStageB + slot_off;
                 if constexpr (kQ8) half_unit_q8(ra, lane >> 4, frag + u * 1024, acc);
                 else unit_mma(ra, ra + 8 * row_b, fbase + u * fstep, g, t, acc);
@@ -657,7 +728,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 // producer before adding anything up.
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[st]);
-                if (u + 16 >= U) {
+                if (u + kLW >= U) {
                     // This warp's last unit of tile k: its row sums to the slot
                     // (MMA consumer: rows g and g + 8 from the lanes t = 0;
                     // integer consumer: row l from lanes l < 16).
@@ -696,7 +767,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     }
                     __threadfence_block();
                     __syncwarp();
-                    const int n_part = min(16, U);
+                    const int n_part = min(kLW, U);
                     int old = 0;
                     if (lane == 0) old = atomicAdd(&arr[sl], 1);
                     old = __shfl_sync(0xFFFFFFFFu, old, 0);

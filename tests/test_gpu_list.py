@@ -15,6 +15,14 @@ against the oracle, through the C ABI.
   2048) run problem by problem and still match the oracle;
 * a row with an infinite scale over all-8 nibbles comes out NaN, as the
   definition gives it;
+* activation hand-overs: a list whose K alternates between sizes whose
+  fragments each warp keeps alone and sizes whose fragments warp pairs
+  share, with runs of K = 4096 problems (activations copied ahead), with
+  distinct, shared and repeated activation vectors and problems too small
+  to reach every CTA, both products, checked entry by entry;
+* the 32-layer decoder sweep at M = 1 (224 GEMVs, every one with its own
+  activation vector) through one call, sampled rows of every problem against
+  the oracle;
 * the act-quant list (qm_gemv_q4_0_q8act_list) against the oracle's
   composition dequant_q8_0(quantize_q8_0(A)) x dequant(W)^T: mixed shapes,
   the decoder chain (exact with one-hot weights), a non-finite scale and a
@@ -257,3 +265,64 @@ def test_q8act_list_non_finite_and_fallback(env):
         C_ref, S_ref = o.matmul_q4_0_q8act(A, blob, N, K)
         assert oracle.within_tolerance(p[2].cpu().numpy(), C_ref, S_ref, REL, ABS).all(), (N, K)
     assert not np.isfinite(o.matmul_q4_0_q8act(*host[0], *shapes[0])[0]).all()
+
+
+# ------------------------------------------- activation hand-overs, sweep
+# (N, K, activation id): ids name activation vectors; a repeated id reuses
+# the same device vector.  K / 256 a multiple of 16 (each warp alone with its
+# fragments) or not (warp pairs share them), runs of K = 4096 problems with
+# new activations each (copied ahead into the other bank), K = 14336 after
+# them and before them; N = 16 and 48 leave most CTAs without a tile.
+HANDOVER = [(4096, 4096, 0), (512, 14336, 1), (2048, 14336, 2), (1024, 8192, 3),
+            (16, 4096, 0), (4096, 2048, 4), (300, 14336, 5), (48, 6144, 6),
+            (1024, 14336, 5), (4096, 4096, 7), (700, 8192, 8), (256, 14336, 9),
+            (2048, 4096, 7), (4096, 4096, 10), (1024, 4096, 11), (16, 4096, 12),
+            (4096, 4096, 13), (2048, 4096, 14), (512, 14336, 15), (4096, 4096, 16),
+            (48, 4096, 17), (1000, 4096, 18)]
+
+
+@pytest.mark.parametrize("q8act", [False, True], ids=["f32", "q8act"])
+def test_list_activation_handovers(env, q8act):
+    qm, o = env
+    acts = {}
+    for (N, K, a) in HANDOVER:
+        if a not in acts:
+            acts[a] = synth.activations(1, K, 800 + a)
+    dacts = {a: torch.from_numpy(A).cuda() for a, A in acts.items()}
+    blobs = [synth.q4_0_weights(N, K, 820 + i) for i, (N, K, _) in enumerate(HANDOVER)]
+    outs = [torch.full((1, N), float("nan"), device="cuda") for (N, _, _) in HANDOVER]
+    problems = [(dacts[a], torch.from_numpy(b).cuda(), C, N, K, -1)
+                for (N, K, a), b, C in zip(HANDOVER, blobs, outs)]
+    for rep in range(2):
+        for C in outs:
+            C.fill_(float("nan"))
+        (run_q8_list if q8act else run_list)(qm, problems, 1)
+        for i, ((N, K, a), blob, C) in enumerate(zip(HANDOVER, blobs, outs)):
+            ref = o.matmul_q4_0_q8act if q8act else o.matmul_q4_0
+            C_ref, S_ref = ref(acts[a], blob, N, K)
+            ok = oracle.within_tolerance(C.cpu().numpy(), C_ref, S_ref, REL, ABS)
+            assert ok.all(), f"run {rep} problem {i} (N={N} K={K}): {int((~ok).sum())} bad"
+
+
+def test_list_decoder_sweep_one_call(env):
+    """The 224 GEMVs of the 32-layer decoder sweep at M = 1 (hidden 4096,
+    GQA), every one with its own activation vector, through one call of
+    qm_gemv_q4_0_list; 24 sampled rows of every problem (the first, the last
+    and 22 random ones) against the oracle, entry by entry."""
+    qm, o = env
+    cases = synth.workload(4, layers=32, sweep_m=(1,))
+    acts = [c.acts() for c in cases]
+    blobs = [c.weights() for c in cases]
+    dev_w = [torch.from_numpy(b).cuda() for b in blobs]
+    dev_a = [torch.from_numpy(A).cuda() for A in acts]
+    outs = [torch.full((1, c.N), float("nan"), device="cuda") for c in cases]
+    problems = [(A, w, C, c.N, c.K, -1) for A, w, C, c in zip(dev_a, dev_w, outs, cases)]
+    run_list(qm, problems, 1)
+    g = synth.rng(840, (0,))
+    for c, A, blob, C in zip(cases, acts, blobs, outs):
+        rows = np.unique(np.concatenate([[0, c.N - 1], g.integers(0, c.N, 22)]))
+        got = C.cpu().numpy().ravel()[rows]
+        C_ref, S_ref = o.matmul_q4_0_entries(A, blob, c.N, c.K, np.zeros_like(rows), rows)
+        ok = oracle.within_tolerance(got, C_ref, S_ref, REL, ABS)
+        assert ok.all(), f"{c.name}: rows {rows[~ok].tolist()} outside tolerance"
+    del dev_w
