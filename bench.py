@@ -989,7 +989,8 @@ def profile_case(args) -> None:
     ``--profile-case q8act --M .. --N .. --K ..``, M <= 8; ``--profile-case
     list --layers L``: the bench step's list for L layers (the decoder
     sweep's shapes, weights and activation vectors) through
-    qm_gemv_q4_0_list (``--q8act``: qm_gemv_q4_0_q8act_list); or
+    qm_gemv_q4_0_list (``--q8act``: qm_gemv_q4_0_q8act_list);
+    ``--profile-case dequant``: dequant_q4_0 of the 14336 x 4096 weight; or
     ``--profile-case q8_0``).
     Prints a one-line note, not a bench line."""
     import torch
@@ -1019,6 +1020,15 @@ def profile_case(args) -> None:
             rc = qm.qm_gemv_q4_0_list_ptr(reps[0]["problems"], 1, 0, sh, q8act=args.q8act)
             if rc != qm.QM_OK:
                 raise RuntimeError(qm.qm_status_string(rc))
+    elif args.profile_case == "dequant":
+        deq = step_cases()[2]
+        nb = deq.weight_bytes // 18
+        w = torch.from_numpy(deq.weights()).to(dev)
+        out = torch.empty(nb * 32, dtype=torch.float32, device=dev)
+        for _ in range(args.calls):
+            rc = qm.qm_dequant_q4_0_ptr(w.data_ptr(), nb, out.data_ptr(), sh)
+            if rc != qm.QM_OK:
+                raise RuntimeError(qm.qm_status_string(rc))
     else:
         n = 14336 * 4096
         x = torch.from_numpy(synth.rng(6, (0,)).standard_normal(n).astype(np.float32)).to(dev)
@@ -1043,7 +1053,7 @@ def main(argv=None) -> None:
                    help="skip the CPU oracle timing (for profiler runs)")
     p.add_argument("--no-sweep", action="store_true",
                    help="skip the M=1 GEMV, decoder-sweep and prefill reports (profiler runs)")
-    p.add_argument("--profile-case", choices=("gemm", "q8act", "list", "q8_0"), default=None,
+    p.add_argument("--profile-case", choices=("gemm", "q8act", "list", "q8_0", "dequant"), default=None,
                    help="run one operation a few times and exit (profiler captures)")
     p.add_argument("--M", type=int, default=512)
     p.add_argument("--N", type=int, default=4096)
