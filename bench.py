@@ -59,6 +59,7 @@ FALLBACK_HBM_GBS = 6800.0
 REPLICAS = 4  # config 1's GEMVs: 4 x 66 MB of weights (plus activations) > 129 MB of L2
 SWEEP_LAYERS = 32
 STEP_REPLICAS = 3  # activation and output buffers of the step (the weights are shared)
+WARMUP_S = 0.3     # minimum seconds of warm-up load before timing
 
 
 def bench_config(world: int) -> dict:
@@ -406,8 +407,15 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    for i in range(args.warmup):
+    # Warm-up: the --warmup steps, then more until the GPU has run for at
+    # least WARMUP_S seconds (the SM clock ramps up under load).
+    t_warm = time.time()
+    i = 0
+    while i < args.warmup or time.time() - t_warm < WARMUP_S:
         step(reps[i % STEP_REPLICAS])
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     if qm.qm_device_status(clear=True) != qm.QM_OK:
         raise RuntimeError("device error word set during warm-up")
@@ -454,7 +462,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
     for i in range(args.steps):
         step(reps[i % STEP_REPLICAS], evs[i])
     torch.cuda.synchronize()
-    launch_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in evs)
+    call_ms = [ev[0].elapsed_time(ev[1]) for ev in evs]
+    launch_ms = statistics.mean(call_ms)
 
     # ---------------------------------------------------------------- e2e
     # Each step copies its activations in from pinned host memory, runs, and
@@ -522,6 +531,8 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> None:
                 "launch_unit": "one qm_gemv_q4_0_list call: two launches of the list kernel (128 and 96 "
                                "problems); achieved and traffic are per call",
                 "launch_ms": launch_ms,
+                "launch_ms_median": statistics.median(call_ms), "launch_ms_min": min(call_ms),
+                "calls_timed": len(call_ms),
                 "weight_gbs_per_launch": wbytes / (launch_ms * 1e-3) / 1e9,
                 "per_config": {}}
 
