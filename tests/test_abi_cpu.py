@@ -200,3 +200,16 @@ def test_list_ordering_rules(lib):
     p1_wait = _p(C_ADDR, W_ADDR + 0x100000, C_ADDR + 0x100000, N=64, K=256, wait_for=0)
     rc = qm.qm_gemv_q4_0_list_ptr([p0, p1_wait], 1)
     assert rc not in (qm.QM_ERR_ALIAS, qm.QM_ERR_SHAPE, qm.QM_ERR_NULL, qm.QM_ERR_ALIGN)
+
+
+def test_list_prebuilt_problem_array_takes_the_same_checks(lib):
+    # gemv_problem_array builds the C array once (for callers that pass the
+    # same list every step); the call then checks it exactly as a tuple list.
+    p0 = _p(A_ADDR, W_ADDR, C_ADDR, N=256, K=256)
+    bad = [p0, _p(C_ADDR, W_ADDR + 0x100000, C_ADDR + 0x100000, N=64, K=256)]
+    arr = qm.gemv_problem_array(bad)
+    assert len(arr) == 2 and arr[1].A == C_ADDR and arr[1].wait_for == -1 and arr[1].reserved == 0
+    assert qm.qm_gemv_q4_0_list_ptr(arr, 1) == qm.qm_gemv_q4_0_list_ptr(bad, 1) == qm.QM_ERR_ALIAS
+    assert qm.qm_gemv_q4_0_list_ptr(qm.gemv_problem_array([]), 1) == qm.QM_OK
+    assert qm.qm_gemv_q4_0_list_ptr(qm.gemv_problem_array([_p(A_ADDR, W_ADDR, C_ADDR, K=33)]), 1) == \
+        qm.QM_ERR_SHAPE
