@@ -496,6 +496,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         int st = 0, issued = 0;
         uint32_t ph = 0;
         bool warmed = false;
+        const float* a_prev = nullptr;
         for (int qi = 0; qi < P.count; ++qi) {
             const ListProblem& q = P.p[qi];
             int first;
@@ -513,6 +514,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
                     tma_prefetch_l2_4d(map, 0, 0, (i % U) / cu, 16 * (first + (i / U) * G));
                 grid_dependency_wait();
             }
+            if (q.A != a_prev && q.wait_for < 0) {
+                // New activations that nothing in this launch writes: on
+                // their way to L2 as this problem's first weights are, a few
+                // stages before the consumers read them.
+                const uint32_t nb = static_cast<uint32_t>(q.K) * 4u;
+                for (uint32_t o = 0; o < nb; o += 16384u)
+                    bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(q.A) + o, min(16384u, nb - o));
+            }
+            a_prev = q.A;
             for (int s0 = 0; s0 < total; s0 += kLW) {
                 if (issued >= kLStages && !wait_idle(&empty[st], ph ^ 1u, abort_flag)) break;
                 if (aborted(abort_flag)) break;
@@ -652,13 +662,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
                 // units about to be rewritten, unless the warp read them alone.
                 if (rounds > 0 && !prev_own) ok = pair_meet();
                 if (!ok) break;
-                if (warp == 0 && lane == 0 && qi + 1 < P.count && P.p[qi + 1].A != q.A &&
-                    P.p[qi + 1].wait_for < 0) {
-                    // The next problem's activations, on their way to L2.
-                    const uint32_t nb = static_cast<uint32_t>(P.p[qi + 1].K) * 4u;
-                    for (uint32_t o = 0; o < nb; o += 16384u)
-                        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(P.p[qi + 1].A) + o, min(16384u, nb - o));
-                }
                 // All of this warp's units in flight at once, then converted.
                 const uint8_t* a_g = reinterpret_cast<const uint8_t*>(q.A);
                 for (int u = warp; u < U; u += kLW) {
