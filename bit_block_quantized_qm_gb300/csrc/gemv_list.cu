@@ -123,8 +123,9 @@ struct ListProblem {
     int c;         // units per box (16 or 8)
 };
 
-// The weight tensor maps first (64-byte aligned), then the problems.
-struct alignas(64) ListParams {
+// The weight tensor maps first (aligned as CUtensorMap requires), then the
+// problems.
+struct ListParams {
     CUtensorMap map[kListMaxProblems];
     ListProblem p[kListMaxProblems];
     int count;
