@@ -160,13 +160,14 @@ def sweep_operands(qm, torch, dev, cases, replicas: int):
     a_host = np.concatenate([cases[j].acts().ravel() for j in inputs])
     reps = []
     for _ in range(replicas):
-        A = torch.from_numpy(a_host).to(dev)
+        A = torch.from_numpy(a_host).to(dev, copy=True)
         C = torch.empty(int(c_off[-1]), dtype=torch.float32, device=dev)
         arr = qm.gemv_problem_array([
             (A.data_ptr() + 4 * int(a_off[i]), weights[i].data_ptr(), C.data_ptr() + 4 * int(c_off[i]),
              c.N, c.K, -1) for i, c in enumerate(cases)])
         reps.append({"A": A, "C": C, "problems": arr})
-    torch.cuda.synchronize()
+    if dev.type == "cuda":
+        torch.cuda.synchronize()
     return weights, a_host, int(c_off[-1]), reps
 
 
